@@ -1,0 +1,357 @@
+// cf_api.cu -- the C ABI (include/cf.h): argument validation, TMA tensor-map
+// encoding, device checks, grid sizing and launch of the fused kernels.
+//
+// Validation runs entirely on the host before any CUDA call, so every
+// argument error is reported synchronously and nothing is enqueued.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "cf_internal.h"
+
+// Device status word written by bounded waits that give up.
+__device__ unsigned int g_cf_status_word;
+
+namespace cf {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  cudaError_t err = cudaSuccess;
+  int sms = 0;
+  int major = 0, minor = 0;
+  unsigned* status = nullptr;
+  bool prepared[4][3] = {};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Returns the current device's cached info, or an error status.
+cf_status current_device(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return CF_ERR_NO_DEVICE;
+  }
+  if (dev >= kMaxDevices) return CF_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    cudaDeviceProp prop;
+    d.err = cudaGetDeviceProperties(&prop, dev);
+    if (d.err == cudaSuccess) {
+      d.sms = prop.multiProcessorCount;
+      d.major = prop.major;
+      d.minor = prop.minor;
+      void* sp = nullptr;
+      d.err = cudaGetSymbolAddress(&sp, g_cf_status_word);
+      d.status = static_cast<unsigned*>(sp);
+    }
+    d.init = true;
+  }
+  if (d.err != cudaSuccess) return CF_ERR_CUDA;
+  if (!(d.major == 10 && d.minor == 3)) return CF_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return CF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(int dtype) { return dtype == CF_BF16 ? 2 : 4; }
+
+// Logical rows x cols view checks shared by every operand.
+cf_status check_matrix(const cf_matrix* m, int dtype, bool allow_trans) {
+  if (!m || !m->ptr) return CF_ERR_INVALID_ARG;
+  if (m->dtype != dtype) return CF_ERR_INVALID_ARG;
+  if (m->trans != 0 && !(allow_trans && m->trans == 1)) return CF_ERR_INVALID_ARG;
+  if (m->rows < 0 || m->cols < 0) return CF_ERR_INVALID_ARG;
+  const int64_t inner = m->trans ? m->rows : m->cols;
+  if (m->ld < inner || m->ld < 1) return CF_ERR_INVALID_ARG;
+  if (!aligned16(m->ptr) || ((m->ld * (int64_t)elem_size(dtype)) % 16) != 0) return CF_ERR_MISALIGNED;
+  return CF_OK;
+}
+
+cf_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return CF_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CF_OK : CF_ERR_CUDA;
+}
+
+long long wait_timeout_cycles() {
+  const char* e = std::getenv("CF_WAIT_TIMEOUT_CYCLES");
+  if (e && *e) {
+    long long v = std::atoll(e);
+    if (v > 0) return v;
+  }
+  return 4000000000LL;  // about two seconds at the maximum SM clock
+}
+
+struct EpiPlan {
+  int rowop = ROW_NONE;
+  float eps = 0.0f;
+  int n_elem = 0;
+  int kinds[CF_EPI_MAX_OPS] = {};
+  float scalars[CF_EPI_MAX_OPS] = {};
+  bool need_bias = false, need_gamma = false, need_beta = false;
+};
+
+cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
+  if (!epi || epi->version != CF_EPI_VERSION || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if (epi->exchange < CF_XCHG_AUTO || epi->exchange > CF_XCHG_GLOBAL) return CF_ERR_INVALID_ARG;
+  for (uint32_t i = 0; i < epi->n_ops; ++i) {
+    const cf_op& op = epi->ops[i];
+    if (!std::isfinite(op.scalar)) return CF_ERR_INVALID_ARG;
+    switch (op.kind) {
+      case CF_OP_BIAS: plan->need_bias = true; break;
+      case CF_OP_SCALE: case CF_OP_RELU: case CF_OP_GELU_TANH: break;
+      case CF_OP_ROW_LAYERNORM: case CF_OP_ROW_RMSNORM: case CF_OP_ROW_SOFTMAX:
+        if (i + 1 != epi->n_ops) return CF_ERR_INVALID_ARG;  // a reduction ends the program
+        if (op.kind != CF_OP_ROW_SOFTMAX && op.scalar < 0.0f) return CF_ERR_INVALID_ARG;
+        plan->rowop = op.kind == CF_OP_ROW_LAYERNORM ? ROW_LAYERNORM
+                      : op.kind == CF_OP_ROW_RMSNORM ? ROW_RMSNORM : ROW_SOFTMAX;
+        plan->eps = op.scalar;
+        plan->need_gamma = op.kind != CF_OP_ROW_SOFTMAX;
+        plan->need_beta = op.kind == CF_OP_ROW_LAYERNORM;
+        continue;
+      default: return CF_ERR_INVALID_ARG;
+    }
+    plan->kinds[plan->n_elem] = op.kind;
+    plan->scalars[plan->n_elem] = op.scalar;
+    plan->n_elem++;
+  }
+  return CF_OK;
+}
+
+// Exchange mode the fused kernel will use (host-only decision).
+int choose_xmode(const EpiPlan& plan, const cf_epi_desc* epi, int64_t tiles_n) {
+  if (plan.rowop == ROW_NONE || tiles_n == 1) return X_NONE;
+  if (epi->exchange == CF_XCHG_GLOBAL) return X_GLOBAL;
+  if (epi->exchange == CF_XCHG_CLUSTER) return X_CLUSTER;
+  return tiles_n <= kMaxClusterCtas ? X_CLUSTER : X_GLOBAL;
+}
+
+size_t ws_bytes_for(int64_t strips, int64_t tiles_n) {
+  const size_t stats = (size_t)strips * (size_t)tiles_n * kBM * sizeof(float2);
+  const size_t counters = (size_t)strips * 4 * sizeof(unsigned);
+  return ((stats + 255) & ~size_t(255)) + ((counters + 255) & ~size_t(255));
+}
+
+struct GemmShape {
+  int64_t M, N, K;
+};
+
+cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float* bias, const float* gamma,
+                            const float* beta, const cf_epi_desc* epi, const cf_matrix* out,
+                            EpiPlan* plan, GemmShape* sh) {
+  cf_status s;
+  if ((s = check_matrix(A, CF_BF16, false)) != CF_OK) return s;
+  if ((s = check_matrix(B, CF_BF16, true)) != CF_OK) return s;
+  if ((s = check_matrix(out, CF_FP32, false)) != CF_OK) return s;
+  if ((s = parse_epi(epi, plan)) != CF_OK) return s;
+  if (epi->out_dtype != CF_FP32) return CF_ERR_INVALID_ARG;
+  const int64_t M = A->rows, K = A->cols, N = B->cols;
+  if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
+  if ((plan->need_bias && !bias) || (plan->need_gamma && !gamma) || (plan->need_beta && !beta))
+    return CF_ERR_INVALID_ARG;
+  if ((bias && !aligned16(bias)) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+    return CF_ERR_MISALIGNED;
+  sh->M = M;
+  sh->N = N;
+  sh->K = K;
+  if (M == 0 || N == 0) return CF_OK;
+  if (M % kBM != 0 || N % kBN != 0 || K % kBK != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
+  if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
+  const int64_t tiles_n = N / kBN;
+  if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)
+    return CF_ERR_UNSUPPORTED_SHAPE;
+  return CF_OK;
+}
+
+}  // namespace
+}  // namespace cf
+
+using namespace cf;
+
+extern "C" {
+
+int cf_abi_version(void) { return CF_ABI_VERSION; }
+
+const char* cf_status_string(cf_status s) {
+  switch (s) {
+    case CF_OK: return "CF_OK";
+    case CF_ERR_INVALID_ARG: return "CF_ERR_INVALID_ARG";
+    case CF_ERR_UNSUPPORTED_SHAPE: return "CF_ERR_UNSUPPORTED_SHAPE";
+    case CF_ERR_MISALIGNED: return "CF_ERR_MISALIGNED";
+    case CF_ERR_UNSUPPORTED_DEVICE: return "CF_ERR_UNSUPPORTED_DEVICE";
+    case CF_ERR_CUDA: return "CF_ERR_CUDA";
+    case CF_ERR_TIMEOUT: return "CF_ERR_TIMEOUT";
+    case CF_ERR_WORKSPACE: return "CF_ERR_WORKSPACE";
+    case CF_ERR_NO_DEVICE: return "CF_ERR_NO_DEVICE";
+  }
+  return "CF_ERR_UNKNOWN";
+}
+
+size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_desc* epi) {
+  if (!A || !B || !epi) return 0;
+  EpiPlan plan;
+  if (parse_epi(epi, &plan) != CF_OK) return 0;
+  const int64_t M = A->rows, N = B->cols;
+  if (M <= 0 || N <= 0 || M % kBM != 0 || N % kBN != 0) return 0;
+  const int64_t tiles_n = N / kBN;
+  // The cluster path may fall back to the workspace path when no cluster of
+  // that size can be resident, so AUTO/CLUSTER strips that fit a cluster
+  // still report the (small) fallback workspace.
+  if (plan.rowop == ROW_NONE || tiles_n == 1) return 0;
+  return ws_bytes_for(M / kBM, tiles_n);
+}
+
+cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* bias, const float* gamma,
+                           const float* beta, const cf_epi_desc* epi, cf_matrix* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  EpiPlan plan;
+  GemmShape sh;
+  cf_status s = validate_gemm_epi(A, B, bias, gamma, beta, epi, out, &plan, &sh);
+  if (s != CF_OK) return s;
+  if (sh.M == 0 || sh.N == 0) return CF_OK;
+  const int64_t tiles_n = sh.N / kBN, strips = sh.M / kBM;
+  int xmode = choose_xmode(plan, epi, tiles_n);
+  const size_t need_ws = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
+  if (xmode == X_GLOBAL && (!workspace || workspace_bytes < need_ws || !aligned16(workspace)))
+    return CF_ERR_WORKSPACE;
+
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != CF_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  GemmEpiLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  GemmEpiParams& p = L.p;
+  if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
+    return s;
+  p.b_mn_major = B->trans == 0 ? 1 : 0;
+  if (p.b_mn_major)
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
+  else
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK, kBN);
+  if (s != CF_OK) return s;
+  if ((s = encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32, 32)) != CF_OK)
+    return s;
+  p.M = (int)sh.M;
+  p.N = (int)sh.N;
+  p.K = (int)sh.K;
+  p.tiles_n = (int)tiles_n;
+  p.strips = (int)strips;
+  p.num_items = (int)(strips * tiles_n);
+  p.n_ops = plan.n_elem;
+  for (int i = 0; i < plan.n_elem; ++i) {
+    p.op_kind[i] = plan.kinds[i];
+    p.op_scalar[i] = plan.scalars[i];
+  }
+  p.eps = plan.eps;
+  p.bias = bias;
+  p.gamma = gamma;
+  p.beta = beta;
+  p.status = dev->status;
+  p.timeout_cycles = wait_timeout_cycles();
+
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int x = X_NONE; x <= X_GLOBAL; ++x) {
+      if (plan.rowop == ROW_NONE && x != X_NONE) continue;
+      if (!dev->prepared[plan.rowop][x]) {
+        if (gemm_epi_prepare(plan.rowop, x) != cudaSuccess) return CF_ERR_CUDA;
+        dev->prepared[plan.rowop][x] = true;
+      }
+    }
+  }
+
+  if (xmode == X_CLUSTER) {
+    int maxc = 0;
+    if (gemm_epi_max_clusters(plan.rowop, (int)tiles_n, &maxc) != cudaSuccess) {
+      cudaGetLastError();
+      maxc = 0;
+    }
+    if (maxc <= 0) {
+      if (epi->exchange == CF_XCHG_CLUSTER) return CF_ERR_UNSUPPORTED_SHAPE;
+      xmode = X_GLOBAL;  // no cluster of this size fits: partial-statistics fallback
+      if (!workspace || workspace_bytes < need_ws || !aligned16(workspace)) return CF_ERR_WORKSPACE;
+    } else {
+      const int64_t nclusters = strips < maxc ? strips : maxc;
+      L.cluster = (int)tiles_n;
+      L.grid = (int)(nclusters * tiles_n);
+    }
+  }
+  if (xmode != X_CLUSTER) {
+    int per_sm = 0;
+    if (gemm_epi_max_blocks_per_sm(plan.rowop, xmode, &per_sm) != cudaSuccess || per_sm < 1) return CF_ERR_CUDA;
+    const int64_t cap = (int64_t)per_sm * dev->sms;
+    L.grid = (int)(p.num_items < cap ? p.num_items : cap);
+    L.cluster = 1;
+  }
+  if (xmode == X_GLOBAL) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t stats = ((size_t)strips * tiles_n * kBM * sizeof(float2) + 255) & ~size_t(255);
+    p.ws_stats = reinterpret_cast<float2*>(ws);
+    p.ws_count = reinterpret_cast<unsigned*>(ws + stats);
+    if (cudaMemsetAsync(p.ws_count, 0, (size_t)strips * 4 * sizeof(unsigned), st) != cudaSuccess) return CF_ERR_CUDA;
+  }
+  L.rowop = plan.rowop;
+  L.xmode = xmode;
+  if (gemm_epi_launch(L, st) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return CF_OK;
+}
+
+cf_status cf_last_device_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  cf_status s = current_device(&dev);
+  if (s != CF_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CF_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return CF_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return CF_ERR_CUDA;
+    return CF_ERR_TIMEOUT;
+  }
+  return CF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// cf_internal.h -- host-side structures shared by the C-ABI layer and the
+// kernel translation units (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/cf.h"
+
+namespace cf {
+
+// Row reduction that ends the epilogue program.
+enum RowOp : int { ROW_NONE = 0, ROW_LAYERNORM = 1, ROW_RMSNORM = 2, ROW_SOFTMAX = 3 };
+// How row statistics cross CTAs.
+enum XMode : int { X_NONE = 0, X_CLUSTER = 1, X_GLOBAL = 2 };
+
+// Tile shape of the fused GEMM-epilogue kernel.
+constexpr int kBM = 128;     // rows per tile = TMEM lanes
+constexpr int kBN = 256;     // columns per tile = one TMEM accumulator
+constexpr int kBK = 64;      // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kMaxClusterCtas = 16;
+
+// Kernel parameters (passed by value as a __grid_constant__).
+struct GemmEpiParams {
+  CUtensorMap tmA;    // A: bf16 [M][K], box {64, 128}, 128B swizzle
+  CUtensorMap tmB;    // B: K-major [N][K] box {64, 256} or MN-major [K][N] box {64, 64}
+  CUtensorMap tmOut;  // out: fp32 [M][N], box {32, 32}, 128B swizzle
+  int M, N, K;
+  int tiles_n;        // N / kBN
+  int strips;         // M / kBM
+  int num_items;      // strips * tiles_n
+  int b_mn_major;     // 1: B stored K x N (N contiguous)
+  int n_ops;          // elementwise ops (row op excluded)
+  int op_kind[CF_EPI_MAX_OPS];
+  float op_scalar[CF_EPI_MAX_OPS];
+  float eps;
+  const float* bias;
+  const float* gamma;
+  const float* beta;
+  float2* ws_stats;       // [strips][tiles_n][kBM] partial row statistics
+  unsigned* ws_count;     // [strips][4] arrival counters (cleared by the host)
+  unsigned* status;       // device status word
+  long long timeout_cycles;
+};
+
+struct GemmEpiLaunch {
+  GemmEpiParams p;
+  int rowop;
+  int xmode;
+  int grid;          // CTAs
+  int cluster;       // CTAs per cluster (X_CLUSTER), else 1
+};
+
+size_t gemm_epi_smem_bytes();
+cudaError_t gemm_epi_prepare(int rowop, int xmode);  // set function attributes
+cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);
+cudaError_t gemm_epi_max_clusters(int rowop, int cluster, int* out);
+cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out);
+
+}  // namespace cf

@@ -1,0 +1,456 @@
+"""Benchmark of the fused GEMM-epilogue / B2BGEMM path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the fused kernel over one batch of synthetic inputs
+that are already resident in HBM; L2 is flushed (a 256 MB write) between
+timed steps.  The default workload is GEMM + bias + tanh-GELU + row RMSNorm
+at M=8192, N=4096, K=4096.  Rank 0 prints ONE JSON line.
+
+``--impl reference`` times the float64 CPU oracle (the reference arm of this
+build, a deliberately slow plain implementation) on the host cores instead.
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload (rows are independent problems; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from back_gemm_fusion_gb300 import inputs as I  # noqa: E402
+
+METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)"
+
+# DRAM traffic (read + write bytes per launch) of the fused kernel, from an
+# ncu capture, keyed by workload; valid only while the kernel source hash
+# matches the one the counters were taken with.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("cf_gemm_epi.cu", "cf_b2b.cu", "cf_ptx.cuh", "cf_internal.h"):
+        with open(os.path.join(ROOT, "back_gemm_fusion_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- workloads
+class Workload:
+    """A fused GEMM-epilogue or B2BGEMM problem with its accounting."""
+
+    def __init__(self, name: str, seed: int = 0):
+        self.name = name
+        if name == "gelu_rmsnorm":
+            self.case = I.gelu_rmsnorm(seed)
+        elif name == "layernorm_256":
+            self.case = I.layernorm_256(seed)
+        elif name == "scaled_softmax":
+            self.case = I.scaled_softmax(seed)
+        elif name == "mlp_b2b":
+            self.case = I.mlp_b2b(seed)
+        elif name in ("attention_softmax", "attention_relu"):
+            op = "scale_softmax" if name == "attention_softmax" else "scale_relu"
+            self.case = I.attention_b2b(seed, op=op)
+        else:
+            raise ValueError(name)
+        self.is_b2b = name in ("mlp_b2b", "attention_softmax", "attention_relu")
+        c = self.case
+        if self.is_b2b:
+            self.flops = 2.0 * c.batch * c.M * (c.K * c.N1 + c.N1 * c.N2)
+            self.bytes = 2.0 * (c.A.numel() + c.W1.numel() + c.W2.numel()) + 4.0 * c.batch * c.M * c.N2
+            self.rows = c.batch * c.M
+        else:
+            vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta) if t is not None)
+            self.flops = 2.0 * c.M * c.N * c.K
+            self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + 4.0 * c.M * c.N
+            self.rows = c.M
+
+    def config(self):
+        c = self.case
+        if self.is_b2b:
+            return {"workload": self.name, "batch": c.batch, "M": c.M, "K": c.K, "N1": c.N1, "N2": c.N2,
+                    "mid_op": c.op, "intermediate": "bf16, on chip"}
+        return {"workload": self.name, "M": c.M, "N": c.N, "K": c.K, "ops": [list(o) for o in c.ops]}
+
+    # -- GPU side
+    def to_device(self):
+        c = self.case
+        dev = {}
+        if self.is_b2b:
+            dev["A"], dev["W1"], dev["W2"] = c.A.cuda(), c.W1.cuda(), c.W2.cuda()
+            dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=torch.float32, device="cuda")
+        else:
+            dev["A"], dev["B"] = c.A.cuda(), c.B.cuda()
+            for k in ("bias", "gamma", "beta"):
+                t = getattr(c, k)
+                dev[k] = None if t is None else t.cuda()
+            dev["out"] = torch.empty((c.M, c.N), dtype=torch.float32, device="cuda")
+        return dev
+
+    def fused_step(self, cf, dev, stream=None, workspace=None):
+        c = self.case
+        if self.is_b2b:
+            A = dev["A"] if c.batch > 1 else dev["A"][0]
+            W1 = dev["W1"] if c.batch > 1 else dev["W1"][0]
+            W2 = dev["W2"] if c.batch > 1 else dev["W2"][0]
+            out = dev["out"] if c.batch > 1 else dev["out"][0]
+            cf.cf_b2bgemm(A, W1, W2, c.op, c.scale, w1_trans=c.w1_k_major, out=out, stream=stream)
+        else:
+            cf.cf_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
+                                out=dev["out"], workspace=workspace, stream=stream)
+
+    def unfused_step(self, cf, dev, scratch, stream=None):
+        c = self.case
+        if self.is_b2b:
+            A = dev["A"] if c.batch > 1 else dev["A"][0]
+            W1 = dev["W1"] if c.batch > 1 else dev["W1"][0]
+            W2 = dev["W2"] if c.batch > 1 else dev["W2"][0]
+            out = dev["out"] if c.batch > 1 else dev["out"][0]
+            s, p = scratch
+            cf.cf_unfused_b2bgemm(A, W1, W2, c.op, c.scale, w1_trans=c.w1_k_major, out=out,
+                                  s_buf=s if c.batch > 1 else s[0], p_buf=p if c.batch > 1 else p[0],
+                                  stream=stream)
+        else:
+            cf.cf_unfused_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
+                                        out=dev["out"], intermediate=scratch, stream=stream)
+
+    def unfused_scratch(self):
+        c = self.case
+        if self.is_b2b:
+            return (torch.empty((c.batch, c.M, c.N1), dtype=torch.float32, device="cuda"),
+                    torch.empty((c.batch, c.M, c.N1), dtype=torch.bfloat16, device="cuda"))
+        return torch.empty((c.M, c.N), dtype=torch.float32, device="cuda")
+
+    # -- oracle side (CPU)
+    def _f64(self, key):
+        cache = self.__dict__.setdefault("_f64_cache", {})
+        if key not in cache:
+            cache[key] = I.to_f64(getattr(self.case, key))
+        return cache[key]
+
+    def oracle_rows(self, rows):
+        """Run the oracle on a subset of output rows (flops of that subset)."""
+        from oracle import cf_oracle as O
+        c = self.case
+        if self.is_b2b:
+            # rows index flattened (batch, row) pairs; group by batch entry
+            b_idx = rows // c.M
+            r_idx = rows % c.M
+            for b in np.unique(b_idx):
+                rr = r_idx[b_idx == b]
+                A = I.to_f64(c.A[b])[rr]
+                W1 = I.to_f64(c.W1[b])
+                W1 = W1.T if c.w1_k_major else W1
+                O.b2bgemm(A, W1, I.to_f64(c.W2[b]), c.op, c.scale)
+            return 2.0 * len(rows) * (c.K * c.N1 + c.N1 * c.N2)
+        A = self._f64("A")[rows]
+        O.gemm_epilogue(A, self._f64("B"), c.ops, self._f64("bias"), self._f64("gamma"), self._f64("beta"))
+        return 2.0 * len(rows) * c.N * c.K
+
+
+# ----------------------------------------------------------------- helpers
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [s for s in sms if s > 0.5 * max(sms)] or sms
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_oracle(wl: Workload, budget_s: float):
+    """Time the oracle on a seeded row sample sized to about budget_s seconds."""
+    rng = np.random.default_rng(0)
+    n = 16 if wl.is_b2b else 64
+    t0 = time.perf_counter()
+    flops = wl.oracle_rows(np.sort(rng.choice(wl.rows, size=min(n, wl.rows), replace=False)))
+    dt = time.perf_counter() - t0
+    rows = int(min(wl.rows, max(n, n * budget_s / max(dt, 1e-3))))
+    sample = np.sort(rng.choice(wl.rows, size=rows, replace=False))
+    t0 = time.perf_counter()
+    flops = wl.oracle_rows(sample)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, rows, dt
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, wl: Workload, dist, rank, world):
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    for _ in range(args.warmup):
+        time_oracle(wl, args.ref_step_seconds / 4)
+    vals, rows_used, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, rows_used, dt = time_oracle(wl, args.ref_step_seconds)
+        vals.append(v)
+        secs += dt
+    value = statistics.mean(vals)
+    sample = f"{rows_used} of {wl.rows} output rows (seeded), float64 numpy oracle, extrapolated per row"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": wl.config(),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl: Workload, dist, rank, world, local):
+    import back_gemm_fusion_gb300 as cf
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    cf.load_library()
+    peaks = load_peaks()
+    dev = wl.to_device()
+    stream = torch.cuda.current_stream()
+    workspace = None
+    if not wl.is_b2b:
+        c = wl.case
+        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda")
+
+    def step():
+        wl.fused_step(cf, dev, stream, workspace)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if cf.cf_last_device_status() != 0:
+        raise RuntimeError("device status reports a timeout after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    if cf.cf_last_device_status() != 0:
+        raise RuntimeError("device status reports a timeout in the timed region")
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = max_over_ranks(dist, statistics.mean(ms))
+    tflops = wl.flops / (ms_step * 1e-3) / 1e12
+    value = tflops * world
+
+    # Unfused comparison (cuBLASLt GEMM + separate epilogue kernel), same run.
+    unfused = None
+    try:
+        scratch = wl.unfused_scratch()
+        for _ in range(2):
+            wl.unfused_step(cf, dev, scratch, stream)
+        torch.cuda.synchronize()
+        um = []
+        for k in range(max(3, args.steps)):
+            flush.fill_(float(k))
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            wl.unfused_step(cf, dev, scratch, stream)
+            e.record(stream)
+            torch.cuda.synchronize()
+            um.append(s.elapsed_time(e))
+        u = statistics.mean(um)
+        unfused = {"ms_per_step": u, "tflops": wl.flops / (u * 1e-3) / 1e12, "fused_speedup": u / ms_step,
+                   "path": "cuBLASLt GEMM -> HBM intermediate -> separate epilogue kernel"}
+        del scratch
+    except Exception as exc:  # the comparison path is optional for the headline
+        unfused = {"error": str(exc)[:200]}
+
+    # End to end through the public API: pinned host inputs -> device, fused
+    # call, device -> pinned host output, all inside the timed region.
+    c = wl.case
+    host_in = []
+    names = ("A", "W1", "W2") if wl.is_b2b else ("A", "B", "bias", "gamma", "beta")
+    for k in names:
+        t = getattr(c, k)
+        if t is not None:
+            host_in.append((k, t.pin_memory()))
+    host_out = torch.empty(dev["out"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
+    d2h = host_out.numel() * 4
+    e2e_ms = []
+    for k in range(max(3, args.steps)):
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for name, t in host_in:
+            dev[name].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(dev["out"], non_blocking=True)
+        e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(s.elapsed_time(e))
+    e2e_step = max_over_ranks(dist, statistics.mean(e2e_ms))
+    e2e_val = wl.flops / (e2e_step * 1e-3) / 1e12 * world
+
+    if rank != 0:
+        return
+    # CPU baseline: the oracle on the host cores, bounded sample.
+    ref_tflops, ref_rows, ref_s = time_oracle(wl, args.cpu_seconds)
+    t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
+    src = kernel_source_hash()
+    tr = NCU_TRAFFIC.get(wl.name)
+    traffic = tr["bytes"] if tr and tr.get("src") == src else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**wl.config(), "l2": "flushed between timed steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst",
+                     "roofline_frac": (t_roof * 1e3) / ms_step},
+        "intermediate_hbm_bytes": (None if traffic is None else max(0.0, traffic - wl.bytes)),
+        "compulsory_bytes": wl.bytes,
+        "cpu_baseline": {"value": ref_tflops, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{ref_rows} of {wl.rows} output rows (seeded), {ref_s:.1f} s"},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_step},
+        "unfused": unfused,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+        "kernel_src": src,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gelu_rmsnorm",
+                    choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
+                             "attention_relu"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0, help="oracle seconds per reference step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    dist, rank, world, local = dist_setup(args)
+    wl = Workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl, dist, rank, world)
+    else:
+        run_ours(args, wl, dist, rank, world, local)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * cf.h -- C ABI of the GB300 (sm_103a) fused GEMM-epilogue / B2BGEMM library.
+ *
+ * What the library computes comes from the Pith review of "ComFuse: Fusing
+ * Complex Memory-Intensive Subgraphs with Compute-Intensive Kernels For
+ * Modern GPU Architectures" (arXiv 2608.03537):
+ *   - "What carries the argument" (Stage-Stream Execution Model): the GEMM's
+ *     output tiles stream, while still on chip, through elementwise nodes at
+ *     fragment granularity; each reduction is a stage boundary aggregated
+ *     hierarchically (within a thread/warp, across warps in shared memory,
+ *     across CTAs of a thread-block cluster through distributed shared memory).
+ *   - Referee report, major comment 1 [Sec. III, Eq. (1)]: a reduction along
+ *     the column dimension of P only needs the row strip {T_{m,n}}_n; when the
+ *     strip is wider than one cluster a multi-cluster fallback is required
+ *     (this library exchanges per-tile partial statistics through a small
+ *     caller-provided workspace).
+ *   - "What carries the argument" and major comment 2 [Sec. IV-A,
+ *     Eqs. (3)-(5)]: back-to-back GEMM (B2BGEMM) keeps the post-processed
+ *     intermediate tile on chip and accumulates the second GEMM from it, so
+ *     the intermediate matrix never reaches global memory.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are described by cf_matrix: element (r, c) of the logical
+ *     rows x cols matrix is at ptr[r * ld + c] when trans == 0 and at
+ *     ptr[c * ld + r] when trans == 1 (ld in elements).  All data pointers
+ *     are DEVICE pointers of the current CUDA device, owned by the caller;
+ *     the library never frees or retains them after the call returns.
+ *   - Calls enqueue work on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and return without synchronising.  Errors found on the host
+ *     are returned synchronously and nothing is enqueued.  A device-side
+ *     bounded wait that gives up is reported by cf_last_device_status().
+ *   - There is no CPU fallback: without an sm_103 device every compute entry
+ *     point returns CF_ERR_UNSUPPORTED_DEVICE (or CF_ERR_NO_DEVICE).
+ *   - Entry points are thread-safe for distinct streams; tensor-map encoding
+ *     is done per call on the host (no global mutable state beyond a
+ *     per-device attribute cache).
+ */
+#ifndef CF_GB300_H
+#define CF_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CF_API __attribute__((visibility("default")))
+#else
+#define CF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CF_ABI_VERSION 1
+
+typedef enum {
+  CF_OK = 0,
+  CF_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, inconsistent dims     */
+  CF_ERR_UNSUPPORTED_SHAPE = 2,  /* dims not multiples of the tile sizes listed  */
+  CF_ERR_MISALIGNED = 3,         /* pointer or leading dim not 16-byte aligned   */
+  CF_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+  CF_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed            */
+  CF_ERR_TIMEOUT = 6,            /* a device-side bounded wait gave up           */
+  CF_ERR_WORKSPACE = 7,          /* workspace missing or smaller than required   */
+  CF_ERR_NO_DEVICE = 8           /* no CUDA device visible                       */
+} cf_status;
+
+typedef enum { CF_BF16 = 0, CF_FP32 = 1 } cf_dtype;
+
+/* A strided 2-D view of caller-owned device memory (see conventions above). */
+typedef struct {
+  void* ptr;
+  int32_t dtype; /* cf_dtype */
+  int32_t trans; /* 0: row-major view, 1: the stored matrix is the transpose */
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;    /* leading dimension of the stored matrix, in elements */
+} cf_matrix;
+
+/* Epilogue operations.  Elementwise ops (kind < 16) are applied in order to
+ * every element of P = A.B; a row reduction (kind >= 16) may appear at most
+ * once and only as the last op (reductions are stage boundaries). */
+typedef enum {
+  CF_OP_BIAS = 1,            /* x += bias[n]                                        */
+  CF_OP_SCALE = 2,           /* x *= scalar                                         */
+  CF_OP_RELU = 3,            /* x = max(x, 0)                                       */
+  CF_OP_GELU_TANH = 4,       /* x = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))  */
+  CF_OP_ROW_LAYERNORM = 16,  /* y = gamma[n] (x - mean) / sqrt(var + scalar) + beta[n], biased var */
+  CF_OP_ROW_RMSNORM = 17,    /* y = gamma[n] x / sqrt(mean(x^2) + scalar)           */
+  CF_OP_ROW_SOFTMAX = 18     /* y = exp(x - max) / sum(exp(x - max))                */
+} cf_op_kind;
+
+typedef struct {
+  int32_t kind;  /* cf_op_kind */
+  float scalar;  /* the scale for CF_OP_SCALE, eps for the norms, unused otherwise */
+} cf_op;
+
+#define CF_EPI_VERSION 1
+#define CF_EPI_MAX_OPS 8
+
+/* Row-statistics exchange used when a row spans several CTAs. */
+typedef enum {
+  CF_XCHG_AUTO = 0,    /* cluster DSMEM when the strip fits one cluster, else workspace */
+  CF_XCHG_CLUSTER = 1, /* force the thread-block-cluster DSMEM exchange (<= 16 CTAs)  */
+  CF_XCHG_GLOBAL = 2   /* force per-tile partial statistics through the workspace    */
+} cf_exchange;
+
+/* A tiny epilogue program: a linear chain of ops (the Stage-Stream model with
+ * one trailing reduction stage). */
+typedef struct {
+  uint32_t version;  /* must be CF_EPI_VERSION */
+  uint32_t n_ops;    /* 0..CF_EPI_MAX_OPS */
+  cf_op ops[CF_EPI_MAX_OPS];
+  int32_t out_dtype; /* cf_dtype of `out`; CF_FP32 in this version */
+  int32_t exchange;  /* cf_exchange */
+} cf_epi_desc;
+
+/*
+ * cf_gemm_epilogue -- out = epilogue(A . B), fused in one kernel.
+ *
+ *   A    : M x K, bf16, trans == 0 (K contiguous).
+ *   B    : K x N, bf16; trans == 0 (stored K x N, N contiguous) or
+ *          trans == 1 (stored N x K, K contiguous, e.g. a Linear weight).
+ *   bias, gamma, beta : device fp32 vectors of length N; required only when
+ *          the program uses CF_OP_BIAS / a norm (beta only for LayerNorm);
+ *          may be NULL otherwise.
+ *   out  : M x N, fp32, trans == 0.
+ *   workspace : device memory of at least cf_workspace_size(...) bytes when
+ *          that is non-zero (per-tile partial row statistics and arrival
+ *          counters; the call clears the counters on `stream`).  Its contents
+ *          are scratch; concurrent calls must use distinct workspaces.
+ *
+ * Shape rules (this version): M % 128 == 0, N % 256 == 0, K % 64 == 0,
+ * K >= 64, all pointers and leading dims 16-byte aligned.  Violations return
+ * CF_ERR_UNSUPPORTED_SHAPE / CF_ERR_MISALIGNED without launching anything.
+ * M == 0 returns CF_OK without launching.
+ */
+CF_API cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
+                           const float* bias, const float* gamma, const float* beta,
+                           const cf_epi_desc* epi, cf_matrix* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace cf_gemm_epilogue needs for these operands (0 if none). */
+CF_API size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_desc* epi);
+
+/* Intermediate ops of a B2BGEMM. */
+typedef enum {
+  CF_MID_RELU = 1,          /* S' = max(S, 0)                    */
+  CF_MID_SCALE_RELU = 2,    /* S' = max(scale S, 0)              */
+  CF_MID_SCALE_SOFTMAX = 3  /* S' = row softmax of (scale S)     */
+} cf_mid_op;
+
+#define CF_B2B_VERSION 1
+
+typedef struct {
+  uint32_t version;  /* must be CF_B2B_VERSION */
+  int32_t mid_op;    /* cf_mid_op */
+  float mid_scale;   /* scale for the SCALE_* ops */
+  int32_t out_dtype; /* CF_FP32 in this version */
+  int64_t batch;     /* number of independent problems (>= 1) */
+  int64_t strideA, strideW1, strideW2, strideOut; /* elements between problems */
+} cf_b2b_desc;
+
+/*
+ * cf_b2bgemm -- out = bf16_rne(F(A . W1)) . W2 per batch entry, fused: the
+ * intermediate S' never reaches global memory.
+ *
+ *   A   : M x K bf16, trans == 0.
+ *   W1  : K x N1 bf16; trans == 0 (stored K x N1) or trans == 1 (stored
+ *         N1 x K, e.g. the key matrix of attention, giving S = Q K^T).
+ *   W2  : N1 x N2 bf16, trans == 0 (stored N1 x N2, e.g. the value matrix).
+ *   out : M x N2 fp32, trans == 0.
+ *   The softmax mid op normalises each row of S over all N1 columns.
+ *
+ * Shape rules (this version): M % 128 == 0, K % 64 == 0, N1 % 128 == 0,
+ * N2 % 64 == 0 with N2 <= 256 for the softmax op (one CTA holds the whole
+ * output row block) and N2 % 256 == 0 otherwise.
+ */
+CF_API cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
+                     const cf_b2b_desc* desc, cf_matrix* out, void* stream);
+
+/*
+ * cf_unfused_gemm_epilogue -- the unfused comparison path: a cuBLASLt GEMM
+ * writes P (M x N fp32) to `intermediate`, then a separate row-epilogue
+ * kernel reads it back and writes `out`.  Same program semantics as
+ * cf_gemm_epilogue.  `intermediate` is caller-owned device memory of
+ * M * N * 4 bytes.
+ */
+CF_API cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
+                                   const float* bias, const float* gamma, const float* beta,
+                                   const cf_epi_desc* epi, cf_matrix* out,
+                                   float* intermediate, void* stream);
+
+/*
+ * cf_unfused_b2bgemm -- unfused comparison path for B2BGEMM: cuBLASLt GEMM1
+ * to `s_buf` (M x N1 fp32), a mid-op kernel writing bf16 S' to `p_buf`
+ * (M x N1 bf16), cuBLASLt GEMM2 to `out`.  Same semantics as cf_b2bgemm.
+ */
+CF_API cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
+                             const cf_b2b_desc* desc, cf_matrix* out,
+                             float* s_buf, void* p_buf, void* stream);
+
+/* Reads and clears the device status word written by bounded waits
+ * (synchronises the stream first).  CF_OK or CF_ERR_TIMEOUT. */
+CF_API cf_status cf_last_device_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+CF_API const char* cf_status_string(cf_status s);
+
+/* ABI version (CF_ABI_VERSION) of the loaded library. */
+CF_API int cf_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CF_GB300_H */

@@ -1,0 +1,110 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds, loads
+and exports every symbol include/cf.h declares; argument validation returns
+the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    from back_gemm_fusion_gb300 import binding
+    return binding.load_library()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "cf.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"CF_API\s+[\w\s\*]+?\b(cf_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = _declared_symbols()
+    for s in ["cf_gemm_epilogue", "cf_b2bgemm", "cf_workspace_size", "cf_status_string",
+              "cf_last_device_status", "cf_unfused_gemm_epilogue", "cf_unfused_b2bgemm", "cf_abi_version"]:
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in _declared_symbols():
+        assert hasattr(lib, s), f"{s} declared in include/cf.h but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.cf_abi_version() == 1
+    from back_gemm_fusion_gb300.binding import STATUS_NAMES
+    for code, name in STATUS_NAMES.items():
+        assert lib.cf_status_string(code).decode() == name
+
+
+def _mats(M=256, N=256, K=256, a_ptr=0x10000, b_ptr=0x20000, o_ptr=0x30000):
+    from back_gemm_fusion_gb300.binding import cf_matrix, CF_BF16, CF_FP32
+    A = cf_matrix(a_ptr, CF_BF16, 0, M, K, K)
+    B = cf_matrix(b_ptr, CF_BF16, 0, K, N, N)
+    O = cf_matrix(o_ptr, CF_FP32, 0, M, N, N)
+    return A, B, O
+
+
+def _call(lib, A, B, O, ops, bias=0x40000, gamma=0x50000, beta=0x60000, exchange="auto", ws=None, ws_bytes=0):
+    from back_gemm_fusion_gb300.binding import epi_desc
+    d = epi_desc(ops, exchange)
+    return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), bias, gamma, beta, ctypes.byref(d),
+                                ctypes.byref(O), ws, ws_bytes, None)
+
+
+LN = [("bias",), ("layernorm", 1e-5)]
+
+
+def test_validation_errors(lib):
+    A, B, O = _mats()
+    assert _call(lib, A, B, O, LN, bias=None) == 1          # missing bias
+    assert _call(lib, A, B, O, LN, beta=None) == 1          # LayerNorm needs beta
+    assert _call(lib, A, B, O, [("softmax",), ("bias",)]) == 1  # reduction must be last
+    assert _call(lib, A, B, O, [("layernorm", -1.0)]) == 1  # negative eps
+    A2, B2, O2 = _mats(K=256)
+    B2.rows = 128
+    assert _call(lib, A2, B2, O2, LN) == 1                  # inconsistent K
+    A3, B3, O3 = _mats(M=200)
+    assert _call(lib, A3, B3, O3, LN) == 2                  # M not a multiple of 128
+    A4, B4, O4 = _mats(N=384)
+    assert _call(lib, A4, B4, O4, LN) == 2                  # N not a multiple of 256
+    A5, B5, O5 = _mats(K=96)
+    assert _call(lib, A5, B5, O5, LN) == 2                  # K not a multiple of 64
+    A6, B6, O6 = _mats(a_ptr=0x10008)
+    assert _call(lib, A6, B6, O6, LN) == 3                  # misaligned pointer
+    A7, B7, O7 = _mats()
+    A7.ld = 260
+    assert _call(lib, A7, B7, O7, LN) == 3                  # ld*2 not a multiple of 16
+    A8, B8, O8 = _mats()
+    assert _call(lib, A8, B8, O8, LN, bias=0x40004) == 3    # misaligned vector
+    A9, B9, O9 = _mats(N=256 * 17)
+    assert _call(lib, A9, B9, O9, LN, exchange="cluster") == 2  # 17 tiles > 16-CTA cluster
+    A10, B10, O10 = _mats(N=256 * 17)
+    assert _call(lib, A10, B10, O10, LN) == 7               # wide rows need a workspace
+    A11, B11, O11 = _mats(M=0)
+    assert _call(lib, A11, B11, O11, LN) == 0               # empty problem: nothing to do
+
+
+def test_valid_call_without_gpu_reports_device(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    A, B, O = _mats()
+    assert _call(lib, A, B, O, LN) in (4, 8)  # unsupported device / no device: never a CPU fallback
+
+
+def test_workspace_size(lib):
+    from back_gemm_fusion_gb300.binding import epi_desc
+    A, B, O = _mats(M=4096, N=16384, K=4096)
+    d = epi_desc([("scale", 1 / 64), ("softmax",)])
+    n = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(d))
+    assert n >= 4096 // 128 * 64 * 128 * 8 + 4096 // 128 * 16
+    assert n < 3 * 2 ** 20
+    d2 = epi_desc([("bias",)])
+    assert lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(d2)) == 0

@@ -1,0 +1,103 @@
+"""GPU parity: fused GEMM + epilogue (cf_gemm_epilogue through the C ABI)
+against the float64 oracle on the same seeded bf16/fp32 inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import cf_oracle as O
+from back_gemm_fusion_gb300 import inputs as I
+from tests.parity import assert_rows_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cf():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    import back_gemm_fusion_gb300 as cf
+    return cf
+
+
+def _dev(t):
+    return None if t is None else t.cuda()
+
+
+def _run(cf, case, b_trans=False, exchange="auto"):
+    A = case.A.cuda()
+    B = case.B.cuda()
+    if b_trans:
+        B = B.t().contiguous()  # stored N x K
+    out = cf.cf_gemm_epilogue(A, B, case.ops, _dev(case.bias), _dev(case.gamma), _dev(case.beta),
+                              b_trans=b_trans, exchange=exchange)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    return out.cpu().numpy()
+
+
+def _oracle(case, rows=None):
+    A = I.to_f64(case.A)
+    if rows is not None:
+        A = A[rows]
+    return O.gemm_epilogue(A, I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                           I.to_f64(case.beta))
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 128), (256, 512, 320), (384, 768, 1024)])
+def test_plain_gemm(cf, M, N, K, b_trans):
+    case = I.gemm_epilogue_case("gemm", M, N, K, [], seed=M + N + K)
+    assert_rows_close(_run(cf, case, b_trans), _oracle(case), strict=1e-4, what=f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_layernorm_256(cf, b_trans):
+    case = I.layernorm_256()
+    assert_rows_close(_run(cf, case, b_trans), _oracle(case), what="gemm+bias+layernorm 256^3")
+
+
+@pytest.mark.parametrize("ops", [[("bias",)], [("bias",), ("relu",)], [("scale", 0.5), ("gelu_tanh",)],
+                                 [("bias",), ("gelu_tanh",), ("scale", -2.0)]])
+def test_elementwise_programs(cf, ops):
+    case = I.gemm_epilogue_case("ew", 256, 512, 192, ops, seed=3, need_bias=True)
+    assert_rows_close(_run(cf, case), _oracle(case), strict=1e-4, what=str(ops))
+
+
+@pytest.mark.parametrize("exchange", ["cluster", "global"])
+@pytest.mark.parametrize("rowop", ["layernorm", "rmsnorm", "softmax"])
+@pytest.mark.parametrize("N", [512, 2048])
+def test_row_ops_multi_tile(cf, rowop, exchange, N):
+    ops = {"layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 1 / 16), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case(rowop, 384, N, 256, ops, seed=N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, exchange=exchange), _oracle(case), what=f"{rowop} N={N} {exchange}")
+
+
+@pytest.mark.parametrize("N", [4096, 4352])
+def test_softmax_wide_rows(cf, N):
+    # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path.
+    case = I.gemm_epilogue_case("sm", 256, N, 128, [("scale", 0.25), ("softmax",)], seed=5)
+    assert_rows_close(_run(cf, case), _oracle(case), what=f"softmax N={N}")
+
+
+def test_gelu_rmsnorm_full_size_sampled(cf):
+    case = I.gelu_rmsnorm()
+    gpu = _run(cf, case)
+    rows = sample_rows(case.M)
+    assert_rows_close(gpu[rows], _oracle(case, rows), what="gemm+bias+gelu+rmsnorm 8192x4096x4096")
+
+
+def test_scaled_softmax_full_size_sampled(cf):
+    case = I.scaled_softmax()
+    gpu = _run(cf, case)
+    rows = sample_rows(case.M)
+    ref = _oracle(case, rows)
+    assert_rows_close(gpu[rows], ref, what="gemm+scaled softmax 4096x16384x4096")
+    # Every row of a softmax sums to one (all rows, not only the sample).
+    assert np.max(np.abs(gpu.sum(1, dtype=np.float64) - 1.0)) < 1e-3
