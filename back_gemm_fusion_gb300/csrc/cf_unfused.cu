@@ -1,11 +1,280 @@
-// cf_unfused.cu -- unfused comparison path (placeholder).
+// cf_unfused.cu -- the unfused comparison path: a cuBLASLt GEMM writes the
+// intermediate to HBM, then separate kernels read it back.
+//
+// This is the baseline the fused kernels are measured against (the
+// materialisation boundary the ComFuse review describes in "The reading":
+// compute-intensive and memory-intensive operators as separate kernels, with
+// the intermediate tensor written to global memory and re-read).  The
+// epilogue kernels here are plain row-per-CTA kernels; the GEMMs are
+// cuBLASLt (bf16 inputs, fp32 accumulate and output).
+#include <cublasLt.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
 #include "cf_internal.h"
 
-extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix*, const cf_matrix*, const float*, const float*,
-                                              const float*, const cf_epi_desc*, cf_matrix*, float*, void*) {
-  return CF_ERR_UNSUPPORTED_SHAPE;
+namespace cf {
+namespace {
+
+constexpr int kMaxDev = 64;
+constexpr size_t kLtWorkspace = 64u << 20;  // cuBLASLt scratch, one per device (comparison path only)
+
+struct LtState {
+  cublasLtHandle_t h = nullptr;
+  void* ws = nullptr;
+  bool init = false;
+};
+std::mutex g_mu;
+LtState g_lt[kMaxDev];
+
+cf_status lt_state(LtState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return CF_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  LtState& s = g_lt[dev];
+  if (!s.init) {
+    if (cublasLtCreate(&s.h) != CUBLAS_STATUS_SUCCESS) return CF_ERR_CUDA;
+    if (cudaMalloc(&s.ws, kLtWorkspace) != cudaSuccess) return CF_ERR_CUDA;
+    s.init = true;
+  }
+  *out = &s;
+  return CF_OK;
 }
-extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix*, const cf_matrix*, const cf_matrix*, const cf_b2b_desc*,
-                                        cf_matrix*, float*, void*, void*) {
-  return CF_ERR_UNSUPPORTED_SHAPE;
+
+// Row-major C[M x N] (fp32) = A[M x K] (bf16, row-major) . B (bf16, K x N
+// row-major if !b_trans, else stored N x K), `batch` problems with element
+// strides.  Expressed column-major as C^T = B^T A^T.
+cf_status lt_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, bool b_trans, void* C, int64_t ldc,
+                  cudaDataType_t ctype, int64_t M, int64_t N, int64_t K, int64_t batch, int64_t sA, int64_t sB,
+                  int64_t sC, cudaStream_t stream) {
+  LtState* lt = nullptr;
+  cf_status st = lt_state(&lt);
+  if (st != CF_OK) return st;
+  cublasLtMatmulDesc_t op = nullptr;
+  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+  cublasLtMatmulPreference_t pref = nullptr;
+  cf_status rs = CF_ERR_CUDA;
+  do {
+    if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) break;
+    cublasOperation_t ta = b_trans ? CUBLAS_OP_T : CUBLAS_OP_N, tb = CUBLAS_OP_N;
+    cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta));
+    cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb));
+    // cuBLAS "A" = B memory: N x K (col-major, ld ldb) or K x N when stored N x K.
+    if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, b_trans ? K : N, b_trans ? N : K, ldb) != CUBLAS_STATUS_SUCCESS)
+      break;
+    if (cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, K, M, lda) != CUBLAS_STATUS_SUCCESS) break;
+    if (cublasLtMatrixLayoutCreate(&lc, ctype, N, M, ldc) != CUBLAS_STATUS_SUCCESS) break;
+    if (batch > 1) {
+      int32_t b32 = (int32_t)batch;
+      cublasLtMatrixLayoutSetAttribute(la, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &b32, sizeof(b32));
+      cublasLtMatrixLayoutSetAttribute(lb, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &b32, sizeof(b32));
+      cublasLtMatrixLayoutSetAttribute(lc, CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &b32, sizeof(b32));
+      cublasLtMatrixLayoutSetAttribute(la, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sB, sizeof(sB));
+      cublasLtMatrixLayoutSetAttribute(lb, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sA, sizeof(sA));
+      cublasLtMatrixLayoutSetAttribute(lc, CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &sC, sizeof(sC));
+    }
+    if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
+    size_t wsb = kLtWorkspace;
+    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb));
+    cublasLtMatmulHeuristicResult_t heur;
+    int found = 0;
+    if (cublasLtMatmulAlgoGetHeuristic(lt->h, op, la, lb, lc, lc, pref, 1, &heur, &found) !=
+            CUBLAS_STATUS_SUCCESS ||
+        found == 0)
+      break;
+    const float alpha = 1.0f, beta = 0.0f;
+    if (cublasLtMatmul(lt->h, op, &alpha, B, la, A, lb, &beta, C, lc, C, lc, &heur.algo, lt->ws, kLtWorkspace,
+                       stream) != CUBLAS_STATUS_SUCCESS)
+      break;
+    rs = CF_OK;
+  } while (false);
+  if (pref) cublasLtMatmulPreferenceDestroy(pref);
+  if (lc) cublasLtMatrixLayoutDestroy(lc);
+  if (lb) cublasLtMatrixLayoutDestroy(lb);
+  if (la) cublasLtMatrixLayoutDestroy(la);
+  if (op) cublasLtMatmulDescDestroy(op);
+  return rs;
+}
+
+struct RowProgram {
+  int n_ops;
+  int kind[CF_EPI_MAX_OPS];
+  float scalar[CF_EPI_MAX_OPS];
+  int rowop;  // 0 none, CF_OP_ROW_* otherwise
+  float eps;
+};
+
+__device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* bias, int n) {
+  for (int o = 0; o < pg.n_ops; ++o) {
+    switch (pg.kind[o]) {
+      case CF_OP_BIAS: x += bias[n]; break;
+      case CF_OP_SCALE: x *= pg.scalar[o]; break;
+      case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
+      case CF_OP_GELU_TANH: x = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x))); break;
+    }
+  }
+  return x;
+}
+
+// Block-wide sum or max of one value per thread (blockDim.x == 256).
+template <bool kMax>
+__device__ float block_reduce(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kMax ? fmaxf(v, w) : v + w;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = kMax ? fmaxf(r, red[i]) : r + red[i];
+  return r;
+}
+
+// One CTA per row: read P back from HBM, elementwise program, row statistic,
+// normalise, write out.  The activated row is kept in shared memory.
+__global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restrict__ P, int64_t ldp,
+                                                           float* __restrict__ out, int64_t ldo, int N,
+                                                           RowProgram pg, const float* __restrict__ bias,
+                                                           const float* __restrict__ gamma,
+                                                           const float* __restrict__ beta) {
+  extern __shared__ float row[];
+  __shared__ float red[32];
+  const float* p = P + (int64_t)blockIdx.x * ldp;
+  float* o = out + (int64_t)blockIdx.x * ldo;
+  float acc = 0.0f, mx = -INFINITY;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    const float x = ew(pg, p[n], bias, n);
+    row[n] = x;
+    acc += x;
+    mx = fmaxf(mx, x);
+  }
+  if (pg.rowop == 0) {
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = row[n];
+    return;
+  }
+  if (pg.rowop == CF_OP_ROW_LAYERNORM) {
+    const float mean = block_reduce<false>(acc, red) / N;
+    float ss = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      const float d = row[n] - mean;
+      ss += d * d;
+    }
+    const float rstd = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = gamma[n] * (row[n] - mean) * rstd + beta[n];
+  } else if (pg.rowop == CF_OP_ROW_RMSNORM) {
+    float ss = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) ss += row[n] * row[n];
+    const float rstd = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = gamma[n] * row[n] * rstd;
+  } else {
+    const float m = block_reduce<true>(mx, red);
+    float s = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) s += __expf(row[n] - m);
+    const float inv = 1.0f / block_reduce<false>(s, red);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = __expf(row[n] - m) * inv;
+  }
+}
+
+// Mid op of the unfused B2BGEMM: S (fp32) -> bf16 S' = F(S), one CTA per row.
+__global__ void __launch_bounds__(256) mid_op_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ Pout,
+                                                     int N1, int op, float scale) {
+  extern __shared__ float row[];
+  __shared__ float red[32];
+  const float* s = S + (int64_t)blockIdx.x * N1;
+  __nv_bfloat16* p = Pout + (int64_t)blockIdx.x * N1;
+  if (op != CF_MID_SCALE_SOFTMAX) {
+    const float sc = op == CF_MID_RELU ? 1.0f : scale;
+    for (int n = threadIdx.x; n < N1; n += blockDim.x) p[n] = __float2bfloat16_rn(fmaxf(sc * s[n], 0.0f));
+    return;
+  }
+  float mx = -INFINITY;
+  for (int n = threadIdx.x; n < N1; n += blockDim.x) {
+    row[n] = scale * s[n];
+    mx = fmaxf(mx, row[n]);
+  }
+  const float m = block_reduce<true>(mx, red);
+  float sum = 0.0f;
+  for (int n = threadIdx.x; n < N1; n += blockDim.x) sum += __expf(row[n] - m);
+  const float inv = 1.0f / block_reduce<false>(sum, red);
+  for (int n = threadIdx.x; n < N1; n += blockDim.x) p[n] = __float2bfloat16_rn(__expf(row[n] - m) * inv);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace cf
+
+using namespace cf;
+
+extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* bias,
+                                              const float* gamma, const float* beta, const cf_epi_desc* epi,
+                                              cf_matrix* out, float* intermediate, void* stream) {
+  if (!A || !B || !epi || !out || !intermediate || !A->ptr || !B->ptr || !out->ptr) return CF_ERR_INVALID_ARG;
+  if (A->dtype != CF_BF16 || B->dtype != CF_BF16 || out->dtype != CF_FP32 || A->trans || out->trans)
+    return CF_ERR_INVALID_ARG;
+  if (epi->version != CF_EPI_VERSION || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  const int64_t M = A->rows, K = A->cols, N = B->cols;
+  if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return CF_OK;
+  if (N > 16384) return CF_ERR_UNSUPPORTED_SHAPE;  // the row must fit the epilogue's shared memory
+  if (!aligned16(A->ptr) || !aligned16(B->ptr) || !aligned16(intermediate)) return CF_ERR_MISALIGNED;
+  RowProgram pg;
+  std::memset(&pg, 0, sizeof(pg));
+  for (uint32_t i = 0; i < epi->n_ops; ++i) {
+    const int k = epi->ops[i].kind;
+    if (k >= CF_OP_ROW_LAYERNORM) {
+      if (i + 1 != epi->n_ops) return CF_ERR_INVALID_ARG;
+      pg.rowop = k;
+      pg.eps = epi->ops[i].scalar;
+    } else {
+      pg.kind[pg.n_ops] = k;
+      pg.scalar[pg.n_ops] = epi->ops[i].scalar;
+      pg.n_ops++;
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cf_status s = lt_gemm(A->ptr, A->ld, B->ptr, B->ld, B->trans != 0, intermediate, N, CUDA_R_32F, M, N, K, 1, 0,
+                        0, 0, st);
+  if (s != CF_OK) return s;
+  const size_t smem = (size_t)N * sizeof(float);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(row_epilogue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return CF_ERR_CUDA;
+  row_epilogue_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, static_cast<float*>(out->ptr), out->ld,
+                                                      (int)N, pg, bias, gamma, beta);
+  return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+}
+
+extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
+                                        const cf_b2b_desc* d, cf_matrix* out, float* s_buf, void* p_buf,
+                                        void* stream) {
+  if (!A || !W1 || !W2 || !d || !out || !s_buf || !p_buf) return CF_ERR_INVALID_ARG;
+  if (d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
+  if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX) return CF_ERR_INVALID_ARG;
+  const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols;
+  if (W1->rows != K || W2->rows != N1 || out->rows != M || out->cols != N2) return CF_ERR_INVALID_ARG;
+  if (N1 > 16384) return CF_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t batch = d->batch;
+  cf_status s = lt_gemm(A->ptr, A->ld, W1->ptr, W1->ld, W1->trans != 0, s_buf, N1, CUDA_R_32F, M, N1, K, batch,
+                        d->strideA, d->strideW1, M * N1, st);
+  if (s != CF_OK) return s;
+  const size_t smem = (size_t)N1 * sizeof(float);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(mid_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return CF_ERR_CUDA;
+  mid_op_kernel<<<(unsigned)(M * batch), 256, smem, st>>>(s_buf, static_cast<__nv_bfloat16*>(p_buf), (int)N1,
+                                                          d->mid_op, d->mid_scale);
+  if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+  return lt_gemm(p_buf, N1, W2->ptr, W2->ld, W2->trans != 0, out->ptr, out->ld, CUDA_R_32F, M, N2, N1, batch,
+                 M * N1, d->strideW2, d->strideOut, st);
 }

@@ -65,8 +65,9 @@ def load_peaks():
 class Workload:
     """A fused GEMM-epilogue or B2BGEMM problem with its accounting."""
 
-    def __init__(self, name: str, seed: int = 0):
+    def __init__(self, name: str, seed: int = 0, exchange: str = "auto"):
         self.name = name
+        self.exchange = exchange
         if name == "gelu_rmsnorm":
             self.case = I.gelu_rmsnorm(seed)
         elif name == "layernorm_256":
@@ -97,7 +98,8 @@ class Workload:
         if self.is_b2b:
             return {"workload": self.name, "batch": c.batch, "M": c.M, "K": c.K, "N1": c.N1, "N2": c.N2,
                     "mid_op": c.op, "intermediate": "bf16, on chip"}
-        return {"workload": self.name, "M": c.M, "N": c.N, "K": c.K, "ops": [list(o) for o in c.ops]}
+        return {"workload": self.name, "M": c.M, "N": c.N, "K": c.K, "ops": [list(o) for o in c.ops],
+                "row_stat_exchange": self.exchange}
 
     # -- GPU side
     def to_device(self):
@@ -124,7 +126,7 @@ class Workload:
             cf.cf_b2bgemm(A, W1, W2, c.op, c.scale, w1_trans=c.w1_k_major, out=out, stream=stream)
         else:
             cf.cf_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
-                                out=dev["out"], workspace=workspace, stream=stream)
+                                out=dev["out"], workspace=workspace, stream=stream, exchange=self.exchange)
 
     def unfused_step(self, cf, dev, scratch, stream=None):
         c = self.case
@@ -310,7 +312,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     workspace = None
     if not wl.is_b2b:
         c = wl.case
-        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops)
+        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops, exchange=args.exchange)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
     flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda")
@@ -438,12 +440,14 @@ def main():
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
                              "attention_relu"])
+    ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
+                    help="row-statistics exchange of the fused GEMM-epilogue kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--ref-step-seconds", type=float, default=5.0, help="oracle seconds per reference step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     dist, rank, world, local = dist_setup(args)
-    wl = Workload(args.workload)
+    wl = Workload(args.workload, exchange=args.exchange)
     if args.impl == "reference":
         run_reference(args, wl, dist, rank, world)
     else:
