@@ -62,6 +62,8 @@ _SIGNATURES = {
                                         ctypes.c_void_p, _P(cf_epi_desc), _P(cf_matrix), ctypes.c_void_p,
                                         ctypes.c_size_t, ctypes.c_void_p]),
     "cf_workspace_size": (ctypes.c_size_t, [_P(cf_matrix), _P(cf_matrix), _P(cf_epi_desc)]),
+    "cf_gemm_epilogue_noalloc": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, _P(cf_epi_desc), _P(cf_matrix), ctypes.c_void_p]),
     "cf_b2bgemm": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), _P(cf_matrix), _P(cf_b2b_desc),
                                   _P(cf_matrix), ctypes.c_void_p]),
     "cf_unfused_gemm_epilogue": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), ctypes.c_void_p, ctypes.c_void_p,
@@ -172,6 +174,24 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
     st = lib.cf_gemm_epilogue(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                               ctypes.byref(d), ctypes.byref(o), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "cf_gemm_epilogue")
+    return out
+
+
+def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bias=None, gamma=None,
+                             beta=None, out: Optional[torch.Tensor] = None, b_trans: bool = False,
+                             exchange: str = "auto", stream=None) -> torch.Tensor:
+    """Same as cf_gemm_epilogue, but the library takes any scratch it needs
+    from its own static device array: nothing is allocated by this call
+    (``out`` must be given by callers that cannot allocate)."""
+    lib = load_library()
+    if out is None:
+        M = A.shape[0]
+        N = B.shape[0] if b_trans else B.shape[1]
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange)
+    st = lib.cf_gemm_epilogue_noalloc(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
+                                      ctypes.byref(d), ctypes.byref(o), _stream(stream))
+    _check(st, "cf_gemm_epilogue_noalloc")
     return out
 
 

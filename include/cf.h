@@ -143,6 +143,40 @@ CF_API cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
 /* Bytes of workspace cf_gemm_epilogue needs for these operands (0 if none). */
 CF_API size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_desc* epi);
 
+/* Size of the library-owned scratch array used by cf_gemm_epilogue_noalloc. */
+#define CF_NOALLOC_WORKSPACE_BYTES (4u << 20)
+
+/*
+ * cf_gemm_epilogue_noalloc -- cf_gemm_epilogue for callers that cannot
+ * allocate device memory.  (The paper has no counterpart; this is a library
+ * convenience.)
+ *
+ * Who needs it: callers that must not call cudaMalloc or any other
+ * allocator where they run this kernel -- code with latency bounds (an
+ * allocation may synchronise the device), plugins whose host framework owns
+ * all device memory and offers no allocator, and steady-state loops that
+ * must not allocate.  Rows wider than one 256-column tile need scratch for
+ * partial row statistics; this call takes it from a static device array of
+ * CF_NOALLOC_WORKSPACE_BYTES (4 MiB) inside the library instead of a
+ * caller-provided workspace.  It calls no allocator.
+ *
+ * Arguments and results are those of cf_gemm_epilogue without the workspace.
+ * Problems needing more scratch than the array holds (cf_workspace_size >
+ * CF_NOALLOC_WORKSPACE_BYTES, i.e. roughly M * N > 2^27 with a row op)
+ * return CF_ERR_WORKSPACE and enqueue nothing.
+ *
+ * Sharing: all calls in the process share the one array per device, which
+ * keeps the last call's contents; each call clears the part that must start
+ * at zero on its own stream.  Calls whose executions overlap on the GPU race
+ * on the array and must be serialised by the caller.  Every GPU that loads
+ * the library holds the array until the process exits.  The first call on a
+ * device looks up the array's address on that device (which must be
+ * current); make that first call before any stream capture.
+ */
+CF_API cf_status cf_gemm_epilogue_noalloc(const cf_matrix* A, const cf_matrix* B,
+                                          const float* bias, const float* gamma, const float* beta,
+                                          const cf_epi_desc* epi, cf_matrix* out, void* stream);
+
 /* Intermediate ops of a B2BGEMM. */
 typedef enum {
   CF_MID_RELU = 1,          /* S' = max(S, 0)                    */
