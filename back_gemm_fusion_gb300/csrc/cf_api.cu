@@ -28,6 +28,8 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   unsigned* status = nullptr;
   bool prepared[4][3] = {};
+  int max_clusters[4][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
+  int blocks_per_sm[4][3] = {};                    // 0 = unknown
 };
 
 std::mutex g_mu;
@@ -111,14 +113,6 @@ cf_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_
   return r == CUDA_SUCCESS ? CF_OK : CF_ERR_CUDA;
 }
 
-long long wait_timeout_cycles() {
-  const char* e = std::getenv("CF_WAIT_TIMEOUT_CYCLES");
-  if (e && *e) {
-    long long v = std::atoll(e);
-    if (v > 0) return v;
-  }
-  return 4000000000LL;  // about two seconds at the maximum SM clock
-}
 
 struct EpiPlan {
   int rowop = ROW_NONE;
@@ -202,6 +196,42 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
 }
 
 }  // namespace
+
+long long wait_timeout_cycles() {
+  const char* e = std::getenv("CF_WAIT_TIMEOUT_CYCLES");
+  if (e && *e) {
+    long long v = std::atoll(e);
+    if (v > 0) return v;
+  }
+  return 4000000000LL;  // about two seconds at the maximum SM clock
+}
+
+cf_status device_query(int* sms, unsigned** status) {
+  DeviceInfo* d = nullptr;
+  cf_status s = current_device(&d);
+  if (s != CF_OK) return s;
+  *sms = d->sms;
+  *status = d->status;
+  return CF_OK;
+}
+
+cf_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* ptr, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || rank < 1 || rank > 5) return CF_ERR_CUDA;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  CUresult r = enc(map, dt, (cuuint32_t)rank, ptr, d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CF_OK : CF_ERR_CUDA;
+}
+
 }  // namespace cf
 
 using namespace cf;
@@ -301,13 +331,28 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
 
   if (xmode == X_CLUSTER) {
     int maxc = 0;
-    if (gemm_epi_max_clusters(plan.rowop, (int)tiles_n, &maxc) != cudaSuccess) {
-      cudaGetLastError();
-      maxc = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      int& cached = dev->max_clusters[plan.rowop][tiles_n];
+      if (cached == 0) {
+        int q = 0;
+        if (gemm_epi_max_clusters(plan.rowop, (int)tiles_n, &q) != cudaSuccess) {
+          cudaGetLastError();
+          q = 0;
+        }
+        cached = q > 0 ? q : -1;
+      }
+      maxc = cached > 0 ? cached : 0;
     }
-    if (maxc <= 0) {
+    // The review leaves the choice of inter-CTA aggregation mode open (its
+    // threshold C_N).  Here the DSMEM exchange is used on AUTO only when the
+    // resident clusters keep at least 90% of the SMs busy; otherwise the
+    // per-tile partial-statistics exchange over a persistent grid of every SM
+    // is faster (measured: 16-CTA clusters fill only 112 of 152 GB300 SMs).
+    const bool fills_gpu = (int64_t)maxc * tiles_n * 10 >= (int64_t)dev->sms * 9;
+    if (maxc <= 0 || (epi->exchange == CF_XCHG_AUTO && !fills_gpu)) {
       if (epi->exchange == CF_XCHG_CLUSTER) return CF_ERR_UNSUPPORTED_SHAPE;
-      xmode = X_GLOBAL;  // no cluster of this size fits: partial-statistics fallback
+      xmode = X_GLOBAL;
       if (!workspace || workspace_bytes < need_ws || !aligned16(workspace)) return CF_ERR_WORKSPACE;
     } else {
       const int64_t nclusters = strips < maxc ? strips : maxc;
@@ -317,7 +362,13 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   }
   if (xmode != X_CLUSTER) {
     int per_sm = 0;
-    if (gemm_epi_max_blocks_per_sm(plan.rowop, xmode, &per_sm) != cudaSuccess || per_sm < 1) return CF_ERR_CUDA;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      int& cached = dev->blocks_per_sm[plan.rowop][xmode];
+      if (cached == 0 && gemm_epi_max_blocks_per_sm(plan.rowop, xmode, &cached) != cudaSuccess) cached = 0;
+      per_sm = cached;
+    }
+    if (per_sm < 1) return CF_ERR_CUDA;
     const int64_t cap = (int64_t)per_sm * dev->sms;
     L.grid = (int)(p.num_items < cap ? p.num_items : cap);
     L.cluster = 1;

@@ -1,7 +1,817 @@
-// cf_b2b.cu -- fused back-to-back GEMM (placeholder until the kernel lands).
-#include "cf_internal.h"
+// cf_b2bgemm.cu -- fused back-to-back GEMM: O = bf16(F(A . W1)) . W2 with the
+// intermediate S' never written to global memory.
+//
+// ComFuse review, "What carries the argument": the B2BGEMM schedule keeps the
+// post-processed intermediate tile S_tile on chip and accumulates the second
+// GEMM's output from it; referee report, major comment 2 [Sec. IV-A,
+// Eqs. (3)-(5)]: the intermediate tile transform F and the segmented
+// accumulation over the co-scheduled CTAs.  The page's "four-stage pipeline"
+// is cut off; it is read here as load -> GEMM1 -> F -> GEMM2, overlapped
+// across intermediate chunks.
+//
+// Two sm_103a kernels:
+//
+// attn_kernel (W1 given as its transpose, K = N2 = 128; the attention shape
+// S = Q K^T):  one CTA owns a 128-row block of A for one batch entry and
+// walks the N1 dimension in 128-wide chunks.  Per chunk j: S_j = A . W1_j in
+// TMEM (two S buffers, so S_{j+1} is computed while F runs on S_j), F on
+// TMEM rows in registers, S'_j rounded to bf16 into a swizzled shared-memory
+// tile, then O += S'_j . W2_j in TMEM.  For the softmax op the row
+// statistics use the online form (running max m and sum l, O rescaled when
+// the max grows; the rescale is skipped while the max grows by less than
+// 2^8, since exp2(x - m) <= 256 stays exact enough in bf16 and fp32), and O
+// is divided by l at the end.  This is the C = 1 (single-CTA) case of the
+// review's Eq. (5) merge.
+//
+// mlp_kernel (general K, N1; N2 = 256 * C): a cluster of C CTAs shares one
+// 128-row strip.  CTA c owns O[:, 256c .. 256c+255] in TMEM (the whole
+// 128 x N2 fp32 strip does not fit one SM's TMEM).  For each round of C
+// chunks of N1, CTA c computes the 128 x 128 chunk S_c = A . W1[:, chunk],
+// applies F, rounds to bf16 and writes it into the same shared-memory slot of
+// every CTA of the cluster (distributed shared memory), so GEMM1 work is never
+// repeated; each CTA then accumulates O_c += [S'_0 .. S'_{C-1}] . W2[round
+// rows, its columns].  This is the review's cluster-cooperative dataflow:
+// the second GEMM's output accumulation is distributed across the cluster.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
-extern "C" cf_status cf_b2bgemm(const cf_matrix*, const cf_matrix*, const cf_matrix*, const cf_b2b_desc*,
-                                cf_matrix*, void*) {
-  return CF_ERR_UNSUPPORTED_SHAPE;
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "cf_internal.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Write 32 fp32 values of row `r` (columns c0..c0+31 of a 128-column K-major
+// bf16 tile) into a 128-byte-swizzled smem tile made of two 64-column
+// regions of 16 KB each.
+__device__ __forceinline__ void store_row_bf16_sw128(uint8_t* tile, int r, int c0, const float (&v)[32]) {
+  const int region = c0 >> 6;
+  uint8_t* base = tile + region * 16384 + r * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = ((c0 & 63) >> 3) + q;  // 16-byte chunk (8 bf16) within the 128-byte row
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+      w[e] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(base + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Round 32 values to bf16 and back (the values the second GEMM consumes).
+__device__ __forceinline__ void round_bf16(float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+}
+
+// Stage a 32 x 32 fp32 block held one row per lane into swizzled smem.
+__device__ __forceinline__ void stage_out_block(uint8_t* buf, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+// ======================================================================
+// Attention-shaped B2BGEMM
+// ======================================================================
+namespace attn {
+
+constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
+constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
+constexpr int kRing = 3;                    // W1/W2 tiles in flight
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kOffQ + kTileBytes;
+constexpr int kOffP = kOffRing + kRing * kTileBytes;
+constexpr int kOffOut = kOffP + 2 * kTileBytes;
+constexpr int kOffBars = kOffOut + kEpiWarps * 4096;
+// q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2], pv_done[2], o_full, o_empty, drain
+constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 5, BAR_SF = 8, BAR_PF = 10, BAR_PV = 12, BAR_OF = 14,
+              BAR_OE = 15, BAR_DRAIN = 16, kNumBars = 17;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+constexpr float kRescaleLog2 = 8.0f;
+
+struct Params {
+  CUtensorMap tmA, tmW1, tmW2, tmO;  // 3-D: {128 cols, rows, batch}
+  int batch, m_blocks, n1_blocks, items;
+  int softmax;       // 1: scaled softmax, 0: ReLU (optionally scaled)
+  float scale;       // multiplies S before F
+  unsigned* status;
+  long long timeout_cycles;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
+  const int nb = p.n1_blocks;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_QF), 1);
+    mbar_init(bar(BAR_QE), 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(bar(BAR_RF + i), 1);
+      mbar_init(bar(BAR_RE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_SF + i), 1);
+      mbar_init(bar(BAR_PF + i), kEpiWarps);
+      mbar_init(bar(BAR_PV + i), 1);
+    }
+    mbar_init(bar(BAR_OF), 1);
+    mbar_init(bar(BAR_OE), kEpiWarps);
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmW1);
+    tma_prefetch_desc(&p.tmW2);
+    tma_prefetch_desc(&p.tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t rs = 0, rph = 0;
+      int it = 0;
+      bool ok = true;
+      auto load_tile = [&](const CUtensorMap* m, int row0, int b) -> bool {
+        if (!mbar_wait(bar(BAR_RE + rs), rph ^ 1, wc)) return false;
+        const uint32_t dst = sbase + kOffRing + rs * kTileBytes;
+        mbar_arrive_expect_tx(bar(BAR_RF + rs), kTileBytes);
+        tma_load_3d(dst, m, bar(BAR_RF + rs), 0, row0, b);
+        tma_load_3d(dst + 16384, m, bar(BAR_RF + rs), 64, row0, b);
+        if (++rs == kRing) { rs = 0; rph ^= 1; }
+        return true;
+      };
+      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+        const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
+        if (!mbar_wait(bar(BAR_QE), (it & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bar(BAR_QF), kTileBytes);
+        tma_load_3d(sbase + kOffQ, &p.tmA, bar(BAR_QF), 0, mb * kTile, b);
+        tma_load_3d(sbase + kOffQ + 16384, &p.tmA, bar(BAR_QF), 64, mb * kTile, b);
+        // Operand order = MMA consumption order: W1_0, W1_1, then W2_j, W1_{j+2}.
+        ok = load_tile(&p.tmW1, 0, b) && (nb < 2 || load_tile(&p.tmW1, kTile, b));
+        for (int j = 0; ok && j < nb; ++j) {
+          ok = load_tile(&p.tmW2, j * kTile, b);
+          if (ok && j + 2 < nb) ok = load_tile(&p.tmW1, (j + 2) * kTile, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 128, 0);   // W1 tile is K-major (rows = N1)
+      const uint32_t id_o = idesc_bf16_f32(128, 128, 1);   // W2 tile is MN-major (rows = K of GEMM2)
+      uint32_t rs = 0, rph = 0;
+      uint32_t g = 0;  // global chunk counter (S/P buffer = g & 1)
+      int it = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t gg) -> bool {
+        if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
+        tc_fence_after();
+        const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
+        const uint32_t d = tmem_base + (gg & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16(d, smem_desc_sw128(sbase + kOffQ + off, 16, 1024), smem_desc_sw128(wt + off, 16, 1024), id_s,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_RE + rs));
+        mma_commit(bar(BAR_SF + (gg & 1)));
+        if (++rs == kRing) { rs = 0; rph ^= 1; }
+        return true;
+      };
+      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+        if (!mbar_wait(bar(BAR_QF), it & 1, wc)) break;
+        tc_fence_after();
+        const uint32_t g0 = g;
+        ok = issue_s(g0) && (nb < 2 || issue_s(g0 + 1));
+        if (ok && nb <= 2) mma_commit(bar(BAR_QE));
+        for (int j = 0; ok && j < nb; ++j, ++g) {
+          if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
+          if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
+          const uint32_t pt = sbase + kOffP + (g & 1) * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_bf16(tmem_base + 256, smem_desc_sw128(pt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                     smem_desc_sw128(wt + kk * 2048, 16384, 1024), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_RE + rs));
+          mma_commit(bar(BAR_PV + (g & 1)));
+          if (++rs == kRing) { rs = 0; rph ^= 1; }
+          if (j + 2 < nb) {
+            ok = issue_s(g + 2);
+            if (ok && j + 3 == nb) mma_commit(bar(BAR_QE));  // last GEMM1 of this item issued
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(BAR_OF));
+      }
+      mma_commit(bar(BAR_DRAIN));
+      mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
+    }
+  } else {
+    // -------------------------------------- F (softmax / ReLU) and epilogue
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    uint8_t* out_buf = smem + kOffOut + (warp - 2) * 4096;
+    const uint32_t out_addr = sbase + kOffOut + (warp - 2) * 4096;
+    const float sl2 = p.scale * kLog2e;
+    uint32_t g = 0;
+    int it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+      const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
+      float m_used = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nb; ++j, ++g) {
+        const uint32_t sb = g & 1, u = g >> 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t s_addr = tmem_base + lane_off + sb * 128;
+        if (p.softmax) {
+          // Block max (log2 units), then a lazy rescale of O and l.
+          float bmax = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(s_addr + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) bmax = fmaxf(bmax, v[e]);
+          }
+          bmax *= sl2;
+          const bool need = bmax > m_used + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? bmax : m_used;
+            const float f = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - m_new);
+            if (j > 0) {
+              // O must hold every earlier S' . W2 product before it is rescaled.
+              const uint32_t pg = g - 1;
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + (pg & 1)), (pg >> 1) & 1, wc))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= f;
+                tmem_st32(tmem_base + lane_off + 256 + c * 32, v);
+              }
+              tmem_wait_st();
+            }
+            l *= f;
+            m_used = m_new;
+          }
+        }
+        // The S' buffer must no longer be read by the S'.W2 product two chunks back.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
+        uint8_t* ptile = smem + kOffP + sb * kTileBytes;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(s_addr + c * 32, v);
+          tmem_wait_ld();
+          if (p.softmax) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = ex2_approx(fmaf(v[e], sl2, -m_used));
+            round_bf16(v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) l += v[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = fmaxf(v[e] * p.scale, 0.0f);
+          }
+          store_row_bf16_sw128(ptile, row, c * 32, v);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_PF + sb));
+      }
+      if (!ok) break;
+      // Epilogue: O / l (softmax) -> fp32 output through swizzled smem + TMA.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), it & 1, wc))) break;
+      tc_fence_after();
+      const float inv = p.softmax ? 1.0f / l : 1.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] *= inv;
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        stage_out_block(out_buf, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tmO, out_addr, c * 32, mb * kTile + 32 * q, b);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_OE));
+    }
+    if (lane == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace attn
+
+
+// ======================================================================
+// MLP-shaped B2BGEMM (cluster-cooperative)
+// ======================================================================
+namespace mlp {
+
+constexpr int kStageBytes = 32768;              // one ring stage
+constexpr int kRing = 3;
+constexpr int kSlotBytes = 128 * 128 * 2;       // one 128 x 128 bf16 S' chunk
+constexpr int kMaxC = 4;                        // CTAs per cluster (N2 / 256)
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kOffRing = 0;
+constexpr int kOffSlots = kRing * kStageBytes;
+constexpr int kOffBars = kOffSlots + kMaxC * kSlotBytes;
+// ring_full[3], ring_empty[3], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain
+constexpr int BAR_RF = 0, BAR_RE = 3, BAR_SF = 6, BAR_SFREE = 8, BAR_SLF = 10, BAR_SLE = 11, BAR_OF = 12,
+              BAR_OE = 13, BAR_DRAIN = 14, kNumBars = 15;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,512)
+
+struct Params {
+  CUtensorMap tmA;   // {K, M, batch}, box {64, 128, 1}
+  CUtensorMap tmW1;  // MN-major: {N1, K, batch} box {64, 64, 1}; K-major: {K, N1, batch} box {64, 128, 1}
+  CUtensorMap tmW2;  // {N2, N1, batch}, box {64, 64, 1}
+  float* out;
+  long long ldo, stride_out;
+  int w1_k_major;
+  int C;             // CTAs per cluster = N2 / 256
+  int kblocks;       // K / 64
+  int rounds;        // N1 / (128 C)
+  int strips, items; // M / 128, batch * strips
+  float scale;       // F(S) = max(scale S, 0)
+  unsigned* status;
+  long long timeout_cycles;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
+  const int C = p.C;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  const int R = p.rounds;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(bar(BAR_RF + i), 1);
+      mbar_init(bar(BAR_RE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_SF + i), 1);
+      mbar_init(bar(BAR_SFREE + i), kEpiWarps);
+    }
+    mbar_init(bar(BAR_SLF), 1);   // one local arrive (+ the peers' bytes)
+    mbar_init(bar(BAR_SLE), C);   // one multicast commit from every CTA's second GEMM
+    mbar_init(bar(BAR_OF), 1);
+    mbar_init(bar(BAR_OE), kEpiWarps);
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmW1);
+    tma_prefetch_desc(&p.tmW2);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t rs = 0, rph = 0;
+      bool ok = true;
+      auto acquire = [&]() -> uint32_t {
+        if (!mbar_wait(bar(BAR_RE + rs), rph ^ 1, wc)) return 0;
+        return 1;
+      };
+      auto advance = [&]() { if (++rs == kRing) { rs = 0; rph ^= 1; } };
+      auto load_g1 = [&](int strip, int b, int r) -> bool {
+        const int h = r * C + (int)rank;  // this CTA's N1 chunk
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!acquire()) return false;
+          const uint32_t dst = sbase + kOffRing + rs * kStageBytes;
+          const uint32_t fb = bar(BAR_RF + rs);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_3d(dst, &p.tmA, fb, kb * 64, strip * 128, b);
+          if (p.w1_k_major) {
+            tma_load_3d(dst + 16384, &p.tmW1, fb, kb * 64, h * 128, b);
+          } else {
+            tma_load_3d(dst + 16384, &p.tmW1, fb, h * 128, kb * 64, b);
+            tma_load_3d(dst + 16384 + 8192, &p.tmW1, fb, h * 128 + 64, kb * 64, b);
+          }
+          advance();
+        }
+        return true;
+      };
+      auto load_g2 = [&](int b, int r) -> bool {
+        for (int c2 = 0; c2 < C; ++c2) {
+          for (int kh = 0; kh < 2; ++kh) {
+            if (!acquire()) return false;
+            const uint32_t dst = sbase + kOffRing + rs * kStageBytes;
+            const uint32_t fb = bar(BAR_RF + rs);
+            const int row0 = (r * C + c2) * 128 + kh * 64;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tma_load_3d(dst + i * 8192, &p.tmW2, fb, (int)rank * 256 + 64 * i, row0, b);
+            advance();
+          }
+        }
+        return true;
+      };
+      for (int item = cid; ok && item < p.items; item += ncl) {
+        const int b = item / p.strips, strip = item - b * p.strips;
+        ok = load_g1(strip, b, 0) && (R < 2 || load_g1(strip, b, 1));
+        for (int r = 0; ok && r < R; ++r) {
+          ok = load_g2(b, r);
+          if (ok && r + 2 < R) ok = load_g1(strip, b, r + 2);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 128, p.w1_k_major ? 0u : 1u);
+      const uint32_t id_o = idesc_bf16_f32(128, 256, 1u);
+      const uint16_t all = (uint16_t)((1u << C) - 1u);
+      uint32_t rs = 0, rph = 0;
+      uint32_t g = 0;  // global round counter
+      int t = 0;
+      bool ok = true;
+      auto g1 = [&](uint32_t gg) -> bool {
+        // The F warps must be done reading the S buffer's previous contents.
+        if (!mbar_wait(bar(BAR_SFREE + (gg & 1)), ((gg >> 1) & 1) ^ 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (gg & 1) * 128;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
+          tc_fence_after();
+          const uint32_t sa = sbase + kOffRing + rs * kStageBytes, sw = sa + 16384;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = p.w1_k_major ? smem_desc_sw128(sw + kk * 32, 16, 1024)
+                                             : smem_desc_sw128(sw + kk * 2048, 8192, 1024);
+            mma_bf16(d, smem_desc_sw128(sa + kk * 32, 16, 1024), bd, id_s, (kb | kk) ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_RE + rs));
+          if (++rs == kRing) { rs = 0; rph ^= 1; }
+        }
+        mma_commit(bar(BAR_SF + (gg & 1)));
+        return true;
+      };
+      for (int item = cid; ok && item < p.items; item += ncl, ++t) {
+        const uint32_t g0 = g;
+        ok = g1(g0) && (R < 2 || g1(g0 + 1));
+        for (int r = 0; ok && r < R; ++r, ++g) {
+          if (!mbar_wait(bar(BAR_SLF), g & 1, wc)) { ok = false; break; }
+          if (r == 0 && !mbar_wait(bar(BAR_OE), (t & 1) ^ 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          for (int c2 = 0; ok && c2 < C; ++c2) {
+            for (int kh = 0; kh < 2; ++kh) {
+              if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t wt = sbase + kOffRing + rs * kStageBytes;
+              const uint32_t at = sbase + kOffSlots + c2 * kSlotBytes + kh * 16384;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16(tmem_base + 256, smem_desc_sw128(at + kk * 32, 16, 1024),
+                         smem_desc_sw128(wt + kk * 2048, 8192, 1024), id_o,
+                         (r | c2 | kh | kk) ? 1u : 0u);
+              }
+              mma_commit(bar(BAR_RE + rs));
+              if (++rs == kRing) { rs = 0; rph ^= 1; }
+            }
+          }
+          if (!ok) break;
+          // Every CTA of the cluster may refill its slot once all have consumed it.
+          mma_commit_multicast(bar(BAR_SLE), all);
+          if (r + 2 < R) ok = g1(g + 2);
+        }
+        if (!ok) break;
+        mma_commit(bar(BAR_OF));
+      }
+      mma_commit(bar(BAR_DRAIN));
+      mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
+      // All peers' multicast arrivals for the last round have landed here.
+      if (ok && g > 0) mbar_wait<false, false>(bar(BAR_SLE), (g - 1) & 1, wc);
+    }
+  } else {
+    // ------------------------------------------------ F warps and epilogue
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    uint8_t* my_slot = smem + kOffSlots + rank * kSlotBytes;
+    const uint32_t my_slot_addr = sbase + kOffSlots + rank * kSlotBytes;
+    uint32_t g = 0;
+    int t = 0;
+    bool ok = true;
+    for (int item = cid; ok && item < p.items; item += ncl, ++t) {
+      const int b = item / p.strips, strip = item - b * p.strips;
+      for (int r = 0; r < R; ++r, ++g) {
+        const uint32_t sb = g & 1, u = g >> 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
+        // The slots may be overwritten once every CTA finished the previous round.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLE), (g & 1) ^ 1, wc))) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tmem_base + lane_off + sb * 128 + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = fmaxf(v[e] * p.scale, 0.0f);
+          store_row_bf16_sw128(my_slot, row, c * 32, v);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
+        named_barrier_sync(1, 32 * kEpiWarps);
+        if (warp == 2 && lane == 0) {
+          mbar_arrive_expect_tx(bar(BAR_SLF), (uint32_t)(C - 1) * kSlotBytes);
+          for (int pr = 1; pr < C; ++pr) {
+            const uint32_t peer = (rank + pr) % C;
+            bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF), peer);
+          }
+        }
+      }
+      if (!ok) break;
+      // Epilogue: this CTA's 128 x 256 block of O, straight from TMEM to HBM.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), t & 1, wc))) break;
+      tc_fence_after();
+      float* orow = p.out + (long long)b * p.stride_out + (long long)(strip * 128 + row) * p.ldo + rank * 256;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float v[32];
+        tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_OE));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  cluster_sync_all();
+}
+
+}  // namespace mlp
+
+std::mutex g_mu;
+bool g_prepared[64][2] = {};
+
+cf_status prepare(int slot, const void* fn, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CF_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_prepared[dev][slot]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return CF_ERR_CUDA;
+    }
+    g_prepared[dev][slot] = true;
+  }
+  return CF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cf_status check_bf16_view(const cf_matrix* m, bool allow_trans) {
+  if (!m || !m->ptr || m->dtype != CF_BF16) return CF_ERR_INVALID_ARG;
+  if (m->trans != 0 && !(allow_trans && m->trans == 1)) return CF_ERR_INVALID_ARG;
+  if (m->rows < 0 || m->cols < 0) return CF_ERR_INVALID_ARG;
+  if (m->ld < (m->trans ? m->rows : m->cols)) return CF_ERR_INVALID_ARG;
+  if (!aligned16(m->ptr) || (m->ld * 2) % 16 != 0) return CF_ERR_MISALIGNED;
+  return CF_OK;
+}
+
+
+cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2, const cf_b2b_desc* d,
+                     cf_matrix* out, int64_t C, int sms, unsigned* status, cudaStream_t stream) {
+  const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols, batch = d->batch;
+  const uint64_t bs = (uint64_t)batch;
+  mlp::Params p;
+  std::memset(&p, 0, sizeof(p));
+  cf_status s;
+  {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)M, bs};
+    const uint64_t st[2] = {(uint64_t)A->ld * 2, (uint64_t)(batch > 1 ? d->strideA : M * A->ld) * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if ((s = encode_tmap(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  p.w1_k_major = W1->trans;
+  if (W1->trans) {  // stored N1 x K
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N1, bs};
+    const uint64_t st[2] = {(uint64_t)W1->ld * 2, (uint64_t)(batch > 1 ? d->strideW1 : N1 * W1->ld) * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if ((s = encode_tmap(&p.tmW1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W1->ptr, dims, st, box)) != CF_OK) return s;
+  } else {          // stored K x N1
+    const uint64_t dims[3] = {(uint64_t)N1, (uint64_t)K, bs};
+    const uint64_t st[2] = {(uint64_t)W1->ld * 2, (uint64_t)(batch > 1 ? d->strideW1 : K * W1->ld) * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    if ((s = encode_tmap(&p.tmW1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W1->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)N2, (uint64_t)N1, bs};
+    const uint64_t st[2] = {(uint64_t)W2->ld * 2, (uint64_t)(batch > 1 ? d->strideW2 : N1 * W2->ld) * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  p.out = static_cast<float*>(out->ptr);
+  p.ldo = out->ld;
+  p.stride_out = batch > 1 ? d->strideOut : 0;
+  p.C = (int)C;
+  p.kblocks = (int)(K / 64);
+  p.rounds = (int)(N1 / (128 * C));
+  p.strips = (int)(M / 128);
+  p.items = (int)(batch * p.strips);
+  p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
+  p.status = status;
+  p.timeout_cycles = wait_timeout_cycles();
+  const void* fn = reinterpret_cast<const void*>(&mlp::mlp_kernel);
+  if ((s = prepare(1, fn, mlp::kSmemBytes)) != CF_OK) return s;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(mlp::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = mlp::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  int maxc = 0;
+  if (cudaOccupancyMaxActiveClusters(&maxc, fn, &cfg) != cudaSuccess || maxc < 1) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  const int64_t ncl = p.items < maxc ? p.items : maxc;
+  cfg.gridDim = dim3((unsigned)(ncl * C), 1, 1);
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return CF_OK;
+}
+}  // namespace
+}  // namespace cf
+
+using namespace cf;
+
+extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2, const cf_b2b_desc* d,
+                                cf_matrix* out, void* stream) {
+  cf_status s;
+  if (!d || d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
+  if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX || !std::isfinite(d->mid_scale))
+    return CF_ERR_INVALID_ARG;
+  if (d->out_dtype != CF_FP32) return CF_ERR_INVALID_ARG;
+  if ((s = check_bf16_view(A, false)) != CF_OK) return s;
+  if ((s = check_bf16_view(W1, true)) != CF_OK) return s;
+  if ((s = check_bf16_view(W2, false)) != CF_OK) return s;
+  if (!out || !out->ptr || out->dtype != CF_FP32 || out->trans) return CF_ERR_INVALID_ARG;
+  if (out->ld < out->cols) return CF_ERR_INVALID_ARG;
+  if (!aligned16(out->ptr) || (out->ld * 4) % 16 != 0) return CF_ERR_MISALIGNED;
+  const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols, batch = d->batch;
+  if (W1->rows != K || W2->rows != N1 || out->rows != M || out->cols != N2) return CF_ERR_INVALID_ARG;
+  if (d->strideA < 0 || d->strideW1 < 0 || d->strideW2 < 0 || d->strideOut < 0) return CF_ERR_INVALID_ARG;
+  if (batch > 1 && ((d->strideA * 2) % 16 || (d->strideW1 * 2) % 16 || (d->strideW2 * 2) % 16 ||
+                    (d->strideOut * 4) % 16))
+    return CF_ERR_MISALIGNED;
+  if (M == 0 || N2 == 0) return CF_OK;
+
+  // Attention shape: W1 stored transposed (N1 x K), K = N2 = 128.
+  const bool attn_shape = W1->trans == 1 && K == 128 && N2 == 128 && N1 % 128 == 0 && N1 >= 128 && M % 128 == 0;
+  // MLP shape: N2 = 256 C with C <= 4 CTAs per cluster, elementwise F only.
+  const int64_t C = N2 / 256;
+  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && M % 128 == 0 && K % 64 == 0 &&
+                         K >= 64 && N2 % 256 == 0 && C >= 1 && C <= mlp::kMaxC && N1 % (128 * C) == 0 && N1 > 0;
+  if (!attn_shape && !mlp_shape) return CF_ERR_UNSUPPORTED_SHAPE;
+
+  int sms = 0;
+  unsigned* status = nullptr;
+  if ((s = device_query(&sms, &status)) != CF_OK) return s;
+  if (mlp_shape) return launch_mlp(A, W1, W2, d, out, C, sms, status, static_cast<cudaStream_t>(stream));
+  attn::Params p;
+  std::memset(&p, 0, sizeof(p));
+  const uint64_t bs = (uint64_t)(batch > 1 ? batch : 1);
+  {
+    const uint64_t dims[3] = {128, (uint64_t)M, bs};
+    const uint64_t st[2] = {(uint64_t)A->ld * 2, (uint64_t)(batch > 1 ? d->strideA : M * A->ld) * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if ((s = encode_tmap(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)N1, bs};
+    const uint64_t st[2] = {(uint64_t)W1->ld * 2, (uint64_t)(batch > 1 ? d->strideW1 : N1 * W1->ld) * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if ((s = encode_tmap(&p.tmW1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W1->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)N1, bs};
+    const uint64_t st[2] = {(uint64_t)W2->ld * 2, (uint64_t)(batch > 1 ? d->strideW2 : N1 * W2->ld) * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)M, bs};
+    const uint64_t st[2] = {(uint64_t)out->ld * 4, (uint64_t)(batch > 1 ? d->strideOut : M * out->ld) * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    if ((s = encode_tmap(&p.tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out->ptr, dims, st, box)) != CF_OK) return s;
+  }
+  p.batch = (int)bs;
+  p.m_blocks = (int)(M / 128);
+  p.n1_blocks = (int)(N1 / 128);
+  p.items = p.batch * p.m_blocks;
+  p.softmax = d->mid_op == CF_MID_SCALE_SOFTMAX ? 1 : 0;
+  p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
+  p.status = status;
+  p.timeout_cycles = wait_timeout_cycles();
+  if ((s = prepare(0, reinterpret_cast<const void*>(&attn::attn_kernel), attn::kSmemBytes)) != CF_OK) return s;
+  const int grid = p.items < sms ? p.items : sms;
+  attn::attn_kernel<<<grid, attn::kThreads, attn::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+  return CF_OK;
 }

@@ -51,6 +51,15 @@ struct GemmEpiLaunch {
   int cluster;       // CTAs per cluster (X_CLUSTER), else 1
 };
 
+// Host helpers implemented in cf_api.cu and shared by the kernel launchers.
+// Current device's SM count and status-word address; fails unless sm_103.
+cf_status device_query(int* sms, unsigned** status);
+// Tiled tensor map with 128-byte swizzle: `rank` dims (innermost first),
+// rank-1 byte strides, box sizes.
+cf_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* ptr, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
+long long wait_timeout_cycles();
+
 size_t gemm_epi_smem_bytes();
 cudaError_t gemm_epi_prepare(int rowop, int xmode);  // set function attributes
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);

@@ -199,6 +199,33 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Same, but the arrive goes to the barrier at this smem offset in every CTA
+// of the cluster whose bit is set in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
+// same-offset buffer of CTA `rank`, completing `bytes` of transaction count
+// on that CTA's mbarrier at offset `bar`.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_local, uint32_t src_local, uint32_t bytes,
+                                                  uint32_t bar_local, uint32_t rank) {
+  asm volatile(
+      "{\n .reg .b32 rd, rb;\n mapa.shared::cluster.u32 rd, %0, %4;\n mapa.shared::cluster.u32 rb, %3, %4;\n"
+      " cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%1], %2, [rb];\n}\n" ::"r"(
+          dst_local),
+      "r"(src_local), "r"(bytes), "r"(bar_local), "r"(rank)
+      : "memory");
+}
+
+// Barrier among `nthreads` threads (a multiple of 32) on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -1,0 +1,115 @@
+"""GPU parity: fused B2BGEMM (cf_b2bgemm through the C ABI) against the
+float64 oracle, on the attention shape (S = Q K^T, F = scaled softmax or
+scaled ReLU, O = bf16(F(S)) V) and the MLP shape (ReLU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import cf_oracle as O
+from back_gemm_fusion_gb300 import inputs as I
+from tests.parity import assert_rows_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cf():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    import back_gemm_fusion_gb300 as cf
+    return cf
+
+
+def b2b_gate(gpu, ref, absbound, what):
+    """Contract gate plus a per-element bound derived from the single bf16
+    rounding of the intermediate: each element of S' may differ by one bf16
+    ulp (2^-8 relative) between the GPU (fp32 S') and the oracle (fp64 S'),
+    so |dO| <= 2^-7 (|S'| . |W2|) covers it with a factor-2 margin (the
+    online-softmax form rounds exp(s - m) before dividing by l)."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
+    err = np.abs(gpu - ref)
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    assert np.all(err <= 1e-2 * np.maximum(1.0, rms)), f"{what}: contract gate, max err {err.max():.3g}"
+    bound = 2.0 ** -7 * absbound + 1e-5 * rms + 1e-7
+    worst = (err / bound).max()
+    assert worst <= 1.0, f"{what}: bf16-derived bound exceeded ({worst:.3g} x)"
+
+
+def _abs_bound(q, k, v, op, scale):
+    """|S'| . |W2| with S' = F(scale q k^T) unrounded (float64)."""
+    S = q @ k.T
+    return np.abs(O.mid_op(S, op, scale)) @ np.abs(v)
+
+
+def _attention_case(batch, L, op, seed, growth=None):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((batch, L, 128))
+    k = rng.standard_normal((batch, L, 128))
+    if growth is not None:  # make later key blocks dominate: forces online rescaling
+        k = k * (1.0 + growth * (np.arange(L) // 128))[None, :, None]
+    v = rng.standard_normal((batch, L, 128))
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    return t(q), t(k), t(v)
+
+
+def _run_attention(cf, Q, K, V, op, scale):
+    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("batch,L", [(1, 128), (2, 256), (3, 384), (2, 1024)])
+def test_attention_small(cf, batch, L, op):
+    Q, K, V = _attention_case(batch, L, op, seed=L + batch)
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, op, scale)
+    q, k, v = (I.to_f64(t) for t in (Q, K, V))
+    for b in range(batch):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} b={b} L={L}")
+
+
+@pytest.mark.parametrize("growth", [2.0, 6.0])
+def test_attention_softmax_rescales(cf, growth):
+    # Logits grow block by block, so the running max increases by more than
+    # 2^8 in exp2 units several times: exercises the O rescale path.
+    Q, K, V = _attention_case(2, 1024, "scale_softmax", seed=11, growth=growth)
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, "scale_softmax", scale)
+    q, k, v = (I.to_f64(t) for t in (Q, K, V))
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], "scale_softmax", scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], "scale_softmax", scale), f"rescale b={b}")
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+def test_attention_full_size_sampled(cf, op):
+    case = I.attention_b2b(op=op)
+    got = _run_attention(cf, case.A, case.W1, case.W2, op, case.scale)
+    rng = np.random.default_rng(1)
+    heads = rng.choice(case.batch, size=8, replace=False)
+    for h in heads:
+        rows = sample_rows(case.M, 32, seed=int(h))
+        q = I.to_f64(case.A[h])
+        k = I.to_f64(case.W1[h])
+        v = I.to_f64(case.W2[h])
+        ref = O.b2bgemm(q[rows], k.T, v, op, case.scale)
+        b2b_gate(got[h][rows], ref, _abs_bound(q[rows], k, v, op, case.scale), f"attention {op} head {h}")
+
+
+def test_attention_zero_keys_column_mean(cf):
+    # Q K^T == 0 -> P = 1/L exactly -> O = column mean of V (closed form).
+    L = 2048
+    Q, _, V = _attention_case(1, L, "scale_softmax", seed=3)
+    K = torch.zeros_like(Q)
+    got = _run_attention(cf, Q, K, V, "scale_softmax", 1 / math.sqrt(128))
+    mean = I.to_f64(V)[0].mean(axis=0)
+    np.testing.assert_allclose(got[0], np.broadcast_to(mean, (L, 128)), rtol=0, atol=2e-6)
