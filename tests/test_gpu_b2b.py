@@ -113,3 +113,47 @@ def test_attention_zero_keys_column_mean(cf):
     got = _run_attention(cf, Q, K, V, "scale_softmax", 1 / math.sqrt(128))
     mean = I.to_f64(V)[0].mean(axis=0)
     np.testing.assert_allclose(got[0], np.broadcast_to(mean, (L, 128)), rtol=0, atol=2e-6)
+
+
+# ------------------------------------------------------------------ MLP shape
+def _mlp_case(M, K, N1, N2, seed):
+    rng = np.random.default_rng(seed)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    X = t(rng.standard_normal((M, K)))
+    W1 = t(rng.standard_normal((K, N1)) / math.sqrt(K))
+    W2 = t(rng.standard_normal((N1, N2)) / math.sqrt(N1))
+    return X, W1, W2
+
+
+@pytest.mark.parametrize("w1_trans", [False, True])
+@pytest.mark.parametrize("op,scale", [("relu", 1.0), ("scale_relu", 0.75)])
+@pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 128, 256), (256, 128, 512, 256), (384, 192, 1024, 512),
+                                       (256, 256, 1024, 1024), (128, 64, 512, 1024)])
+def test_mlp_small(cf, M, K, N1, N2, op, scale, w1_trans):
+    X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M + K + N1 + N2)
+    W1d = W1.t().contiguous().cuda() if w1_trans else W1.cuda()
+    out = cf.cf_b2bgemm(X.cuda(), W1d, W2.cuda(), op, scale, w1_trans=w1_trans)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, op, scale)
+    bound = np.abs(O.mid_op(x @ w1, op, scale)) @ np.abs(w2)
+    b2b_gate(out.cpu().numpy(), ref, bound, f"mlp {op} {M}x{K}x{N1}x{N2} trans={w1_trans}")
+
+
+def test_mlp_full_size_sampled(cf):
+    case = I.mlp_b2b()
+    out = cf.cf_b2bgemm(case.A[0].cuda(), case.W1[0].cuda(), case.W2[0].cuda(), "relu")
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    rows = sample_rows(case.M)
+    x, w1, w2 = I.to_f64(case.A[0])[rows], I.to_f64(case.W1[0]), I.to_f64(case.W2[0])
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
+    b2b_gate(out.cpu().numpy()[rows], ref, bound, "mlp 16384x1024x4096x1024")
+
+
+def test_b2b_rejects_unsupported(cf):
+    X, W1, W2 = _mlp_case(128, 64, 384, 1024, seed=1)  # N1 not a multiple of 128 * 4
+    with pytest.raises(cf.CFError):
+        cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu")
