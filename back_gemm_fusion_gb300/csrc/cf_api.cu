@@ -29,6 +29,7 @@ struct DeviceInfo {
   unsigned* status = nullptr;
   bool prepared[4][3] = {};
   int max_clusters[4][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
+  int max_pairs[4][3] = {};                        // resident 2-CTA clusters per (rowop, xmode)
   int blocks_per_sm[4][3] = {};                    // 0 = unknown
 };
 
@@ -293,10 +294,13 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
     return s;
   p.b_mn_major = B->trans == 0 ? 1 : 0;
+  // Pair mode (2-CTA clusters along M sharing B) needs an even number of strips.
+  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
   if (p.b_mn_major)
     s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
   else
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK, kBN);
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK,
+                  want_pair ? kBN / 2 : kBN);
   if (s != CF_OK) return s;
   if ((s = encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32, 32)) != CF_OK)
     return s;
@@ -336,7 +340,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       int& cached = dev->max_clusters[plan.rowop][tiles_n];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(plan.rowop, (int)tiles_n, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(plan.rowop, X_CLUSTER, (int)tiles_n, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -360,7 +364,27 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       L.grid = (int)(nclusters * tiles_n);
     }
   }
-  if (xmode != X_CLUSTER) {
+  if (xmode != X_CLUSTER && want_pair) {
+    int maxp = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      int& cached = dev->max_pairs[plan.rowop][xmode];
+      if (cached == 0) {
+        int q = 0;
+        if (gemm_epi_max_clusters(plan.rowop, xmode, 2, &q) != cudaSuccess) {
+          cudaGetLastError();
+          q = 0;
+        }
+        cached = q > 0 ? q : -1;
+      }
+      maxp = cached > 0 ? cached : 0;
+    }
+    if (maxp <= 0) return CF_ERR_CUDA;  // the B box was encoded for pair mode
+    p.pair = 1;
+    p.pair_items = (int)(strips / 2 * tiles_n);
+    L.grid = 2 * (p.pair_items < maxp ? p.pair_items : maxp);
+    L.cluster = 2;
+  } else if (xmode != X_CLUSTER) {
     int per_sm = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);

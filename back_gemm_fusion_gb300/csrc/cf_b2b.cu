@@ -48,37 +48,34 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Write 32 fp32 values of row `r` (columns c0..c0+31 of a 128-column K-major
-// bf16 tile) into a 128-byte-swizzled smem tile made of two 64-column
-// regions of 16 KB each.
-__device__ __forceinline__ void store_row_bf16_sw128(uint8_t* tile, int r, int c0, const float (&v)[32]) {
-  const int region = c0 >> 6;
-  uint8_t* base = tile + region * 16384 + r * 128;
+// Pack 32 fp32 values into 16 bf16x2 words (round to nearest even, one
+// packed conversion per pair).
+__device__ __forceinline__ void pack_bf16(const float (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int chunk = ((c0 & 63) >> 3) + q;  // 16-byte chunk (8 bf16) within the 128-byte row
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
-      w[e] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(base + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int e = 0; e < 16; ++e) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+    w[e] = *reinterpret_cast<uint32_t*>(&h);
   }
 }
 
-// Round 32 values to bf16 and back (the values the second GEMM consumes).
-__device__ __forceinline__ void round_bf16(float (&v)[32]) {
+// Sum of the 32 bf16 values held in 16 packed words (exact widening).
+__device__ __forceinline__ float sum_packed_bf16(const uint32_t (&w)[16]) {
+  float s = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+  for (int e = 0; e < 16; ++e) s += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
+  return s;
 }
 
-// Stage a 32 x 32 fp32 block held one row per lane into swizzled smem.
-__device__ __forceinline__ void stage_out_block(uint8_t* buf, int lane, const float (&v)[32]) {
+// Write 32 packed bf16 values of row `r` (columns c0..c0+31 of a 128-column
+// K-major tile) into a 128-byte-swizzled smem tile of two 64-column regions.
+__device__ __forceinline__ void store_row_packed_sw128(uint8_t* tile, int r, int c0, const uint32_t (&w)[16]) {
+  uint8_t* base = tile + (c0 >> 6) * 16384 + r * 128;
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) * 16)) =
-        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = ((c0 & 63) >> 3) + q;
+    *reinterpret_cast<uint4*>(base + ((chunk ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
 }
 
 // ======================================================================
@@ -88,24 +85,27 @@ namespace attn {
 
 constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
-constexpr int kRing = 3;                    // W1/W2 tiles in flight
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kRing = 4;                    // W1/W2 tiles in flight
+constexpr int kFWarps = 8;                  // two warpgroups: columns 0..63 and 64..127 of every row
+constexpr int kThreads = 64 + 32 * kFWarps;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kTileBytes;
 constexpr int kOffP = kOffRing + kRing * kTileBytes;
-constexpr int kOffOut = kOffP + 2 * kTileBytes;
-constexpr int kOffBars = kOffOut + kEpiWarps * 4096;
-// q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2], pv_done[2], o_full, o_empty, drain
-constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 5, BAR_SF = 8, BAR_PF = 10, BAR_PV = 12, BAR_OF = 14,
-              BAR_OE = 15, BAR_DRAIN = 16, kNumBars = 17;
+constexpr int kOffX = kOffP + kTileBytes;   // float [3][2 halves][128]: block max (2 parities), row sum
+constexpr int kOffBars = kOffX + 3 * 2 * 128 * 4;
+// q_full, q_empty, ring_full[4], ring_empty[4], s_full[2], p_full, pv_done, o_full, o_empty, drain,
+// max exchange [2 parities][4 quarters], sum exchange [4 quarters]
+constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 6, BAR_SF = 10, BAR_PF = 12, BAR_PV = 13, BAR_OF = 14,
+              BAR_OE = 15, BAR_DRAIN = 16, BAR_XM = 17, BAR_XL = 25, kNumBars = 29;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
 constexpr float kRescaleLog2 = 8.0f;
 
 struct Params {
-  CUtensorMap tmA, tmW1, tmW2, tmO;  // 3-D: {128 cols, rows, batch}
+  CUtensorMap tmA, tmW1, tmW2;  // 3-D: {128 cols, rows, batch}
+  float* out;
+  long long ldo, stride_out;
   int batch, m_blocks, n1_blocks, items;
   int softmax;       // 1: scaled softmax, 0: ReLU (optionally scaled)
   float scale;       // multiplies S before F
@@ -131,14 +131,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(bar(BAR_RF + i), 1);
       mbar_init(bar(BAR_RE + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_SF + i), 1);
-      mbar_init(bar(BAR_PF + i), kEpiWarps);
-      mbar_init(bar(BAR_PV + i), 1);
-    }
+    mbar_init(bar(BAR_SF + 0), 1);
+    mbar_init(bar(BAR_SF + 1), 1);
+    mbar_init(bar(BAR_PF), kFWarps);
+    mbar_init(bar(BAR_PV), 1);
     mbar_init(bar(BAR_OF), 1);
-    mbar_init(bar(BAR_OE), kEpiWarps);
+    mbar_init(bar(BAR_OE), kFWarps);
     mbar_init(bar(BAR_DRAIN), 1);
+    for (int i = 0; i < 12; ++i) mbar_init(bar(BAR_XM + i), 2);  // one arrival per half
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -146,7 +146,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmW1);
     tma_prefetch_desc(&p.tmW2);
-    tma_prefetch_desc(&p.tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -192,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0);   // W1 tile is K-major (rows = N1)
       const uint32_t id_o = idesc_bf16_f32(128, 128, 1);   // W2 tile is MN-major (rows = K of GEMM2)
       uint32_t rs = 0, rph = 0;
-      uint32_t g = 0;  // global chunk counter (S/P buffer = g & 1)
+      uint32_t g = 0;  // global chunk counter (S buffer = g & 1)
       int it = 0;
       bool ok = true;
       auto issue_s = [&](uint32_t gg) -> bool {
@@ -218,19 +217,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         ok = issue_s(g0) && (nb < 2 || issue_s(g0 + 1));
         if (ok && nb <= 2) mma_commit(bar(BAR_QE));
         for (int j = 0; ok && j < nb; ++j, ++g) {
-          if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PF), g & 1, wc)) { ok = false; break; }
           if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
           if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
-          const uint32_t pt = sbase + kOffP + (g & 1) * kTileBytes;
+          const uint32_t pt = sbase + kOffP;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             mma_bf16(tmem_base + 256, smem_desc_sw128(pt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                      smem_desc_sw128(wt + kk * 2048, 16384, 1024), id_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_RE + rs));
-          mma_commit(bar(BAR_PV + (g & 1)));
+          mma_commit(bar(BAR_PV));
           if (++rs == kRing) { rs = 0; rph ^= 1; }
           if (j + 2 < nb) {
             ok = issue_s(g + 2);
@@ -245,12 +244,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
   } else {
     // -------------------------------------- F (softmax / ReLU) and epilogue
+    // Two warpgroups: half h owns columns 64h..64h+63 of every S' row; the
+    // warps of both halves that share a TMEM lane quarter exchange their
+    // half-row max (and, at the end, half-row sums) through shared memory,
+    // synchronised by per-quarter mbarriers (bounded waits).
+    const int half = (warp - 2) >> 2;
     const int q = warp & 3;
     const int row = 32 * q + lane;
+    const int c0 = 64 * half;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    uint8_t* out_buf = smem + kOffOut + (warp - 2) * 4096;
-    const uint32_t out_addr = sbase + kOffOut + (warp - 2) * 4096;
+    float* xch = reinterpret_cast<float*>(smem + kOffX);  // [slot][half][row]
+    // Publish `v` for this row, then read the other half's value (bounded).
+    auto exchange = [&](float v, int slot, int barid, uint32_t parity, float& other) -> bool {
+      float* xb = xch + slot * 256;
+      xb[half * 128 + row] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(barid));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(barid), parity, wc))) return false;
+      other = xb[(half ^ 1) * 128 + row];
+      return true;
+    };
     const float sl2 = p.scale * kLog2e;
+    uint8_t* ptile = smem + kOffP;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
@@ -261,98 +276,94 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const uint32_t sb = g & 1, u = g >> 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_addr = tmem_base + lane_off + sb * 128;
+        const uint32_t s_addr = tmem_base + lane_off + sb * 128 + c0;
+        float va[32], vb[32];
+        tmem_ld32(s_addr, va);
+        tmem_ld32(s_addr + 32, vb);
+        tmem_wait_ld();
+        bool pv_waited = false;
         if (p.softmax) {
-          // Block max (log2 units), then a lazy rescale of O and l.
-          float bmax = -INFINITY;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            tmem_ld32(s_addr + c * 32, v);
-            tmem_wait_ld();
+          float hm = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) bmax = fmaxf(bmax, v[e]);
-          }
-          bmax *= sl2;
+          for (int e = 0; e < 32; ++e) hm = fmaxf(hm, fmaxf(va[e], vb[e]));
+          float hm_other;
+          if (!exchange(hm, g & 1, BAR_XM + (g & 1) * 4 + q, (g >> 1) & 1, hm_other)) { ok = false; break; }
+          const float bmax = fmaxf(hm, hm_other) * sl2;
+          // Lazy rescale: only when the block max exceeds the max in use by
+          // more than 2^8 (in exp2 units) does O (and l) move to a new max.
           const bool need = bmax > m_used + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? bmax : m_used;
             const float f = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - m_new);
             if (j > 0) {
               // O must hold every earlier S' . W2 product before it is rescaled.
-              const uint32_t pg = g - 1;
-              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + (pg & 1)), (pg >> 1) & 1, wc))) {
-                ok = false;
-                break;
-              }
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV), (g & 1) ^ 1, wc))) { ok = false; break; }
+              pv_waited = true;
               tc_fence_after();
 #pragma unroll 1
-              for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
+              for (int c = 0; c < 2; ++c) {
+                float o[32];
+                tmem_ld32(tmem_base + lane_off + 256 + c0 + c * 32, o);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] *= f;
-                tmem_st32(tmem_base + lane_off + 256 + c * 32, v);
+                for (int e = 0; e < 32; ++e) o[e] *= f;
+                tmem_st32(tmem_base + lane_off + 256 + c0 + c * 32, o);
               }
               tmem_wait_st();
             }
             l *= f;
             m_used = m_new;
           }
-        }
-        // The S' buffer must no longer be read by the S'.W2 product two chunks back.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
-        uint8_t* ptile = smem + kOffP + sb * kTileBytes;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(s_addr + c * 32, v);
-          tmem_wait_ld();
-          if (p.softmax) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = ex2_approx(fmaf(v[e], sl2, -m_used));
-            round_bf16(v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) l += v[e];
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = fmaxf(v[e] * p.scale, 0.0f);
+          for (int e = 0; e < 32; ++e) {
+            va[e] = ex2_approx(fmaf(va[e], sl2, -m_used));
+            vb[e] = ex2_approx(fmaf(vb[e], sl2, -m_used));
           }
-          store_row_bf16_sw128(ptile, row, c * 32, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            va[e] = fmaxf(va[e] * p.scale, 0.0f);
+            vb[e] = fmaxf(vb[e] * p.scale, 0.0f);
+          }
         }
+        uint32_t wa[16], wb[16];
+        pack_bf16(va, wa);
+        pack_bf16(vb, wb);
+        if (p.softmax) l += sum_packed_bf16(wa) + sum_packed_bf16(wb);  // exactly what GEMM2 consumes
+        // S' is single-buffered: the previous chunk's S' . W2 must have read it.
+        if (!pv_waited && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV), (g & 1) ^ 1, wc))) { ok = false; break; }
+        store_row_packed_sw128(ptile, row, c0, wa);
+        store_row_packed_sw128(ptile, row, c0 + 32, wb);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_PF + sb));
+        if (lane == 0) mbar_arrive(bar(BAR_PF));
       }
       if (!ok) break;
-      // Epilogue: O / l (softmax) -> fp32 output through swizzled smem + TMA.
+      // Epilogue: O / l (softmax) -> fp32 output rows.
+      float inv = 1.0f;
+      if (p.softmax) {
+        float l_other;
+        if (!exchange(l, 2, BAR_XL + q, it & 1, l_other)) break;
+        inv = 1.0f / (l + l_other);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), it & 1, wc))) break;
       tc_fence_after();
-      const float inv = p.softmax ? 1.0f / l : 1.0f;
+      float* orow = p.out + (long long)b * p.stride_out + (long long)(mb * kTile + row) * p.ldo + c0;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
+        tmem_ld32(tmem_base + lane_off + 256 + c0 + c * 32, v);
         tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] *= inv;
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-        stage_out_block(out_buf, lane, v);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&p.tmO, out_addr, c * 32, mb * kTile + 32 * q, b);
-          bulk_commit();
-        }
+        for (int e = 0; e < 8; ++e)
+          dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_OE));
     }
-    if (lane == 0) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -379,9 +390,10 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kOffRing = 0;
 constexpr int kOffSlots = kRing * kStageBytes;
 constexpr int kOffBars = kOffSlots + kMaxC * kSlotBytes;
-// ring_full[3], ring_empty[3], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain
+// ring_full[3], ring_empty[3], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain,
+// slot_written (the F warps finished writing this CTA's S' chunk)
 constexpr int BAR_RF = 0, BAR_RE = 3, BAR_SF = 6, BAR_SFREE = 8, BAR_SLF = 10, BAR_SLE = 11, BAR_OF = 12,
-              BAR_OE = 13, BAR_DRAIN = 14, kNumBars = 15;
+              BAR_OE = 13, BAR_DRAIN = 14, BAR_SLW = 15, kNumBars = 16;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,512)
@@ -430,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     mbar_init(bar(BAR_OF), 1);
     mbar_init(bar(BAR_OE), kEpiWarps);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_SLW), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -592,18 +605,26 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = fmaxf(v[e] * p.scale, 0.0f);
-          store_row_bf16_sw128(my_slot, row, c * 32, v);
+          uint32_t w[16];
+          pack_bf16(v, w);
+          store_row_packed_sw128(my_slot, row, c * 32, w);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
-        named_barrier_sync(1, 32 * kEpiWarps);
-        if (warp == 2 && lane == 0) {
-          mbar_arrive_expect_tx(bar(BAR_SLF), (uint32_t)(C - 1) * kSlotBytes);
-          for (int pr = 1; pr < C; ++pr) {
-            const uint32_t peer = (rank + pr) % C;
-            bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF), peer);
+        if (lane == 0) {
+          mbar_arrive(bar(BAR_SFREE + sb));
+          mbar_arrive(bar(BAR_SLW));
+        }
+        if (warp == 2) {
+          // The whole chunk is in this CTA's slot: publish it to the peers.
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLW), g & 1, wc))) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(BAR_SLF), (uint32_t)(C - 1) * kSlotBytes);
+            for (int pr = 1; pr < C; ++pr) {
+              const uint32_t peer = (rank + pr) % C;
+              bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF), peer);
+            }
           }
         }
       }
@@ -795,12 +816,9 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
     const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
   }
-  {
-    const uint64_t dims[3] = {128, (uint64_t)M, bs};
-    const uint64_t st[2] = {(uint64_t)out->ld * 4, (uint64_t)(batch > 1 ? d->strideOut : M * out->ld) * 4};
-    const uint32_t box[3] = {32, 32, 1};
-    if ((s = encode_tmap(&p.tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out->ptr, dims, st, box)) != CF_OK) return s;
-  }
+  p.out = static_cast<float*>(out->ptr);
+  p.ldo = out->ld;
+  p.stride_out = batch > 1 ? d->strideOut : 0;
   p.batch = (int)bs;
   p.m_blocks = (int)(M / 128);
   p.n1_blocks = (int)(N1 / 128);

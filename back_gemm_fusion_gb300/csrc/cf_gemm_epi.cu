@@ -143,6 +143,12 @@ __device__ __forceinline__ Work make_work(const GemmEpiParams& p) {
     w.step = (int)num_clusters_x();
     w.end = p.strips;
     w.rank = (int)cluster_ctarank();
+  } else if (p.pair) {
+    // A pair of CTAs takes strips (2 sp, 2 sp + 1) of the same N tile.
+    w.i = (int)cluster_id_x();
+    w.step = (int)num_clusters_x();
+    w.end = p.pair_items;
+    w.rank = (int)cluster_ctarank();
   } else {
     w.i = blockIdx.x;
     w.step = gridDim.x;
@@ -153,10 +159,14 @@ __device__ __forceinline__ Work make_work(const GemmEpiParams& p) {
 }
 
 template <int XMODE>
-__device__ __forceinline__ void item_coords(const Work& w, int& strip, int& tile) {
+__device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& w, int& strip, int& tile) {
   if (XMODE == X_CLUSTER) {
     strip = w.i;
     tile = w.rank;
+  } else if (p.pair) {
+    const int sp = w.i / w.tiles_n;
+    tile = w.i - sp * w.tiles_n;
+    strip = 2 * sp + w.rank;
   } else {
     strip = w.i / w.tiles_n;
     tile = w.i - strip * w.tiles_n;
@@ -184,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), p.pair ? 2 : 1);  // pair: both CTAs' MMAs must release it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(BAR_TFULL + a), 1);
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
-  if (XMODE == X_CLUSTER) cluster_sync_all();
+  if (XMODE == X_CLUSTER || p.pair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = p.K / kBK;
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       bool ok = true;
       for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next()) {
         int strip, tile;
-        item_coords<XMODE>(w, strip, tile);
+        item_coords<XMODE>(p, w, strip, tile);
         const int m0 = strip * kBM, n0 = tile * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1, wc)) { ok = false; break; }
@@ -230,12 +240,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           const uint32_t fb = bar(BAR_FULL + stage);
           mbar_arrive_expect_tx(fb, kStageBytes);
           tma_load_2d(sa, &p.tmA, fb, kb * kBK, m0);
-          if (p.b_mn_major) {
+          if (p.pair) {
+            // This CTA fetches half of the B tile for both CTAs of the pair.
+            const uint32_t r = (uint32_t)w.rank;
+            if (p.b_mn_major) {
+              for (int i = 2 * r; i < 2 * (int)r + 2; ++i)
+                tma_load_2d_multicast(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK, 0x3);
+            } else {
+              tma_load_2d_multicast(sb + r * (128 * kBK * 2), &p.tmB, fb, kb * kBK, n0 + 128 * r, 0x3);
+            }
+          } else if (p.b_mn_major) {
 #pragma unroll
             for (int i = 0; i < kBN / 64; ++i) tma_load_2d(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK);
           } else {
             tma_load_2d(sb, &p.tmB, fb, kb * kBK, n0);
           }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (p.pair) {
+        // The peer's MMA releases reach this CTA's barriers asynchronously:
+        // wait until every stage's last release has landed before exiting.
+        for (int s2 = 0; s2 < kStages; ++s2) {
+          mbar_wait<false, false>(bar(BAR_EMPTY + stage), phase ^ 1, wc);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -264,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
                                              : smem_desc_sw128(sb + kk * 32, 16, 1024);
             mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(bar(BAR_EMPTY + stage));
+          if (p.pair) mma_commit_multicast(bar(BAR_EMPTY + stage), 0x3);  // frees the stage in both CTAs
+          else mma_commit(bar(BAR_EMPTY + stage));
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -284,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     int t = 0;
     for (Work w = make_work<XMODE>(p); w.valid(); w.next(), ++t) {
       int strip, tile;
-      item_coords<XMODE>(w, strip, tile);
+      item_coords<XMODE>(p, w, strip, tile);
       const int m0 = strip * kBM, n0 = tile * kBN;
       const int acc = t & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_TFULL + acc), (t >> 1) & 1, wc))) break;
@@ -459,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  if (XMODE == X_CLUSTER) cluster_sync_all();
+  if (XMODE == X_CLUSTER || p.pair) cluster_sync_all();
 }
 
 template <int R, int X>
@@ -493,12 +521,12 @@ cudaError_t gemm_epi_prepare(int rowop, int xmode) {
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (xmode == X_CLUSTER) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
-cudaError_t gemm_epi_max_clusters(int rowop, int cluster, int* out) {
-  const void* k = select_kernel(rowop, X_CLUSTER);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, int cluster, int* out) {
+  const void* k = select_kernel(rowop, xmode);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -526,7 +554,7 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   int na = 0;
-  if (L.xmode == X_CLUSTER) {
+  if (L.cluster > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = L.cluster;
     attr[na].val.clusterDim.y = 1;
@@ -535,6 +563,8 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   }
   if (L.xmode == X_GLOBAL) {
     // All CTAs must be co-resident: tiles of a strip wait for one another.
+    // The grid never exceeds the resident capacity; the cooperative
+    // attribute additionally asks the driver to guarantee it.
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;
     ++na;
@@ -546,7 +576,15 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = na;
   void* args[] = {const_cast<GemmEpiParams*>(&L.p)};
-  return cudaLaunchKernelExC(&cfg, k, args);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
+  if (e != cudaSuccess && L.xmode == X_GLOBAL && L.cluster > 1) {
+    // Cooperative launches of clustered grids may be unsupported: launch
+    // without the attribute (the grid still fits the resident capacity).
+    cudaGetLastError();
+    cfg.numAttrs = na - 1;
+    e = cudaLaunchKernelExC(&cfg, k, args);
+  }
+  return e;
 }
 
 }  // namespace cf

@@ -30,6 +30,8 @@ struct GemmEpiParams {
   int strips;         // M / kBM
   int num_items;      // strips * tiles_n
   int b_mn_major;     // 1: B stored K x N (N contiguous)
+  int pair;           // 1: 2-CTA clusters along M share (multicast) each B tile
+  int pair_items;     // (strips / 2) * tiles_n when pair == 1
   int n_ops;          // elementwise ops (row op excluded)
   int op_kind[CF_EPI_MAX_OPS];
   float op_scalar[CF_EPI_MAX_OPS];
@@ -48,7 +50,7 @@ struct GemmEpiLaunch {
   int rowop;
   int xmode;
   int grid;          // CTAs
-  int cluster;       // CTAs per cluster (X_CLUSTER), else 1
+  int cluster;       // CTAs per cluster (X_CLUSTER: tiles_n; pair mode: 2), else 1
 };
 
 // Host helpers implemented in cf_api.cu and shared by the kernel launchers.
@@ -63,7 +65,7 @@ long long wait_timeout_cycles();
 size_t gemm_epi_smem_bytes();
 cudaError_t gemm_epi_prepare(int rowop, int xmode);  // set function attributes
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);
-cudaError_t gemm_epi_max_clusters(int rowop, int cluster, int* out);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, int cluster, int* out);
 cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out);
 
 }  // namespace cf

@@ -348,6 +348,37 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     tflops = wl.flops / (ms_step * 1e-3) / 1e12
     value = tflops * world
 
+    # Other row-statistics exchanges of the same fused kernel, same run.
+    variants = {}
+    if not wl.is_b2b and any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in wl.case.ops):
+        for xch in ("cluster", "global"):
+            if xch == args.exchange:
+                continue
+            try:
+                wv = Workload.__new__(Workload)
+                wv.__dict__.update(wl.__dict__)
+                wv.exchange = xch
+                ws = workspace
+                if ws is None:
+                    need = cf.cf_workspace_size(dev["A"], dev["B"], wl.case.ops, exchange=xch)
+                    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+                for _ in range(2):
+                    wv.fused_step(cf, dev, stream, ws)
+                torch.cuda.synchronize()
+                vm = []
+                for k in range(max(3, args.steps)):
+                    flush.fill_(float(k))
+                    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s0.record(stream)
+                    wv.fused_step(cf, dev, stream, ws)
+                    e0.record(stream)
+                    torch.cuda.synchronize()
+                    vm.append(s0.elapsed_time(e0))
+                v = statistics.mean(vm)
+                variants[xch] = {"ms_per_step": v, "tflops": wl.flops / (v * 1e-3) / 1e12}
+            except Exception as exc:
+                variants[xch] = {"error": str(exc)[:200]}
+
     # Unfused comparison (cuBLASLt GEMM + separate epilogue kernel), same run.
     unfused = None
     try:
@@ -423,6 +454,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step},
         "unfused": unfused,
+        "exchange_variants": variants or None,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
