@@ -294,8 +294,12 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
     return s;
   p.b_mn_major = B->trans == 0 ? 1 : 0;
-  // Pair mode (2-CTA clusters along M sharing B) needs an even number of strips.
-  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
+  // Pair mode: 2-CTA clusters along M share (multicast) each B tile, which
+  // halves B's L2 -> SM traffic but couples the two CTAs' main loops.
+  // Measured on GB300: +6% for 64-tile rows (softmax 4096x16384x4096),
+  // -3..5% for 16-tile rows, so it is used for wide rows (>= 32 tiles) only;
+  // it needs an even number of strips.
+  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0 && tiles_n >= 32;
   if (p.b_mn_major)
     s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
   else

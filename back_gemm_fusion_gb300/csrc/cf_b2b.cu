@@ -85,21 +85,21 @@ namespace attn {
 
 constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
-constexpr int kRing = 4;                    // W1/W2 tiles in flight
+constexpr int kRing = 5;                    // W1/W2 tiles in flight
 constexpr int kFWarps = 8;                  // two warpgroups: columns 0..63 and 64..127 of every row
 constexpr int kThreads = 64 + 32 * kFWarps;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kTileBytes;
-constexpr int kOffP = kOffRing + kRing * kTileBytes;
-constexpr int kOffX = kOffP + kTileBytes;   // float [3][2 halves][128]: block max (2 parities), row sum
+constexpr int kOffX = kOffRing + kRing * kTileBytes;  // float [3][2 halves][128]: block max (2 parities), row sum
 constexpr int kOffBars = kOffX + 3 * 2 * 128 * 4;
-// q_full, q_empty, ring_full[4], ring_empty[4], s_full[2], p_full, pv_done, o_full, o_empty, drain,
+// q_full, q_empty, ring_full[5], ring_empty[5], s_full[2], p_full, pv_done, o_full, o_empty, drain,
 // max exchange [2 parities][4 quarters], sum exchange [4 quarters]
-constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 6, BAR_SF = 10, BAR_PF = 12, BAR_PV = 13, BAR_OF = 14,
-              BAR_OE = 15, BAR_DRAIN = 16, BAR_XM = 17, BAR_XL = 25, kNumBars = 29;
+constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 7, BAR_SF = 12, BAR_PF = 14, BAR_PV = 15, BAR_OF = 16,
+              BAR_OE = 17, BAR_DRAIN = 18, BAR_XM = 19, BAR_XL = 27, kNumBars = 31;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S' (bf16 pairs) [384,448)
+constexpr int kTmemP = 384;
 constexpr float kRescaleLog2 = 8.0f;
 
 struct Params {
@@ -222,11 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
-          const uint32_t pt = sbase + kOffP;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            mma_bf16(tmem_base + 256, smem_desc_sw128(pt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                     smem_desc_sw128(wt + kk * 2048, 16384, 1024), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+            // A = S' from TMEM (16 K elements = 8 packed columns per step).
+            mma_bf16_ts(tmem_base + 256, tmem_base + kTmemP + 8 * kk, smem_desc_sw128(wt + kk * 2048, 16384, 1024),
+                        id_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_RE + rs));
           mma_commit(bar(BAR_PV));
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       return true;
     };
     const float sl2 = p.scale * kLog2e;
-    uint8_t* ptile = smem + kOffP;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
@@ -332,9 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (p.softmax) l += sum_packed_bf16(wa) + sum_packed_bf16(wb);  // exactly what GEMM2 consumes
         // S' is single-buffered: the previous chunk's S' . W2 must have read it.
         if (!pv_waited && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV), (g & 1) ^ 1, wc))) { ok = false; break; }
-        store_row_packed_sw128(ptile, row, c0, wa);
-        store_row_packed_sw128(ptile, row, c0 + 32, wb);
-        fence_proxy_async_smem();
+        tc_fence_after();
+        {
+          float packed[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            packed[e] = __uint_as_float(wa[e]);
+            packed[16 + e] = __uint_as_float(wb[e]);
+          }
+          tmem_st32(tmem_base + lane_off + kTmemP + 32 * half, packed);
+          tmem_wait_st();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PF));

@@ -60,6 +60,14 @@ def test_layernorm_256(cf, b_trans):
     assert_rows_close(_run(cf, case, b_trans), _oracle(case), what="gemm+bias+layernorm 256^3")
 
 
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_layernorm_pairs_wide(cf, b_trans):
+    # 32 tiles per row with an even number of strips: 2-CTA pairs multicast B.
+    case = I.gemm_epilogue_case("ln_wide", 256, 8192, 128, [("bias",), ("layernorm", 1e-5)], seed=9,
+                                need_bias=True, need_gamma=True, need_beta=True)
+    assert_rows_close(_run(cf, case, b_trans), _oracle(case), what="layernorm 32 tiles, pairs")
+
+
 @pytest.mark.parametrize("ops", [[("bias",)], [("bias",), ("relu",)], [("scale", 0.5), ("gelu_tanh",)],
                                  [("bias",), ("gelu_tanh",), ("scale", -2.0)]])
 def test_elementwise_programs(cf, ops):
@@ -79,9 +87,10 @@ def test_row_ops_multi_tile(cf, rowop, exchange, N):
     assert_rows_close(_run(cf, case, exchange=exchange), _oracle(case), what=f"{rowop} N={N} {exchange}")
 
 
-@pytest.mark.parametrize("N", [4096, 4352])
+@pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
-    # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path.
+    # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;
+    # 32 tiles: workspace path with 2-CTA pairs sharing B.
     case = I.gemm_epilogue_case("sm", 256, N, 128, [("scale", 0.25), ("softmax",)], seed=5)
     assert_rows_close(_run(cf, case), _oracle(case), what=f"softmax N={N}")
 
