@@ -27,7 +27,7 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   unsigned* status = nullptr;
-  bool prepared[4][3] = {};
+  bool prepared[4][3][2] = {};
   int max_clusters[4][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
   int max_pairs[4][3] = {};                        // resident 2-CTA clusters per (rowop, xmode)
   int blocks_per_sm[4][3] = {};                    // 0 = unknown
@@ -294,17 +294,16 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
     return s;
   p.b_mn_major = B->trans == 0 ? 1 : 0;
-  // Pair mode: 2-CTA clusters along M share (multicast) each B tile, which
-  // halves B's L2 -> SM traffic but couples the two CTAs' main loops.
-  // Measured on GB300: +6% for 64-tile rows (softmax 4096x16384x4096),
-  // -3..5% for 16-tile rows, so it is used for wide rows (>= 32 tiles) only;
-  // it needs an even number of strips.
-  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0 && tiles_n >= 32;
+  // Pair mode: CTA pairs (2-CTA clusters along M) run 256 x 256 tiles with
+  // cta_group::2 MMAs; each CTA loads its A rows and half of the B tile,
+  // halving per-SM shared-memory traffic per MMA.  Needs an even number of
+  // strips; the cluster (DSMEM) exchange keeps 1-CTA tiles.
+  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
   if (p.b_mn_major)
     s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
   else
     s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK,
-                  want_pair ? kBN / 2 : kBN);
+                  want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
   if (s != CF_OK) return s;
   if ((s = encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32, 32)) != CF_OK)
     return s;
@@ -330,9 +329,12 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     std::lock_guard<std::mutex> lk(g_mu);
     for (int x = X_NONE; x <= X_GLOBAL; ++x) {
       if (plan.rowop == ROW_NONE && x != X_NONE) continue;
-      if (!dev->prepared[plan.rowop][x]) {
-        if (gemm_epi_prepare(plan.rowop, x) != cudaSuccess) return CF_ERR_CUDA;
-        dev->prepared[plan.rowop][x] = true;
+      for (int pr = 0; pr < 2; ++pr) {
+        if (pr == 1 && x == X_CLUSTER) continue;
+        if (!dev->prepared[plan.rowop][x][pr]) {
+          if (gemm_epi_prepare(plan.rowop, x, pr == 1) != cudaSuccess) return CF_ERR_CUDA;
+          dev->prepared[plan.rowop][x][pr] = true;
+        }
       }
     }
   }
@@ -344,7 +346,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       int& cached = dev->max_clusters[plan.rowop][tiles_n];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(plan.rowop, X_CLUSTER, (int)tiles_n, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(plan.rowop, X_CLUSTER, false, (int)tiles_n, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -375,7 +377,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       int& cached = dev->max_pairs[plan.rowop][xmode];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(plan.rowop, xmode, 2, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(plan.rowop, xmode, true, 2, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }

@@ -85,16 +85,16 @@ namespace attn {
 
 constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
-constexpr int kRing = 5;                    // W1/W2 tiles in flight
+constexpr int kRing = 4;                    // W1/W2 tiles in flight
 constexpr int kFWarps = 8;                  // two warpgroups: columns 0..63 and 64..127 of every row
 constexpr int kThreads = 64 + 32 * kFWarps;
-constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kTileBytes;
+constexpr int kOffQ = 0;                    // two A tiles: the next item's is loaded during this one
+constexpr int kOffRing = kOffQ + 2 * kTileBytes;
 constexpr int kOffX = kOffRing + kRing * kTileBytes;  // float [3][2 halves][128]: block max (2 parities), row sum
 constexpr int kOffBars = kOffX + 3 * 2 * 128 * 4;
-// q_full, q_empty, ring_full[5], ring_empty[5], s_full[2], p_full, pv_done, o_full, o_empty, drain,
+// q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], p_full, pv_done, o_full, o_empty, drain,
 // max exchange [2 parities][4 quarters], sum exchange [4 quarters]
-constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF = 2, BAR_RE = 7, BAR_SF = 12, BAR_PF = 14, BAR_PV = 15, BAR_OF = 16,
+constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_PF = 14, BAR_PV = 15, BAR_OF = 16,
               BAR_OE = 17, BAR_DRAIN = 18, BAR_XM = 19, BAR_XL = 27, kNumBars = 31;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -125,8 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int nb = p.n1_blocks;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_QF), 1);
-    mbar_init(bar(BAR_QE), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_QF + i), 1);
+      mbar_init(bar(BAR_QE + i), 1);
+    }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(bar(BAR_RF + i), 1);
       mbar_init(bar(BAR_RE + i), 1);
@@ -173,10 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       };
       for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
         const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
-        if (!mbar_wait(bar(BAR_QE), (it & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bar(BAR_QF), kTileBytes);
-        tma_load_3d(sbase + kOffQ, &p.tmA, bar(BAR_QF), 0, mb * kTile, b);
-        tma_load_3d(sbase + kOffQ + 16384, &p.tmA, bar(BAR_QF), 64, mb * kTile, b);
+        const int qb = it & 1;
+        if (!mbar_wait(bar(BAR_QE + qb), ((it >> 1) & 1) ^ 1, wc)) break;
+        const uint32_t qdst = sbase + kOffQ + qb * kTileBytes;
+        mbar_arrive_expect_tx(bar(BAR_QF + qb), kTileBytes);
+        tma_load_3d(qdst, &p.tmA, bar(BAR_QF + qb), 0, mb * kTile, b);
+        tma_load_3d(qdst + 16384, &p.tmA, bar(BAR_QF + qb), 64, mb * kTile, b);
         // Operand order = MMA consumption order: W1_0, W1_1, then W2_j, W1_{j+2}.
         ok = load_tile(&p.tmW1, 0, b) && (nb < 2 || load_tile(&p.tmW1, kTile, b));
         for (int j = 0; ok && j < nb; ++j) {
@@ -194,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       uint32_t g = 0;  // global chunk counter (S buffer = g & 1)
       int it = 0;
       bool ok = true;
+      uint32_t qaddr = sbase + kOffQ;
       auto issue_s = [&](uint32_t gg) -> bool {
         if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
         tc_fence_after();
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16(d, smem_desc_sw128(sbase + kOffQ + off, 16, 1024), smem_desc_sw128(wt + off, 16, 1024), id_s,
+          mma_bf16(d, smem_desc_sw128(qaddr + off, 16, 1024), smem_desc_sw128(wt + off, 16, 1024), id_s,
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(BAR_RE + rs));
@@ -211,11 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         return true;
       };
       for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
-        if (!mbar_wait(bar(BAR_QF), it & 1, wc)) break;
+        const int qb = it & 1;
+        if (!mbar_wait(bar(BAR_QF + qb), (it >> 1) & 1, wc)) break;
         tc_fence_after();
+        qaddr = sbase + kOffQ + qb * kTileBytes;
         const uint32_t g0 = g;
         ok = issue_s(g0) && (nb < 2 || issue_s(g0 + 1));
-        if (ok && nb <= 2) mma_commit(bar(BAR_QE));
+        if (ok && nb <= 2) mma_commit(bar(BAR_QE + qb));
         for (int j = 0; ok && j < nb; ++j, ++g) {
           if (!mbar_wait(bar(BAR_PF), g & 1, wc)) { ok = false; break; }
           if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           if (++rs == kRing) { rs = 0; rph ^= 1; }
           if (j + 2 < nb) {
             ok = issue_s(g + 2);
-            if (ok && j + 3 == nb) mma_commit(bar(BAR_QE));  // last GEMM1 of this item issued
+            if (ok && j + 3 == nb) mma_commit(bar(BAR_QE + qb));  // last GEMM1 of this item issued
           }
         }
         if (!ok) break;

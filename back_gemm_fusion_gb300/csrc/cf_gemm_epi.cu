@@ -40,25 +40,28 @@
 namespace cf {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kAStageBytes = kBM * kBK * 2;              // 16 KB
-constexpr int kBStageBytes = kBN * kBK * 2;              // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes; // 48 KB
 constexpr int kOutStageBytes = 32 * 32 * 4;              // 4 KB per epilogue warp
 constexpr int kTmemCols = 2 * kBN;                       // two accumulators
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int kOffStages = 0;
-constexpr int kOffOut = kOffStages + kStages * kStageBytes;
-constexpr int kOffSlots = kOffOut + kEpiWarps * kOutStageBytes;  // float2 [2][128]
-constexpr int kOffBars = kOffSlots + 2 * kBM * 8;
-// barriers: full[S], empty[S], tfull[2], tempty[2], sfull[2][4], sempty[2][4], drain
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32)
-constexpr int kSmemUsed = kOffMisc + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
+// Per-mode geometry.  CTA2: a CTA pair runs 256 x 256 MMAs (cta_group::2),
+// each CTA holding its 128 rows of A and half (128 columns) of the B tile,
+// so a stage is 32 KB and six fit; otherwise 48 KB stages, four of them.
+template <bool CTA2>
+struct Geo {
+  static constexpr int kStages = CTA2 ? 6 : 4;
+  static constexpr int kBStageBytes = (CTA2 ? kBN / 2 : kBN) * kBK * 2;
+  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr int kOffOut = kStages * kStageBytes;
+  static constexpr int kOffSlots = kOffOut + kEpiWarps * kOutStageBytes;  // float2 [2][128]
+  static constexpr int kOffBars = kOffSlots + 2 * kBM * 8;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[2][4], sempty[2][4], drain
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32)
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack for the 1024-byte alignment
+};
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -173,13 +176,20 @@ __device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& 
   }
 }
 
-template <int ROWOP, int XMODE>
+template <int ROWOP, int XMODE, bool CTA2>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmEpiParams p) {
+  using G = Geo<CTA2>;
+  constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kOffOut = G::kOffOut,
+                kOffSlots = G::kOffSlots, kOffBars = G::kOffBars, kOffMisc = G::kOffMisc;
+  constexpr int kOffStages = 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA2: rank 0 of the pair issues every MMA ("leader").
+  const uint32_t pair_rank = CTA2 ? cluster_ctarank() : 0u;
+  const bool leader = pair_rank == 0;
 
   auto bar = [&](int idx) -> uint32_t { return sbase + kOffBars + 8 * idx; };
   const int BAR_FULL = 0, BAR_EMPTY = kStages, BAR_TFULL = 2 * kStages, BAR_TEMPTY = 2 * kStages + 2;
@@ -194,11 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), p.pair ? 2 : 1);  // pair: both CTAs' MMAs must release it
+      mbar_init(bar(BAR_EMPTY + s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(BAR_TFULL + a), 1);
-      mbar_init(bar(BAR_TEMPTY + a), kEpiWarps);
+      // CTA2: the leader's barrier collects both CTAs' epilogue warps.
+      mbar_init(bar(BAR_TEMPTY + a), CTA2 ? 2 * kEpiWarps : kEpiWarps);
     }
     for (int k = 0; k < 8; ++k) {
       mbar_init(bar(BAR_SFULL + k), cn);
@@ -214,12 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     tma_prefetch_desc(&p.tmOut);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish();
+    if (CTA2) {
+      tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (XMODE == X_CLUSTER || p.pair) cluster_sync_all();
+  if (XMODE == X_CLUSTER || CTA2) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int kblocks = p.K / kBK;
@@ -238,28 +254,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           const uint32_t sa = sbase + kOffStages + stage * kStageBytes;
           const uint32_t sb = sa + kAStageBytes;
           const uint32_t fb = bar(BAR_FULL + stage);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(sa, &p.tmA, fb, kb * kBK, m0);
-          if (p.pair) {
-            // This CTA fetches half of the B tile for both CTAs of the pair.
-            const uint32_t r = (uint32_t)w.rank;
+          if (CTA2) {
+            // Both CTAs' bytes land on the leader's "full" barrier.
+            const uint32_t fbl = mapa_shared(fb, 0);
+            if (leader) mbar_arrive_expect_tx(fb, 2 * kStageBytes);
+            tma_load_2d_pair(sa, &p.tmA, fbl, kb * kBK, m0);
+            const int nb0 = n0 + (kBN / 2) * (int)pair_rank;  // this CTA's half of the B tile
             if (p.b_mn_major) {
-              for (int i = 2 * r; i < 2 * (int)r + 2; ++i)
-                tma_load_2d_multicast(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK, 0x3);
+              tma_load_2d_pair(sb, &p.tmB, fbl, nb0, kb * kBK);
+              tma_load_2d_pair(sb + 64 * kBK * 2, &p.tmB, fbl, nb0 + 64, kb * kBK);
             } else {
-              tma_load_2d_multicast(sb + r * (128 * kBK * 2), &p.tmB, fb, kb * kBK, n0 + 128 * r, 0x3);
+              tma_load_2d_pair(sb, &p.tmB, fbl, kb * kBK, nb0);
             }
-          } else if (p.b_mn_major) {
-#pragma unroll
-            for (int i = 0; i < kBN / 64; ++i) tma_load_2d(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK);
           } else {
-            tma_load_2d(sb, &p.tmB, fb, kb * kBK, n0);
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            tma_load_2d(sa, &p.tmA, fb, kb * kBK, m0);
+            if (p.b_mn_major) {
+#pragma unroll
+              for (int i = 0; i < kBN / 64; ++i)
+                tma_load_2d(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK);
+            } else {
+              tma_load_2d(sb, &p.tmB, fb, kb * kBK, n0);
+            }
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (p.pair) {
-        // The peer's MMA releases reach this CTA's barriers asynchronously:
+      if (CTA2) {
+        // The leader's MMA releases reach this CTA's barriers asynchronously:
         // wait until every stage's last release has landed before exiting.
         for (int s2 = 0; s2 < kStages; ++s2) {
           mbar_wait<false, false>(bar(BAR_EMPTY + stage), phase ^ 1, wc);
@@ -269,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, kBN, (uint32_t)p.b_mn_major);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(CTA2 ? 2 * kBM : kBM, kBN, (uint32_t)p.b_mn_major);
       uint32_t stage = 0, phase = 0;
       int t = 0;
       bool ok = true;
       for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next(), ++t) {
         const int acc = t & 1;
-        if (!mbar_wait(bar(BAR_TEMPTY + acc), ((t >> 1) & 1) ^ 1, wc)) { ok = false; break; }
+        // CTA2: the peer's epilogue arrives remotely, so acquire at cluster scope.
+        if (!mbar_wait<CTA2>(bar(BAR_TEMPTY + acc), ((t >> 1) & 1) ^ 1, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -287,20 +310,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            // MN-major B: 64-column atoms 8 KB apart (LBO), 8-row groups 1 KB apart (SBO).
             const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048, 64 * kBK * 2, 1024)
                                              : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (CTA2) mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (p.pair) mma_commit_multicast(bar(BAR_EMPTY + stage), 0x3);  // frees the stage in both CTAs
+          if (CTA2) mma_commit_pair(bar(BAR_EMPTY + stage), 0x3);  // frees the stage in both CTAs
           else mma_commit(bar(BAR_EMPTY + stage));
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        mma_commit(bar(BAR_TFULL + acc));
+        if (CTA2) mma_commit_pair(bar(BAR_TFULL + acc), 0x3);
+        else mma_commit(bar(BAR_TFULL + acc));
       }
       // Drain: every MMA issued above has completed before TMEM is freed.
-      mma_commit(bar(BAR_DRAIN));
+      if (CTA2) mma_commit_pair(bar(BAR_DRAIN), 0x1);
+      else mma_commit(bar(BAR_DRAIN));
       mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
+      if (CTA2 && ok) {
+        // Every remote "accumulator empty" arrival from the peer has landed.
+        for (int t2 = t; t2 < t + 2; ++t2)
+          mbar_wait<true, false>(bar(BAR_TEMPTY + (t2 & 1)), ((t2 >> 1) & 1) ^ 1, wc);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -476,57 +508,76 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_TEMPTY + acc));
+      if (lane == 0) {
+        if (CTA2 && !leader) mbar_arrive_cluster(bar(BAR_TEMPTY + acc), 0);  // the leader issues the MMAs
+        else mbar_arrive(bar(BAR_TEMPTY + acc));
+      }
     }
     if (lane == 0) bulk_wait0();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+  if (CTA2) {
+    cluster_sync_all();  // the peer's TMEM and smem are in use until the leader is done
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+  } else {
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if (XMODE == X_CLUSTER) cluster_sync_all();
   }
-  if (XMODE == X_CLUSTER || p.pair) cluster_sync_all();
 }
 
-template <int R, int X>
+template <int R, int X, bool P>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X>);
+  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P>);
 }
 
-const void* select_kernel(int rowop, int xmode) {
-#define CF_CASE(R, X) \
-  if (rowop == R && xmode == X) return kernel_ptr<R, X>();
-  CF_CASE(ROW_NONE, X_NONE)
-  CF_CASE(ROW_LAYERNORM, X_NONE)
-  CF_CASE(ROW_LAYERNORM, X_CLUSTER)
-  CF_CASE(ROW_LAYERNORM, X_GLOBAL)
-  CF_CASE(ROW_RMSNORM, X_NONE)
-  CF_CASE(ROW_RMSNORM, X_CLUSTER)
-  CF_CASE(ROW_RMSNORM, X_GLOBAL)
-  CF_CASE(ROW_SOFTMAX, X_NONE)
-  CF_CASE(ROW_SOFTMAX, X_CLUSTER)
-  CF_CASE(ROW_SOFTMAX, X_GLOBAL)
+const void* select_kernel(int rowop, int xmode, bool pair) {
+#define CF_CASE(R, X, P) \
+  if (rowop == R && xmode == X && pair == P) return kernel_ptr<R, X, P>();
+  CF_CASE(ROW_NONE, X_NONE, false)
+  CF_CASE(ROW_NONE, X_NONE, true)
+  CF_CASE(ROW_LAYERNORM, X_NONE, false)
+  CF_CASE(ROW_LAYERNORM, X_NONE, true)
+  CF_CASE(ROW_LAYERNORM, X_CLUSTER, false)
+  CF_CASE(ROW_LAYERNORM, X_GLOBAL, false)
+  CF_CASE(ROW_LAYERNORM, X_GLOBAL, true)
+  CF_CASE(ROW_RMSNORM, X_NONE, false)
+  CF_CASE(ROW_RMSNORM, X_NONE, true)
+  CF_CASE(ROW_RMSNORM, X_CLUSTER, false)
+  CF_CASE(ROW_RMSNORM, X_GLOBAL, false)
+  CF_CASE(ROW_RMSNORM, X_GLOBAL, true)
+  CF_CASE(ROW_SOFTMAX, X_NONE, false)
+  CF_CASE(ROW_SOFTMAX, X_NONE, true)
+  CF_CASE(ROW_SOFTMAX, X_CLUSTER, false)
+  CF_CASE(ROW_SOFTMAX, X_GLOBAL, false)
+  CF_CASE(ROW_SOFTMAX, X_GLOBAL, true)
 #undef CF_CASE
   return nullptr;
 }
 
+int smem_for(bool pair) { return pair ? Geo<true>::kSmemBytes : Geo<false>::kSmemBytes; }
+
 }  // namespace
 
-size_t gemm_epi_smem_bytes() { return (size_t)kSmemBytes; }
+size_t gemm_epi_smem_bytes() { return (size_t)smem_for(false); }
 
-cudaError_t gemm_epi_prepare(int rowop, int xmode) {
-  const void* k = select_kernel(rowop, xmode);
+cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair) {
+  const void* k = select_kernel(rowop, xmode, pair);
   if (!k) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for(pair));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-cudaError_t gemm_epi_max_clusters(int rowop, int xmode, int cluster, int* out) {
-  const void* k = select_kernel(rowop, xmode);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int cluster, int* out) {
+  const void* k = select_kernel(rowop, xmode, pair);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -536,20 +587,20 @@ cudaError_t gemm_epi_max_clusters(int rowop, int xmode, int cluster, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(cluster, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_for(pair);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(out, k, &cfg);
 }
 
 cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out) {
-  const void* k = select_kernel(rowop, xmode);
+  const void* k = select_kernel(rowop, xmode, false);
   if (!k) return cudaErrorInvalidValue;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, k, kThreads, kSmemBytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, k, kThreads, smem_for(false));
 }
 
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
-  const void* k = select_kernel(L.rowop, L.xmode);
+  const void* k = select_kernel(L.rowop, L.xmode, L.p.pair != 0);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -571,7 +622,7 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   }
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_for(L.p.pair != 0);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = na;

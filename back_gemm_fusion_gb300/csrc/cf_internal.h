@@ -30,7 +30,7 @@ struct GemmEpiParams {
   int strips;         // M / kBM
   int num_items;      // strips * tiles_n
   int b_mn_major;     // 1: B stored K x N (N contiguous)
-  int pair;           // 1: 2-CTA clusters along M share (multicast) each B tile
+  int pair;           // 1: CTA pairs run 256 x 256 tiles with cta_group::2 MMAs
   int pair_items;     // (strips / 2) * tiles_n when pair == 1
   int n_ops;          // elementwise ops (row op excluded)
   int op_kind[CF_EPI_MAX_OPS];
@@ -63,9 +63,9 @@ cf_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
 long long wait_timeout_cycles();
 
 size_t gemm_epi_smem_bytes();
-cudaError_t gemm_epi_prepare(int rowop, int xmode);  // set function attributes
+cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair);  // set function attributes
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);
-cudaError_t gemm_epi_max_clusters(int rowop, int xmode, int cluster, int* out);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int cluster, int* out);
 cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out);
 
 }  // namespace cf

@@ -178,6 +178,69 @@ class Workload:
 
 
 # ----------------------------------------------------------------- helpers
+class NvmlSampler:
+    """Samples SM clocks and clock-event (throttle) reasons through NVML
+    (libnvidia-ml via ctypes, read-only queries) every ~1 ms while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        import threading
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(torch_index)
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.lib, self.h, self.ctypes = lib, h, ctypes
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        c = self.ctypes
+        clk, rs = c.c_uint(), c.c_ulonglong()
+        while not self.stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.reason_fn(self.h, c.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(0.001)
+
+    def __enter__(self):
+        import threading
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self.stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
+                "samples": len(self.samples), "source": "nvml"}
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
@@ -328,7 +391,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         raise RuntimeError("device status reports a timeout after warm-up")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk, NvmlSampler(torch.cuda.current_device()) as nv:
         barrier(dist)
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -340,7 +403,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         torch.cuda.synchronize()
         barrier(dist)
         t_wall = time.perf_counter() - t_wall
-    clocks = clk.summary()
+    clocks = nv.summary() or clk.summary()
     if cf.cf_last_device_status() != 0:
         raise RuntimeError("device status reports a timeout in the timed region")
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
