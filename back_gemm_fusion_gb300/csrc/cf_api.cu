@@ -188,7 +188,9 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   sh->N = N;
   sh->K = K;
   if (M == 0 || N == 0) return CF_OK;
-  if (M % kBM != 0 || N % kBN != 0 || K % kBK != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
+  // Any M >= 1: rows past M are zero-filled by the TMA loads and clipped by
+  // the TMA stores of the last (ragged) 128-row strip; rows are independent.
+  if (N % kBN != 0 || K % kBK != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
   const int64_t tiles_n = N / kBN;
   if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)
@@ -261,13 +263,13 @@ size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_de
   EpiPlan plan;
   if (parse_epi(epi, &plan) != CF_OK) return 0;
   const int64_t M = A->rows, N = B->cols;
-  if (M <= 0 || N <= 0 || M % kBM != 0 || N % kBN != 0) return 0;
+  if (M <= 0 || N <= 0 || N % kBN != 0) return 0;
   const int64_t tiles_n = N / kBN;
   // The cluster path may fall back to the workspace path when no cluster of
   // that size can be resident, so AUTO/CLUSTER strips that fit a cluster
   // still report the (small) fallback workspace.
   if (plan.rowop == ROW_NONE || tiles_n == 1) return 0;
-  return ws_bytes_for(M / kBM, tiles_n);
+  return ws_bytes_for((M + kBM - 1) / kBM, tiles_n);
 }
 
 cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* bias, const float* gamma,
@@ -278,7 +280,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   cf_status s = validate_gemm_epi(A, B, bias, gamma, beta, epi, out, &plan, &sh);
   if (s != CF_OK) return s;
   if (sh.M == 0 || sh.N == 0) return CF_OK;
-  const int64_t tiles_n = sh.N / kBN, strips = sh.M / kBM;
+  const int64_t tiles_n = sh.N / kBN, strips = (sh.M + kBM - 1) / kBM;
   int xmode = choose_xmode(plan, epi, tiles_n);
   const size_t need_ws = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
   if (xmode == X_GLOBAL && (!workspace || workspace_bytes < need_ws || !aligned16(workspace)))
@@ -294,17 +296,6 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
     return s;
   p.b_mn_major = B->trans == 0 ? 1 : 0;
-  // Pair mode: CTA pairs (2-CTA clusters along M) run 256 x 256 tiles with
-  // cta_group::2 MMAs; each CTA loads its A rows and half of the B tile,
-  // halving per-SM shared-memory traffic per MMA.  Needs an even number of
-  // strips; the cluster (DSMEM) exchange keeps 1-CTA tiles.
-  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
-  if (p.b_mn_major)
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
-  else
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK,
-                  want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
-  if (s != CF_OK) return s;
   if ((s = encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32, 32)) != CF_OK)
     return s;
   p.M = (int)sh.M;
@@ -370,7 +361,19 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       L.grid = (int)(nclusters * tiles_n);
     }
   }
-  if (xmode != X_CLUSTER && want_pair) {
+  // Pair mode (decided once the exchange mode is final): CTA pairs (2-CTA
+  // clusters along M) run 256 x 256 tiles with cta_group::2 MMAs; each CTA
+  // loads its A rows and half of the B tile, halving per-SM shared-memory
+  // traffic per MMA.  Needs an even number of strips; the cluster (DSMEM)
+  // exchange keeps 1-CTA tiles.
+  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
+  if (p.b_mn_major)
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
+  else
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK,
+                  want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
+  if (s != CF_OK) return s;
+  if (want_pair) {
     int maxp = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);

@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -92,14 +93,17 @@ constexpr int kOffQ = 0;                    // two A tiles: the next item's is l
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;
 constexpr int kOffX = kOffRing + kRing * kTileBytes;  // float [3][2 halves][128]: block max (2 parities), row sum
 constexpr int kOffBars = kOffX + 3 * 2 * 128 * 4;
-// q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], p_full, pv_done, o_full, o_empty, drain,
-// max exchange [2 parities][4 quarters], sum exchange [4 quarters]
-constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_PF = 14, BAR_PV = 15, BAR_OF = 16,
-              BAR_OE = 17, BAR_DRAIN = 18, BAR_XM = 19, BAR_XL = 27, kNumBars = 31;
+// q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], p_full[2], pv_done[2], o_full, o_empty,
+// drain, max exchange [2 parities][4 quarters], sum exchange [4 quarters].
+// p_full is per S' buffer: eight warps arrive per chunk, and a warp may
+// finish chunk g+1 before another finishes chunk g, so one barrier per
+// buffer keeps each chunk's arrivals in its own phase.
+constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_PF = 14, BAR_PV = 16, BAR_OF = 18,
+              BAR_OE = 19, BAR_DRAIN = 20, BAR_XM = 21, BAR_XL = 29, kNumBars = 33;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S' (bf16 pairs) [384,448)
-constexpr int kTmemP = 384;
+constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S'0 [384,448), S'1 [448,512)
+constexpr int kTmemP = 384;     // S' buffer b (bf16 pairs, 64 columns) at kTmemP + 64 b
 constexpr float kRescaleLog2 = 8.0f;
 
 struct Params {
@@ -135,8 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     mbar_init(bar(BAR_SF + 0), 1);
     mbar_init(bar(BAR_SF + 1), 1);
-    mbar_init(bar(BAR_PF), kFWarps);
-    mbar_init(bar(BAR_PV), 1);
+    mbar_init(bar(BAR_PF + 0), kFWarps);
+    mbar_init(bar(BAR_PF + 1), kFWarps);
+    mbar_init(bar(BAR_PV + 0), 1);
+    mbar_init(bar(BAR_PV + 1), 1);
     mbar_init(bar(BAR_OF), 1);
     mbar_init(bar(BAR_OE), kFWarps);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         ok = issue_s(g0) && (nb < 2 || issue_s(g0 + 1));
         if (ok && nb <= 2) mma_commit(bar(BAR_QE + qb));
         for (int j = 0; ok && j < nb; ++j, ++g) {
-          if (!mbar_wait(bar(BAR_PF), g & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
           if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
           if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
@@ -232,11 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             // A = S' from TMEM (16 K elements = 8 packed columns per step).
-            mma_bf16_ts(tmem_base + 256, tmem_base + kTmemP + 8 * kk, smem_desc_sw128(wt + kk * 2048, 16384, 1024),
-                        id_o, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem_base + 256, tmem_base + kTmemP + 64 * (g & 1) + 8 * kk,
+                        smem_desc_sw128(wt + kk * 2048, 16384, 1024), id_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_RE + rs));
-          mma_commit(bar(BAR_PV));
+          mma_commit(bar(BAR_PV + (g & 1)));
           if (++rs == kRing) { rs = 0; rph ^= 1; }
           if (j + 2 < nb) {
             ok = issue_s(g + 2);
@@ -287,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         tmem_ld32(s_addr, va);
         tmem_ld32(s_addr + 32, vb);
         tmem_wait_ld();
-        bool pv_waited = false;
         if (p.softmax) {
           float hm = -INFINITY;
 #pragma unroll
@@ -303,8 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             const float f = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - m_new);
             if (j > 0) {
               // O must hold every earlier S' . W2 product before it is rescaled.
-              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV), (g & 1) ^ 1, wc))) { ok = false; break; }
-              pv_waited = true;
+              const uint32_t pg = g - 1;
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + (pg & 1)), (pg >> 1) & 1, wc))) {
+                ok = false;
+                break;
+              }
               tc_fence_after();
 #pragma unroll 1
               for (int c = 0; c < 2; ++c) {
@@ -336,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         pack_bf16(va, wa);
         pack_bf16(vb, wb);
         if (p.softmax) l += sum_packed_bf16(wa) + sum_packed_bf16(wb);  // exactly what GEMM2 consumes
-        // S' is single-buffered: the previous chunk's S' . W2 must have read it.
-        if (!pv_waited && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV), (g & 1) ^ 1, wc))) { ok = false; break; }
+        // S' buffer g & 1 was last read by the S' . W2 product two chunks back.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
         tc_fence_after();
         {
           float packed[32];
@@ -346,12 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             packed[e] = __uint_as_float(wa[e]);
             packed[16 + e] = __uint_as_float(wb[e]);
           }
-          tmem_st32(tmem_base + lane_off + kTmemP + 32 * half, packed);
+          tmem_st32(tmem_base + lane_off + kTmemP + 64 * sb + 32 * half, packed);
           tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_PF));
+        if (lane == 0) mbar_arrive(bar(BAR_PF + sb));
       }
       if (!ok) break;
       // Epilogue: O / l (softmax) -> fp32 output rows.
@@ -672,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
 
 }  // namespace mlp
 
+
 std::mutex g_mu;
 bool g_prepared[64][2] = {};
 
@@ -699,6 +708,7 @@ cf_status check_bf16_view(const cf_matrix* m, bool allow_trans) {
   if (!aligned16(m->ptr) || (m->ld * 2) % 16 != 0) return CF_ERR_MISALIGNED;
   return CF_OK;
 }
+
 
 
 cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2, const cf_b2b_desc* d,

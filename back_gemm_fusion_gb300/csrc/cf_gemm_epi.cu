@@ -612,10 +612,11 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (L.xmode == X_GLOBAL) {
+  if (L.xmode == X_GLOBAL && L.cluster == 1) {
     // All CTAs must be co-resident: tiles of a strip wait for one another.
-    // The grid never exceeds the resident capacity; the cooperative
-    // attribute additionally asks the driver to guarantee it.
+    // The grid never exceeds the resident capacity (for clustered grids,
+    // the resident-cluster count from the occupancy query); for plain grids
+    // the cooperative attribute additionally asks the driver to guarantee it.
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;
     ++na;
@@ -627,15 +628,7 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = na;
   void* args[] = {const_cast<GemmEpiParams*>(&L.p)};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
-  if (e != cudaSuccess && L.xmode == X_GLOBAL && L.cluster > 1) {
-    // Cooperative launches of clustered grids may be unsupported: launch
-    // without the attribute (the grid still fits the resident capacity).
-    cudaGetLastError();
-    cfg.numAttrs = na - 1;
-    e = cudaLaunchKernelExC(&cfg, k, args);
-  }
-  return e;
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace cf

@@ -184,6 +184,125 @@ __global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restri
   }
 }
 
+// Bandwidth-oriented row epilogue for N = 1024 * VPT: each of 256 threads
+// keeps VPT float4 vectors of the row in registers, so P is read once and
+// the output written once.
+template <int VPT>
+__global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __restrict__ P, int64_t ldp,
+                                                               float* __restrict__ out, int64_t ldo, int N,
+                                                               RowProgram pg, const float* __restrict__ bias,
+                                                               const float* __restrict__ gamma,
+                                                               const float* __restrict__ beta) {
+  __shared__ float red[32];
+  const float4* p = reinterpret_cast<const float4*>(P + (int64_t)blockIdx.x * ldp);
+  float4* o = reinterpret_cast<float4*>(out + (int64_t)blockIdx.x * ldo);
+  float4 v[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * 256 + threadIdx.x;  // float4 index
+    float4 x = p[c];
+    x.x = ew(pg, x.x, bias, 4 * c);
+    x.y = ew(pg, x.y, bias, 4 * c + 1);
+    x.z = ew(pg, x.z, bias, 4 * c + 2);
+    x.w = ew(pg, x.w, bias, 4 * c + 3);
+    v[i] = x;
+  }
+  float mul = 1.0f, add = 0.0f;  // y = (x * mul + add) [* gamma + beta]
+  if (pg.rowop == CF_OP_ROW_LAYERNORM) {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) s += v[i].x + v[i].y + v[i].z + v[i].w;
+    const float mean = block_reduce<false>(s, red) / N;
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+      ss += a * a + b * b + c * c + d * d;
+    }
+    mul = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+    add = -mean * mul;
+  } else if (pg.rowop == CF_OP_ROW_RMSNORM) {
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    mul = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+  } else if (pg.rowop == CF_OP_ROW_SOFTMAX) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) mx = fmaxf(fmaxf(mx, fmaxf(v[i].x, v[i].y)), fmaxf(v[i].z, v[i].w));
+    const float m = block_reduce<true>(mx, red);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      v[i].x = __expf(v[i].x - m);
+      v[i].y = __expf(v[i].y - m);
+      v[i].z = __expf(v[i].z - m);
+      v[i].w = __expf(v[i].w - m);
+      s += v[i].x + v[i].y + v[i].z + v[i].w;
+    }
+    mul = 1.0f / block_reduce<false>(s, red);
+  }
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * 256 + threadIdx.x;
+    float4 y = make_float4(fmaf(v[i].x, mul, add), fmaf(v[i].y, mul, add), fmaf(v[i].z, mul, add),
+                           fmaf(v[i].w, mul, add));
+    if (pg.rowop == CF_OP_ROW_LAYERNORM || pg.rowop == CF_OP_ROW_RMSNORM) {
+      const float4 g = reinterpret_cast<const float4*>(gamma)[c];
+      y.x *= g.x; y.y *= g.y; y.z *= g.z; y.w *= g.w;
+      if (pg.rowop == CF_OP_ROW_LAYERNORM) {
+        const float4 b = reinterpret_cast<const float4*>(beta)[c];
+        y.x += b.x; y.y += b.y; y.z += b.z; y.w += b.w;
+      }
+    }
+    o[c] = y;
+  }
+}
+
+// Register-resident mid op for N1 = 1024 * VPT (one CTA of 256 threads per row).
+template <int VPT>
+__global__ void __launch_bounds__(256) mid_op_reg_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ Pout,
+                                                         int N1, int op, float scale) {
+  __shared__ float red[32];
+  const float4* s = reinterpret_cast<const float4*>(S + (int64_t)blockIdx.x * N1);
+  uint2* o = reinterpret_cast<uint2*>(Pout + (int64_t)blockIdx.x * N1);
+  float4 v[VPT];
+  const float sc = op == CF_MID_RELU ? 1.0f : scale;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    float4 x = s[i * 256 + threadIdx.x];
+    v[i] = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
+  }
+  float mul = 1.0f;
+  if (op == CF_MID_SCALE_SOFTMAX) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) mx = fmaxf(fmaxf(mx, fmaxf(v[i].x, v[i].y)), fmaxf(v[i].z, v[i].w));
+    const float m = block_reduce<true>(mx, red);
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      v[i].x = __expf(v[i].x - m);
+      v[i].y = __expf(v[i].y - m);
+      v[i].z = __expf(v[i].z - m);
+      v[i].w = __expf(v[i].w - m);
+      sum += v[i].x + v[i].y + v[i].z + v[i].w;
+    }
+    mul = 1.0f / block_reduce<false>(sum, red);
+  }
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    float4 y = v[i];
+    if (op == CF_MID_SCALE_SOFTMAX) {
+      y.x *= mul; y.y *= mul; y.z *= mul; y.w *= mul;
+    } else {
+      y.x = fmaxf(y.x, 0.0f); y.y = fmaxf(y.y, 0.0f); y.z = fmaxf(y.z, 0.0f); y.w = fmaxf(y.w, 0.0f);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
+    o[i * 256 + threadIdx.x] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
 // Mid op of the unfused B2BGEMM: S (fp32) -> bf16 S' = F(S), one CTA per row.
 __global__ void __launch_bounds__(256) mid_op_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ Pout,
                                                      int N1, int op, float scale) {
@@ -245,12 +364,24 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   cf_status s = lt_gemm(A->ptr, A->ld, B->ptr, B->ld, B->trans != 0, intermediate, N, CUDA_R_32F, M, N, K, 1, 0,
                         0, 0, st);
   if (s != CF_OK) return s;
-  const size_t smem = (size_t)N * sizeof(float);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(row_epilogue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return CF_ERR_CUDA;
-  row_epilogue_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, static_cast<float*>(out->ptr), out->ld,
-                                                      (int)N, pg, bias, gamma, beta);
+  float* o = static_cast<float*>(out->ptr);
+  const bool vec = N % 1024 == 0 && (out->ld % 4) == 0 && aligned16(out->ptr) && (!bias || aligned16(bias)) &&
+                   (!gamma || aligned16(gamma)) && (!beta || aligned16(beta));
+  switch (vec ? N / 1024 : 0) {
+    case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    case 4: row_epilogue_reg_kernel<4><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    case 8: row_epilogue_reg_kernel<8><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    case 16: row_epilogue_reg_kernel<16><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    default: {
+      const size_t smem = (size_t)N * sizeof(float);
+      if (smem > 48 * 1024 &&
+          cudaFuncSetAttribute(row_epilogue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+              cudaSuccess)
+        return CF_ERR_CUDA;
+      row_epilogue_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta);
+    }
+  }
   return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
 }
 
@@ -268,12 +399,22 @@ extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1,
   cf_status s = lt_gemm(A->ptr, A->ld, W1->ptr, W1->ld, W1->trans != 0, s_buf, N1, CUDA_R_32F, M, N1, K, batch,
                         d->strideA, d->strideW1, M * N1, st);
   if (s != CF_OK) return s;
-  const size_t smem = (size_t)N1 * sizeof(float);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(mid_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return CF_ERR_CUDA;
-  mid_op_kernel<<<(unsigned)(M * batch), 256, smem, st>>>(s_buf, static_cast<__nv_bfloat16*>(p_buf), (int)N1,
-                                                          d->mid_op, d->mid_scale);
+  __nv_bfloat16* pb = static_cast<__nv_bfloat16*>(p_buf);
+  const unsigned rows = (unsigned)(M * batch);
+  switch (N1 % 1024 == 0 && aligned16(p_buf) ? N1 / 1024 : 0) {
+    case 1: mid_op_reg_kernel<1><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
+    case 2: mid_op_reg_kernel<2><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
+    case 4: mid_op_reg_kernel<4><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
+    case 8: mid_op_reg_kernel<8><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
+    case 16: mid_op_reg_kernel<16><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
+    default: {
+      const size_t smem = (size_t)N1 * sizeof(float);
+      if (smem > 48 * 1024 &&
+          cudaFuncSetAttribute(mid_op_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CF_ERR_CUDA;
+      mid_op_kernel<<<rows, 256, smem, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale);
+    }
+  }
   if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
   return lt_gemm(p_buf, N1, W2->ptr, W2->ld, W2->trans != 0, out->ptr, out->ld, CUDA_R_32F, M, N2, N1, batch,
                  M * N1, d->strideW2, d->strideOut, st);

@@ -130,10 +130,11 @@ typedef struct {
  *          counters; the call clears the counters on `stream`).  Its contents
  *          are scratch; concurrent calls must use distinct workspaces.
  *
- * Shape rules (this version): M % 128 == 0, N % 256 == 0, K % 64 == 0,
- * K >= 64, all pointers and leading dims 16-byte aligned.  Violations return
- * CF_ERR_UNSUPPORTED_SHAPE / CF_ERR_MISALIGNED without launching anything.
- * M == 0 returns CF_OK without launching.
+ * Shape rules (this version): any M >= 0 (a ragged last 128-row strip is
+ * handled), N % 256 == 0, K % 64 == 0, K >= 64, all pointers and leading
+ * dims 16-byte aligned.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
+ * CF_ERR_MISALIGNED without launching anything.  M == 0 or N == 0 returns
+ * CF_OK without launching.
  */
 CF_API cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
                            const float* bias, const float* gamma, const float* beta,

@@ -72,7 +72,7 @@ def test_validation_errors(lib):
     B2.rows = 128
     assert _call(lib, A2, B2, O2, LN) == 1                  # inconsistent K
     A3, B3, O3 = _mats(M=200)
-    assert _call(lib, A3, B3, O3, LN) == 2                  # M not a multiple of 128
+    assert _call(lib, A3, B3, O3, LN) in (0, 4, 8)          # ragged M is supported (device check follows)
     A4, B4, O4 = _mats(N=384)
     assert _call(lib, A4, B4, O4, LN) == 2                  # N not a multiple of 256
     A5, B5, O5 = _mats(K=96)

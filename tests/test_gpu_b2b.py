@@ -128,7 +128,8 @@ def _mlp_case(M, K, N1, N2, seed):
 @pytest.mark.parametrize("w1_trans", [False, True])
 @pytest.mark.parametrize("op,scale", [("relu", 1.0), ("scale_relu", 0.75)])
 @pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 128, 256), (256, 128, 512, 256), (384, 192, 1024, 512),
-                                       (256, 256, 1024, 1024), (128, 64, 512, 1024)])
+                                       (256, 256, 1024, 1024), (128, 64, 512, 1024), (512, 192, 1024, 512),
+                                       (768, 64, 2048, 1024)])
 def test_mlp_small(cf, M, K, N1, N2, op, scale, w1_trans):
     X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M + K + N1 + N2)
     W1d = W1.t().contiguous().cuda() if w1_trans else W1.cuda()

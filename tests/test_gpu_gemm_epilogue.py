@@ -87,6 +87,19 @@ def test_row_ops_multi_tile(cf, rowop, exchange, N):
     assert_rows_close(_run(cf, case, exchange=exchange), _oracle(case), what=f"{rowop} N={N} {exchange}")
 
 
+@pytest.mark.parametrize("M", [1, 77, 200, 333, 640])
+@pytest.mark.parametrize("rowop", ["none", "layernorm", "rmsnorm", "softmax"])
+def test_ragged_m(cf, M, rowop):
+    # The last 128-row strip is partial: zero-filled loads, clipped stores.
+    ops = {"none": [("bias",), ("gelu_tanh",)], "layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.125), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case("ragged", M, 1024, 128, ops, seed=M, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case), _oracle(case), strict=1e-4 if rowop == "none" else 2e-3,
+                      what=f"ragged M={M} {rowop}")
+
+
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
     # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;

@@ -1,0 +1,63 @@
+"""GPU parity of the unfused comparison path (cuBLASLt GEMM -> HBM
+intermediate -> separate epilogue / mid-op kernel), so the fused-vs-unfused
+numbers compare two correct implementations."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import cf_oracle as O
+from back_gemm_fusion_gb300 import inputs as I
+from tests.parity import assert_rows_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cf():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    import back_gemm_fusion_gb300 as cf
+    return cf
+
+
+@pytest.mark.parametrize("N", [256, 1024, 4096])
+@pytest.mark.parametrize("rowop", ["layernorm", "rmsnorm", "softmax"])
+def test_unfused_gemm_epilogue(cf, N, rowop):
+    ops = {"layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 1 / 16), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case(rowop, 256, N, 256, ops, seed=N, need_bias=True, need_gamma=True, need_beta=True)
+    vec = [None if t is None else t.cuda() for t in (case.bias, case.gamma, case.beta)]
+    out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, *vec)
+    torch.cuda.synchronize()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta))
+    assert_rows_close(out.cpu().numpy(), ref, what=f"unfused {rowop} N={N}")
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+def test_unfused_attention(cf, op):
+    case = I.attention_b2b(batch=2, heads=2, L=1024, op=op)
+    out = cf.cf_unfused_b2bgemm(case.A.cuda(), case.W1.cuda(), case.W2.cuda(), op, case.scale, w1_trans=True)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for h in range(case.batch):
+        q, k, v = (I.to_f64(t[h]) for t in (case.A, case.W1, case.W2))
+        ref = O.b2bgemm(q, k.T, v, op, case.scale)
+        err = np.abs(got[h] - ref)
+        bound = 2.0 ** -7 * (np.abs(O.mid_op(q @ k.T, op, case.scale)) @ np.abs(v)) + 1e-6
+        assert np.all(err <= bound), f"unfused attention {op} head {h}: {(err / bound).max():.3g}x"
+
+
+def test_unfused_mlp(cf):
+    case = I.mlp_b2b(M=256, K=256, N1=2048, N2=512)
+    out = cf.cf_unfused_b2bgemm(case.A[0].cuda(), case.W1[0].cuda(), case.W2[0].cuda(), "relu")
+    torch.cuda.synchronize()
+    x, w1, w2 = I.to_f64(case.A[0]), I.to_f64(case.W1[0]), I.to_f64(case.W2[0])
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = 2.0 ** -7 * (np.abs(np.maximum(x @ w1, 0)) @ np.abs(w2)) + 1e-6
+    assert np.all(np.abs(out.cpu().numpy() - ref) <= bound)
