@@ -404,20 +404,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 namespace mlp {
 
 constexpr int kStageBytes = 32768;              // one ring stage
-constexpr int kRing = 3;
+constexpr int kMaxRing = 6;
 constexpr int kSlotBytes = 128 * 128 * 2;       // one 128 x 128 bf16 S' chunk
 constexpr int kMaxC = 4;                        // CTAs per cluster (N2 / 256)
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kOffRing = 0;
-constexpr int kOffSlots = kRing * kStageBytes;
-constexpr int kOffBars = kOffSlots + kMaxC * kSlotBytes;
-// ring_full[3], ring_empty[3], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain,
+// Shared memory: the C slots, the barriers, then as many ring stages as fit
+// (C = 1: 6, C = 2: 5, C = 4: 3); the host computes the ring depth.
+// ring_full[6], ring_empty[6], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain,
 // slot_written (the F warps finished writing this CTA's S' chunk)
-constexpr int BAR_RF = 0, BAR_RE = 3, BAR_SF = 6, BAR_SFREE = 8, BAR_SLF = 10, BAR_SLE = 11, BAR_OF = 12,
-              BAR_OE = 13, BAR_DRAIN = 14, BAR_SLW = 15, kNumBars = 16;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int BAR_RF = 0, BAR_RE = 6, BAR_SF = 12, BAR_SFREE = 14, BAR_SLF = 16, BAR_SLE = 17, BAR_OF = 18,
+              BAR_OE = 19, BAR_DRAIN = 20, BAR_SLW = 21, kNumBars = 22;
+constexpr int kSmemLimit = 232448;
+constexpr int kFixedBytes = 1024 + kNumBars * 8 + 16;  // alignment slack, barriers, misc
+__host__ __device__ constexpr int ring_for(int C) {
+  return (kSmemLimit - kFixedBytes - C * kSlotBytes) / kStageBytes > kMaxRing
+             ? kMaxRing
+             : (kSmemLimit - kFixedBytes - C * kSlotBytes) / kStageBytes;
+}
+__host__ __device__ constexpr int smem_for(int C) { return ring_for(C) * kStageBytes + C * kSlotBytes + kFixedBytes; }
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,512)
 
 struct Params {
@@ -428,6 +433,7 @@ struct Params {
   long long ldo, stride_out;
   int w1_k_major;
   int C;             // CTAs per cluster = N2 / 256
+  int ring;          // ring stages (ring_for(C))
   int kblocks;       // K / 64
   int rounds;        // N1 / (128 C)
   int strips, items; // M / 128, batch * strips
@@ -441,6 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kRing = p.ring;
+  const int kOffRing = 0;
+  const int kOffSlots = kRing * kStageBytes;
+  const int kOffBars = kOffSlots + p.C * kSlotBytes;
+  const int kOffMisc = kOffBars + kNumBars * 8;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -530,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         const int b = item / p.strips, strip = item - b * p.strips;
         ok = load_g1(strip, b, 0) && (R < 2 || load_g1(strip, b, 1));
         for (int r = 0; ok && r < R; ++r) {
-          ok = load_g2(b, r);
-          if (ok && r + 2 < R) ok = load_g1(strip, b, r + 2);
+          if (r + 2 < R) ok = load_g1(strip, b, r + 2);  // same order as the MMA issuer
+          if (ok) ok = load_g2(b, r);
         }
       }
     }
@@ -570,6 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         const uint32_t g0 = g;
         ok = g1(g0) && (R < 2 || g1(g0 + 1));
         for (int r = 0; ok && r < R; ++r, ++g) {
+          // The next-but-one S chunk only needs the F warps to have read S(r):
+          // issue it first so it overlaps the S' exchange of round r.
+          if (r + 2 < R && !(ok = g1(g + 2))) break;
           if (!mbar_wait(bar(BAR_SLF), g & 1, wc)) { ok = false; break; }
           if (r == 0 && !mbar_wait(bar(BAR_OE), (t & 1) ^ 1, wc)) { ok = false; break; }
           tc_fence_after();
@@ -592,7 +606,6 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
           if (!ok) break;
           // Every CTA of the cluster may refill its slot once all have consumed it.
           mma_commit_multicast(bar(BAR_SLE), all);
-          if (r + 2 < R) ok = g1(g + 2);
         }
         if (!ok) break;
         mma_commit(bar(BAR_OF));
@@ -617,27 +630,33 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       for (int r = 0; r < R; ++r, ++g) {
         const uint32_t sb = g & 1, u = g >> 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
-        // The slots may be overwritten once every CTA finished the previous round.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLE), (g & 1) ^ 1, wc))) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tmem_base + lane_off + sb * 128 + c * 32, v);
+        // Read this S chunk into registers (F applied, packed to bf16) and
+        // release its TMEM buffer at once, so the next-but-one chunk's GEMM1
+        // can start while the slots are still being exchanged.
+        uint32_t w[4][16];
+        {
+          float v[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tmem_base + lane_off + sb * 128 + c * 32, v[c]);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = fmaxf(v[e] * p.scale, 0.0f);
-          uint32_t w[16];
-          pack_bf16(v, w);
-          store_row_packed_sw128(my_slot, row, c * 32, w);
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[c][e] = fmaxf(v[c][e] * p.scale, 0.0f);
+            pack_bf16(v[c], w[c]);
+          }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(BAR_SFREE + sb));
-          mbar_arrive(bar(BAR_SLW));
-        }
+        if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
+        // The slots may be overwritten once every CTA finished the previous round.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLE), (g & 1) ^ 1, wc))) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_row_packed_sw128(my_slot, row, c * 32, w[c]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SLW));
         if (warp == 2) {
           // The whole chunk is in this CTA's slot: publish it to the peers.
           if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLW), g & 1, wc))) { ok = false; break; }
@@ -746,6 +765,7 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.C = (int)C;
+  p.ring = mlp::ring_for((int)C);
   p.kblocks = (int)(K / 64);
   p.rounds = (int)(N1 / (128 * C));
   p.strips = (int)(M / 128);
@@ -754,7 +774,8 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.status = status;
   p.timeout_cycles = wait_timeout_cycles();
   const void* fn = reinterpret_cast<const void*>(&mlp::mlp_kernel);
-  if ((s = prepare(1, fn, mlp::kSmemBytes)) != CF_OK) return s;
+  const int smem = mlp::smem_for((int)C);
+  if ((s = prepare(1, fn, mlp::smem_for(1))) != CF_OK) return s;  // the largest layout
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -762,7 +783,7 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(mlp::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = mlp::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
