@@ -61,10 +61,14 @@ __device__ __forceinline__ void pack_bf16(const float (&v)[32], uint32_t (&w)[16
 
 // Sum of the 32 bf16 values held in 16 packed words (exact widening).
 __device__ __forceinline__ float sum_packed_bf16(const uint32_t (&w)[16]) {
-  float s = 0.0f;
+  float t[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) s += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
-  return s;
+  for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
+#pragma unroll
+  for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+    for (int e = 0; e < h; ++e) t[e] += t[e + h];  // pairwise: log-depth dependency chain
+  return t[0];
 }
 
 // Write 32 packed bf16 values of row `r` (columns c0..c0+31 of a 128-column
@@ -87,22 +91,24 @@ namespace attn {
 constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
 constexpr int kRing = 4;                    // W1/W2 tiles in flight
-constexpr int kFWarps = 8;                  // two warpgroups: columns 0..63 and 64..127 of every row
+constexpr int kW1Ahead = 3;                 // W1 chunks loaded ahead of the W2 stream
+constexpr int kFWarps = 8;                  // two warpgroups; group G takes the chunks g with g % 2 == G
 constexpr int kThreads = 64 + 32 * kFWarps;
 constexpr int kOffQ = 0;                    // two A tiles: the next item's is loaded during this one
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;
-constexpr int kOffX = kOffRing + kRing * kTileBytes;  // float [3][2 halves][128]: block max (2 parities), row sum
-constexpr int kOffBars = kOffX + 3 * 2 * 128 * 4;
-// q_full[2], q_empty[2], ring_full[4], ring_empty[4], s_full[2], p_full[2], pv_done[2], o_full, o_empty,
-// drain, max exchange [2 parities][4 quarters], sum exchange [4 quarters].
-// p_full is per S' buffer: eight warps arrive per chunk, and a warp may
-// finish chunk g+1 before another finishes chunk g, so one barrier per
-// buffer keeps each chunk's arrivals in its own phase.
-constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_PF = 14, BAR_PV = 16, BAR_OF = 18,
-              BAR_OE = 19, BAR_DRAIN = 20, BAR_XM = 21, BAR_XL = 29, kNumBars = 33;
+constexpr int kOffM = kOffRing + kRing * kTileBytes;  // float [2 chunk parities][128]: running max hand-off
+constexpr int kOffL = kOffM + 2 * 128 * 4;            // float2 [2 item parities][128]: (l, m) of a group
+constexpr int kOffBars = kOffL + 2 * 128 * 8;
+// q_full[2], q_empty[2], ring_full[4], ring_empty[4], and per S buffer b
+// (= chunk parity = F group): s_full, s_free (group b holds S_b in registers),
+// p_full, pv_done; then o_full, o_empty, drain, running-max hand-off
+// [2 chunk parities][4 quarters], (l, m) hand-off [2 item parities][4 quarters].
+constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_SFREE = 14, BAR_PF = 16,
+              BAR_PV = 18, BAR_OF = 20, BAR_OE = 21, BAR_DRAIN = 22, BAR_MB = 23, BAR_XL = 31, kNumBars = 39;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S'0 [384,448), S'1 [448,512)
+constexpr int kTmemO = 256;
 constexpr int kTmemP = 384;     // S' buffer b (bf16 pairs, 64 columns) at kTmemP + 64 b
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -116,6 +122,10 @@ struct Params {
   unsigned* status;
   long long timeout_cycles;
 };
+
+__device__ __forceinline__ float (&part32(float (&v)[128], int c))[32] {
+  return *reinterpret_cast<float(*)[32]>(&v[32 * c]);
+}
 
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -132,21 +142,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_QF + i), 1);
       mbar_init(bar(BAR_QE + i), 1);
+      mbar_init(bar(BAR_SF + i), 1);
+      mbar_init(bar(BAR_SFREE + i), 4);  // the four warps of F group i
+      mbar_init(bar(BAR_PF + i), 4);
+      mbar_init(bar(BAR_PV + i), 1);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(bar(BAR_RF + i), 1);
       mbar_init(bar(BAR_RE + i), 1);
     }
-    mbar_init(bar(BAR_SF + 0), 1);
-    mbar_init(bar(BAR_SF + 1), 1);
-    mbar_init(bar(BAR_PF + 0), kFWarps);
-    mbar_init(bar(BAR_PF + 1), kFWarps);
-    mbar_init(bar(BAR_PV + 0), 1);
-    mbar_init(bar(BAR_PV + 1), 1);
     mbar_init(bar(BAR_OF), 1);
-    mbar_init(bar(BAR_OE), kFWarps);
+    mbar_init(bar(BAR_OE), 4);  // the group that writes the item's output
     mbar_init(bar(BAR_DRAIN), 1);
-    for (int i = 0; i < 12; ++i) mbar_init(bar(BAR_XM + i), 2);  // one arrival per half
+    for (int i = 0; i < 16; ++i) mbar_init(bar(BAR_MB + i), 1);  // MB[8] then XL[8]: one publishing warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -187,11 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         mbar_arrive_expect_tx(bar(BAR_QF + qb), kTileBytes);
         tma_load_3d(qdst, &p.tmA, bar(BAR_QF + qb), 0, mb * kTile, b);
         tma_load_3d(qdst + 16384, &p.tmA, bar(BAR_QF + qb), 64, mb * kTile, b);
-        // Operand order = MMA consumption order: W1_0, W1_1, then W2_j, W1_{j+2}.
-        ok = load_tile(&p.tmW1, 0, b) && (nb < 2 || load_tile(&p.tmW1, kTile, b));
+        // Load order = MMA consumption order: W1_0, W1_1, W1_2, then pairs
+        // W2_j, W1_{j+3} (GEMM1 of chunk j+2 is issued before GEMM2 of j).
+        for (int i = 0; ok && i < nb && i < kW1Ahead; ++i) ok = load_tile(&p.tmW1, i * kTile, b);
         for (int j = 0; ok && j < nb; ++j) {
           ok = load_tile(&p.tmW2, j * kTile, b);
-          if (ok && j + 2 < nb) ok = load_tile(&p.tmW1, (j + 2) * kTile, b);
+          if (ok && j + kW1Ahead < nb) ok = load_tile(&p.tmW1, (j + kW1Ahead) * kTile, b);
         }
       }
     }
@@ -201,23 +210,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0);   // W1 tile is K-major (rows = N1)
       const uint32_t id_o = idesc_bf16_f32(128, 128, 1);   // W2 tile is MN-major (rows = K of GEMM2)
       uint32_t rs = 0, rph = 0;
-      uint32_t g = 0;  // global chunk counter (S buffer = g & 1)
+      uint32_t g = 0;  // global chunk counter (S buffer and F group = g & 1)
       int it = 0;
       bool ok = true;
-      uint32_t qaddr = sbase + kOffQ;
-      auto issue_s = [&](uint32_t gg) -> bool {
+      // Descriptors (K-major A and W1 tiles, MN-major W2 tiles) of buffer 0;
+      // a tile of buffer i starts i * kTileBytes / 16 further in the low half.
+      const SDesc dq = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      const SDesc dk = sdesc_sw128(sbase + kOffRing, 16, 1024);
+      const SDesc dv = sdesc_sw128(sbase + kOffRing, 16384, 1024);
+      constexpr uint32_t kTileStep = kTileBytes >> 4;
+      uint32_t q_lo = dq.lo;
+      // S_h = A . W1 chunk into S buffer h & 1, once F group h & 1 holds S_{h-2}
+      // in registers.
+      auto issue_s = [&](uint32_t h) -> bool {
+        if (h >= 2 && !mbar_wait(bar(BAR_SFREE + (h & 1)), ((h - 2) >> 1) & 1, wc)) return false;
         if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
         tc_fence_after();
-        const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
-        const uint32_t d = tmem_base + (gg & 1) * 128;
+        const uint32_t k_lo = dk.lo + rs * kTileStep;
+        const uint32_t d = tmem_base + (h & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16(d, smem_desc_sw128(qaddr + off, 16, 1024), smem_desc_sw128(wt + off, 16, 1024), id_s,
-                   kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(d, q_lo + off, dq.hi, k_lo + off, dk.hi, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(BAR_RE + rs));
-        mma_commit(bar(BAR_SF + (gg & 1)));
+        mma_commit(bar(BAR_SF + (h & 1)));
         if (++rs == kRing) { rs = 0; rph ^= 1; }
         return true;
       };
@@ -225,29 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const int qb = it & 1;
         if (!mbar_wait(bar(BAR_QF + qb), (it >> 1) & 1, wc)) break;
         tc_fence_after();
-        qaddr = sbase + kOffQ + qb * kTileBytes;
-        const uint32_t g0 = g;
-        ok = issue_s(g0) && (nb < 2 || issue_s(g0 + 1));
+        q_lo = dq.lo + qb * kTileStep;
+        ok = issue_s(g) && (nb < 2 || issue_s(g + 1));
         if (ok && nb <= 2) mma_commit(bar(BAR_QE + qb));
         for (int j = 0; ok && j < nb; ++j, ++g) {
+          if (j + 2 < nb) {
+            ok = issue_s(g + 2);
+            if (!ok) break;
+            if (j + 3 == nb) mma_commit(bar(BAR_QE + qb));  // last GEMM1 of this item issued
+          }
           if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
           if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
           if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t wt = sbase + kOffRing + rs * kTileBytes;
+          const uint32_t v_lo = dv.lo + rs * kTileStep;
+          const uint32_t p_col = tmem_base + kTmemP + 64 * (g & 1);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // A = S' from TMEM (16 K elements = 8 packed columns per step).
-            mma_bf16_ts(tmem_base + 256, tmem_base + kTmemP + 64 * (g & 1) + 8 * kk,
-                        smem_desc_sw128(wt + kk * 2048, 16384, 1024), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+            // A = S' from TMEM (16 K elements = 8 packed columns per step);
+            // B = W2 rows 16 kk .. 16 kk + 15 (2048 bytes per step).
+            mma_ts(tmem_base + kTmemO, p_col + 8 * kk, v_lo + kk * (2048 >> 4), dv.hi, id_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_RE + rs));
           mma_commit(bar(BAR_PV + (g & 1)));
           if (++rs == kRing) { rs = 0; rph ^= 1; }
-          if (j + 2 < nb) {
-            ok = issue_s(g + 2);
-            if (ok && j + 3 == nb) mma_commit(bar(BAR_QE + qb));  // last GEMM1 of this item issued
-          }
         }
         if (!ok) break;
         mma_commit(bar(BAR_OF));
@@ -257,134 +276,164 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
   } else {
     // -------------------------------------- F (softmax / ReLU) and epilogue
-    // Two warpgroups: half h owns columns 64h..64h+63 of every S' row; the
-    // warps of both halves that share a TMEM lane quarter exchange their
-    // half-row max (and, at the end, half-row sums) through shared memory,
-    // synchronised by per-quarter mbarriers (bounded waits).
-    const int half = (warp - 2) >> 2;
+    // F group G = 0, 1 takes the chunks g with g % 2 == G: a thread owns one
+    // S row (TMEM lane) and all 128 columns of the chunk, so two chunks are
+    // in F at once.  Softmax keeps one running max per row for both groups:
+    // the owner of chunk g receives the max in use after chunk g-1 from the
+    // other group (shared memory + a per-quarter mbarrier), decides the max
+    // for chunk g, and passes it on at once, before its exponentials.  Each
+    // group keeps its own running sum l in the scale of the last max it used;
+    // the group that owns an item's last chunk merges both sums and writes
+    // the output rows.
+    const int grp = (warp - 2) >> 2;
     const int q = warp & 3;
     const int row = 32 * q + lane;
-    const int c0 = 64 * half;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    float* xch = reinterpret_cast<float*>(smem + kOffX);  // [slot][half][row]
-    // Publish `v` for this row, then read the other half's value (bounded).
-    auto exchange = [&](float v, int slot, int barid, uint32_t parity, float& other) -> bool {
-      float* xb = xch + slot * 256;
-      xb[half * 128 + row] = v;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(barid));
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(barid), parity, wc))) return false;
-      other = xb[(half ^ 1) * 128 + row];
-      return true;
-    };
+    float* mrun = reinterpret_cast<float*>(smem + kOffM);   // [chunk parity][row]
+    float2* lm = reinterpret_cast<float2*>(smem + kOffL);   // [item parity][row]
     const float sl2 = p.scale * kLog2e;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
       const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
-      float m_used = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nb; ++j, ++g) {
-        const uint32_t sb = g & 1, u = g >> 1;
+      const uint32_t g0 = g;
+      const uint32_t g_last = g0 + (uint32_t)nb - 1;
+      float l = 0.0f, m_last = -INFINITY;   // this group's sum, and the max it is scaled to
+      for (uint32_t gg = g0 + ((g0 & 1) != (uint32_t)grp ? 1u : 0u); gg <= g_last; gg += 2) {
+        const int j = (int)(gg - g0);
+        const uint32_t sb = gg & 1, u = gg >> 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t s_addr = tmem_base + lane_off + sb * 128 + c0;
-        float va[32], vb[32];
-        tmem_ld32(s_addr, va);
-        tmem_ld32(s_addr + 32, vb);
+        float v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem_base + lane_off + sb * 128 + 32 * c, part32(v, c));
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));  // S_sb may be overwritten now
         if (p.softmax) {
-          float hm = -INFINITY;
+          float mx[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) hm = fmaxf(hm, fmaxf(va[e], vb[e]));
-          float hm_other;
-          if (!exchange(hm, g & 1, BAR_XM + (g & 1) * 4 + q, (g >> 1) & 1, hm_other)) { ok = false; break; }
-          const float bmax = fmaxf(hm, hm_other) * sl2;
-          // Lazy rescale: only when the block max exceeds the max in use by
-          // more than 2^8 (in exp2 units) does O (and l) move to a new max.
-          const bool need = bmax > m_used + kRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? bmax : m_used;
-            const float f = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - m_new);
-            if (j > 0) {
-              // O must hold every earlier S' . W2 product before it is rescaled.
-              const uint32_t pg = g - 1;
-              if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + (pg & 1)), (pg >> 1) & 1, wc))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-#pragma unroll 1
-              for (int c = 0; c < 2; ++c) {
-                float o[32];
-                tmem_ld32(tmem_base + lane_off + 256 + c0 + c * 32, o);
-                tmem_wait_ld();
+          for (int e = 0; e < 16; ++e)
+            mx[e] = fmaxf(fmaxf(fmaxf(v[e], v[e + 16]), fmaxf(v[e + 32], v[e + 48])),
+                          fmaxf(fmaxf(v[e + 64], v[e + 80]), fmaxf(v[e + 96], v[e + 112])));
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] *= f;
-                tmem_st32(tmem_base + lane_off + 256 + c0 + c * 32, o);
-              }
-              tmem_wait_st();
+          for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+            for (int e = 0; e < h; ++e) mx[e] = fmaxf(mx[e], mx[e + h]);
+          const float bmax = mx[0] * sl2;
+          // Max in use after chunk gg-1 (every chunk but the CTA's first
+          // waits, so hand-offs alternate strictly between the groups).
+          float m_prev = -INFINITY;
+          if (gg > 0) {
+            const uint32_t pg = gg - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_MB + (pg & 1) * 4 + q), (pg >> 1) & 1, wc))) {
+              ok = false;
+              break;
             }
-            l *= f;
-            m_used = m_new;
+            if (j > 0) m_prev = mrun[(pg & 1) * 128 + row];
           }
+          // Lazy rescale: the max in use moves only when the block max
+          // exceeds it by more than 2^8 (in exp2 units).
+          const bool need = bmax > m_prev + kRescaleLog2;
+          const float m_new = need ? bmax : m_prev;
+          mrun[sb * 128 + row] = m_new;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_MB + sb * 4 + q));
+          if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // O must hold every earlier S' . W2 product before it is rescaled.
+            const uint32_t pg = gg - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + (pg & 1)), (pg >> 1) & 1, wc))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float f = ex2_approx(m_prev - m_new);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {  // 16 columns at a time: v[] stays in registers
+              float o[16];
+              tmem_ld16(tmem_base + lane_off + kTmemO + c * 16, o);
+              tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            va[e] = ex2_approx(fmaf(va[e], sl2, -m_used));
-            vb[e] = ex2_approx(fmaf(vb[e], sl2, -m_used));
+              for (int e = 0; e < 16; ++e) o[e] *= f;
+              tmem_st16(tmem_base + lane_off + kTmemO + c * 16, o);
+            }
+            tmem_wait_st();
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            va[e] = fmaxf(va[e] * p.scale, 0.0f);
-            vb[e] = fmaxf(vb[e] * p.scale, 0.0f);
-          }
+          l *= ex2_approx(m_last - m_new);  // 0 on this group's first chunk of the item
+          m_last = m_new;
         }
-        uint32_t wa[16], wb[16];
-        pack_bf16(va, wa);
-        pack_bf16(vb, wb);
-        if (p.softmax) l += sum_packed_bf16(wa) + sum_packed_bf16(wb);  // exactly what GEMM2 consumes
-        // S' buffer g & 1 was last read by the S' . W2 product two chunks back.
+        // S' buffer sb was last read by the S' . W2 product two chunks back.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
         tc_fence_after();
-        {
-          float packed[32];
+        // F, bf16 rounding, the S' store and (softmax) the row sum of exactly
+        // what GEMM2 consumes, 32 columns at a time.
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            packed[e] = __uint_as_float(wa[e]);
-            packed[16 + e] = __uint_as_float(wb[e]);
+        for (int c = 0; c < 4; ++c) {
+          float(&vc)[32] = part32(v, c);
+          uint32_t w[16];
+          if (p.softmax) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) vc[e] = ex2_approx(fmaf(vc[e], sl2, -m_last));
+            pack_bf16(vc, w);
+            l += sum_packed_bf16(w);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) vc[e] = fmaxf(vc[e] * p.scale, 0.0f);
+            pack_bf16(vc, w);
           }
-          tmem_st32(tmem_base + lane_off + kTmemP + 64 * sb + 32 * half, packed);
-          tmem_wait_st();
+          tmem_st16(tmem_base + lane_off + kTmemP + 64 * sb + 16 * c, *reinterpret_cast<float(*)[16]>(&w[0]));
         }
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PF + sb));
       }
+      g = g_last + 1;
       if (!ok) break;
-      // Epilogue: O / l (softmax) -> fp32 output rows.
+      const bool writer = (g_last & 1) == (uint32_t)grp;
+      const uint32_t xl = (uint32_t)(it & 1);
+      if (!writer) {
+        // Hand this group's (l, max) to the writer of the item's output.
+        if (p.softmax && nb >= 2) {
+          lm[xl * 128 + row] = make_float2(l, m_last);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_XL + xl * 4 + q));
+        }
+        continue;
+      }
+      // Writer: O / l -> fp32 output rows (all 128 columns of its rows).
       float inv = 1.0f;
       if (p.softmax) {
-        float l_other;
-        if (!exchange(l, 2, BAR_XL + q, it & 1, l_other)) break;
-        inv = 1.0f / (l + l_other);
+        float lt = l;
+        if (nb >= 2) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_XL + xl * 4 + q), (it >> 1) & 1, wc))) break;
+          const float2 o = lm[xl * 128 + row];
+          // m_last is the final max (the max in use never decreases).
+          lt = l + o.x * ex2_approx(o.y - m_last);
+        }
+        inv = 1.0f / lt;
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), it & 1, wc))) break;
       tc_fence_after();
-      float* orow = p.out + (long long)b * p.stride_out + (long long)(mb * kTile + row) * p.ldo + c0;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tmem_base + lane_off + 256 + c0 + c * 32, v);
-        tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+      float4* dst = reinterpret_cast<float4*>(p.out + (long long)b * p.stride_out +
+                                              (long long)(mb * kTile + row) * p.ldo);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
+      for (int h = 0; h < 2; ++h) {
+        float o[64];
+        tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h, *reinterpret_cast<float(*)[32]>(&o[0]));
+        tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
+        tmem_wait_ld();
+        if (h == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          dst[16 * h + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_OE));
     }
   }
   tc_fence_before();
@@ -556,6 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       uint32_t g = 0;  // global round counter
       int t = 0;
       bool ok = true;
+      // Stage-0 descriptors: A (X) tile, W1 tile (K- or MN-major), W2 tile
+      // (MN-major, 64-column atoms 8 KB apart), and S' slot 0.
+      constexpr uint32_t kStageStep = kStageBytes >> 4;
+      const SDesc dx = sdesc_sw128(sbase + kOffRing, 16, 1024);
+      const SDesc dw1 = sdesc_sw128(sbase + kOffRing + 16384, p.w1_k_major ? 16u : 8192u, 1024);
+      const uint32_t w1_step = p.w1_k_major ? (32u >> 4) : (2048u >> 4);  // per 16 K elements
+      const SDesc dw2 = sdesc_sw128(sbase + kOffRing, 8192, 1024);
+      const SDesc dsl = sdesc_sw128(sbase + kOffSlots, 16, 1024);
       auto g1 = [&](uint32_t gg) -> bool {
         // The F warps must be done reading the S buffer's previous contents.
         if (!mbar_wait(bar(BAR_SFREE + (gg & 1)), ((gg >> 1) & 1) ^ 1, wc)) return false;
@@ -564,13 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         for (int kb = 0; kb < p.kblocks; ++kb) {
           if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
           tc_fence_after();
-          const uint32_t sa = sbase + kOffRing + rs * kStageBytes, sw = sa + 16384;
+          const uint32_t x_lo = dx.lo + rs * kStageStep, w_lo = dw1.lo + rs * kStageStep;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = p.w1_k_major ? smem_desc_sw128(sw + kk * 32, 16, 1024)
-                                             : smem_desc_sw128(sw + kk * 2048, 8192, 1024);
-            mma_bf16(d, smem_desc_sw128(sa + kk * 32, 16, 1024), bd, id_s, (kb | kk) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(d, x_lo + kk * (32u >> 4), dx.hi, w_lo + kk * w1_step, dw1.hi, id_s, (kb | kk) ? 1u : 0u);
           mma_commit(bar(BAR_RE + rs));
           if (++rs == kRing) { rs = 0; rph ^= 1; }
         }
@@ -591,14 +645,12 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
             for (int kh = 0; kh < 2; ++kh) {
               if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t wt = sbase + kOffRing + rs * kStageBytes;
-              const uint32_t at = sbase + kOffSlots + c2 * kSlotBytes + kh * 16384;
+              const uint32_t w_lo = dw2.lo + rs * kStageStep;
+              const uint32_t a_lo = dsl.lo + ((uint32_t)(c2 * kSlotBytes + kh * 16384) >> 4);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem_base + 256, smem_desc_sw128(at + kk * 32, 16, 1024),
-                         smem_desc_sw128(wt + kk * 2048, 8192, 1024), id_o,
-                         (r | c2 | kh | kk) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tmem_base + 256, a_lo + kk * (32u >> 4), dsl.hi, w_lo + kk * (2048u >> 4), dw2.hi, id_o,
+                       (r | c2 | kh | kk) ? 1u : 0u);
               mma_commit(bar(BAR_RE + rs));
               if (++rs == kRing) { rs = 0; rph ^= 1; }
             }

@@ -293,6 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_bf16_f32(CTA2 ? 2 * kBM : kBM, kBN, (uint32_t)p.b_mn_major);
+      // Stage-0 descriptors; per 16 K elements A advances 32 bytes, B 32
+      // bytes (K-major) or 16 rows = 2048 bytes (MN-major: 64-column atoms
+      // 8 KB apart, 8-row groups 1 KB apart).
+      const SDesc da = sdesc_sw128(sbase + kOffStages, 16, 1024);
+      const SDesc db = sdesc_sw128(sbase + kOffStages + kAStageBytes, p.b_mn_major ? 64 * kBK * 2 : 16, 1024);
+      const uint32_t b_step = p.b_mn_major ? (2048u >> 4) : (32u >> 4);
       uint32_t stage = 0, phase = 0;
       int t = 0;
       bool ok = true;
@@ -305,16 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(bar(BAR_FULL + stage), phase, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = sbase + kOffStages + stage * kStageBytes;
-          const uint32_t sb = sa + kAStageBytes;
+          const uint32_t a_lo = da.lo + stage * (kStageBytes >> 4);
+          const uint32_t b_lo = db.lo + stage * (kStageBytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            // MN-major B: 64-column atoms 8 KB apart (LBO), 8-row groups 1 KB apart (SBO).
-            const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + kk * 2048, 64 * kBK * 2, 1024)
-                                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            if (CTA2) mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (CTA2) mma_ss_pair(d, a_lo + kk * 2, da.hi, b_lo + kk * b_step, db.hi, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else mma_ss(d, a_lo + kk * 2, da.hi, b_lo + kk * b_step, db.hi, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           if (CTA2) mma_commit_pair(bar(BAR_EMPTY + stage), 0x3);  // frees the stage in both CTAs
           else mma_commit(bar(BAR_EMPTY + stage));
