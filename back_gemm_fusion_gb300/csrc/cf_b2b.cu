@@ -90,21 +90,28 @@ namespace attn {
 
 constexpr int kTile = 128;                  // rows of A per CTA, N1 chunk, K and N2
 constexpr int kTileBytes = 128 * 128 * 2;   // one bf16 128 x 128 tile (two 64-column regions)
-constexpr int kRing = 4;                    // W1/W2 tiles in flight
-constexpr int kW1Ahead = 3;                 // W1 chunks loaded ahead of the W2 stream
+constexpr int kRing1 = 3;                   // W1 tiles in flight (GEMM1 operand ring)
+constexpr int kRing2 = 2;                   // W2 tiles in flight (GEMM2 operand ring)
 constexpr int kFWarps = 8;                  // two warpgroups; group G takes the chunks g with g % 2 == G
-constexpr int kThreads = 64 + 32 * kFWarps;
-constexpr int kOffQ = 0;                    // two A tiles: the next item's is loaded during this one
-constexpr int kOffRing = kOffQ + 2 * kTileBytes;
-constexpr int kOffM = kOffRing + kRing * kTileBytes;  // float [2 chunk parities][128]: running max hand-off
+// Warps: 0 loads A and W1, 1 issues GEMM1 (and owns TMEM), 2..9 run F,
+// 10 loads W2, 11 issues GEMM2.
+constexpr int kWarpLoad2 = 2 + kFWarps, kWarpMma2 = 3 + kFWarps;
+constexpr int kThreads = 32 * (4 + kFWarps);
+constexpr int kOffQ = 0;                    // the A tile (reloaded once the item's last GEMM1 is done)
+constexpr int kOffW1 = kOffQ + kTileBytes;
+constexpr int kOffW2 = kOffW1 + kRing1 * kTileBytes;
+constexpr int kOffM = kOffW2 + kRing2 * kTileBytes;   // float [2 chunk parities][128]: running max hand-off
 constexpr int kOffL = kOffM + 2 * 128 * 4;            // float2 [2 item parities][128]: (l, m) of a group
 constexpr int kOffBars = kOffL + 2 * 128 * 8;
-// q_full[2], q_empty[2], ring_full[4], ring_empty[4], and per S buffer b
-// (= chunk parity = F group): s_full, s_free (group b holds S_b in registers),
-// p_full, pv_done; then o_full, o_empty, drain, running-max hand-off
-// [2 chunk parities][4 quarters], (l, m) hand-off [2 item parities][4 quarters].
-constexpr int BAR_QF = 0, BAR_QE = 2, BAR_RF = 4, BAR_RE = 8, BAR_SF = 12, BAR_SFREE = 14, BAR_PF = 16,
-              BAR_PV = 18, BAR_OF = 20, BAR_OE = 21, BAR_DRAIN = 22, BAR_MB = 23, BAR_XL = 31, kNumBars = 39;
+// q_full, q_empty, W1 ring full/empty, W2 ring full/empty, and per S buffer
+// b (= chunk parity = F group): s_full, s_free (group b holds S_b in
+// registers), p_full, pv_done; then o_full, o_empty, one drain barrier per
+// MMA issuer, running-max hand-off [2 chunk parities][4 quarters], (l, m)
+// hand-off [2 item parities][4 quarters].
+constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF1 = 2, BAR_RE1 = BAR_RF1 + kRing1, BAR_RF2 = BAR_RE1 + kRing1,
+              BAR_RE2 = BAR_RF2 + kRing2, BAR_SF = BAR_RE2 + kRing2, BAR_SFREE = BAR_SF + 2, BAR_PF = BAR_SFREE + 2,
+              BAR_PV = BAR_PF + 2, BAR_OF = BAR_PV + 2, BAR_OE = BAR_OF + 1, BAR_DRAIN1 = BAR_OE + 1,
+              BAR_DRAIN2 = BAR_DRAIN1 + 1, BAR_MB = BAR_DRAIN2 + 1, BAR_XL = BAR_MB + 8, kNumBars = BAR_XL + 8;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S'0 [384,448), S'1 [448,512)
@@ -127,6 +134,11 @@ __device__ __forceinline__ float (&part32(float (&v)[128], int c))[32] {
   return *reinterpret_cast<float(*)[32]>(&v[32 * c]);
 }
 
+// Two MMA-issuing threads: a 128 x 128 x 16 MMA lasts only 64 cycles and the
+// tensor pipe runs barely one instruction ahead of its issuing thread, so a
+// single thread that also waits on barriers between GEMM1 and GEMM2 bursts
+// leaves the pipe idle for every wait.  With GEMM1 and GEMM2 issued from
+// different warps, one keeps the pipe fed while the other waits.
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,21 +151,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int nb = p.n1_blocks;
 
   if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_QF), 1);
+    mbar_init(bar(BAR_QE), 1);
+    for (int i = 0; i < kRing1; ++i) {
+      mbar_init(bar(BAR_RF1 + i), 1);
+      mbar_init(bar(BAR_RE1 + i), 1);
+    }
+    for (int i = 0; i < kRing2; ++i) {
+      mbar_init(bar(BAR_RF2 + i), 1);
+      mbar_init(bar(BAR_RE2 + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_QF + i), 1);
-      mbar_init(bar(BAR_QE + i), 1);
       mbar_init(bar(BAR_SF + i), 1);
       mbar_init(bar(BAR_SFREE + i), 4);  // the four warps of F group i
       mbar_init(bar(BAR_PF + i), 4);
       mbar_init(bar(BAR_PV + i), 1);
     }
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(bar(BAR_RF + i), 1);
-      mbar_init(bar(BAR_RE + i), 1);
-    }
     mbar_init(bar(BAR_OF), 1);
     mbar_init(bar(BAR_OE), 4);  // the group that writes the item's output
-    mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN1), 1);
+    mbar_init(bar(BAR_DRAIN2), 1);
     for (int i = 0; i < 16; ++i) mbar_init(bar(BAR_MB + i), 1);  // MB[8] then XL[8]: one publishing warp
     *abort_flag = 0;
     fence_mbar_init();
@@ -172,88 +189,87 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kWarpLoad2) {
+    // ----------------------------------------------------------- producers
+    // Warp 0: the A tile and the W1 ring; warp 10: the W2 ring.  Each ring is
+    // consumed in load order by one MMA issuer.
     if (lane == 0) {
+      const bool w1 = warp == 0;
+      const int depth = w1 ? kRing1 : kRing2;
+      const int off = w1 ? kOffW1 : kOffW2;
+      const int rf = w1 ? BAR_RF1 : BAR_RF2, re = w1 ? BAR_RE1 : BAR_RE2;
+      const CUtensorMap* m = w1 ? &p.tmW1 : &p.tmW2;
       uint32_t rs = 0, rph = 0;
       int it = 0;
       bool ok = true;
-      auto load_tile = [&](const CUtensorMap* m, int row0, int b) -> bool {
-        if (!mbar_wait(bar(BAR_RE + rs), rph ^ 1, wc)) return false;
-        const uint32_t dst = sbase + kOffRing + rs * kTileBytes;
-        mbar_arrive_expect_tx(bar(BAR_RF + rs), kTileBytes);
-        tma_load_3d(dst, m, bar(BAR_RF + rs), 0, row0, b);
-        tma_load_3d(dst + 16384, m, bar(BAR_RF + rs), 64, row0, b);
-        if (++rs == kRing) { rs = 0; rph ^= 1; }
-        return true;
-      };
       for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
         const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
-        const int qb = it & 1;
-        if (!mbar_wait(bar(BAR_QE + qb), ((it >> 1) & 1) ^ 1, wc)) break;
-        const uint32_t qdst = sbase + kOffQ + qb * kTileBytes;
-        mbar_arrive_expect_tx(bar(BAR_QF + qb), kTileBytes);
-        tma_load_3d(qdst, &p.tmA, bar(BAR_QF + qb), 0, mb * kTile, b);
-        tma_load_3d(qdst + 16384, &p.tmA, bar(BAR_QF + qb), 64, mb * kTile, b);
-        // Load order = MMA consumption order: W1_0, W1_1, W1_2, then pairs
-        // W2_j, W1_{j+3} (GEMM1 of chunk j+2 is issued before GEMM2 of j).
-        for (int i = 0; ok && i < nb && i < kW1Ahead; ++i) ok = load_tile(&p.tmW1, i * kTile, b);
-        for (int j = 0; ok && j < nb; ++j) {
-          ok = load_tile(&p.tmW2, j * kTile, b);
-          if (ok && j + kW1Ahead < nb) ok = load_tile(&p.tmW1, (j + kW1Ahead) * kTile, b);
+        if (w1) {
+          if (!mbar_wait(bar(BAR_QE), (it & 1) ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bar(BAR_QF), kTileBytes);
+          tma_load_3d(sbase + kOffQ, &p.tmA, bar(BAR_QF), 0, mb * kTile, b);
+          tma_load_3d(sbase + kOffQ + 16384, &p.tmA, bar(BAR_QF), 64, mb * kTile, b);
+        }
+        for (int j = 0; j < nb; ++j) {
+          if (!mbar_wait(bar(re + rs), rph ^ 1, wc)) { ok = false; break; }
+          const uint32_t dst = sbase + off + rs * kTileBytes;
+          mbar_arrive_expect_tx(bar(rf + rs), kTileBytes);
+          tma_load_3d(dst, m, bar(rf + rs), 0, j * kTile, b);
+          tma_load_3d(dst + 16384, m, bar(rf + rs), 64, j * kTile, b);
+          if (++rs == (uint32_t)depth) { rs = 0; rph ^= 1; }
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------- GEMM1 issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 128, 0);   // W1 tile is K-major (rows = N1)
-      const uint32_t id_o = idesc_bf16_f32(128, 128, 1);   // W2 tile is MN-major (rows = K of GEMM2)
+      const SDesc dq = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      const SDesc dk = sdesc_sw128(sbase + kOffW1, 16, 1024);
+      constexpr uint32_t kTileStep = kTileBytes >> 4;
       uint32_t rs = 0, rph = 0;
       uint32_t g = 0;  // global chunk counter (S buffer and F group = g & 1)
       int it = 0;
       bool ok = true;
-      // Descriptors (K-major A and W1 tiles, MN-major W2 tiles) of buffer 0;
-      // a tile of buffer i starts i * kTileBytes / 16 further in the low half.
-      const SDesc dq = sdesc_sw128(sbase + kOffQ, 16, 1024);
-      const SDesc dk = sdesc_sw128(sbase + kOffRing, 16, 1024);
-      const SDesc dv = sdesc_sw128(sbase + kOffRing, 16384, 1024);
-      constexpr uint32_t kTileStep = kTileBytes >> 4;
-      uint32_t q_lo = dq.lo;
-      // S_h = A . W1 chunk into S buffer h & 1, once F group h & 1 holds S_{h-2}
-      // in registers.
-      auto issue_s = [&](uint32_t h) -> bool {
-        if (h >= 2 && !mbar_wait(bar(BAR_SFREE + (h & 1)), ((h - 2) >> 1) & 1, wc)) return false;
-        if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
-        tc_fence_after();
-        const uint32_t k_lo = dk.lo + rs * kTileStep;
-        const uint32_t d = tmem_base + (h & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss(d, q_lo + off, dq.hi, k_lo + off, dk.hi, id_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(BAR_RE + rs));
-        mma_commit(bar(BAR_SF + (h & 1)));
-        if (++rs == kRing) { rs = 0; rph ^= 1; }
-        return true;
-      };
       for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
-        const int qb = it & 1;
-        if (!mbar_wait(bar(BAR_QF + qb), (it >> 1) & 1, wc)) break;
-        tc_fence_after();
-        q_lo = dq.lo + qb * kTileStep;
-        ok = issue_s(g) && (nb < 2 || issue_s(g + 1));
-        if (ok && nb <= 2) mma_commit(bar(BAR_QE + qb));
-        for (int j = 0; ok && j < nb; ++j, ++g) {
-          if (j + 2 < nb) {
-            ok = issue_s(g + 2);
-            if (!ok) break;
-            if (j + 3 == nb) mma_commit(bar(BAR_QE + qb));  // last GEMM1 of this item issued
+        if (!mbar_wait(bar(BAR_QF), it & 1, wc)) break;
+        for (int j = 0; j < nb; ++j, ++g) {
+          // S buffer g & 1 is free once F group g & 1 holds S_{g-2} in registers.
+          if (g >= 2 && !mbar_wait(bar(BAR_SFREE + (g & 1)), ((g - 2) >> 1) & 1, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_RF1 + rs), rph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_lo = dk.lo + rs * kTileStep;
+          const uint32_t d = tmem_base + (g & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(d, dq.lo + koff, dq.hi, k_lo + koff, dk.hi, id_s, kk > 0 ? 1u : 0u);
           }
+          mma_commit(bar(BAR_RE1 + rs));
+          mma_commit(bar(BAR_SF + (g & 1)));
+          if (++rs == kRing1) { rs = 0; rph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(bar(BAR_QE));  // every GEMM1 of this item has read the A tile
+      }
+      mma_commit(bar(BAR_DRAIN1));
+      mbar_wait<false, false>(bar(BAR_DRAIN1), 0, wc);
+    }
+  } else if (warp == kWarpMma2) {
+    // ------------------------------------------------------- GEMM2 issuer
+    if (lane == 0) {
+      const uint32_t id_o = idesc_bf16_f32(128, 128, 1);   // W2 tile is MN-major (rows = K of GEMM2)
+      const SDesc dv = sdesc_sw128(sbase + kOffW2, 16384, 1024);
+      constexpr uint32_t kTileStep = kTileBytes >> 4;
+      uint32_t rs = 0, rph = 0;
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+        for (int j = 0; j < nb; ++j, ++g) {
           if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
           if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
-          if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_RF2 + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t v_lo = dv.lo + rs * kTileStep;
           const uint32_t p_col = tmem_base + kTmemP + 64 * (g & 1);
@@ -264,15 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             mma_ts(tmem_base + kTmemO, p_col + 8 * kk, v_lo + kk * (2048 >> 4), dv.hi, id_o,
                    (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(BAR_RE + rs));
+          mma_commit(bar(BAR_RE2 + rs));
           mma_commit(bar(BAR_PV + (g & 1)));
-          if (++rs == kRing) { rs = 0; rph ^= 1; }
+          if (++rs == kRing2) { rs = 0; rph ^= 1; }
         }
         if (!ok) break;
         mma_commit(bar(BAR_OF));
       }
-      mma_commit(bar(BAR_DRAIN));
-      mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
+      mma_commit(bar(BAR_DRAIN2));
+      mbar_wait<false, false>(bar(BAR_DRAIN2), 0, wc);
     }
   } else {
     // -------------------------------------- F (softmax / ReLU) and epilogue
