@@ -169,12 +169,20 @@ __device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& 
   } else if (p.pair) {
     const int sp = w.i / w.tiles_n;
     tile = w.i - sp * w.tiles_n;
+    if (sp & 1) tile = w.tiles_n - 1 - tile;  // serpentine, see below
     strip = 2 * sp + w.rank;
   } else {
     strip = w.i / w.tiles_n;
     tile = w.i - strip * w.tiles_n;
+    if (strip & 1) tile = w.tiles_n - 1 - tile;
   }
 }
+// Serpentine tile order: consecutive (pairs of) strips walk the N tiles in
+// opposite directions, so a strip starts on the B tiles its predecessor read
+// last, while they are still in L2.  When B is about the size of L2 (the
+// 4096 x 16384 softmax head: 128 MB), a plain order re-reads all of B from
+// DRAM for every strip.  Items of a strip stay contiguous, so the row
+// statistics exchange keeps its strip-major schedule.
 
 template <int ROWOP, int XMODE, bool CTA2>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmEpiParams p) {
@@ -341,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;      // row within the tile
     const uint32_t out_buf = sbase + kOffOut + (warp - 2) * kOutStageBytes;
+    // The output is streamed out once: let it leave L2 first, keeping the
+    // operand tiles the next items reread.
+    const uint64_t out_policy = l2_policy_evict_first();
     uint8_t* out_ptr = smem + kOffOut + (warp - 2) * kOutStageBytes;
     float2* slots = reinterpret_cast<float2*>(smem + kOffSlots);
     int t = 0;
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&p.tmOut, out_buf, n, m0 + 32 * q);
+          tma_store_2d_hint(&p.tmOut, out_buf, n, m0 + 32 * q, out_policy);
           bulk_commit();
         }
       }

@@ -383,6 +383,15 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     def step():
         wl.fused_step(cf, dev, stream, workspace)
 
+    if args.once:
+        # One fused launch and nothing else (for a profiler's kernel filter).
+        step()
+        torch.cuda.synchronize()
+        st = cf.cf_last_device_status()
+        print(json.dumps({"workload": wl.name, "once": True, "device_status": st}), flush=True)
+        if st != 0:
+            raise RuntimeError("device status reports a timeout")
+        return
     for _ in range(args.warmup):
         flush.fill_(1.0)
         step()
@@ -541,6 +550,8 @@ def main():
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--ref-step-seconds", type=float, default=5.0, help="oracle seconds per reference step")
+    ap.add_argument("--once", action="store_true",
+                    help="run the fused kernel of the workload once and exit (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     dist, rank, world, local = dist_setup(args)
