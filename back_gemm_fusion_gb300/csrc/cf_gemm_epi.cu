@@ -253,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      // B tiles are reread by every strip: keep them in L2 ahead of the
+      // streamed output.
+      const uint64_t b_policy = l2_policy_evict_last();
       for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next()) {
         int strip, tile;
         item_coords<XMODE>(p, w, strip, tile);
@@ -269,10 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             tma_load_2d_pair(sa, &p.tmA, fbl, kb * kBK, m0);
             const int nb0 = n0 + (kBN / 2) * (int)pair_rank;  // this CTA's half of the B tile
             if (p.b_mn_major) {
-              tma_load_2d_pair(sb, &p.tmB, fbl, nb0, kb * kBK);
-              tma_load_2d_pair(sb + 64 * kBK * 2, &p.tmB, fbl, nb0 + 64, kb * kBK);
+              tma_load_2d_pair_hint(sb, &p.tmB, fbl, nb0, kb * kBK, b_policy);
+              tma_load_2d_pair_hint(sb + 64 * kBK * 2, &p.tmB, fbl, nb0 + 64, kb * kBK, b_policy);
             } else {
-              tma_load_2d_pair(sb, &p.tmB, fbl, kb * kBK, nb0);
+              tma_load_2d_pair_hint(sb, &p.tmB, fbl, kb * kBK, nb0, b_policy);
             }
           } else {
             mbar_arrive_expect_tx(fb, kStageBytes);
