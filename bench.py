@@ -35,10 +35,17 @@ from back_gemm_fusion_gb300 import inputs as I  # noqa: E402
 
 METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)"
 
-# DRAM traffic (read + write bytes per launch) of the fused kernel, from an
-# ncu capture, keyed by workload; valid only while the kernel source hash
-# matches the one the counters were taken with.
-NCU_TRAFFIC = {}
+# DRAM traffic of one fused launch (dram__bytes_read.sum, dram__bytes_write.sum)
+# from an ncu --set full capture of `bench.py --workload W --once` on a GB300,
+# keyed by workload; valid only while the kernel source hash matches the one
+# the counters were taken with (profiles/ has the summaries and commands).
+NCU_TRAFFIC = {
+    "gelu_rmsnorm": {"read": 116985856, "write": 90224128, "src": "2ba0528af4f710b2"},
+    "scaled_softmax": {"read": 1384278016, "write": 239182080, "src": "2ba0528af4f710b2"},
+    "mlp_b2b": {"read": 50442240, "write": 15169536, "src": "2ba0528af4f710b2"},
+    "attention_softmax": {"read": 805538304, "write": 496984320, "src": "2ba0528af4f710b2"},
+    "attention_relu": {"read": 805420032, "write": 494765568, "src": "2ba0528af4f710b2"},
+}
 
 
 def kernel_source_hash() -> str:
@@ -85,12 +92,19 @@ class Workload:
         c = self.case
         if self.is_b2b:
             self.flops = 2.0 * c.batch * c.M * (c.K * c.N1 + c.N1 * c.N2)
-            self.bytes = 2.0 * (c.A.numel() + c.W1.numel() + c.W2.numel()) + 4.0 * c.batch * c.M * c.N2
+            self.out_bytes = 4.0 * c.batch * c.M * c.N2
+            self.bytes = 2.0 * (c.A.numel() + c.W1.numel() + c.W2.numel()) + self.out_bytes
+            self.stat_bytes = 0.0
             self.rows = c.batch * c.M
         else:
             vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta) if t is not None)
             self.flops = 2.0 * c.M * c.N * c.K
-            self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + 4.0 * c.M * c.N
+            self.out_bytes = 4.0 * c.M * c.N
+            self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + self.out_bytes
+            # Row statistics of rows wider than one 256-column tile: 8 bytes
+            # per row per tile in the workspace (written once, read per tile).
+            has_row = any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in c.ops)
+            self.stat_bytes = 8.0 * c.M * (c.N // 256) if has_row and c.N > 256 else 0.0
             self.rows = c.M
 
     def config(self):
@@ -510,7 +524,11 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
     src = kernel_source_hash()
     tr = NCU_TRAFFIC.get(wl.name)
-    traffic = tr["bytes"] if tr and tr.get("src") == src else None
+    tr = tr if tr and tr.get("src") == src else None
+    traffic = (tr["read"] + tr["write"]) if tr else None
+    # An intermediate that went to HBM would have to be written there: DRAM
+    # writes beyond the output and the row-statistics workspace.
+    inter = max(0.0, tr["write"] - wl.out_bytes - wl.stat_bytes) if tr else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -521,7 +539,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
                      "frac": tflops / peaks["bf16_tflops"], "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst",
                      "roofline_frac": (t_roof * 1e3) / ms_step},
-        "intermediate_hbm_bytes": (None if traffic is None else max(0.0, traffic - wl.bytes)),
+        "intermediate_hbm_bytes": inter,
+        "dram_bytes": ({"read": tr["read"], "write": tr["write"], "source": "ncu, one launch"} if tr else None),
         "compulsory_bytes": wl.bytes,
         "cpu_baseline": {"value": ref_tflops, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{ref_rows} of {wl.rows} output rows (seeded), {ref_s:.1f} s"},
