@@ -190,7 +190,9 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   if (M == 0 || N == 0) return CF_OK;
   // Any M >= 1: rows past M are zero-filled by the TMA loads and clipped by
   // the TMA stores of the last (ragged) 128-row strip; rows are independent.
-  if (N % kBN != 0 || K % kBK != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
+  // K >= 64 with K % 8 == 0: the last 64-wide K block reads zeros past K
+  // (TMA out-of-bounds fill), which add nothing to the products.
+  if (N % kBN != 0 || K % 8 != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
   const int64_t tiles_n = N / kBN;
   if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)

@@ -123,6 +123,7 @@ struct Params {
   CUtensorMap tmA, tmW1, tmW2;  // 3-D: {128 cols, rows, batch}
   float* out;
   long long ldo, stride_out;
+  int M;             // rows of A per batch entry (the last 128-row block may be ragged)
   int batch, m_blocks, n1_blocks, items;
   int softmax;       // 1: scaled softmax, 0: ReLU (optionally scaled)
   float scale;       // multiplies S before F
@@ -446,9 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
         }
+        if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          dst[16 * h + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+          for (int e = 0; e < 16; ++e)
+            dst[16 * h + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        }
       }
     }
   }
@@ -496,10 +499,11 @@ struct Params {
   CUtensorMap tmW2;  // {N2, N1, batch}, box {64, 64, 1}
   float* out;
   long long ldo, stride_out;
+  int M;             // rows of A per batch entry (the last 128-row strip may be ragged)
   int w1_k_major;
   int C;             // CTAs per cluster = N2 / 256
   int ring;          // ring stages (ring_for(C))
-  int kblocks;       // K / 64
+  int kblocks;       // ceil(K / 64): the last block's columns past K are zero-filled
   int rounds;        // N1 / (128 C)
   int strips, items; // M / 128, batch * strips
   float scale;       // F(S) = max(scale S, 0)
@@ -748,8 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
         tmem_wait_ld();
         float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+        if (strip * 128 + row < p.M) {  // rows past M (ragged last strip) are not stored
 #pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -834,9 +840,10 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.C = (int)C;
   p.ring = mlp::ring_for((int)C);
-  p.kblocks = (int)(K / 64);
+  p.kblocks = (int)((K + 63) / 64);
   p.rounds = (int)(N1 / (128 * C));
-  p.strips = (int)(M / 128);
+  p.M = (int)M;
+  p.strips = (int)((M + 127) / 128);
   p.items = (int)(batch * p.strips);
   p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
   p.status = status;
@@ -897,10 +904,10 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   if (M == 0 || N2 == 0) return CF_OK;
 
   // Attention shape: W1 stored transposed (N1 x K), K = N2 = 128.
-  const bool attn_shape = W1->trans == 1 && K == 128 && N2 == 128 && N1 % 128 == 0 && N1 >= 128 && M % 128 == 0;
+  const bool attn_shape = W1->trans == 1 && K == 128 && N2 == 128 && N1 % 128 == 0 && N1 >= 128;
   // MLP shape: N2 = 256 C with C <= 4 CTAs per cluster, elementwise F only.
   const int64_t C = N2 / 256;
-  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && M % 128 == 0 && K % 64 == 0 &&
+  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 &&
                          K >= 64 && N2 % 256 == 0 && C >= 1 && C <= mlp::kMaxC && N1 % (128 * C) == 0 && N1 > 0;
   if (!attn_shape && !mlp_shape) return CF_ERR_UNSUPPORTED_SHAPE;
 
@@ -933,7 +940,8 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.batch = (int)bs;
-  p.m_blocks = (int)(M / 128);
+  p.M = (int)M;
+  p.m_blocks = (int)((M + 127) / 128);
   p.n1_blocks = (int)(N1 / 128);
   p.items = p.batch * p.m_blocks;
   p.softmax = d->mid_op == CF_MID_SCALE_SOFTMAX ? 1 : 0;

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   if (XMODE == X_CLUSTER || CTA2) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int kblocks = p.K / kBK;
+  const int kblocks = (p.K + kBK - 1) / kBK;  // the last block is zero-filled past K
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -113,6 +113,15 @@ def mlp_b2b(seed: int = 0, M: int = 16384, K: int = 1024, N1: int = 4096, N2: in
     return B2BCase("b2b_mlp_relu", 1, M, K, N1, N2, "relu", 1.0, False, X, W1, W2)
 
 
+def mlp_bottom(seed: int = 0, rows: int = 64, K: int = 512, N1: int = 128, N2: int = 256) -> B2BCase:
+    """The small-batch bottom-MLP regime of the B2BGEMM evaluation: feature
+    dims 512 -> 128 -> 256 (in the order the evaluation lists them), ReLU,
+    ``rows`` = batch in 1..64; same draws as mlp_b2b."""
+    c = mlp_b2b(seed, M=rows, K=K, N1=N1, N2=N2)
+    c.name = "b2b_mlp_bottom_relu"
+    return c
+
+
 def attention_b2b(seed: int = 0, batch: int = 32, heads: int = 16, L: int = 2048, d: int = 128,
                   op: str = "scale_softmax") -> B2BCase:
     """Q, K, V [batch*heads, L, d] ~ N(0, 1); S = Q K^T / sqrt(d); F = softmax or ReLU."""

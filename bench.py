@@ -72,7 +72,7 @@ def load_peaks():
 class Workload:
     """A fused GEMM-epilogue or B2BGEMM problem with its accounting."""
 
-    def __init__(self, name: str, seed: int = 0, exchange: str = "auto"):
+    def __init__(self, name: str, seed: int = 0, exchange: str = "auto", rows: int = 64):
         self.name = name
         self.exchange = exchange
         if name == "gelu_rmsnorm":
@@ -83,12 +83,14 @@ class Workload:
             self.case = I.scaled_softmax(seed)
         elif name == "mlp_b2b":
             self.case = I.mlp_b2b(seed)
+        elif name == "mlp_bottom":
+            self.case = I.mlp_bottom(seed, rows=rows)
         elif name in ("attention_softmax", "attention_relu"):
             op = "scale_softmax" if name == "attention_softmax" else "scale_relu"
             self.case = I.attention_b2b(seed, op=op)
         else:
             raise ValueError(name)
-        self.is_b2b = name in ("mlp_b2b", "attention_softmax", "attention_relu")
+        self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu")
         c = self.case
         if self.is_b2b:
             self.flops = 2.0 * c.batch * c.M * (c.K * c.N1 + c.N1 * c.N2)
@@ -564,7 +566,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
-                             "attention_relu"])
+                             "attention_relu", "mlp_bottom"])
+    ap.add_argument("--rows", type=int, default=64, help="batch rows of the mlp_bottom workload (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
@@ -574,7 +577,7 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     dist, rank, world, local = dist_setup(args)
-    wl = Workload(args.workload, exchange=args.exchange)
+    wl = Workload(args.workload, exchange=args.exchange, rows=args.rows)
     if args.impl == "reference":
         run_reference(args, wl, dist, rank, world)
     else:

@@ -131,8 +131,8 @@ typedef struct {
  *          are scratch; concurrent calls must use distinct workspaces.
  *
  * Shape rules (this version): any M >= 0 (a ragged last 128-row strip is
- * handled), N % 256 == 0, K % 64 == 0, K >= 64, all pointers and leading
- * dims 16-byte aligned.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
+ * handled), N % 256 == 0, K % 8 == 0 with K >= 64 (a ragged last 64-wide K
+ * block reads zeros), all pointers and leading dims 16-byte aligned.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
  * CF_ERR_MISALIGNED without launching anything.  M == 0 or N == 0 returns
  * CF_OK without launching.
  */
@@ -207,9 +207,14 @@ typedef struct {
  *   out : M x N2 fp32, trans == 0.
  *   The softmax mid op normalises each row of S over all N1 columns.
  *
- * Shape rules (this version): M % 128 == 0, K % 64 == 0, N1 % 128 == 0,
- * N2 % 64 == 0 with N2 <= 256 for the softmax op (one CTA holds the whole
- * output row block) and N2 % 256 == 0 otherwise.
+ * Shape rules (this version), two kernels:
+ *   attention shape: W1 given transposed (trans == 1), K == N2 == 128,
+ *     N1 % 128 == 0; any mid op (the softmax normalises over all N1);
+ *   MLP shape: mid op ReLU or scaled ReLU, K % 8 == 0 with K >= 64,
+ *     N2 == 256 C with C <= 4 CTAs per cluster, N1 % (128 C) == 0.
+ *   Both: any M >= 0 (a ragged last 128-row block is handled), pointers and
+ *   leading dims 16-byte aligned.  Other shapes return
+ *   CF_ERR_UNSUPPORTED_SHAPE without launching anything.
  */
 CF_API cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
                      const cf_b2b_desc* desc, cf_matrix* out, void* stream);

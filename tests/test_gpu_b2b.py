@@ -105,6 +105,25 @@ def test_attention_full_size_sampled(cf, op):
         b2b_gate(got[h][rows], ref, _abs_bound(q[rows], k, v, op, case.scale), f"attention {op} head {h}")
 
 
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("Lq", [1, 77, 200])
+def test_attention_ragged_queries(cf, Lq, op):
+    # Fewer (or not a multiple of 128) query rows than keys: the last query
+    # block is zero-filled on load and its rows past Lq are not stored.
+    rng = np.random.default_rng(Lq)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    Q = t(rng.standard_normal((2, Lq, 128)))
+    K = t(rng.standard_normal((2, 256, 128)))
+    V = t(rng.standard_normal((2, 256, 128)))
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, op, scale)
+    assert got.shape == (2, Lq, 128)
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} Lq={Lq} b={b}")
+
+
 def test_attention_zero_keys_column_mean(cf):
     # Q K^T == 0 -> P = 1/L exactly -> O = column mean of V (closed form).
     L = 2048
@@ -140,6 +159,25 @@ def test_mlp_small(cf, M, K, N1, N2, op, scale, w1_trans):
     ref = O.b2bgemm(x, w1, w2, op, scale)
     bound = np.abs(O.mid_op(x @ w1, op, scale)) @ np.abs(w2)
     b2b_gate(out.cpu().numpy(), ref, bound, f"mlp {op} {M}x{K}x{N1}x{N2} trans={w1_trans}")
+
+
+@pytest.mark.parametrize("w1_trans", [False, True])
+@pytest.mark.parametrize("M,K,N1,N2", [(1, 512, 128, 256), (8, 512, 128, 256), (64, 512, 128, 256),
+                                       (77, 200, 512, 256), (300, 72, 1024, 1024)])
+def test_mlp_ragged(cf, M, K, N1, N2, w1_trans):
+    # Ragged M (the last 128-row strip is partial: zero-filled loads, rows
+    # past M not stored) and K not a multiple of 64 (the last K block reads
+    # zeros); the first three are the bottom-MLP shape 512 -> 128 -> 256 at
+    # batch 1, 8 and 64.
+    X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M * 7 + K)
+    W1d = W1.t().contiguous().cuda() if w1_trans else W1.cuda()
+    out = cf.cf_b2bgemm(X.cuda(), W1d, W2.cuda(), "relu", 1.0, w1_trans=w1_trans)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu", 1.0)
+    bound = np.abs(O.mid_op(x @ w1, "relu", 1.0)) @ np.abs(w2)
+    b2b_gate(out.cpu().numpy(), ref, bound, f"mlp ragged {M}x{K}x{N1}x{N2} trans={w1_trans}")
 
 
 def test_mlp_full_size_sampled(cf):

@@ -100,6 +100,20 @@ def test_ragged_m(cf, M, rowop):
                       what=f"ragged M={M} {rowop}")
 
 
+@pytest.mark.parametrize("b_trans", [False, True])
+@pytest.mark.parametrize("M,K,rowop", [(128, 72, "none"), (256, 200, "layernorm"), (384, 1000, "rmsnorm"),
+                                       (333, 136, "softmax")])
+def test_ragged_k(cf, M, K, rowop, b_trans):
+    # K not a multiple of the 64-wide K block: the last block reads zeros.
+    ops = {"none": [("bias",), ("relu",)], "layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.125), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case("ragged_k", M, 512, K, ops, seed=M + K, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, b_trans), _oracle(case), strict=1e-4 if rowop == "none" else 2e-3,
+                      what=f"ragged K={K} M={M} {rowop} b_trans={b_trans}")
+
+
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
     # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;
