@@ -28,7 +28,9 @@ written out:
 
 1. P = A . B, summed exactly enough in float64 (no bf16 rounding of P: the
    kernels accumulate in fp32 and never round P).
-2. Elementwise ops in descriptor order (bias, scale, ReLU, tanh-GELU).
+2. Elementwise ops in descriptor order (bias, scale, ReLU, tanh-GELU, and
+   the residual add x + R[m, n] of the "post-norm" MatMul + Add + norm
+   subgraphs the evaluation fuses).
 3. At most one trailing row reduction (LayerNorm, RMSNorm, softmax).
 4. For B2BGEMM the single rounding point is the intermediate S' = F(S), which
    is rounded to bfloat16 round-to-nearest-even before the second GEMM.
@@ -152,15 +154,21 @@ def _gelu_tanh(x: np.ndarray) -> np.ndarray:
     return 0.5 * x * (1.0 + np.tanh(c * (x + 0.044715 * x ** 3)))
 
 
-def elementwise(x: np.ndarray, op: str, scalar: float = 0.0, bias=None) -> np.ndarray:
+def elementwise(x: np.ndarray, op: str, scalar: float = 0.0, bias=None, residual=None) -> np.ndarray:
     """One elementwise epilogue node, applied per element of a row strip.
 
-    ``bias`` adds bias[n] along the column index; ``scale`` multiplies by the
-    scalar; ``relu`` is max(x, 0); ``gelu_tanh`` is the tanh approximation of
-    GELU.
+    ``bias`` adds bias[n] along the column index; ``residual`` adds the
+    matrix R[m, n] of the same shape (the residual stream of a post-norm
+    block); ``scale`` multiplies by the scalar; ``relu`` is max(x, 0);
+    ``gelu_tanh`` is the tanh approximation of GELU.
     """
     if op == "bias":
         return x + np.asarray(bias, dtype=np.float64)[None, :]
+    if op == "residual":
+        r = np.asarray(residual, dtype=np.float64)
+        if r.shape != x.shape:
+            raise ValueError("the residual must have the shape of the GEMM output")
+        return x + r
     if op == "scale":
         return x * float(scalar)
     if op == "relu":
@@ -200,7 +208,7 @@ def row_softmax(x) -> np.ndarray:
 _ROW_OPS = ("layernorm", "rmsnorm", "softmax")
 
 
-def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta) -> np.ndarray:
+def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta, residual=None) -> np.ndarray:
     """Run an epilogue program: elementwise nodes, at most one trailing row op.
 
     ``ops`` is a sequence of ``(name,)`` or ``(name, scalar)`` tuples; the
@@ -220,16 +228,17 @@ def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta) -> np.ndarray:
         elif name == "softmax":
             x = row_softmax(x)
         else:
-            x = elementwise(x, name, scalar, bias)
+            x = elementwise(x, name, scalar, bias, residual)
     return x
 
 
-def gemm_epilogue(A, B, ops: Iterable[tuple], bias=None, gamma=None, beta=None) -> np.ndarray:
+def gemm_epilogue(A, B, ops: Iterable[tuple], bias=None, gamma=None, beta=None, residual=None) -> np.ndarray:
     """GEMM followed by an epilogue program, all in float64.
 
-    A: M x K, B: K x N (row-major, bf16 values as float64).  Returns M x N.
+    A: M x K, B: K x N (row-major, bf16 values as float64); ``residual``
+    (M x N) is read by the ``residual`` op.  Returns M x N.
     """
-    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta)
+    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta, residual)
 
 
 def mid_op(S, op: str, scale: float = 1.0) -> np.ndarray:

@@ -53,6 +53,34 @@ def test_hand_example_b2b_relu_exact():
     assert O_.tolist() == h["b2b_relu_out"]
 
 
+def test_hand_example_residual():
+    # Residual add: exact integer sums (R is not symmetric, so a transposed
+    # or misindexed residual fails), then RMSNorm of the sum.
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    R = np.array(h["R"], float)
+    assert O.gemm_epilogue(A, B, [("residual",)], residual=R).tolist() == h["P_plus_R"]
+    exp = np.array([[_closed(v) for v in row] for row in h["residual_rmsnorm_eps0"]], float)
+    got = O.gemm_epilogue(A, B, [("residual",), ("rmsnorm", 0.0)], gamma=np.ones(4), residual=R)
+    np.testing.assert_allclose(got, exp, rtol=0, atol=1e-12)
+
+
+def test_residual_order_in_program():
+    # With R = -P - 1, residual-then-ReLU is all zeros, while ReLU-then-residual
+    # is relu(P) - P - 1: the node order of the program is respected.
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    P = np.array(h["P"], float)
+    R = -P - 1.0
+    assert np.all(O.gemm_epilogue(A, B, [("residual",), ("relu",)], residual=R) == 0.0)
+    got = O.gemm_epilogue(A, B, [("relu",), ("residual",)], residual=R)
+    assert got.tolist() == (np.maximum(P, 0.0) - P - 1.0).tolist()
+    with pytest.raises(ValueError):
+        O.gemm_epilogue(A, B, [("residual",)], residual=R.T)
+
+
 def _closed(expr: str) -> float:
     """Evaluate a closed form written in the golden file (sqrt, exp, tanh only)."""
     return float(eval(expr, {"__builtins__": {}},
