@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "CF_OK", 1: "CF_ERR_INVALID_ARG", 2: "CF_ERR_UNSUPPORTED_SHAP
                 4: "CF_ERR_UNSUPPORTED_DEVICE", 5: "CF_ERR_CUDA", 6: "CF_ERR_TIMEOUT", 7: "CF_ERR_WORKSPACE",
                 8: "CF_ERR_NO_DEVICE"}
 CF_BF16, CF_FP32 = 0, 1
-OP_CODES = {"bias": 1, "scale": 2, "relu": 3, "gelu_tanh": 4, "layernorm": 16, "rmsnorm": 17, "softmax": 18}
+OP_CODES = {"bias": 1, "scale": 2, "relu": 3, "gelu_tanh": 4, "residual": 5, "layernorm": 16, "rmsnorm": 17,
+            "softmax": 18}
 MID_CODES = {"relu": 1, "scale_relu": 2, "scale_softmax": 3}
 EXCHANGE_CODES = {"auto": 0, "cluster": 1, "global": 2}
 EPI_MAX_OPS = 8
@@ -41,7 +42,7 @@ class cf_op(ctypes.Structure):
 
 class cf_epi_desc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("n_ops", ctypes.c_uint32), ("ops", cf_op * EPI_MAX_OPS),
-                ("out_dtype", ctypes.c_int32), ("exchange", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("exchange", ctypes.c_int32), ("residual", cf_matrix)]
 
 
 class cf_b2b_desc(ctypes.Structure):
@@ -118,9 +119,10 @@ def matrix(t: torch.Tensor, trans: bool = False) -> cf_matrix:
     return cf_matrix(t.data_ptr(), _dtype_code(t), 1 if trans else 0, rows, cols, max(t.stride(0), 1))
 
 
-def epi_desc(ops: Sequence[Tuple], exchange: str = "auto") -> cf_epi_desc:
+def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[torch.Tensor] = None) -> cf_epi_desc:
+    """Descriptor (version 2); ``residual`` is the M x N matrix read by the ``residual`` op."""
     d = cf_epi_desc()
-    d.version = 1
+    d.version = 2
     d.n_ops = len(ops)
     if len(ops) > EPI_MAX_OPS:
         raise ValueError("too many epilogue ops")
@@ -129,6 +131,8 @@ def epi_desc(ops: Sequence[Tuple], exchange: str = "auto") -> cf_epi_desc:
         d.ops[i].scalar = float(op[1]) if len(op) > 1 else 0.0
     d.out_dtype = CF_FP32
     d.exchange = EXCHANGE_CODES[exchange]
+    if residual is not None:
+        d.residual = matrix(residual)
     return d
 
 
@@ -157,15 +161,17 @@ def cf_workspace_size(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], b_
 
 def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bias=None, gamma=None, beta=None,
                      out: Optional[torch.Tensor] = None, b_trans: bool = False, exchange: str = "auto",
-                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                     workspace: Optional[torch.Tensor] = None, stream=None,
+                     residual: Optional[torch.Tensor] = None) -> torch.Tensor:
     """out = epilogue(A @ B) in one fused kernel.  ``B`` is K x N, or N x K
-    with ``b_trans=True``.  A workspace is allocated if needed and not given."""
+    with ``b_trans=True``; ``residual`` (M x N, fp32 or bf16) feeds the
+    ``residual`` op.  A workspace is allocated if needed and not given."""
     lib = load_library()
     M = A.shape[0]
     N = B.shape[0] if b_trans else B.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange)
+    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange, residual)
     need = int(lib.cf_workspace_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
@@ -179,7 +185,8 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
 
 def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bias=None, gamma=None,
                              beta=None, out: Optional[torch.Tensor] = None, b_trans: bool = False,
-                             exchange: str = "auto", stream=None) -> torch.Tensor:
+                             exchange: str = "auto", stream=None,
+                             residual: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Same as cf_gemm_epilogue, but the library takes any scratch it needs
     from its own static device array: nothing is allocated by this call
     (``out`` must be given by callers that cannot allocate)."""
@@ -188,7 +195,7 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
         M = A.shape[0]
         N = B.shape[0] if b_trans else B.shape[1]
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange)
+    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange, residual)
     st = lib.cf_gemm_epilogue_noalloc(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _stream(stream))
     _check(st, "cf_gemm_epilogue_noalloc")
@@ -234,7 +241,7 @@ def cf_b2bgemm(A: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, op: str, sca
 
 
 def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=None, b_trans=False,
-                             intermediate=None, stream=None):
+                             intermediate=None, stream=None, residual=None):
     """Comparison path: cuBLASLt GEMM to an fp32 intermediate, then a separate epilogue kernel."""
     lib = load_library()
     M = A.shape[0]
@@ -243,7 +250,7 @@ def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=No
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if intermediate is None:
         intermediate = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops)
+    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, residual=residual)
     st = lib.cf_unfused_gemm_epilogue(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _ptr(intermediate), _stream(stream))
     _check(st, "cf_unfused_gemm_epilogue")

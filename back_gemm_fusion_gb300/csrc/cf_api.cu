@@ -121,17 +121,21 @@ struct EpiPlan {
   int n_elem = 0;
   int kinds[CF_EPI_MAX_OPS] = {};
   float scalars[CF_EPI_MAX_OPS] = {};
-  bool need_bias = false, need_gamma = false, need_beta = false;
+  bool need_bias = false, need_gamma = false, need_beta = false, need_residual = false;
 };
 
 cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
-  if (!epi || epi->version != CF_EPI_VERSION || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if (!epi || (epi->version != 1 && epi->version != 2) || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
   if (epi->exchange < CF_XCHG_AUTO || epi->exchange > CF_XCHG_GLOBAL) return CF_ERR_INVALID_ARG;
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
     const cf_op& op = epi->ops[i];
     if (!std::isfinite(op.scalar)) return CF_ERR_INVALID_ARG;
     switch (op.kind) {
       case CF_OP_BIAS: plan->need_bias = true; break;
+      case CF_OP_ADD_RESIDUAL:
+        if (epi->version < 2) return CF_ERR_INVALID_ARG;  // the residual view exists from version 2
+        plan->need_residual = true;
+        break;
       case CF_OP_SCALE: case CF_OP_RELU: case CF_OP_GELU_TANH: break;
       case CF_OP_ROW_LAYERNORM: case CF_OP_ROW_RMSNORM: case CF_OP_ROW_SOFTMAX:
         if (i + 1 != epi->n_ops) return CF_ERR_INVALID_ARG;  // a reduction ends the program
@@ -184,6 +188,12 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
     return CF_ERR_INVALID_ARG;
   if ((bias && !aligned16(bias)) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
     return CF_ERR_MISALIGNED;
+  if (plan->need_residual) {
+    const cf_matrix& r = epi->residual;
+    if (!r.ptr || r.trans || r.rows != M || r.cols != N || r.ld < N || (r.dtype != CF_FP32 && r.dtype != CF_BF16))
+      return CF_ERR_INVALID_ARG;
+    if (!aligned16(r.ptr) || (r.ld * (r.dtype == CF_FP32 ? 4 : 2)) % 16 != 0) return CF_ERR_MISALIGNED;
+  }
   sh->M = M;
   sh->N = N;
   sh->K = K;
@@ -315,6 +325,11 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   p.bias = bias;
   p.gamma = gamma;
   p.beta = beta;
+  if (plan.need_residual) {
+    p.res = epi->residual.ptr;
+    p.res_ld = epi->residual.ld;
+    p.res_bf16 = epi->residual.dtype == CF_BF16 ? 1 : 0;
+  }
   p.status = dev->status;
   p.timeout_cycles = wait_timeout_cycles();
 

@@ -65,7 +65,7 @@ struct Geo {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum OpKind : int { OP_BIAS = 1, OP_SCALE = 2, OP_RELU = 3, OP_GELU_TANH = 4 };
+enum OpKind : int { OP_BIAS = 1, OP_SCALE = 2, OP_RELU = 3, OP_GELU_TANH = 4, OP_ADD_RESIDUAL = 5 };
 
 __device__ __forceinline__ float gelu_tanh(float x) {
   // 0.5 x (1 + tanh(u)) == x * sigmoid(2u) == x / (1 + exp(-2u)),
@@ -75,10 +75,42 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 
 // Apply the elementwise program to 32 consecutive columns starting at n.
-__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n) {
+// Elementwise program on 32 consecutive columns n.. of row m of the tile.
+__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m) {
   for (int o = 0; o < p.n_ops; ++o) {
     const int kind = p.op_kind[o];
-    if (kind == OP_BIAS) {
+    if (kind == OP_ADD_RESIDUAL) {
+      // Each thread owns one row: 128 (fp32) or 64 (bf16) contiguous bytes of
+      // the residual row, read with 16-byte loads.  Rows past M (a ragged
+      // last strip) are never stored, so they skip the read.
+      if (m < p.M) {
+        if (p.res_bf16) {
+          const uint4* r4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.res) +
+                                                           (long long)m * p.res_ld + n);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 w = __ldg(r4 + j);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * j + 2 * e] += __uint_as_float(ww[e] << 16);
+              v[8 * j + 2 * e + 1] += __uint_as_float(ww[e] & 0xffff0000u);
+            }
+          }
+        } else {
+          const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.res) +
+                                                             (long long)m * p.res_ld + n);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 r = __ldg(r4 + j);
+            v[4 * j + 0] += r.x;
+            v[4 * j + 1] += r.y;
+            v[4 * j + 2] += r.z;
+            v[4 * j + 3] += r.w;
+          }
+        }
+      }
+    } else if (kind == OP_BIAS) {
       const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -378,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           tmem_ld32(taddr + c * 32, v);
           tmem_wait_ld();
           if (p.n_ops > 0) {
-            apply_program(p, v, n0 + c * 32);
+            apply_program(p, v, n0 + c * 32, m0 + row);
             tmem_st32(taddr + c * 32, v);
           }
 #pragma unroll
@@ -480,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         tmem_wait_ld();
         const int n = n0 + c * 32;
         if (ROWOP == ROW_NONE) {
-          apply_program(p, v, n);
+          apply_program(p, v, n, m0 + row);
         } else if (ROWOP == ROW_SOFTMAX) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;

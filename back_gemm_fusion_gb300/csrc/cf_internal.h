@@ -39,6 +39,9 @@ struct GemmEpiParams {
   const float* bias;
   const float* gamma;
   const float* beta;
+  const void* res;        // residual matrix (CF_OP_ADD_RESIDUAL), M x N, leading dim res_ld
+  long long res_ld;
+  int res_bf16;           // 1: bf16 residual, 0: fp32
   float2* ws_stats;       // [strips][tiles_n][kBM] partial row statistics
   unsigned* ws_count;     // [strips][4] arrival counters (cleared by the host)
   unsigned* status;       // device status word

@@ -111,10 +111,27 @@ struct RowProgram {
   float eps;
 };
 
-__device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* bias, int n) {
+// The CF_OP_ADD_RESIDUAL matrix (fp32 or bf16) of a program; passed to the
+// kernels apart from RowProgram so that the program stays in parameter space.
+struct ResView {
+  const void* ptr;
+  long long ld;
+  int bf16;
+};
+
+// Residual value of element (m, n) (0 when the program has no residual op).
+__device__ __forceinline__ float res_at(const void* res, long long ld, int bf16, int m, int n) {
+  if (!res) return 0.0f;
+  return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(res)[(long long)m * ld + n])
+              : static_cast<const float*>(res)[(long long)m * ld + n];
+}
+
+// Elementwise program for element (m, n); `r` is residual[m][n].
+__device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* bias, int n, float r) {
   for (int o = 0; o < pg.n_ops; ++o) {
     switch (pg.kind[o]) {
       case CF_OP_BIAS: x += bias[n]; break;
+      case CF_OP_ADD_RESIDUAL: x += r; break;
       case CF_OP_SCALE: x *= pg.scalar[o]; break;
       case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
       case CF_OP_GELU_TANH: x = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x))); break;
@@ -145,14 +162,17 @@ __global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restri
                                                            float* __restrict__ out, int64_t ldo, int N,
                                                            RowProgram pg, const float* __restrict__ bias,
                                                            const float* __restrict__ gamma,
-                                                           const float* __restrict__ beta) {
+                                                           const float* __restrict__ beta, ResView rv) {
   extern __shared__ float row[];
   __shared__ float red[32];
+  const void* res = rv.ptr;
+  const long long res_ld = rv.ld;
+  const int res_bf16 = rv.bf16;
   const float* p = P + (int64_t)blockIdx.x * ldp;
   float* o = out + (int64_t)blockIdx.x * ldo;
   float acc = 0.0f, mx = -INFINITY;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const float x = ew(pg, p[n], bias, n);
+    const float x = ew(pg, p[n], bias, n, res_at(res, res_ld, res_bf16, (int)blockIdx.x, n));
     row[n] = x;
     acc += x;
     mx = fmaxf(mx, x);
@@ -192,8 +212,11 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
                                                                float* __restrict__ out, int64_t ldo, int N,
                                                                RowProgram pg, const float* __restrict__ bias,
                                                                const float* __restrict__ gamma,
-                                                               const float* __restrict__ beta) {
+                                                               const float* __restrict__ beta, ResView rv) {
   __shared__ float red[32];
+  const void* res = rv.ptr;
+  const long long res_ld = rv.ld;
+  const int res_bf16 = rv.bf16;
   const float4* p = reinterpret_cast<const float4*>(P + (int64_t)blockIdx.x * ldp);
   float4* o = reinterpret_cast<float4*>(out + (int64_t)blockIdx.x * ldo);
   float4 v[VPT];
@@ -201,10 +224,10 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
   for (int i = 0; i < VPT; ++i) {
     const int c = i * 256 + threadIdx.x;  // float4 index
     float4 x = p[c];
-    x.x = ew(pg, x.x, bias, 4 * c);
-    x.y = ew(pg, x.y, bias, 4 * c + 1);
-    x.z = ew(pg, x.z, bias, 4 * c + 2);
-    x.w = ew(pg, x.w, bias, 4 * c + 3);
+    x.x = ew(pg, x.x, bias, 4 * c, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c));
+    x.y = ew(pg, x.y, bias, 4 * c + 1, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 1));
+    x.z = ew(pg, x.z, bias, 4 * c + 2, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 2));
+    x.w = ew(pg, x.w, bias, 4 * c + 3, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 3));
     v[i] = x;
   }
   float mul = 1.0f, add = 0.0f;  // y = (x * mul + add) [* gamma + beta]
@@ -340,7 +363,7 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   if (!A || !B || !epi || !out || !intermediate || !A->ptr || !B->ptr || !out->ptr) return CF_ERR_INVALID_ARG;
   if (A->dtype != CF_BF16 || B->dtype != CF_BF16 || out->dtype != CF_FP32 || A->trans || out->trans)
     return CF_ERR_INVALID_ARG;
-  if (epi->version != CF_EPI_VERSION || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if ((epi->version != 1 && epi->version != 2) || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
   const int64_t M = A->rows, K = A->cols, N = B->cols;
   if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return CF_OK;
@@ -348,8 +371,18 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   if (!aligned16(A->ptr) || !aligned16(B->ptr) || !aligned16(intermediate)) return CF_ERR_MISALIGNED;
   RowProgram pg;
   std::memset(&pg, 0, sizeof(pg));
+  ResView rv = {nullptr, 0, 0};
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
     const int k = epi->ops[i].kind;
+    if (k == CF_OP_ADD_RESIDUAL) {
+      const cf_matrix& r = epi->residual;
+      if (epi->version < 2 || !r.ptr || r.trans || r.rows != M || r.cols != N || r.ld < N ||
+          (r.dtype != CF_FP32 && r.dtype != CF_BF16))
+        return CF_ERR_INVALID_ARG;
+      rv.ptr = r.ptr;
+      rv.ld = r.ld;
+      rv.bf16 = r.dtype == CF_BF16;
+    }
     if (k >= CF_OP_ROW_LAYERNORM) {
       if (i + 1 != epi->n_ops) return CF_ERR_INVALID_ARG;
       pg.rowop = k;
@@ -368,18 +401,18 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   const bool vec = N % 1024 == 0 && (out->ld % 4) == 0 && aligned16(out->ptr) && (!bias || aligned16(bias)) &&
                    (!gamma || aligned16(gamma)) && (!beta || aligned16(beta));
   switch (vec ? N / 1024 : 0) {
-    case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
-    case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
-    case 4: row_epilogue_reg_kernel<4><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
-    case 8: row_epilogue_reg_kernel<8><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
-    case 16: row_epilogue_reg_kernel<16><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta); break;
+    case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
+    case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
+    case 4: row_epilogue_reg_kernel<4><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
+    case 8: row_epilogue_reg_kernel<8><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
+    case 16: row_epilogue_reg_kernel<16><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
     default: {
       const size_t smem = (size_t)N * sizeof(float);
       if (smem > 48 * 1024 &&
           cudaFuncSetAttribute(row_epilogue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
               cudaSuccess)
         return CF_ERR_CUDA;
-      row_epilogue_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta);
+      row_epilogue_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv);
     }
   }
   return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;

@@ -44,6 +44,7 @@ class GemmEpilogueCase:
     bias: Optional[torch.Tensor] = None
     gamma: Optional[torch.Tensor] = None
     beta: Optional[torch.Tensor] = None
+    residual: Optional[torch.Tensor] = None  # M x N, read by the ("residual",) op
     meta: Dict = field(default_factory=dict)
 
 
@@ -65,6 +66,18 @@ def gemm_epilogue_case(name: str, M: int, N: int, K: int, ops: List[Tuple], seed
 
 
 # The three GEMM + epilogue workloads, by what they are.
+def postnorm_layernorm(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 4096) -> GemmEpilogueCase:
+    """Post-norm block: GEMM + bias + residual add + row LayerNorm (eps 1e-5),
+    fp32 out; the residual stream R ~ N(0, 1) is bf16 and drawn after the
+    vectors."""
+    c = gemm_epilogue_case("gemm_bias_residual_layernorm", M, N, K,
+                           [("bias",), ("residual",), ("layernorm", 1e-5)], seed,
+                           need_bias=True, need_gamma=True, need_beta=True)
+    rng = np.random.default_rng([seed, 1])
+    c.residual = _bf16(rng.standard_normal((M, N)))
+    return c
+
+
 def layernorm_256(seed: int = 0, M: int = 256, N: int = 256, K: int = 256) -> GemmEpilogueCase:
     """GEMM + bias + row LayerNorm (eps 1e-5), fp32 out; 256^3 by default."""
     return gemm_epilogue_case("gemm_bias_layernorm", M, N, K,

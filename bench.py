@@ -81,6 +81,8 @@ class Workload:
             self.case = I.layernorm_256(seed)
         elif name == "scaled_softmax":
             self.case = I.scaled_softmax(seed)
+        elif name == "postnorm_layernorm":
+            self.case = I.postnorm_layernorm(seed)
         elif name == "mlp_b2b":
             self.case = I.mlp_b2b(seed)
         elif name == "mlp_bottom":
@@ -102,7 +104,8 @@ class Workload:
             vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta) if t is not None)
             self.flops = 2.0 * c.M * c.N * c.K
             self.out_bytes = 4.0 * c.M * c.N
-            self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + self.out_bytes
+            res = 0.0 if c.residual is None else float(c.residual.numel() * c.residual.element_size())
+            self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + res + self.out_bytes
             # Row statistics of rows wider than one 256-column tile: 8 bytes
             # per row per tile in the workspace (written once, read per tile).
             has_row = any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in c.ops)
@@ -126,7 +129,7 @@ class Workload:
             dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=torch.float32, device="cuda")
         else:
             dev["A"], dev["B"] = c.A.cuda(), c.B.cuda()
-            for k in ("bias", "gamma", "beta"):
+            for k in ("bias", "gamma", "beta", "residual"):
                 t = getattr(c, k)
                 dev[k] = None if t is None else t.cuda()
             dev["out"] = torch.empty((c.M, c.N), dtype=torch.float32, device="cuda")
@@ -142,7 +145,8 @@ class Workload:
             cf.cf_b2bgemm(A, W1, W2, c.op, c.scale, w1_trans=c.w1_k_major, out=out, stream=stream)
         else:
             cf.cf_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
-                                out=dev["out"], workspace=workspace, stream=stream, exchange=self.exchange)
+                                out=dev["out"], workspace=workspace, stream=stream, exchange=self.exchange,
+                                residual=dev["residual"])
 
     def unfused_step(self, cf, dev, scratch, stream=None):
         c = self.case
@@ -157,7 +161,8 @@ class Workload:
                                   stream=stream)
         else:
             cf.cf_unfused_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
-                                        out=dev["out"], intermediate=scratch, stream=stream)
+                                        out=dev["out"], intermediate=scratch, stream=stream,
+                                        residual=dev["residual"])
 
     def unfused_scratch(self):
         c = self.case
@@ -189,7 +194,9 @@ class Workload:
                 O.b2bgemm(A, W1, I.to_f64(c.W2[b]), c.op, c.scale)
             return 2.0 * len(rows) * (c.K * c.N1 + c.N1 * c.N2)
         A = self._f64("A")[rows]
-        O.gemm_epilogue(A, self._f64("B"), c.ops, self._f64("bias"), self._f64("gamma"), self._f64("beta"))
+        R = None if c.residual is None else self._f64("residual")[rows]
+        O.gemm_epilogue(A, self._f64("B"), c.ops, self._f64("bias"), self._f64("gamma"), self._f64("beta"),
+                        residual=R)
         return 2.0 * len(rows) * c.N * c.K
 
 
@@ -496,7 +503,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     # call, device -> pinned host output, all inside the timed region.
     c = wl.case
     host_in = []
-    names = ("A", "W1", "W2") if wl.is_b2b else ("A", "B", "bias", "gamma", "beta")
+    names = ("A", "W1", "W2") if wl.is_b2b else ("A", "B", "bias", "gamma", "beta", "residual")
     for k in names:
         t = getattr(c, k)
         if t is not None:
@@ -566,7 +573,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
-                             "attention_relu", "mlp_bottom"])
+                             "attention_relu", "mlp_bottom", "postnorm_layernorm"])
     ap.add_argument("--rows", type=int, default=64, help="batch rows of the mlp_bottom workload (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")

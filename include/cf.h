@@ -85,6 +85,7 @@ typedef enum {
   CF_OP_SCALE = 2,           /* x *= scalar                                         */
   CF_OP_RELU = 3,            /* x = max(x, 0)                                       */
   CF_OP_GELU_TANH = 4,       /* x = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))  */
+  CF_OP_ADD_RESIDUAL = 5,    /* x += residual[m][n] (descriptor version 2)          */
   CF_OP_ROW_LAYERNORM = 16,  /* y = gamma[n] (x - mean) / sqrt(var + scalar) + beta[n], biased var */
   CF_OP_ROW_RMSNORM = 17,    /* y = gamma[n] x / sqrt(mean(x^2) + scalar)           */
   CF_OP_ROW_SOFTMAX = 18     /* y = exp(x - max) / sum(exp(x - max))                */
@@ -95,7 +96,7 @@ typedef struct {
   float scalar;  /* the scale for CF_OP_SCALE, eps for the norms, unused otherwise */
 } cf_op;
 
-#define CF_EPI_VERSION 1
+#define CF_EPI_VERSION 2  /* version 1 (no residual field) is still accepted */
 #define CF_EPI_MAX_OPS 8
 
 /* Row-statistics exchange used when a row spans several CTAs. */
@@ -108,11 +109,16 @@ typedef enum {
 /* A tiny epilogue program: a linear chain of ops (the Stage-Stream model with
  * one trailing reduction stage). */
 typedef struct {
-  uint32_t version;  /* must be CF_EPI_VERSION */
+  uint32_t version;  /* 1 or 2 (CF_EPI_VERSION); version 1 ends after `exchange` */
   uint32_t n_ops;    /* 0..CF_EPI_MAX_OPS */
   cf_op ops[CF_EPI_MAX_OPS];
   int32_t out_dtype; /* cf_dtype of `out`; CF_FP32 in this version */
   int32_t exchange;  /* cf_exchange */
+  /* Version 2: the matrix read by CF_OP_ADD_RESIDUAL (the residual stream of
+   * a post-norm block): M x N, fp32 or bf16, trans == 0, pointer and leading
+   * dim 16-byte aligned, caller-owned.  Ignored (may be all zero) when the
+   * program has no CF_OP_ADD_RESIDUAL; the fused kernel reads it once. */
+  cf_matrix residual;
 } cf_epi_desc;
 
 /*

@@ -110,3 +110,29 @@ def test_workspace_size(lib):
     assert n < 3 * 2 ** 20
     d2 = epi_desc([("bias",)])
     assert lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(d2)) == 0
+
+
+def test_residual_validation(lib):
+    from back_gemm_fusion_gb300.binding import cf_matrix, epi_desc, CF_FP32, CF_BF16
+    A, B, O = _mats()
+    POST = [("bias",), ("residual",), ("layernorm", 1e-5)]
+
+    def call(residual, version=2):
+        d = epi_desc(POST)
+        d.version = version
+        if residual is not None:
+            d.residual = residual
+        return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                    ctypes.byref(O), None, 0, None)
+
+    assert call(None) == 1                                              # residual op without a residual
+    assert call(cf_matrix(0x70000, CF_FP32, 0, 256, 128, 256)) == 1     # wrong shape
+    assert call(cf_matrix(0x70000, CF_FP32, 1, 256, 256, 256)) == 1     # transposed view
+    assert call(cf_matrix(0x70008, CF_FP32, 0, 256, 256, 256)) == 3     # misaligned pointer
+    assert call(cf_matrix(0x70000, CF_BF16, 0, 256, 256, 260)) == 3     # leading dim not 16-byte aligned
+    assert call(cf_matrix(0x70000, CF_FP32, 0, 256, 256, 256), version=1) == 1  # version 1 has no residual
+    assert call(cf_matrix(0x70000, CF_BF16, 0, 256, 256, 256)) in (0, 4, 8)    # valid: device check follows
+    d = epi_desc(LN)
+    d.version = 1                                                       # version-1 descriptors still accepted
+    assert lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                ctypes.byref(O), None, 0, None) in (0, 4, 8)

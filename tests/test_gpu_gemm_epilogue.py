@@ -114,6 +114,31 @@ def test_ragged_k(cf, M, K, rowop, b_trans):
                       what=f"ragged K={K} M={M} {rowop} b_trans={b_trans}")
 
 
+@pytest.mark.parametrize("res_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K,prog", [(256, 512, 128, "layernorm"), (333, 1024, 256, "rmsnorm"),
+                                        (256, 4352, 128, "softmax"), (200, 256, 64, "none"),
+                                        (512, 2048, 256, "layernorm")])
+def test_residual_postnorm(cf, M, N, K, prog, res_dtype):
+    # Post-norm blocks: the residual stream is added in the epilogue before the
+    # row reduction (fp32 or bf16 residual; ragged M; cluster and workspace
+    # exchanges; 1-CTA and CTA-pair tiles).
+    ops = {"layernorm": [("bias",), ("residual",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("residual",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.25), ("residual",), ("softmax",)],
+           "none": [("residual",), ("relu",), ("residual",)]}[prog]
+    case = I.gemm_epilogue_case("residual", M, N, K, ops, seed=M + N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    R = torch.from_numpy(np.random.default_rng(M * 3 + N).standard_normal((M, N)).astype(np.float32)).to(res_dtype)
+    out = cf.cf_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma),
+                              _dev(case.beta), residual=R.cuda())
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), residual=I.to_f64(R))
+    assert_rows_close(out.cpu().numpy(), ref, strict=1e-4 if prog == "none" else 2e-3,
+                      what=f"residual {prog} {M}x{N}x{K} {res_dtype}")
+
+
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
     # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;

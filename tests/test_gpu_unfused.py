@@ -39,6 +39,20 @@ def test_unfused_gemm_epilogue(cf, N, rowop):
     assert_rows_close(out.cpu().numpy(), ref, what=f"unfused {rowop} N={N}")
 
 
+@pytest.mark.parametrize("res_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("N", [512, 4096])
+def test_unfused_residual(cf, N, res_dtype):
+    ops = [("bias",), ("residual",), ("layernorm", 1e-5)]
+    case = I.gemm_epilogue_case("res", 256, N, 256, ops, seed=N + 1, need_bias=True, need_gamma=True, need_beta=True)
+    R = torch.from_numpy(np.random.default_rng(N).standard_normal((256, N)).astype(np.float32)).to(res_dtype)
+    vec = [t.cuda() for t in (case.bias, case.gamma, case.beta)]
+    out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, *vec, residual=R.cuda())
+    torch.cuda.synchronize()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), residual=I.to_f64(R))
+    assert_rows_close(out.cpu().numpy(), ref, what=f"unfused residual N={N} {res_dtype}")
+
+
 @pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
 def test_unfused_attention(cf, op):
     case = I.attention_b2b(batch=2, heads=2, L=1024, op=op)
