@@ -31,7 +31,10 @@ written out:
 2. Elementwise ops in descriptor order (bias, scale, ReLU, tanh-GELU, and
    the residual add x + R[m, n] of the "post-norm" MatMul + Add + norm
    subgraphs the evaluation fuses).
-3. At most one trailing row reduction (LayerNorm, RMSNorm, softmax).
+3. Row reductions (LayerNorm, RMSNorm, softmax), each a stage boundary: a
+   program is elementwise nodes, a reduction, and optionally more elementwise
+   nodes and a second reduction that ends it (the Stage-Stream model's chain
+   of stages; the kernels support up to two).
 4. For B2BGEMM the single rounding point is the intermediate S' = F(S), which
    is rounded to bfloat16 round-to-nearest-even before the second GEMM.
 
@@ -208,37 +211,48 @@ def row_softmax(x) -> np.ndarray:
 _ROW_OPS = ("layernorm", "rmsnorm", "softmax")
 
 
-def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta, residual=None) -> np.ndarray:
-    """Run an epilogue program: elementwise nodes, at most one trailing row op.
+def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta, residual=None, stage0_gamma=None,
+                   stage0_beta=None) -> np.ndarray:
+    """Run an epilogue program: elementwise nodes and row reductions in order.
 
     ``ops`` is a sequence of ``(name,)`` or ``(name, scalar)`` tuples; the
-    scalar is the scale for ``scale`` and eps for the norms.
+    scalar is the scale for ``scale`` and eps for the norms.  At most two row
+    reductions, and if there is one the program ends with a reduction.  The
+    last reduction uses ``gamma`` / ``beta``; an earlier one uses
+    ``stage0_gamma`` / ``stage0_beta`` (None: 1 and 0, no affine transform).
     """
     names = [o[0] for o in ops]
-    for i, n in enumerate(names):
-        if n in _ROW_OPS and i != len(names) - 1:
-            raise ValueError("a row reduction must be the last op of the program")
-    for op in ops:
+    row_at = [i for i, n in enumerate(names) if n in _ROW_OPS]
+    if len(row_at) > 2 or (row_at and row_at[-1] != len(names) - 1):
+        raise ValueError("at most two row reductions, the last one ending the program")
+    N = x.shape[1]
+    for i, op in enumerate(ops):
         name = op[0]
         scalar = op[1] if len(op) > 1 else 0.0
-        if name == "layernorm":
-            x = row_layernorm(x, gamma, beta, scalar)
-        elif name == "rmsnorm":
-            x = row_rmsnorm(x, gamma, scalar)
-        elif name == "softmax":
-            x = row_softmax(x)
+        if name in _ROW_OPS:
+            last = i == len(names) - 1
+            g = gamma if last else (np.ones(N) if stage0_gamma is None else stage0_gamma)
+            b = beta if last else (np.zeros(N) if stage0_beta is None else stage0_beta)
+            if name == "layernorm":
+                x = row_layernorm(x, g, b, scalar)
+            elif name == "rmsnorm":
+                x = row_rmsnorm(x, g, scalar)
+            else:
+                x = row_softmax(x)
         else:
             x = elementwise(x, name, scalar, bias, residual)
     return x
 
 
-def gemm_epilogue(A, B, ops: Iterable[tuple], bias=None, gamma=None, beta=None, residual=None) -> np.ndarray:
+def gemm_epilogue(A, B, ops: Iterable[tuple], bias=None, gamma=None, beta=None, residual=None,
+                  stage0_gamma=None, stage0_beta=None) -> np.ndarray:
     """GEMM followed by an epilogue program, all in float64.
 
     A: M x K, B: K x N (row-major, bf16 values as float64); ``residual``
-    (M x N) is read by the ``residual`` op.  Returns M x N.
+    (M x N) is read by the ``residual`` op; ``stage0_gamma`` / ``stage0_beta``
+    are the affine vectors of the first of two row reductions.  Returns M x N.
     """
-    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta, residual)
+    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta, residual, stage0_gamma, stage0_beta)
 
 
 def mid_op(S, op: str, scale: float = 1.0) -> np.ndarray:

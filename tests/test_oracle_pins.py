@@ -81,6 +81,38 @@ def test_residual_order_in_program():
         O.gemm_epilogue(A, B, [("residual",)], residual=R.T)
 
 
+def test_chained_reductions_hand_example():
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    ln = np.array([[_closed(v) for v in row] for row in h["layernorm_eps0"]], float)
+    ones, zeros = np.ones(4), np.zeros(4)
+    # LayerNorm rows have mean 0 and mean square 1, so RMSNorm leaves them unchanged.
+    got = O.gemm_epilogue(A, B, [("layernorm", 0.0), ("rmsnorm", 0.0)], gamma=ones, beta=zeros)
+    np.testing.assert_allclose(got, ln, rtol=0, atol=1e-12)
+    # Softmax of the LayerNorm rows (closed form in the golden file).
+    exp = np.array([[_closed(v) for v in row] for row in h["layernorm_then_softmax"]], float)
+    got = O.gemm_epilogue(A, B, [("layernorm", 0.0), ("softmax",)], gamma=ones, beta=zeros)
+    np.testing.assert_allclose(got, exp, rtol=0, atol=1e-12)
+    # The first reduction's own affine vectors: z = 2 LN + 1 has mean square 5,
+    # and the last reduction's gamma (3) scales the result.
+    got = O.gemm_epilogue(A, B, [("layernorm", 0.0), ("rmsnorm", 0.0)], gamma=3 * ones, beta=zeros,
+                          stage0_gamma=2 * ones, stage0_beta=ones)
+    np.testing.assert_allclose(got, 3 * (2 * ln + 1) / math.sqrt(5.0), rtol=0, atol=1e-12)
+
+
+def test_chained_reductions_rules():
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    with pytest.raises(ValueError):  # three reductions
+        O.gemm_epilogue(A, B, [("layernorm", 0.0), ("rmsnorm", 0.0), ("softmax",)], gamma=np.ones(4),
+                        beta=np.zeros(4))
+    with pytest.raises(ValueError):  # a reduction that does not end the program
+        O.gemm_epilogue(A, B, [("layernorm", 0.0), ("rmsnorm", 0.0), ("relu",)], gamma=np.ones(4),
+                        beta=np.zeros(4))
+
+
 def _closed(expr: str) -> float:
     """Evaluate a closed form written in the golden file (sqrt, exp, tanh only)."""
     return float(eval(expr, {"__builtins__": {}},
