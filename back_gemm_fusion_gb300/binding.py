@@ -42,7 +42,8 @@ class cf_op(ctypes.Structure):
 
 class cf_epi_desc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("n_ops", ctypes.c_uint32), ("ops", cf_op * EPI_MAX_OPS),
-                ("out_dtype", ctypes.c_int32), ("exchange", ctypes.c_int32), ("residual", cf_matrix)]
+                ("out_dtype", ctypes.c_int32), ("exchange", ctypes.c_int32), ("residual", cf_matrix),
+                ("stage0_gamma", ctypes.c_void_p), ("stage0_beta", ctypes.c_void_p)]
 
 
 class cf_b2b_desc(ctypes.Structure):
@@ -119,8 +120,11 @@ def matrix(t: torch.Tensor, trans: bool = False) -> cf_matrix:
     return cf_matrix(t.data_ptr(), _dtype_code(t), 1 if trans else 0, rows, cols, max(t.stride(0), 1))
 
 
-def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[torch.Tensor] = None) -> cf_epi_desc:
-    """Descriptor (version 2); ``residual`` is the M x N matrix read by the ``residual`` op."""
+def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[torch.Tensor] = None,
+             stage0_gamma: Optional[torch.Tensor] = None, stage0_beta: Optional[torch.Tensor] = None) -> cf_epi_desc:
+    """Descriptor (version 2); ``residual`` is the M x N matrix read by the
+    ``residual`` op, ``stage0_gamma`` / ``stage0_beta`` the affine vectors of
+    the first of two row reductions."""
     d = cf_epi_desc()
     d.version = 2
     d.n_ops = len(ops)
@@ -133,6 +137,8 @@ def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[to
     d.exchange = EXCHANGE_CODES[exchange]
     if residual is not None:
         d.residual = matrix(residual)
+    d.stage0_gamma = None if stage0_gamma is None else stage0_gamma.data_ptr()
+    d.stage0_beta = None if stage0_beta is None else stage0_beta.data_ptr()
     return d
 
 
@@ -162,7 +168,8 @@ def cf_workspace_size(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], b_
 def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bias=None, gamma=None, beta=None,
                      out: Optional[torch.Tensor] = None, b_trans: bool = False, exchange: str = "auto",
                      workspace: Optional[torch.Tensor] = None, stream=None,
-                     residual: Optional[torch.Tensor] = None) -> torch.Tensor:
+                     residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
+                     stage0_beta: Optional[torch.Tensor] = None) -> torch.Tensor:
     """out = epilogue(A @ B) in one fused kernel.  ``B`` is K x N, or N x K
     with ``b_trans=True``; ``residual`` (M x N, fp32 or bf16) feeds the
     ``residual`` op.  A workspace is allocated if needed and not given."""
@@ -171,7 +178,8 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
     N = B.shape[0] if b_trans else B.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange, residual)
+    a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta))
     need = int(lib.cf_workspace_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
@@ -186,7 +194,8 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
 def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bias=None, gamma=None,
                              beta=None, out: Optional[torch.Tensor] = None, b_trans: bool = False,
                              exchange: str = "auto", stream=None,
-                             residual: Optional[torch.Tensor] = None) -> torch.Tensor:
+                             residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
+                             stage0_beta: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Same as cf_gemm_epilogue, but the library takes any scratch it needs
     from its own static device array: nothing is allocated by this call
     (``out`` must be given by callers that cannot allocate)."""
@@ -195,7 +204,8 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
         M = A.shape[0]
         N = B.shape[0] if b_trans else B.shape[1]
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, exchange, residual)
+    a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta))
     st = lib.cf_gemm_epilogue_noalloc(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _stream(stream))
     _check(st, "cf_gemm_epilogue_noalloc")
@@ -241,7 +251,7 @@ def cf_b2bgemm(A: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, op: str, sca
 
 
 def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=None, b_trans=False,
-                             intermediate=None, stream=None, residual=None):
+                             intermediate=None, stream=None, residual=None, stage0_gamma=None, stage0_beta=None):
     """Comparison path: cuBLASLt GEMM to an fp32 intermediate, then a separate epilogue kernel."""
     lib = load_library()
     M = A.shape[0]
@@ -250,7 +260,7 @@ def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=No
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if intermediate is None:
         intermediate = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, residual=residual)
+    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, residual=residual, stage0_gamma=stage0_gamma, stage0_beta=stage0_beta)
     st = lib.cf_unfused_gemm_epilogue(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _ptr(intermediate), _stream(stream))
     _check(st, "cf_unfused_gemm_epilogue")

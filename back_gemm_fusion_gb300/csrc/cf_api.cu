@@ -27,10 +27,11 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   unsigned* status = nullptr;
-  bool prepared[4][3][2] = {};
-  int max_clusters[4][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
-  int max_pairs[4][3] = {};                        // resident 2-CTA clusters per (rowop, xmode)
-  int blocks_per_sm[4][3] = {};                    // 0 = unknown
+  // Indexed by the kernel variant's row code (row_code(first, last row op)).
+  bool prepared[kRowCodes][3][2] = {};
+  int max_clusters[kRowCodes][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
+  int max_pairs[kRowCodes][3] = {};                        // resident 2-CTA clusters per (row code, xmode)
+  int blocks_per_sm[kRowCodes][3] = {};                    // 0 = unknown
 };
 
 std::mutex g_mu;
@@ -118,6 +119,10 @@ cf_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_
 struct EpiPlan {
   int rowop = ROW_NONE;
   float eps = 0.0f;
+  int rowop0 = ROW_NONE;  // first of two chained reductions
+  float eps0 = 0.0f;
+  int n_elem0 = 0;        // elementwise ops before it
+  int code() const { return row_code(rowop0, rowop); }
   int n_elem = 0;
   int kinds[CF_EPI_MAX_OPS] = {};
   float scalars[CF_EPI_MAX_OPS] = {};
@@ -137,15 +142,24 @@ cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
         plan->need_residual = true;
         break;
       case CF_OP_SCALE: case CF_OP_RELU: case CF_OP_GELU_TANH: break;
-      case CF_OP_ROW_LAYERNORM: case CF_OP_ROW_RMSNORM: case CF_OP_ROW_SOFTMAX:
-        if (i + 1 != epi->n_ops) return CF_ERR_INVALID_ARG;  // a reduction ends the program
+      case CF_OP_ROW_LAYERNORM: case CF_OP_ROW_RMSNORM: case CF_OP_ROW_SOFTMAX: {
         if (op.kind != CF_OP_ROW_SOFTMAX && op.scalar < 0.0f) return CF_ERR_INVALID_ARG;
-        plan->rowop = op.kind == CF_OP_ROW_LAYERNORM ? ROW_LAYERNORM
+        const int r = op.kind == CF_OP_ROW_LAYERNORM ? ROW_LAYERNORM
                       : op.kind == CF_OP_ROW_RMSNORM ? ROW_RMSNORM : ROW_SOFTMAX;
+        if (i + 1 != epi->n_ops) {
+          // A first reduction stage: version 2, a norm, at most one of them.
+          if (epi->version < 2 || plan->rowop0 != ROW_NONE || r == ROW_SOFTMAX) return CF_ERR_INVALID_ARG;
+          plan->rowop0 = r;
+          plan->eps0 = op.scalar;
+          plan->n_elem0 = plan->n_elem;
+          continue;
+        }
+        plan->rowop = r;
         plan->eps = op.scalar;
         plan->need_gamma = op.kind != CF_OP_ROW_SOFTMAX;
         plan->need_beta = op.kind == CF_OP_ROW_LAYERNORM;
         continue;
+      }
       default: return CF_ERR_INVALID_ARG;
     }
     plan->kinds[plan->n_elem] = op.kind;
@@ -158,6 +172,7 @@ cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
 // Exchange mode the fused kernel will use (host-only decision).
 int choose_xmode(const EpiPlan& plan, const cf_epi_desc* epi, int64_t tiles_n) {
   if (plan.rowop == ROW_NONE || tiles_n == 1) return X_NONE;
+  if (plan.rowop0 != ROW_NONE) return X_GLOBAL;  // chained stages: workspace exchange only
   if (epi->exchange == CF_XCHG_GLOBAL) return X_GLOBAL;
   if (epi->exchange == CF_XCHG_CLUSTER) return X_CLUSTER;
   return tiles_n <= kMaxClusterCtas ? X_CLUSTER : X_GLOBAL;
@@ -187,6 +202,10 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   if ((plan->need_bias && !bias) || (plan->need_gamma && !gamma) || (plan->need_beta && !beta))
     return CF_ERR_INVALID_ARG;
   if ((bias && !aligned16(bias)) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
+    return CF_ERR_MISALIGNED;
+  if (plan->rowop0 != ROW_NONE && epi->exchange == CF_XCHG_CLUSTER && N > kBN) return CF_ERR_UNSUPPORTED_SHAPE;
+  if (plan->rowop0 != ROW_NONE &&
+      ((epi->stage0_gamma && !aligned16(epi->stage0_gamma)) || (epi->stage0_beta && !aligned16(epi->stage0_beta))))
     return CF_ERR_MISALIGNED;
   if (plan->need_residual) {
     const cf_matrix& r = epi->residual;
@@ -281,7 +300,8 @@ size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_de
   // that size can be resident, so AUTO/CLUSTER strips that fit a cluster
   // still report the (small) fallback workspace.
   if (plan.rowop == ROW_NONE || tiles_n == 1) return 0;
-  return ws_bytes_for((M + kBM - 1) / kBM, tiles_n);
+  // Chained reductions: one statistics region per stage.
+  return (plan.rowop0 != ROW_NONE ? 2 : 1) * ws_bytes_for((M + kBM - 1) / kBM, tiles_n);
 }
 
 cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* bias, const float* gamma,
@@ -294,7 +314,9 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if (sh.M == 0 || sh.N == 0) return CF_OK;
   const int64_t tiles_n = sh.N / kBN, strips = (sh.M + kBM - 1) / kBM;
   int xmode = choose_xmode(plan, epi, tiles_n);
-  const size_t need_ws = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
+  const int code = plan.code();
+  const size_t ws_stage = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
+  const size_t need_ws = (plan.rowop0 != ROW_NONE ? 2 : 1) * ws_stage;
   if (xmode == X_GLOBAL && (!workspace || workspace_bytes < need_ws || !aligned16(workspace)))
     return CF_ERR_WORKSPACE;
 
@@ -322,6 +344,12 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     p.op_scalar[i] = plan.scalars[i];
   }
   p.eps = plan.eps;
+  p.n_ops0 = plan.n_elem0;
+  p.eps0 = plan.eps0;
+  if (plan.rowop0 != ROW_NONE) {
+    p.gamma0 = epi->stage0_gamma;
+    p.beta0 = epi->stage0_beta;
+  }
   p.bias = bias;
   p.gamma = gamma;
   p.beta = beta;
@@ -337,11 +365,12 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     std::lock_guard<std::mutex> lk(g_mu);
     for (int x = X_NONE; x <= X_GLOBAL; ++x) {
       if (plan.rowop == ROW_NONE && x != X_NONE) continue;
+      if (plan.rowop0 != ROW_NONE && x == X_CLUSTER) continue;  // not instantiated for chained stages
       for (int pr = 0; pr < 2; ++pr) {
         if (pr == 1 && x == X_CLUSTER) continue;
-        if (!dev->prepared[plan.rowop][x][pr]) {
-          if (gemm_epi_prepare(plan.rowop, x, pr == 1) != cudaSuccess) return CF_ERR_CUDA;
-          dev->prepared[plan.rowop][x][pr] = true;
+        if (!dev->prepared[code][x][pr]) {
+          if (gemm_epi_prepare(code, x, pr == 1) != cudaSuccess) return CF_ERR_CUDA;
+          dev->prepared[code][x][pr] = true;
         }
       }
     }
@@ -351,10 +380,10 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int maxc = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_clusters[plan.rowop][tiles_n];
+      int& cached = dev->max_clusters[code][tiles_n];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(plan.rowop, X_CLUSTER, false, (int)tiles_n, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, X_CLUSTER, false, (int)tiles_n, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -394,10 +423,10 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int maxp = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_pairs[plan.rowop][xmode];
+      int& cached = dev->max_pairs[code][xmode];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(plan.rowop, xmode, true, 2, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, xmode, true, 2, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -414,8 +443,8 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int per_sm = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->blocks_per_sm[plan.rowop][xmode];
-      if (cached == 0 && gemm_epi_max_blocks_per_sm(plan.rowop, xmode, &cached) != cudaSuccess) cached = 0;
+      int& cached = dev->blocks_per_sm[code][xmode];
+      if (cached == 0 && gemm_epi_max_blocks_per_sm(code, xmode, &cached) != cudaSuccess) cached = 0;
       per_sm = cached;
     }
     if (per_sm < 1) return CF_ERR_CUDA;
@@ -429,8 +458,14 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     p.ws_stats = reinterpret_cast<float2*>(ws);
     p.ws_count = reinterpret_cast<unsigned*>(ws + stats);
     if (cudaMemsetAsync(p.ws_count, 0, (size_t)strips * 4 * sizeof(unsigned), st) != cudaSuccess) return CF_ERR_CUDA;
+    if (plan.rowop0 != ROW_NONE) {  // the first stage's region follows the last stage's
+      p.ws_stats0 = reinterpret_cast<float2*>(ws + ws_stage);
+      p.ws_count0 = reinterpret_cast<unsigned*>(ws + ws_stage + stats);
+      if (cudaMemsetAsync(p.ws_count0, 0, (size_t)strips * 4 * sizeof(unsigned), st) != cudaSuccess)
+        return CF_ERR_CUDA;
+    }
   }
-  L.rowop = plan.rowop;
+  L.rowop = code;
   L.xmode = xmode;
   if (gemm_epi_launch(L, st) != cudaSuccess) {
     cudaGetLastError();

@@ -75,9 +75,10 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 
 // Apply the elementwise program to 32 consecutive columns starting at n.
-// Elementwise program on 32 consecutive columns n.. of row m of the tile.
-__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m) {
-  for (int o = 0; o < p.n_ops; ++o) {
+// Elementwise ops [o0, o1) of the program on 32 consecutive columns n.. of
+// row m of the tile.
+__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m, int o0, int o1) {
+  for (int o = o0; o < o1; ++o) {
     const int kind = p.op_kind[o];
     if (kind == OP_ADD_RESIDUAL) {
       // Each thread owns one row: 128 (fp32) or 64 (bf16) contiguous bytes of
@@ -163,6 +164,39 @@ struct Stat {
   }
 };
 
+// Strip-wide merge of per-tile row statistics `st` through the workspace
+// (the fallback exchange): publish, count arrivals (release), wait (bounded,
+// acquire) for every tile of the strip, merge in tile order.
+template <int R>
+__device__ __forceinline__ bool global_exchange(const GemmEpiParams& p, float2* ws_stats, unsigned* ws_count,
+                                                int strip, int tile, int row, int q, int lane,
+                                                volatile int* abort_flag, const WaitCtx& wc, float2& st) {
+  float2* wsrow = ws_stats + (size_t)strip * p.tiles_n * kBM + row;
+  __stcg(wsrow + (size_t)tile * kBM, st);
+  __threadfence();
+  __syncwarp();
+  unsigned* cnt = ws_count + strip * 4 + q;
+  if (lane == 0) red_release_gpu_add(cnt, 1u);
+  bool ok = true;
+  if (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
+      __nanosleep(64);
+      if (*abort_flag) { ok = false; break; }
+      if (clock64() - t0 > p.timeout_cycles) { record_timeout(wc); ok = false; break; }
+    }
+  }
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  float2 tot = __ldcg(wsrow);
+  float n_acc = (float)kBN;
+  for (int j = 1; j < p.tiles_n; ++j) {
+    tot = Stat<R>::merge(tot, __ldcg(wsrow + (size_t)j * kBM), n_acc);
+    n_acc += (float)kBN;
+  }
+  st = tot;
+  return true;
+}
+
 struct Work {
   int i, step, end, rank, tiles_n;
   __device__ bool valid() const { return i < end; }
@@ -216,7 +250,10 @@ __device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& 
 // DRAM for every strip.  Items of a strip stay contiguous, so the row
 // statistics exchange keeps its strip-major schedule.
 
-template <int ROWOP, int XMODE, bool CTA2>
+// ROWOP0 != ROW_NONE: the program has two chained row reductions, ROWOP0
+// (LayerNorm or RMSNorm) then ROWOP; only the per-tile and workspace
+// exchanges are instantiated for it.
+template <int ROWOP, int XMODE, bool CTA2, int ROWOP0 = ROW_NONE>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmEpiParams p) {
   using G = Geo<CTA2>;
   constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kOffOut = G::kOffOut,
@@ -399,6 +436,57 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kBN);
 
+      // Chained programs: the first reduction stage.  Its elementwise ops
+      // [0, n_ops0) are applied and written back to TMEM, its statistics
+      // are merged across the strip (same exchange as the last stage), and
+      // pass 1 below normalises with (sc0, sh0) and its affine vectors
+      // before the ops that follow it.
+      float sc0 = 1.0f, sh0 = 0.0f;
+      if constexpr (ROWOP0 != ROW_NONE) {
+        float s1 = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_wait_ld();
+          if (p.n_ops0 > 0) {
+            apply_program(p, v, n0 + c * 32, m0 + row, 0, p.n_ops0);
+            tmem_st32(taddr + c * 32, v);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s1 = (ROWOP0 == ROW_RMSNORM) ? fmaf(v[j], v[j], s1) : s1 + v[j];
+        }
+        if (p.n_ops0 > 0) tmem_wait_st();
+        float2 st0;
+        if (ROWOP0 == ROW_RMSNORM) {
+          st0 = make_float2(s1, 0.0f);
+        } else {
+          const float ref = s1 * (1.0f / kBN);
+          float s2 = 0.0f;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = v[j] - ref;
+              s2 = fmaf(d, d, s2);
+            }
+          }
+          st0 = make_float2(ref, s2);
+        }
+        if (XMODE == X_GLOBAL &&
+            !global_exchange<ROWOP0>(p, p.ws_stats0, p.ws_count0, strip, tile, row, q, lane, abort_flag, wc, st0))
+          break;
+        if (ROWOP0 == ROW_RMSNORM) {
+          sc0 = rsqrtf(st0.x / (float)p.N + p.eps0);
+        } else {
+          sc0 = rsqrtf(st0.y / (float)p.N + p.eps0);
+          sh0 = -st0.x * sc0;
+        }
+      }
+
       float2 st = Stat<ROWOP>::identity();
       float scale_a = 1.0f, shift_a = 0.0f;  // y = gamma * (x * scale_a + shift_a) (+ beta)
       if (ROWOP != ROW_NONE) {
@@ -409,8 +497,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           float v[32];
           tmem_ld32(taddr + c * 32, v);
           tmem_wait_ld();
-          if (p.n_ops > 0) {
-            apply_program(p, v, n0 + c * 32, m0 + row);
+          if constexpr (ROWOP0 != ROW_NONE) {
+            const int n = n0 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
+            if (p.gamma0) {
+              const float4* g4 = reinterpret_cast<const float4*>(p.gamma0 + n);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 g = __ldg(g4 + j);
+                v[4 * j + 0] *= g.x;
+                v[4 * j + 1] *= g.y;
+                v[4 * j + 2] *= g.z;
+                v[4 * j + 3] *= g.w;
+              }
+            }
+            if (ROWOP0 == ROW_LAYERNORM && p.beta0) {
+              const float4* b4 = reinterpret_cast<const float4*>(p.beta0 + n);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 bb = __ldg(b4 + j);
+                v[4 * j + 0] += bb.x;
+                v[4 * j + 1] += bb.y;
+                v[4 * j + 2] += bb.z;
+                v[4 * j + 3] += bb.w;
+              }
+            }
+          }
+          if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
+            apply_program(p, v, n0 + c * 32, m0 + row, ROWOP0 != ROW_NONE ? p.n_ops0 : 0, p.n_ops);
             tmem_st32(taddr + c * 32, v);
           }
 #pragma unroll
@@ -420,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             else s1 += v[j];
           }
         }
-        if (p.n_ops > 0) tmem_wait_st();
+        if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
         if (ROWOP == ROW_RMSNORM) {
           st = make_float2(s1, 0.0f);
         } else {
@@ -512,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         tmem_wait_ld();
         const int n = n0 + c * 32;
         if (ROWOP == ROW_NONE) {
-          apply_program(p, v, n, m0 + row);
+          apply_program(p, v, n, m0 + row, 0, p.n_ops);
         } else if (ROWOP == ROW_SOFTMAX) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;
@@ -581,9 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   }
 }
 
-template <int R, int X, bool P>
+template <int R, int X, bool P, int R0 = ROW_NONE>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P>);
+  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P, R0>);
 }
 
 const void* select_kernel(int rowop, int xmode, bool pair) {
@@ -607,6 +722,20 @@ const void* select_kernel(int rowop, int xmode, bool pair) {
   CF_CASE(ROW_SOFTMAX, X_GLOBAL, false)
   CF_CASE(ROW_SOFTMAX, X_GLOBAL, true)
 #undef CF_CASE
+  // Two chained reductions (per-tile or workspace exchange only).
+#define CF_CASE2(R0, R)                                                                            \
+  if (rowop == row_code(R0, R)) {                                                                  \
+    if (xmode == X_NONE) return pair ? kernel_ptr<R, X_NONE, true, R0>() : kernel_ptr<R, X_NONE, false, R0>();       \
+    if (xmode == X_GLOBAL) return pair ? kernel_ptr<R, X_GLOBAL, true, R0>() : kernel_ptr<R, X_GLOBAL, false, R0>(); \
+    return nullptr;                                                                                \
+  }
+  CF_CASE2(ROW_LAYERNORM, ROW_LAYERNORM)
+  CF_CASE2(ROW_LAYERNORM, ROW_RMSNORM)
+  CF_CASE2(ROW_LAYERNORM, ROW_SOFTMAX)
+  CF_CASE2(ROW_RMSNORM, ROW_LAYERNORM)
+  CF_CASE2(ROW_RMSNORM, ROW_RMSNORM)
+  CF_CASE2(ROW_RMSNORM, ROW_SOFTMAX)
+#undef CF_CASE2
   return nullptr;
 }
 

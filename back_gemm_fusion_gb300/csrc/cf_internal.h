@@ -19,6 +19,10 @@ constexpr int kBM = 128;     // rows per tile = TMEM lanes
 constexpr int kBN = 256;     // columns per tile = one TMEM accumulator
 constexpr int kBK = 64;      // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kMaxClusterCtas = 16;
+// Kernel variant of a program: the last row op plus 4 x the first of two
+// chained row ops (ROW_NONE, ROW_LAYERNORM or ROW_RMSNORM).
+constexpr int kRowCodes = 12;
+constexpr int row_code(int rowop0, int rowop) { return rowop + 4 * rowop0; }
 
 // Kernel parameters (passed by value as a __grid_constant__).
 struct GemmEpiParams {
@@ -39,6 +43,14 @@ struct GemmEpiParams {
   const float* bias;
   const float* gamma;
   const float* beta;
+  // First of two chained row reductions (row op code / 4; see row_code):
+  // elementwise ops [0, n_ops0) precede it, ops [n_ops0, n_ops) follow it.
+  int n_ops0;
+  float eps0;
+  const float* gamma0;    // may be null: no affine transform
+  const float* beta0;
+  float2* ws_stats0;      // its partial statistics and arrival counters (workspace exchange)
+  unsigned* ws_count0;
   const void* res;        // residual matrix (CF_OP_ADD_RESIDUAL), M x N, leading dim res_ld
   long long res_ld;
   int res_bf16;           // 1: bf16 residual, 0: fp32

@@ -140,6 +140,31 @@ __device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* 
   return x;
 }
 
+// Elementwise ops [o0, o1) of the program for element (m, n); `r` is residual[m][n].
+__device__ __forceinline__ float ew_range(const RowProgram& pg, float x, const float* bias, int n, float r, int o0,
+                                          int o1) {
+  for (int o = o0; o < o1; ++o) {
+    switch (pg.kind[o]) {
+      case CF_OP_BIAS: x += bias[n]; break;
+      case CF_OP_ADD_RESIDUAL: x += r; break;
+      case CF_OP_SCALE: x *= pg.scalar[o]; break;
+      case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
+      case CF_OP_GELU_TANH: x = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x))); break;
+    }
+  }
+  return x;
+}
+
+// The first of two chained row reductions of a program (LayerNorm or
+// RMSNorm); ops [0, n_ops0) precede it.
+struct ChainStage {
+  int rowop;
+  float eps;
+  int n_ops0;
+  const float* gamma;  // may be null (no affine transform)
+  const float* beta;
+};
+
 // Block-wide sum or max of one value per thread (blockDim.x == 256).
 template <bool kMax>
 __device__ float block_reduce(float v, float* red) {
@@ -201,6 +226,73 @@ __global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restri
     for (int n = threadIdx.x; n < N; n += blockDim.x) s += __expf(row[n] - m);
     const float inv = 1.0f / block_reduce<false>(s, red);
     for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = __expf(row[n] - m) * inv;
+  }
+}
+
+// Chained programs, one CTA per row: first stage (ops, reduction, affine),
+// then the remaining ops and the last reduction; the row stays in shared
+// memory between the stages.
+__global__ void __launch_bounds__(256) row_epilogue_chain_kernel(const float* __restrict__ P, int64_t ldp,
+                                                                 float* __restrict__ out, int64_t ldo, int N,
+                                                                 RowProgram pg, ChainStage c0,
+                                                                 const float* __restrict__ bias,
+                                                                 const float* __restrict__ gamma,
+                                                                 const float* __restrict__ beta, ResView rv) {
+  extern __shared__ float row[];
+  __shared__ float red[32];
+  const int m = (int)blockIdx.x;
+  const float* p = P + (int64_t)m * ldp;
+  float* o = out + (int64_t)m * ldo;
+  float acc = 0.0f;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    const float x = ew_range(pg, p[n], bias, n, res_at(rv.ptr, rv.ld, rv.bf16, m, n), 0, c0.n_ops0);
+    row[n] = x;
+    acc += (c0.rowop == CF_OP_ROW_RMSNORM) ? x * x : x;
+  }
+  float sc, sh = 0.0f;
+  if (c0.rowop == CF_OP_ROW_LAYERNORM) {
+    const float mean = block_reduce<false>(acc, red) / N;
+    float ss = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      const float d = row[n] - mean;
+      ss += d * d;
+    }
+    sc = rsqrtf(block_reduce<false>(ss, red) / N + c0.eps);
+    sh = -mean * sc;
+  } else {
+    sc = rsqrtf(block_reduce<false>(acc, red) / N + c0.eps);
+  }
+  acc = 0.0f;
+  float mx = -INFINITY;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    float x = row[n] * sc + sh;
+    if (c0.gamma) x *= c0.gamma[n];
+    if (c0.rowop == CF_OP_ROW_LAYERNORM && c0.beta) x += c0.beta[n];
+    x = ew_range(pg, x, bias, n, res_at(rv.ptr, rv.ld, rv.bf16, m, n), c0.n_ops0, pg.n_ops);
+    row[n] = x;
+    acc += x;
+    mx = fmaxf(mx, x);
+  }
+  if (pg.rowop == CF_OP_ROW_LAYERNORM) {
+    const float mean = block_reduce<false>(acc, red) / N;
+    float ss = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      const float d = row[n] - mean;
+      ss += d * d;
+    }
+    const float rstd = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = gamma[n] * (row[n] - mean) * rstd + beta[n];
+  } else if (pg.rowop == CF_OP_ROW_RMSNORM) {
+    float ss = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) ss += row[n] * row[n];
+    const float rstd = rsqrtf(block_reduce<false>(ss, red) / N + pg.eps);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = gamma[n] * row[n] * rstd;
+  } else {
+    const float mm = block_reduce<true>(mx, red);
+    float sum = 0.0f;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) sum += __expf(row[n] - mm);
+    const float inv = 1.0f / block_reduce<false>(sum, red);
+    for (int n = threadIdx.x; n < N; n += blockDim.x) o[n] = __expf(row[n] - mm) * inv;
   }
 }
 
@@ -372,8 +464,18 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   RowProgram pg;
   std::memset(&pg, 0, sizeof(pg));
   ResView rv = {nullptr, 0, 0};
+  ChainStage c0 = {0, 0.0f, 0, nullptr, nullptr};
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
     const int k = epi->ops[i].kind;
+    if (k >= CF_OP_ROW_LAYERNORM && i + 1 != epi->n_ops) {  // first of two chained reductions
+      if (epi->version < 2 || c0.rowop != 0 || k == CF_OP_ROW_SOFTMAX) return CF_ERR_INVALID_ARG;
+      c0.rowop = k;
+      c0.eps = epi->ops[i].scalar;
+      c0.n_ops0 = pg.n_ops;
+      c0.gamma = epi->stage0_gamma;
+      c0.beta = epi->stage0_beta;
+      continue;
+    }
     if (k == CF_OP_ADD_RESIDUAL) {
       const cf_matrix& r = epi->residual;
       if (epi->version < 2 || !r.ptr || r.trans || r.rows != M || r.cols != N || r.ld < N ||
@@ -400,6 +502,16 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   float* o = static_cast<float*>(out->ptr);
   const bool vec = N % 1024 == 0 && (out->ld % 4) == 0 && aligned16(out->ptr) && (!bias || aligned16(bias)) &&
                    (!gamma || aligned16(gamma)) && (!beta || aligned16(beta));
+  if (c0.rowop != 0) {
+    const size_t smem = (size_t)N * sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(row_epilogue_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return CF_ERR_CUDA;
+    row_epilogue_chain_kernel<<<(unsigned)M, 256, smem, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias,
+                                                              gamma, beta, rv);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+  }
   switch (vec ? N / 1024 : 0) {
     case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
     case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;

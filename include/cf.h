@@ -78,8 +78,12 @@ typedef struct {
 } cf_matrix;
 
 /* Epilogue operations.  Elementwise ops (kind < 16) are applied in order to
- * every element of P = A.B; a row reduction (kind >= 16) may appear at most
- * once and only as the last op (reductions are stage boundaries). */
+ * every element of P = A.B; row reductions (kind >= 16) are stage
+ * boundaries.  A program has at most two reductions, and if it has any it
+ * ends with one: [elementwise...] [R0 [elementwise...]] R1.  A first
+ * reduction R0 (descriptor version 2) must be LayerNorm or RMSNorm; its
+ * affine vectors are stage0_gamma / stage0_beta, the last reduction's are the
+ * gamma / beta arguments. */
 typedef enum {
   CF_OP_BIAS = 1,            /* x += bias[n]                                        */
   CF_OP_SCALE = 2,           /* x *= scalar                                         */
@@ -119,6 +123,10 @@ typedef struct {
    * dim 16-byte aligned, caller-owned.  Ignored (may be all zero) when the
    * program has no CF_OP_ADD_RESIDUAL; the fused kernel reads it once. */
   cf_matrix residual;
+  /* Version 2: affine vectors (fp32 [N], 16-byte aligned) of the first of two
+   * row reductions; NULL means gamma = 1 / beta = 0 (no affine transform). */
+  const float* stage0_gamma;
+  const float* stage0_beta;
 } cf_epi_desc;
 
 /*

@@ -136,3 +136,26 @@ def test_residual_validation(lib):
     d.version = 1                                                       # version-1 descriptors still accepted
     assert lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
                                 ctypes.byref(O), None, 0, None) in (0, 4, 8)
+
+
+def test_chained_reduction_rules(lib):
+    from back_gemm_fusion_gb300.binding import epi_desc
+    A, B, O = _mats(N=1024)
+
+    def call(ops, version=2, exchange="auto"):
+        d = epi_desc(ops, exchange)
+        d.version = version
+        return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                    ctypes.byref(O), None, 0, None)
+
+    LN_RMS = [("layernorm", 1e-5), ("rmsnorm", 1e-6)]
+    assert call(LN_RMS, version=1) == 1                                  # chaining needs version 2
+    assert call([("softmax",), ("rmsnorm", 1e-6)]) == 1                  # the first stage must be a norm
+    assert call([("layernorm", 1e-5), ("rmsnorm", 1e-6), ("softmax",)]) == 1  # at most two reductions
+    assert call(LN_RMS, exchange="cluster") == 2                        # chained stages: no DSMEM exchange
+    assert call(LN_RMS) == 7                                             # workspace exchange needs a workspace
+    from back_gemm_fusion_gb300.binding import cf_matrix, CF_BF16
+    d = epi_desc(LN_RMS)
+    one = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(epi_desc([("rmsnorm", 1e-6)])))
+    two = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(d))
+    assert one > 0 and two == 2 * one                                    # one statistics region per stage

@@ -139,6 +139,53 @@ def test_residual_postnorm(cf, M, N, K, prog, res_dtype):
                       what=f"residual {prog} {M}x{N}x{K} {res_dtype}")
 
 
+CHAINS = {
+    "ln_gelu_rms": [("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+    "rms_ln": [("rmsnorm", 1e-6), ("layernorm", 1e-5)],
+    "ln_scale_softmax": [("bias",), ("layernorm", 1e-5), ("scale", 2.0), ("softmax",)],
+    "res_rms_relu_rms": [("residual",), ("rmsnorm", 1e-6), ("relu",), ("rmsnorm", 1e-6)],
+}
+
+
+@pytest.mark.parametrize("affine0", [False, True])
+@pytest.mark.parametrize("M,N", [(256, 256), (384, 1024), (200, 4352), (512, 2048)])
+@pytest.mark.parametrize("chain", sorted(CHAINS))
+def test_chained_reductions(cf, chain, M, N, affine0):
+    # Two reduction stages in one epilogue: per-tile (N = 256) and workspace
+    # exchanges, 1-CTA (odd strip count) and CTA-pair tiles, ragged M.
+    ops = CHAINS[chain]
+    case = I.gemm_epilogue_case("chain", M, N, 128, ops, seed=M + N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    rng = np.random.default_rng(N)
+    g0 = b0 = R = None
+    if affine0:
+        g0 = torch.from_numpy((1.0 + 0.3 * rng.standard_normal(N)).astype(np.float32))
+        b0 = torch.from_numpy((0.3 * rng.standard_normal(N)).astype(np.float32))
+    if any(o[0] == "residual" for o in ops):
+        R = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32))
+    out = cf.cf_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma),
+                              _dev(case.beta), residual=_dev(R), stage0_gamma=_dev(g0), stage0_beta=_dev(b0))
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), residual=I.to_f64(R), stage0_gamma=I.to_f64(g0),
+                          stage0_beta=I.to_f64(b0))
+    assert_rows_close(out.cpu().numpy(), ref, what=f"chain {chain} {M}x{N} affine0={affine0}")
+
+
+def test_chained_reductions_unfused(cf):
+    ops = CHAINS["ln_gelu_rms"]
+    case = I.gemm_epilogue_case("chain_unfused", 256, 2048, 128, ops, seed=7, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    g0 = torch.from_numpy((1.0 + 0.3 * np.random.default_rng(3).standard_normal(2048)).astype(np.float32))
+    out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma),
+                                      _dev(case.beta), stage0_gamma=g0.cuda())
+    torch.cuda.synchronize()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), stage0_gamma=I.to_f64(g0))
+    assert_rows_close(out.cpu().numpy(), ref, what="unfused chain ln_gelu_rms")
+
+
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
     # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;
