@@ -45,6 +45,8 @@ class GemmEpilogueCase:
     gamma: Optional[torch.Tensor] = None
     beta: Optional[torch.Tensor] = None
     residual: Optional[torch.Tensor] = None  # M x N, read by the ("residual",) op
+    stage0_gamma: Optional[torch.Tensor] = None  # affine vectors of the first of two row reductions
+    stage0_beta: Optional[torch.Tensor] = None
     meta: Dict = field(default_factory=dict)
 
 
@@ -75,6 +77,19 @@ def postnorm_layernorm(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 409
                            need_bias=True, need_gamma=True, need_beta=True)
     rng = np.random.default_rng([seed, 1])
     c.residual = _bf16(rng.standard_normal((M, N)))
+    return c
+
+
+def chained_ln_gelu_rms(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 4096) -> GemmEpilogueCase:
+    """Two reduction stages in one epilogue: GEMM + bias + LayerNorm (its own
+    gamma0/beta0) + tanh-GELU + RMSNorm (gamma), fp32 out; the first stage's
+    vectors are drawn after the others, like the bias/gamma/beta."""
+    c = gemm_epilogue_case("gemm_bias_layernorm_gelu_rmsnorm", M, N, K,
+                           [("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)], seed,
+                           need_bias=True, need_gamma=True)
+    rng = np.random.default_rng([seed, 2])
+    c.stage0_gamma = _f32(1.0 + rng.standard_normal(N) * math.sqrt(0.1))
+    c.stage0_beta = _f32(rng.standard_normal(N) * math.sqrt(0.1))
     return c
 
 

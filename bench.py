@@ -40,11 +40,13 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # keyed by workload; valid only while the kernel source hash matches the one
 # the counters were taken with (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "gelu_rmsnorm": {"read": 116985856, "write": 90224128, "src": "2ba0528af4f710b2"},
-    "scaled_softmax": {"read": 1384278016, "write": 239182080, "src": "2ba0528af4f710b2"},
-    "mlp_b2b": {"read": 50442240, "write": 15169536, "src": "2ba0528af4f710b2"},
-    "attention_softmax": {"read": 805538304, "write": 496984320, "src": "2ba0528af4f710b2"},
-    "attention_relu": {"read": 805420032, "write": 494765568, "src": "2ba0528af4f710b2"},
+    "gelu_rmsnorm": {"read": 110362880, "write": 91411712, "src": "f9cc6d4cb667d654"},
+    "scaled_softmax": {"read": 1396333568, "write": 239146752, "src": "f9cc6d4cb667d654"},
+    "mlp_b2b": {"read": 50470400, "write": 14872576, "src": "f9cc6d4cb667d654"},
+    "attention_softmax": {"read": 805418496, "write": 497545984, "src": "f9cc6d4cb667d654"},
+    "attention_relu": {"read": 805729280, "write": 495820800, "src": "f9cc6d4cb667d654"},
+    "postnorm_layernorm": {"read": 193516288, "write": 95745024, "src": "f9cc6d4cb667d654"},
+    "chained_ln_gelu_rms": {"read": 109929216, "write": 88441088, "src": "f9cc6d4cb667d654"},
 }
 
 
@@ -83,6 +85,8 @@ class Workload:
             self.case = I.scaled_softmax(seed)
         elif name == "postnorm_layernorm":
             self.case = I.postnorm_layernorm(seed)
+        elif name == "chained_ln_gelu_rms":
+            self.case = I.chained_ln_gelu_rms(seed)
         elif name == "mlp_b2b":
             self.case = I.mlp_b2b(seed)
         elif name == "mlp_bottom":
@@ -101,15 +105,15 @@ class Workload:
             self.stat_bytes = 0.0
             self.rows = c.batch * c.M
         else:
-            vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta) if t is not None)
+            vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta, c.stage0_gamma, c.stage0_beta) if t is not None)
             self.flops = 2.0 * c.M * c.N * c.K
             self.out_bytes = 4.0 * c.M * c.N
             res = 0.0 if c.residual is None else float(c.residual.numel() * c.residual.element_size())
             self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + res + self.out_bytes
             # Row statistics of rows wider than one 256-column tile: 8 bytes
             # per row per tile in the workspace (written once, read per tile).
-            has_row = any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in c.ops)
-            self.stat_bytes = 8.0 * c.M * (c.N // 256) if has_row and c.N > 256 else 0.0
+            n_row = sum(o[0] in ("layernorm", "rmsnorm", "softmax") for o in c.ops)
+            self.stat_bytes = 8.0 * n_row * c.M * (c.N // 256) if c.N > 256 else 0.0
             self.rows = c.M
 
     def config(self):
@@ -129,7 +133,7 @@ class Workload:
             dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=torch.float32, device="cuda")
         else:
             dev["A"], dev["B"] = c.A.cuda(), c.B.cuda()
-            for k in ("bias", "gamma", "beta", "residual"):
+            for k in ("bias", "gamma", "beta", "residual", "stage0_gamma", "stage0_beta"):
                 t = getattr(c, k)
                 dev[k] = None if t is None else t.cuda()
             dev["out"] = torch.empty((c.M, c.N), dtype=torch.float32, device="cuda")
@@ -146,7 +150,8 @@ class Workload:
         else:
             cf.cf_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
                                 out=dev["out"], workspace=workspace, stream=stream, exchange=self.exchange,
-                                residual=dev["residual"])
+                                residual=dev["residual"], stage0_gamma=dev["stage0_gamma"],
+                                stage0_beta=dev["stage0_beta"])
 
     def unfused_step(self, cf, dev, scratch, stream=None):
         c = self.case
@@ -162,7 +167,8 @@ class Workload:
         else:
             cf.cf_unfused_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
                                         out=dev["out"], intermediate=scratch, stream=stream,
-                                        residual=dev["residual"])
+                                        residual=dev["residual"], stage0_gamma=dev["stage0_gamma"],
+                                        stage0_beta=dev["stage0_beta"])
 
     def unfused_scratch(self):
         c = self.case
@@ -196,7 +202,7 @@ class Workload:
         A = self._f64("A")[rows]
         R = None if c.residual is None else self._f64("residual")[rows]
         O.gemm_epilogue(A, self._f64("B"), c.ops, self._f64("bias"), self._f64("gamma"), self._f64("beta"),
-                        residual=R)
+                        residual=R, stage0_gamma=self._f64("stage0_gamma"), stage0_beta=self._f64("stage0_beta"))
         return 2.0 * len(rows) * c.N * c.K
 
 
@@ -503,7 +509,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     # call, device -> pinned host output, all inside the timed region.
     c = wl.case
     host_in = []
-    names = ("A", "W1", "W2") if wl.is_b2b else ("A", "B", "bias", "gamma", "beta", "residual")
+    names = ("A", "W1", "W2") if wl.is_b2b else ("A", "B", "bias", "gamma", "beta", "residual", "stage0_gamma",
+                                                  "stage0_beta")
     for k in names:
         t = getattr(c, k)
         if t is not None:
@@ -573,7 +580,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
-                             "attention_relu", "mlp_bottom", "postnorm_layernorm"])
+                             "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms"])
     ap.add_argument("--rows", type=int, default=64, help="batch rows of the mlp_bottom workload (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")
