@@ -26,13 +26,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ bool elect_one_sync() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -123,17 +116,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Same as tma_load_2d, but the tile lands at the same smem offset in every
-// CTA of the cluster set in `cta_mask`, each of whose barriers (same
-// offset as `bar`) receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
-                                                      int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z) {
@@ -144,13 +126,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x,
-                                             int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::
-                   "l"(reinterpret_cast<uint64_t>(m)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
 
 // L2 eviction-priority policy for streaming data (written once, not read
 // again by this kernel), and a TMA store that carries it.
@@ -168,14 +143,6 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* m, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int32_t x,
-                                             int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(src), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
@@ -209,20 +176,12 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-// mma_bf16 with split descriptors.  No "memory" clobber: operand
-// readiness is ordered by the (volatile, clobbering) mbarrier waits and
-// commits around the MMAs, and the clobber would make the compiler reload
-// values from memory between consecutive MMAs.
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 in, fp32 accumulate),
+// with split descriptors (SDesc halves); accumulate == 0 overwrites D.  No
+// "memory" clobber: operand readiness is ordered by the (volatile,
+// clobbering) mbarrier waits and commits around the MMAs, and the clobber
+// would make the compiler reload values from memory between consecutive MMAs.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -230,6 +189,8 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t 
       " setp.ne.b32 p, %6, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
 }
+// D[tmem] (+)= A[tmem] * B[smem]: A is read from Tensor Memory (row i in
+// lane i, two consecutive K elements packed per 32-bit column).
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
@@ -238,16 +199,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate));
 }
 
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is read from Tensor Memory
-// (row i in lane i, two consecutive K elements packed per 32-bit column).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // Arrive (once) on a CTA-local mbarrier when all prior tcgen05 async ops of
 // this thread have completed.
@@ -279,10 +230,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_local, uint32_t s
       : "memory");
 }
 
-// Barrier among `nthreads` threads (a multiple of 32) on hardware barrier `id`.
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -340,25 +287,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma (version 1 layout):
-// start address, leading/stride byte offsets (all >> 4), swizzle mode in
-// bits 61..63 (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1u << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)2u << 61;  // SWIZZLE_128B
-  return d;
-}
-
-// The same descriptor as two 32-bit halves.  Stepping the start address
-// (bits 0-13: address >> 4; shared addresses stay below 256 KB, so the field
-// never carries) changes only the low half, so an MMA loop adds a constant
-// to one register per step instead of rebuilding a 64-bit descriptor: the
-// single issuing thread must keep up with 64-cycle 128 x 128 x 16 MMAs.
+// Shared-memory matrix descriptor for tcgen05.mma (version 1 layout), kept
+// as two 32-bit halves: low = start address >> 4 (bits 0-13) | leading byte
+// offset >> 4 (bits 16-29); high = stride byte offset >> 4 (bits 32-45),
+// version 1 (bit 46), swizzle mode 2 = 128-byte swizzle (bits 61-63).
+// Stepping the start address changes only the low half (shared addresses
+// stay below 256 KB, so the field never carries), so an MMA loop adds a
+// constant to one register per step instead of rebuilding a 64-bit
+// descriptor: the single issuing thread must keep up with 64-cycle
+// 128 x 128 x 16 MMAs.
 struct SDesc {
   uint32_t lo, hi;
 };
@@ -392,19 +329,10 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// Issued by the even CTA of the pair: M = 256 rows, rows 0..127 from this
-// CTA's A tile and 128..255 from the peer's (same smem offset); the N
-// columns of B are split between the two CTAs' tiles; each CTA's TMEM
-// receives its own 128 rows.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// mma_bf16_pair with split descriptors (see mma_ss).
+// CTA-pair form of mma_ss, issued by the even CTA of the pair: M = 256 rows,
+// rows 0..127 from this CTA's A tile and 128..255 from the peer's (same smem
+// offset); the N columns of B are split between the two CTAs' tiles; each
+// CTA's TMEM receives its own 128 rows.
 __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
                                             uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
