@@ -121,10 +121,11 @@ def matrix(t: torch.Tensor, trans: bool = False) -> cf_matrix:
 
 
 def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[torch.Tensor] = None,
-             stage0_gamma: Optional[torch.Tensor] = None, stage0_beta: Optional[torch.Tensor] = None) -> cf_epi_desc:
+             stage0_gamma: Optional[torch.Tensor] = None, stage0_beta: Optional[torch.Tensor] = None,
+             out_dtype: int = CF_FP32) -> cf_epi_desc:
     """Descriptor (version 2); ``residual`` is the M x N matrix read by the
     ``residual`` op, ``stage0_gamma`` / ``stage0_beta`` the affine vectors of
-    the first of two row reductions."""
+    the first of two row reductions, ``out_dtype`` CF_FP32 or CF_BF16."""
     d = cf_epi_desc()
     d.version = 2
     d.n_ops = len(ops)
@@ -133,7 +134,7 @@ def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[to
     for i, op in enumerate(ops):
         d.ops[i].kind = OP_CODES[op[0]]
         d.ops[i].scalar = float(op[1]) if len(op) > 1 else 0.0
-    d.out_dtype = CF_FP32
+    d.out_dtype = out_dtype
     d.exchange = EXCHANGE_CODES[exchange]
     if residual is not None:
         d.residual = matrix(residual)
@@ -169,17 +170,19 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
                      out: Optional[torch.Tensor] = None, b_trans: bool = False, exchange: str = "auto",
                      workspace: Optional[torch.Tensor] = None, stream=None,
                      residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
-                     stage0_beta: Optional[torch.Tensor] = None) -> torch.Tensor:
+                     stage0_beta: Optional[torch.Tensor] = None,
+                     out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
     """out = epilogue(A @ B) in one fused kernel.  ``B`` is K x N, or N x K
     with ``b_trans=True``; ``residual`` (M x N, fp32 or bf16) feeds the
-    ``residual`` op.  A workspace is allocated if needed and not given."""
+    ``residual`` op.  ``out`` is fp32 or bf16 (``out_dtype`` when it is
+    allocated here).  A workspace is allocated if needed and not given."""
     lib = load_library()
     M = A.shape[0]
     N = B.shape[0] if b_trans else B.shape[1]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
-                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta))
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out)))
     need = int(lib.cf_workspace_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
@@ -195,7 +198,8 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
                              beta=None, out: Optional[torch.Tensor] = None, b_trans: bool = False,
                              exchange: str = "auto", stream=None,
                              residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
-                             stage0_beta: Optional[torch.Tensor] = None) -> torch.Tensor:
+                             stage0_beta: Optional[torch.Tensor] = None,
+                             out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
     """Same as cf_gemm_epilogue, but the library takes any scratch it needs
     from its own static device array: nothing is allocated by this call
     (``out`` must be given by callers that cannot allocate)."""
@@ -203,21 +207,21 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
     if out is None:
         M = A.shape[0]
         N = B.shape[0] if b_trans else B.shape[1]
-        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
-                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta))
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out)))
     st = lib.cf_gemm_epilogue_noalloc(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _stream(stream))
     _check(st, "cf_gemm_epilogue_noalloc")
     return out
 
 
-def b2b_desc(op: str, scale: float, batch: int, strides=(0, 0, 0, 0)) -> cf_b2b_desc:
+def b2b_desc(op: str, scale: float, batch: int, strides=(0, 0, 0, 0), out_dtype: int = CF_FP32) -> cf_b2b_desc:
     d = cf_b2b_desc()
     d.version = 1
     d.mid_op = MID_CODES[op]
     d.mid_scale = float(scale)
-    d.out_dtype = CF_FP32
+    d.out_dtype = out_dtype
     d.batch = batch
     d.strideA, d.strideW1, d.strideW2, d.strideOut = strides
     return d
@@ -236,14 +240,16 @@ def _b2b_views(A, W1, W2, w1_trans, out):
 
 
 def cf_b2bgemm(A: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, op: str, scale: float = 1.0,
-               w1_trans: bool = False, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """out = bf16(F(A @ W1)) @ W2, fused; tensors may carry a leading batch dim."""
+               w1_trans: bool = False, out: Optional[torch.Tensor] = None, stream=None,
+               out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """out = bf16(F(A @ W1)) @ W2, fused; tensors may carry a leading batch
+    dim.  ``out`` is fp32 or bf16 (``out_dtype`` when it is allocated here)."""
     lib = load_library()
     if out is None:
         shape = A.shape[:-1] + (W2.shape[-1],)
-        out = torch.empty(shape, dtype=torch.float32, device=A.device)
+        out = torch.empty(shape, dtype=out_dtype, device=A.device)
     batch, (a, w1, w2, o), strides = _b2b_views(A, W1, W2, w1_trans, out)
-    d = b2b_desc(op, scale, batch, strides)
+    d = b2b_desc(op, scale, batch, strides, _dtype_code(out))
     st = lib.cf_b2bgemm(ctypes.byref(a), ctypes.byref(w1), ctypes.byref(w2), ctypes.byref(d), ctypes.byref(o),
                         _stream(stream))
     _check(st, "cf_b2bgemm")
@@ -279,7 +285,7 @@ def cf_unfused_b2bgemm(A, W1, W2, op, scale=1.0, w1_trans=False, out=None, s_buf
     if p_buf is None:
         p_buf = torch.empty(mid_shape, dtype=torch.bfloat16, device=A.device)
     batch, (a, w1, w2, o), strides = _b2b_views(A, W1, W2, w1_trans, out)
-    d = b2b_desc(op, scale, batch, strides)
+    d = b2b_desc(op, scale, batch, strides, _dtype_code(out))
     st = lib.cf_unfused_b2bgemm(ctypes.byref(a), ctypes.byref(w1), ctypes.byref(w2), ctypes.byref(d),
                                 ctypes.byref(o), _ptr(s_buf), _ptr(p_buf), _stream(stream))
     _check(st, "cf_unfused_b2bgemm")

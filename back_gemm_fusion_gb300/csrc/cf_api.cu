@@ -102,16 +102,16 @@ cf_status check_matrix(const cf_matrix* m, int dtype, bool allow_trans) {
 }
 
 cf_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_t inner, uint64_t outer,
-                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return CF_ERR_CUDA;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(map, dt, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, dt, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CF_OK : CF_ERR_CUDA;
 }
 
@@ -194,9 +194,9 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   cf_status s;
   if ((s = check_matrix(A, CF_BF16, false)) != CF_OK) return s;
   if ((s = check_matrix(B, CF_BF16, true)) != CF_OK) return s;
-  if ((s = check_matrix(out, CF_FP32, false)) != CF_OK) return s;
   if ((s = parse_epi(epi, plan)) != CF_OK) return s;
-  if (epi->out_dtype != CF_FP32) return CF_ERR_INVALID_ARG;
+  if (epi->out_dtype != CF_FP32 && epi->out_dtype != CF_BF16) return CF_ERR_INVALID_ARG;
+  if ((s = check_matrix(out, epi->out_dtype, false)) != CF_OK) return s;
   const int64_t M = A->rows, K = A->cols, N = B->cols;
   if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
   if ((plan->need_bias && !bias) || (plan->need_gamma && !gamma) || (plan->need_beta && !beta))
@@ -330,7 +330,13 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
     return s;
   p.b_mn_major = B->trans == 0 ? 1 : 0;
-  if ((s = encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32, 32)) != CF_OK)
+  // fp32 out: 32 x 32 blocks of 128-byte rows, 128-byte swizzle; bf16 out:
+  // 32 x 32 blocks of 64-byte rows, unswizzled.
+  p.out_bf16 = epi->out_dtype == CF_BF16 ? 1 : 0;
+  if ((s = p.out_bf16 ? encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out->ptr, sh.N, sh.M, out->ld * 2, 32,
+                                  32, CU_TENSOR_MAP_SWIZZLE_NONE)
+                      : encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32,
+                                  32)) != CF_OK)
     return s;
   p.M = (int)sh.M;
   p.N = (int)sh.N;

@@ -83,6 +83,31 @@ __device__ __forceinline__ void store_row_packed_sw128(uint8_t* tile, int r, int
   }
 }
 
+// Store W values v[i] * s of one output row at element offset `off` of
+// `out`: fp32 (16-byte vector stores) or bf16 rounded to nearest even
+// (8 values per 16-byte store). W is a multiple of 8; `off` keeps each store
+// 16-byte aligned (row pitch and column offsets are checked on the host).
+template <int W>
+__device__ __forceinline__ void store_row(void* out, int bf16, long long off, const float* v, float s) {
+  if (bf16) {
+    uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
+#pragma unroll
+    for (int j = 0; j < W / 8; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * e] * s, v[8 * j + 2 * e + 1] * s);
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      d[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + off);
+#pragma unroll
+    for (int j = 0; j < W / 4; ++j) d[j] = make_float4(v[4 * j] * s, v[4 * j + 1] * s, v[4 * j + 2] * s, v[4 * j + 3] * s);
+  }
+}
+
 // ======================================================================
 // Attention-shaped B2BGEMM
 // ======================================================================
@@ -121,8 +146,9 @@ constexpr float kRescaleLog2 = 8.0f;
 
 struct Params {
   CUtensorMap tmA, tmW1, tmW2;  // 3-D: {128 cols, rows, batch}
-  float* out;
+  void* out;        // fp32 or bf16 (out_bf16), element offsets below
   long long ldo, stride_out;
+  int out_bf16;
   int M;             // rows of A per batch entry (the last 128-row block may be ragged)
   int batch, m_blocks, n1_blocks, items;
   int softmax;       // 1: scaled softmax, 0: ReLU (optionally scaled)
@@ -434,8 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), it & 1, wc))) break;
       tc_fence_after();
-      float4* dst = reinterpret_cast<float4*>(p.out + (long long)b * p.stride_out +
-                                              (long long)(mb * kTile + row) * p.ldo);
+      const long long orow = (long long)b * p.stride_out + (long long)(mb * kTile + row) * p.ldo;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float o[64];
@@ -448,9 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
         }
         if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            dst[16 * h + e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+          store_row<64>(p.out, p.out_bf16, orow + 64 * h, o, inv);
         }
       }
     }
@@ -497,8 +520,9 @@ struct Params {
   CUtensorMap tmA;   // {K, M, batch}, box {64, 128, 1}
   CUtensorMap tmW1;  // MN-major: {N1, K, batch} box {64, 64, 1}; K-major: {K, N1, batch} box {64, 128, 1}
   CUtensorMap tmW2;  // {N2, N1, batch}, box {64, 64, 1}
-  float* out;
+  void* out;        // fp32 or bf16 (out_bf16), element offsets below
   long long ldo, stride_out;
+  int out_bf16;
   int M;             // rows of A per batch entry (the last 128-row strip may be ragged)
   int w1_k_major;
   int C;             // CTAs per cluster = N2 / 256
@@ -745,16 +769,14 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       // Epilogue: this CTA's 128 x 256 block of O, straight from TMEM to HBM.
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), t & 1, wc))) break;
       tc_fence_after();
-      float* orow = p.out + (long long)b * p.stride_out + (long long)(strip * 128 + row) * p.ldo + rank * 256;
+      const long long orow = (long long)b * p.stride_out + (long long)(strip * 128 + row) * p.ldo + rank * 256;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         float v[32];
         tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
         tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
         if (strip * 128 + row < p.M) {  // rows past M (ragged last strip) are not stored
-#pragma unroll
-          for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          store_row<32>(p.out, p.out_bf16, orow + c * 32, v, 1.0f);
         }
       }
       tc_fence_before();
@@ -835,7 +857,8 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
     const uint32_t box[3] = {64, 64, 1};
     if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
   }
-  p.out = static_cast<float*>(out->ptr);
+  p.out = out->ptr;
+  p.out_bf16 = out->dtype == CF_BF16 ? 1 : 0;
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.C = (int)C;
@@ -888,18 +911,19 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   if (!d || d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
   if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX || !std::isfinite(d->mid_scale))
     return CF_ERR_INVALID_ARG;
-  if (d->out_dtype != CF_FP32) return CF_ERR_INVALID_ARG;
+  if (d->out_dtype != CF_FP32 && d->out_dtype != CF_BF16) return CF_ERR_INVALID_ARG;
   if ((s = check_bf16_view(A, false)) != CF_OK) return s;
   if ((s = check_bf16_view(W1, true)) != CF_OK) return s;
   if ((s = check_bf16_view(W2, false)) != CF_OK) return s;
-  if (!out || !out->ptr || out->dtype != CF_FP32 || out->trans) return CF_ERR_INVALID_ARG;
+  if (!out || !out->ptr || out->dtype != d->out_dtype || out->trans) return CF_ERR_INVALID_ARG;
   if (out->ld < out->cols) return CF_ERR_INVALID_ARG;
-  if (!aligned16(out->ptr) || (out->ld * 4) % 16 != 0) return CF_ERR_MISALIGNED;
+  const int64_t out_elem = out->dtype == CF_BF16 ? 2 : 4;
+  if (!aligned16(out->ptr) || (out->ld * out_elem) % 16 != 0) return CF_ERR_MISALIGNED;
   const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols, batch = d->batch;
   if (W1->rows != K || W2->rows != N1 || out->rows != M || out->cols != N2) return CF_ERR_INVALID_ARG;
   if (d->strideA < 0 || d->strideW1 < 0 || d->strideW2 < 0 || d->strideOut < 0) return CF_ERR_INVALID_ARG;
   if (batch > 1 && ((d->strideA * 2) % 16 || (d->strideW1 * 2) % 16 || (d->strideW2 * 2) % 16 ||
-                    (d->strideOut * 4) % 16))
+                    (d->strideOut * out_elem) % 16))
     return CF_ERR_MISALIGNED;
   if (M == 0 || N2 == 0) return CF_OK;
 
@@ -936,7 +960,8 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
     const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
   }
-  p.out = static_cast<float*>(out->ptr);
+  p.out = out->ptr;
+  p.out_bf16 = out->dtype == CF_BF16 ? 1 : 0;
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.batch = (int)bs;

@@ -32,6 +32,7 @@
 // the output and (for the wide-row fallback) 8 bytes per row per tile of
 // statistics touch global memory.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "cf_internal.h"
@@ -656,11 +657,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         // The previous TMA store from this buffer must have read it.
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
-        // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r & 7).
+        if (p.out_bf16) {
+          // bf16: 64-byte rows, unswizzled; lane l writes its 16-byte chunks
+          // starting at chunk l & 3 to spread them over the banks.
+          uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float4* dst = reinterpret_cast<float4*>(out_ptr + lane * 128 + ((j ^ (lane & 7)) * 16));
-          *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = (jj + lane) & 3;
+            uint4 val;
+            switch (j) {  // constant register indices for each case
+              case 0: val = make_uint4(w[0], w[1], w[2], w[3]); break;
+              case 1: val = make_uint4(w[4], w[5], w[6], w[7]); break;
+              case 2: val = make_uint4(w[8], w[9], w[10], w[11]); break;
+              default: val = make_uint4(w[12], w[13], w[14], w[15]); break;
+            }
+            *reinterpret_cast<uint4*>(out_ptr + lane * 64 + j * 16) = val;
+          }
+        } else {
+          // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r & 7).
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4* dst = reinterpret_cast<float4*>(out_ptr + lane * 128 + ((j ^ (lane & 7)) * 16));
+            *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();

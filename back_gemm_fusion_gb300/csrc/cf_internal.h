@@ -28,7 +28,7 @@ constexpr int row_code(int rowop0, int rowop) { return rowop + 4 * rowop0; }
 struct GemmEpiParams {
   CUtensorMap tmA;    // A: bf16 [M][K], box {64, 128}, 128B swizzle
   CUtensorMap tmB;    // B: K-major [N][K] box {64, 256} or MN-major [K][N] box {64, 64}
-  CUtensorMap tmOut;  // out: fp32 [M][N], box {32, 32}, 128B swizzle
+  CUtensorMap tmOut;  // out: fp32 [M][N], box {32, 32}, 128B swizzle; or bf16, box {32, 32}, no swizzle
   int M, N, K;
   int tiles_n;        // N / kBN
   int strips;         // M / kBM
@@ -54,6 +54,7 @@ struct GemmEpiParams {
   const void* res;        // residual matrix (CF_OP_ADD_RESIDUAL), M x N, leading dim res_ld
   long long res_ld;
   int res_bf16;           // 1: bf16 residual, 0: fp32
+  int out_bf16;           // 1: bf16 output (rounded to nearest even), 0: fp32
   float2* ws_stats;       // [strips][tiles_n][kBM] partial row statistics
   unsigned* ws_count;     // [strips][4] arrival counters (cleared by the host)
   unsigned* status;       // device status word

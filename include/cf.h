@@ -116,7 +116,9 @@ typedef struct {
   uint32_t version;  /* 1 or 2 (CF_EPI_VERSION); version 1 ends after `exchange` */
   uint32_t n_ops;    /* 0..CF_EPI_MAX_OPS */
   cf_op ops[CF_EPI_MAX_OPS];
-  int32_t out_dtype; /* cf_dtype of `out`; CF_FP32 in this version */
+  int32_t out_dtype; /* cf_dtype of `out`: CF_FP32, or CF_BF16 (each value
+                        rounded to nearest even from the fp32 epilogue
+                        result; the fused entry points only) */
   int32_t exchange;  /* cf_exchange */
   /* Version 2: the matrix read by CF_OP_ADD_RESIDUAL (the residual stream of
    * a post-norm block): M x N, fp32 or bf16, trans == 0, pointer and leading
@@ -138,7 +140,7 @@ typedef struct {
  *   bias, gamma, beta : device fp32 vectors of length N; required only when
  *          the program uses CF_OP_BIAS / a norm (beta only for LayerNorm);
  *          may be NULL otherwise.
- *   out  : M x N, fp32, trans == 0.
+ *   out  : M x N, trans == 0, dtype == epi->out_dtype (fp32 or bf16).
  *   workspace : device memory of at least cf_workspace_size(...) bytes when
  *          that is non-zero (per-tile partial row statistics and arrival
  *          counters; the call clears the counters on `stream`).  Its contents
@@ -205,7 +207,9 @@ typedef struct {
   uint32_t version;  /* must be CF_B2B_VERSION */
   int32_t mid_op;    /* cf_mid_op */
   float mid_scale;   /* scale for the SCALE_* ops */
-  int32_t out_dtype; /* CF_FP32 in this version */
+  int32_t out_dtype; /* cf_dtype of `out`: CF_FP32, or CF_BF16 (rounded to
+                        nearest even from the fp32 accumulator; cf_b2bgemm
+                        only) */
   int64_t batch;     /* number of independent problems (>= 1) */
   int64_t strideA, strideW1, strideW2, strideOut; /* elements between problems */
 } cf_b2b_desc;
@@ -218,7 +222,7 @@ typedef struct {
  *   W1  : K x N1 bf16; trans == 0 (stored K x N1) or trans == 1 (stored
  *         N1 x K, e.g. the key matrix of attention, giving S = Q K^T).
  *   W2  : N1 x N2 bf16, trans == 0 (stored N1 x N2, e.g. the value matrix).
- *   out : M x N2 fp32, trans == 0.
+ *   out : M x N2, trans == 0, dtype == desc->out_dtype (fp32 or bf16).
  *   The softmax mid op normalises each row of S over all N1 columns.
  *
  * Shape rules (this version), two kernels:
@@ -237,8 +241,8 @@ CF_API cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_ma
  * cf_unfused_gemm_epilogue -- the unfused comparison path: a cuBLASLt GEMM
  * writes P (M x N fp32) to `intermediate`, then a separate row-epilogue
  * kernel reads it back and writes `out`.  Same program semantics as
- * cf_gemm_epilogue.  `intermediate` is caller-owned device memory of
- * M * N * 4 bytes.
+ * cf_gemm_epilogue, fp32 `out` only.  `intermediate` is caller-owned
+ * device memory of M * N * 4 bytes.
  */
 CF_API cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
                                    const float* bias, const float* gamma, const float* beta,
@@ -248,7 +252,8 @@ CF_API cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B
 /*
  * cf_unfused_b2bgemm -- unfused comparison path for B2BGEMM: cuBLASLt GEMM1
  * to `s_buf` (M x N1 fp32), a mid-op kernel writing bf16 S' to `p_buf`
- * (M x N1 bf16), cuBLASLt GEMM2 to `out`.  Same semantics as cf_b2bgemm.
+ * (M x N1 bf16), cuBLASLt GEMM2 to `out` (fp32 or bf16).  Same semantics
+ * as cf_b2bgemm.
  */
 CF_API cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
                              const cf_b2b_desc* desc, cf_matrix* out,

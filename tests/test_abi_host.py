@@ -159,3 +159,56 @@ def test_chained_reduction_rules(lib):
     one = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(epi_desc([("rmsnorm", 1e-6)])))
     two = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(B), ctypes.byref(d))
     assert one > 0 and two == 2 * one                                    # one statistics region per stage
+
+
+def test_output_dtype_rules(lib):
+    # out may be fp32 or bf16; its dtype must match the descriptor's, and a
+    # bf16 leading dimension must keep 16-byte row alignment (8 elements).
+    from back_gemm_fusion_gb300.binding import cf_matrix, epi_desc, CF_FP32, CF_BF16
+    A, B, _ = _mats()
+
+    def call(out, out_dtype):
+        d = epi_desc(LN, out_dtype=out_dtype)
+        return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                    ctypes.byref(out), None, 0, None)
+
+    assert call(cf_matrix(0x30000, CF_BF16, 0, 256, 256, 256), CF_FP32) == 1   # dtype differs from the descriptor
+    assert call(cf_matrix(0x30000, CF_FP32, 0, 256, 256, 256), CF_BF16) == 1
+    assert call(cf_matrix(0x30000, CF_BF16, 0, 256, 256, 256), 7) == 1         # unknown dtype
+    assert call(cf_matrix(0x30000, CF_BF16, 0, 256, 256, 260), CF_BF16) == 3   # 520-byte rows
+    assert call(cf_matrix(0x30008, CF_BF16, 0, 256, 256, 256), CF_BF16) == 3   # misaligned pointer
+    assert call(cf_matrix(0x30000, CF_BF16, 0, 256, 256, 264), CF_BF16) in (0, 4, 8)  # valid: device check follows
+    assert call(cf_matrix(0x30000, CF_FP32, 0, 256, 256, 260), CF_FP32) in (0, 4, 8)
+
+
+def test_b2b_validation(lib):
+    from back_gemm_fusion_gb300.binding import cf_matrix, b2b_desc, CF_FP32, CF_BF16
+    Q = cf_matrix(0x10000, CF_BF16, 0, 256, 128, 128)
+    K = cf_matrix(0x20000, CF_BF16, 1, 128, 512, 128)   # stored 512 x 128, used transposed
+    V = cf_matrix(0x30000, CF_BF16, 0, 512, 128, 128)
+
+    def call(out, out_dtype=CF_FP32, op="scale_softmax", W1=K, A=Q, batch=1):
+        d = b2b_desc(op, 0.125, batch, out_dtype=out_dtype)
+        return lib.cf_b2bgemm(ctypes.byref(A), ctypes.byref(W1), ctypes.byref(V), ctypes.byref(d),
+                              ctypes.byref(out), None)
+
+    O32 = cf_matrix(0x40000, CF_FP32, 0, 256, 128, 128)
+    O16 = cf_matrix(0x40000, CF_BF16, 0, 256, 128, 128)
+    assert call(O32) in (0, 4, 8)                                       # attention shape, fp32 out
+    assert call(O16, CF_BF16) in (0, 4, 8)                              # attention shape, bf16 out
+    assert call(O16, CF_FP32) == 1                                      # out dtype differs from the descriptor
+    assert call(cf_matrix(0x40000, CF_BF16, 0, 256, 128, 132), CF_BF16) == 3  # 264-byte rows
+    assert call(O32, batch=0) == 1                                      # no problems
+    assert call(cf_matrix(0x40000, CF_FP32, 0, 256, 64, 128)) == 1      # out shape differs
+    assert call(O32, W1=cf_matrix(0x20000, CF_BF16, 0, 128, 512, 512)) == 2  # softmax needs the attention shape
+    X = cf_matrix(0x10000, CF_BF16, 0, 256, 128, 128)
+    W1 = cf_matrix(0x20000, CF_BF16, 0, 128, 512, 512)
+    W2 = cf_matrix(0x30000, CF_BF16, 0, 512, 256, 256)
+
+    def mlp(out, out_dtype=CF_FP32, op="relu"):
+        d = b2b_desc(op, 1.0, 1, out_dtype=out_dtype)
+        return lib.cf_b2bgemm(ctypes.byref(X), ctypes.byref(W1), ctypes.byref(W2), ctypes.byref(d),
+                              ctypes.byref(out), None)
+
+    assert mlp(cf_matrix(0x40000, CF_BF16, 0, 256, 256, 256), CF_BF16) in (0, 4, 8)  # MLP shape, bf16 out
+    assert mlp(cf_matrix(0x40000, CF_FP32, 0, 256, 256, 256), op="scale_softmax") == 2  # MLP: elementwise F only

@@ -196,3 +196,57 @@ def test_b2b_rejects_unsupported(cf):
     X, W1, W2 = _mlp_case(128, 64, 384, 1024, seed=1)  # N1 not a multiple of 128 * 4
     with pytest.raises(cf.CFError):
         cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu")
+
+
+def _bf16_gate(gpu, ref, absbound, what):
+    """bf16 output: the fp32 result (within the B2B bound of the oracle) is
+    rounded once more to nearest even (unit roundoff 2^-8), which adds
+    2^-8 |ref| (plus its own
+    small share of the fp32 bound).  The fp32 contract gate is taken on the
+    fp32 output of the same call; a bf16 value of magnitude 2^k carries a
+    half-ulp of 2^(k-8), more than 1e-2 rms for large elements."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    bound = (2.0 ** -7 * absbound + 1e-5 * rms + 1e-7) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref)
+    worst = (np.abs(gpu - ref) / bound).max()
+    assert worst <= 1.0, f"{what}: bf16-output bound exceeded ({worst:.3g} x)"
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("batch,Lq,L", [(2, 256, 256), (2, 77, 384), (1, 128, 1024)])
+def test_attention_bf16_output(cf, batch, Lq, L, op):
+    rng = np.random.default_rng(Lq + L)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    Q, K, V = (t(rng.standard_normal((batch, n, 128))) for n in (Lq, L, L))
+    scale = 1 / math.sqrt(128)
+    g = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, out_dtype=torch.bfloat16)
+    f = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert g.dtype == torch.bfloat16 and g.shape == (batch, Lq, 128)
+    assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16)), "bf16 out differs from the rounded fp32 out"
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    got = g.float().cpu().numpy()
+    got32 = f.cpu().numpy()
+    for b in range(batch):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        bound = _abs_bound(q[b], k[b], v[b], op, scale)
+        b2b_gate(got32[b], ref, bound, f"attention fp32 {op} b={b}")
+        _bf16_gate(got[b], ref, bound, f"attention bf16 {op} b={b}")
+
+
+@pytest.mark.parametrize("M,K,N1,N2", [(77, 200, 512, 256), (256, 128, 1024, 1024), (8, 512, 128, 256)])
+def test_mlp_bf16_output(cf, M, K, N1, N2):
+    X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M + 3 * K)
+    g = cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu", out_dtype=torch.bfloat16)
+    f = cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu")
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16)), "bf16 out differs from the rounded fp32 out"
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
+    b2b_gate(f.cpu().numpy(), ref, bound, f"mlp fp32 {M}x{K}x{N1}x{N2}")
+    _bf16_gate(g.float().cpu().numpy(), ref, bound, f"mlp bf16 {M}x{K}x{N1}x{N2}")

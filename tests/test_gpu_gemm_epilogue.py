@@ -209,3 +209,70 @@ def test_scaled_softmax_full_size_sampled(cf):
     assert_rows_close(gpu[rows], ref, what="gemm+scaled softmax 4096x16384x4096")
     # Every row of a softmax sums to one (all rows, not only the sample).
     assert np.max(np.abs(gpu.sum(1, dtype=np.float64) - 1.0)) < 1e-3
+
+
+def bf16_out_gate(gpu, ref, strict, what):
+    """bf16 output: the kernel's fp32 value f (within strict * rms of the
+    oracle row) is rounded once to nearest even (8-bit significand, unit
+    roundoff 2^-8), |g - f| <= 2^-8 |f|, so
+    |g - ref| <= 2^-8 |ref| + (1 + 2^-8) strict * rms per element.  The fp32
+    contract gate is taken on the fp32 output of the same program."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
+    err = np.abs(gpu - ref)
+    rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+    bound = 2.0 ** -8 * np.abs(ref) + (1 + 2.0 ** -8) * strict * rms + 1e-30
+    worst = (err / bound).max()
+    assert worst <= 1.0, f"{what}: bf16-output bound exceeded ({worst:.3g} x)"
+
+
+BF16_PROGRAMS = {
+    "gelu": ([("bias",), ("gelu_tanh",)], 1e-4),
+    "layernorm": ([("bias",), ("layernorm", 1e-5)], 2e-3),
+    "rmsnorm": ([("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)], 2e-3),
+    "softmax": ([("scale", 0.125), ("softmax",)], 2e-3),
+    "chained": ([("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)], 2e-3),
+}
+
+
+@pytest.mark.parametrize("exchange", ["auto", "global"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (333, 2048, 200), (128, 4352, 64)])
+@pytest.mark.parametrize("prog", sorted(BF16_PROGRAMS))
+def test_bf16_output(cf, prog, M, N, K, exchange):
+    # bf16 output tiles: rounded in the epilogue, stored by TMA from an
+    # unswizzled staging buffer (ragged M and K, cluster and workspace
+    # exchanges, 1-CTA and CTA-pair tiles).
+    ops, strict = BF16_PROGRAMS[prog]
+    if prog == "chained" and exchange == "auto":
+        exchange = "global"  # chained programs take the workspace exchange in any case
+    case = I.gemm_epilogue_case("bf16_out", M, N, K, ops, seed=M + N + K, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    A, B = case.A.cuda(), case.B.cuda()
+    args = (A, B, case.ops, _dev(case.bias), _dev(case.gamma), _dev(case.beta))
+    g = cf.cf_gemm_epilogue(*args, exchange=exchange, out_dtype=torch.bfloat16)
+    f = cf.cf_gemm_epilogue(*args, exchange=exchange)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert g.dtype == torch.bfloat16
+    ref = _oracle(case)
+    assert_rows_close(f.cpu().numpy(), ref, strict=strict, what=f"fp32 out {prog} {M}x{N}x{K} {exchange}")
+    bf16_out_gate(g.float().cpu().numpy(), ref, strict, f"bf16 out {prog} {M}x{N}x{K} {exchange}")
+    # The same epilogue value is rounded: the bf16 tile is the fp32 tile
+    # rounded to nearest even, element for element.
+    assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16)), f"bf16 out {prog}: differs from rounded fp32 out"
+
+
+def test_bf16_output_strided_noalloc(cf):
+    # A bf16 output view with a padded leading dimension, written through the
+    # no-allocation entry point; the padding columns stay untouched.
+    case = I.gemm_epilogue_case("bf16_ld", 200, 1024, 128, [("bias",), ("rmsnorm", 1e-6)], seed=5, need_bias=True,
+                                need_gamma=True)
+    buf = torch.full((200, 1024 + 40), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[:, :1024]
+    cf.cf_gemm_epilogue_noalloc(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma), None,
+                                out=out)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    bf16_out_gate(out.float().cpu().numpy(), _oracle(case), 2e-3, "bf16 out, padded ld")
+    assert torch.all(buf[:, 1024:] == 7.0)

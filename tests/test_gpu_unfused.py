@@ -75,3 +75,16 @@ def test_unfused_mlp(cf):
     ref = O.b2bgemm(x, w1, w2, "relu")
     bound = 2.0 ** -7 * (np.abs(np.maximum(x @ w1, 0)) @ np.abs(w2)) + 1e-6
     assert np.all(np.abs(out.cpu().numpy() - ref) <= bound)
+
+
+def test_unfused_mlp_bf16_output(cf):
+    # bf16 output from the second cuBLASLt GEMM (fp32 accumulation, one
+    # rounding to nearest even at the store).
+    case = I.mlp_b2b(M=256, K=256, N1=1024, N2=512)
+    out = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+    cf.cf_unfused_b2bgemm(case.A[0].cuda(), case.W1[0].cuda(), case.W2[0].cuda(), "relu", out=out)
+    torch.cuda.synchronize()
+    x, w1, w2 = I.to_f64(case.A[0]), I.to_f64(case.W1[0]), I.to_f64(case.W2[0])
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = 2.0 ** -7 * (np.abs(np.maximum(x @ w1, 0)) @ np.abs(w2)) + 2.0 ** -8 * np.abs(ref) * 1.01 + 1e-6
+    assert np.all(np.abs(out.float().cpu().numpy() - ref) <= bound)
