@@ -28,10 +28,11 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   unsigned* status = nullptr;
   // Indexed by the kernel variant's row code (row_code(first, last row op)).
-  bool prepared[kRowCodes][3][2] = {};
-  int max_clusters[kRowCodes][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
-  int max_pairs[kRowCodes][3] = {};                        // resident 2-CTA clusters per (row code, xmode)
-  int blocks_per_sm[kRowCodes][3] = {};                    // 0 = unknown
+  // Indexed [row code][ragged-N kernels][...].
+  bool prepared[kRowCodes][2][3][2] = {};
+  int max_clusters[kRowCodes][2][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
+  int max_pairs[kRowCodes][2][3] = {};                        // resident 2-CTA clusters per (row code, xmode)
+  int blocks_per_sm[kRowCodes][2][3] = {};                    // 0 = unknown
 };
 
 std::mutex g_mu;
@@ -221,9 +222,12 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   // the TMA stores of the last (ragged) 128-row strip; rows are independent.
   // K >= 64 with K % 8 == 0: the last 64-wide K block reads zeros past K
   // (TMA out-of-bounds fill), which add nothing to the products.
-  if (N % kBN != 0 || K % 8 != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
+  // Any N >= 1: the last 256-column tile of a row may be ragged; its B
+  // columns past N load as zeros, the epilogue keeps them out of the row
+  // statistics and never reads a vector past N, and the TMA stores clip them.
+  if (K % 8 != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
-  const int64_t tiles_n = N / kBN;
+  const int64_t tiles_n = (N + kBN - 1) / kBN;
   if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)
     return CF_ERR_UNSUPPORTED_SHAPE;
   return CF_OK;
@@ -294,8 +298,8 @@ size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_de
   EpiPlan plan;
   if (parse_epi(epi, &plan) != CF_OK) return 0;
   const int64_t M = A->rows, N = B->cols;
-  if (M <= 0 || N <= 0 || N % kBN != 0) return 0;
-  const int64_t tiles_n = N / kBN;
+  if (M <= 0 || N <= 0) return 0;
+  const int64_t tiles_n = (N + kBN - 1) / kBN;
   // The cluster path may fall back to the workspace path when no cluster of
   // that size can be resident, so AUTO/CLUSTER strips that fit a cluster
   // still report the (small) fallback workspace.
@@ -312,7 +316,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   cf_status s = validate_gemm_epi(A, B, bias, gamma, beta, epi, out, &plan, &sh);
   if (s != CF_OK) return s;
   if (sh.M == 0 || sh.N == 0) return CF_OK;
-  const int64_t tiles_n = sh.N / kBN, strips = (sh.M + kBM - 1) / kBM;
+  const int64_t tiles_n = (sh.N + kBN - 1) / kBN, strips = (sh.M + kBM - 1) / kBM;
   int xmode = choose_xmode(plan, epi, tiles_n);
   const int code = plan.code();
   const size_t ws_stage = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
@@ -367,6 +371,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   p.status = dev->status;
   p.timeout_cycles = wait_timeout_cycles();
 
+  const int rag = sh.N % kBN != 0 ? 1 : 0;  // the last tile of each row is ragged
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int x = X_NONE; x <= X_GLOBAL; ++x) {
@@ -374,9 +379,9 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       if (plan.rowop0 != ROW_NONE && x == X_CLUSTER) continue;  // not instantiated for chained stages
       for (int pr = 0; pr < 2; ++pr) {
         if (pr == 1 && x == X_CLUSTER) continue;
-        if (!dev->prepared[code][x][pr]) {
-          if (gemm_epi_prepare(code, x, pr == 1) != cudaSuccess) return CF_ERR_CUDA;
-          dev->prepared[code][x][pr] = true;
+        if (!dev->prepared[code][rag][x][pr]) {
+          if (gemm_epi_prepare(code, x, pr == 1, rag != 0) != cudaSuccess) return CF_ERR_CUDA;
+          dev->prepared[code][rag][x][pr] = true;
         }
       }
     }
@@ -386,10 +391,10 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int maxc = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_clusters[code][tiles_n];
+      int& cached = dev->max_clusters[code][rag][tiles_n];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(code, X_CLUSTER, false, (int)tiles_n, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, X_CLUSTER, false, rag != 0, (int)tiles_n, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -429,10 +434,10 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int maxp = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_pairs[code][xmode];
+      int& cached = dev->max_pairs[code][rag][xmode];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(code, xmode, true, 2, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, xmode, true, rag != 0, 2, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -449,8 +454,8 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int per_sm = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->blocks_per_sm[code][xmode];
-      if (cached == 0 && gemm_epi_max_blocks_per_sm(code, xmode, &cached) != cudaSuccess) cached = 0;
+      int& cached = dev->blocks_per_sm[code][rag][xmode];
+      if (cached == 0 && gemm_epi_max_blocks_per_sm(code, xmode, rag != 0, &cached) != cudaSuccess) cached = 0;
       per_sm = cached;
     }
     if (per_sm < 1) return CF_ERR_CUDA;

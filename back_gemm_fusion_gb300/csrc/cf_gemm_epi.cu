@@ -1,784 +1,32 @@
-// cf_gemm_epi.cu -- fused GEMM + epilogue program for sm_103a.
-//
-// The Stage-Stream Execution Model of the ComFuse review ("What carries the
-// argument"): the GEMM's accumulator tile streams through the elementwise
-// nodes while still on chip, and the trailing row reduction (LayerNorm,
-// RMSNorm, softmax) is a stage boundary whose statistics are aggregated
-// hierarchically.  Tile-strip locality (referee report, major comment 1
-// [Sec. III, Eq. (1)]) means one output row depends only on the CTAs that
-// share its 128-row strip.
-//
-// GB300 design (not the pages' Hopper/CUTLASS one):
-//   * warp 0   : TMA producer -- A [128 x 64] and B [256 x 64] bf16 tiles,
-//                128-byte swizzle, into a 4-stage shared-memory ring.
-//   * warp 1   : TMEM allocator and single-thread tcgen05.mma issuer,
-//                128 x 256 x 16 bf16 MMAs accumulating fp32 in TMEM; two
-//                256-column accumulators so tile t+1's main loop overlaps
-//                tile t's epilogue (the review's PingPong overlap, Sec. III-C).
-//   * warps 2-5: epilogue.  tcgen05.ld's 32x32b shape gives each thread one
-//                accumulator row, so the "intra-warp" level of the review's
-//                three-level reduction is a register loop over the thread's
-//                own columns; the activated values are written back to TMEM
-//                so the normalisation pass does not recompute them.
-//   * level 3  : CTAs sharing a row strip exchange per-row partial statistics
-//                either through distributed shared memory inside one
-//                thread-block cluster (<= 16 CTAs; peer-to-peer all-gather,
-//                the review's "cross-broadcast" mode, Sec. III-A) or, when
-//                the strip is wider than a cluster, through a small global
-//                workspace of per-tile partials with bounded waits.
-//   * output   : each epilogue warp stages a 32 x 32 fp32 block in swizzled
-//                shared memory and writes it with a TMA store.
-// The pre-normalisation tile never leaves the SM: only A, B, the vectors,
-// the output and (for the wide-row fallback) 8 bytes per row per tile of
-// statistics touch global memory.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
-#include "cf_internal.h"
-#include "cf_ptx.cuh"
+// cf_gemm_epi.cu -- host side of the fused GEMM + epilogue kernel: kernel
+// selection, function attributes, occupancy queries and the launch.  This
+// unit instantiates the full-tile kernels (N a multiple of 256);
+// cf_gemm_epi_ragged.cu the ones whose last tile per row is ragged.
+#include "cf_gemm_epi_kernel.cuh"
 
 namespace cf {
+
+// Defined in cf_gemm_epi_ragged.cu.
+const void* gemm_epi_select_ragged(int rowop, int xmode, bool pair);
+
 namespace {
-
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kAStageBytes = kBM * kBK * 2;              // 16 KB
-constexpr int kOutStageBytes = 32 * 32 * 4;              // 4 KB per epilogue warp
-constexpr int kTmemCols = 2 * kBN;                       // two accumulators
-
-// Per-mode geometry.  CTA2: a CTA pair runs 256 x 256 MMAs (cta_group::2),
-// each CTA holding its 128 rows of A and half (128 columns) of the B tile,
-// so a stage is 32 KB and six fit; otherwise 48 KB stages, four of them.
-template <bool CTA2>
-struct Geo {
-  static constexpr int kStages = CTA2 ? 6 : 4;
-  static constexpr int kBStageBytes = (CTA2 ? kBN / 2 : kBN) * kBK * 2;
-  static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
-  static constexpr int kOffOut = kStages * kStageBytes;
-  static constexpr int kOffSlots = kOffOut + kEpiWarps * kOutStageBytes;  // float2 [2][128]
-  static constexpr int kOffBars = kOffSlots + 2 * kBM * 8;
-  // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[2][4], sempty[2][4], drain
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32)
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack for the 1024-byte alignment
-};
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-enum OpKind : int { OP_BIAS = 1, OP_SCALE = 2, OP_RELU = 3, OP_GELU_TANH = 4, OP_ADD_RESIDUAL = 5 };
-
-__device__ __forceinline__ float gelu_tanh(float x) {
-  // 0.5 x (1 + tanh(u)) == x * sigmoid(2u) == x / (1 + exp(-2u)),
-  // u = sqrt(2/pi) (x + 0.044715 x^3).
-  const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-  return __fdividef(x, 1.0f + ex2_approx(-2.0f * kLog2e * u));
+const void* select_kernel(int rowop, int xmode, bool pair, bool rag) {
+  return rag ? gemm_epi_select_ragged(rowop, xmode, pair) : select_kernel_t<false>(rowop, xmode, pair);
 }
-
-// Apply the elementwise program to 32 consecutive columns starting at n.
-// Elementwise ops [o0, o1) of the program on 32 consecutive columns n.. of
-// row m of the tile.
-__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m, int o0, int o1) {
-  for (int o = o0; o < o1; ++o) {
-    const int kind = p.op_kind[o];
-    if (kind == OP_ADD_RESIDUAL) {
-      // Each thread owns one row: 128 (fp32) or 64 (bf16) contiguous bytes of
-      // the residual row, read with 16-byte loads.  Rows past M (a ragged
-      // last strip) are never stored, so they skip the read.
-      if (m < p.M) {
-        if (p.res_bf16) {
-          const uint4* r4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.res) +
-                                                           (long long)m * p.res_ld + n);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 w = __ldg(r4 + j);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[8 * j + 2 * e] += __uint_as_float(ww[e] << 16);
-              v[8 * j + 2 * e + 1] += __uint_as_float(ww[e] & 0xffff0000u);
-            }
-          }
-        } else {
-          const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.res) +
-                                                             (long long)m * p.res_ld + n);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 r = __ldg(r4 + j);
-            v[4 * j + 0] += r.x;
-            v[4 * j + 1] += r.y;
-            v[4 * j + 2] += r.z;
-            v[4 * j + 3] += r.w;
-          }
-        }
-      }
-    } else if (kind == OP_BIAS) {
-      const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 b = __ldg(b4 + j);
-        v[4 * j + 0] += b.x;
-        v[4 * j + 1] += b.y;
-        v[4 * j + 2] += b.z;
-        v[4 * j + 3] += b.w;
-      }
-    } else if (kind == OP_SCALE) {
-      const float s = p.op_scalar[o];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= s;
-    } else if (kind == OP_RELU) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
-    } else if (kind == OP_GELU_TANH) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
-    }
-  }
-}
-
-// Per-row statistics of a row segment and their merge (fixed order in every
-// CTA, so all CTAs of a strip derive bit-identical row statistics).
-//   LayerNorm: (mean, M2) over kBN columns, merged with Chan et al.'s
-//              pairwise update for equal counts.
-//   RMSNorm:   (sum x^2, 0), merged by addition.
-//   softmax:   (max, sum exp(x - max)), merged by rescaling to the new max.
-template <int ROWOP>
-struct Stat {
-  __device__ static float2 identity() {
-    if (ROWOP == ROW_SOFTMAX) return make_float2(-INFINITY, 0.0f);
-    return make_float2(0.0f, 0.0f);
-  }
-  // Merge segment b (of n_b = kBN columns) into a (of n_a columns).
-  __device__ static float2 merge(float2 a, float2 b, float n_a) {
-    if (ROWOP == ROW_RMSNORM) return make_float2(a.x + b.x, 0.0f);
-    if (ROWOP == ROW_SOFTMAX) {
-      const float m = fmaxf(a.x, b.x);
-      const float la = (a.y == 0.0f) ? 0.0f : a.y * ex2_approx((a.x - m) * kLog2e);
-      const float lb = (b.y == 0.0f) ? 0.0f : b.y * ex2_approx((b.x - m) * kLog2e);
-      return make_float2(m, la + lb);
-    }
-    // LayerNorm
-    const float n_b = (float)kBN;
-    const float n = n_a + n_b;
-    const float d = b.x - a.x;
-    return make_float2(a.x + d * (n_b / n), a.y + b.y + d * d * (n_a * n_b / n));
-  }
-};
-
-// Strip-wide merge of per-tile row statistics `st` through the workspace
-// (the fallback exchange): publish, count arrivals (release), wait (bounded,
-// acquire) for every tile of the strip, merge in tile order.
-template <int R>
-__device__ __forceinline__ bool global_exchange(const GemmEpiParams& p, float2* ws_stats, unsigned* ws_count,
-                                                int strip, int tile, int row, int q, int lane,
-                                                volatile int* abort_flag, const WaitCtx& wc, float2& st) {
-  float2* wsrow = ws_stats + (size_t)strip * p.tiles_n * kBM + row;
-  __stcg(wsrow + (size_t)tile * kBM, st);
-  __threadfence();
-  __syncwarp();
-  unsigned* cnt = ws_count + strip * 4 + q;
-  if (lane == 0) red_release_gpu_add(cnt, 1u);
-  bool ok = true;
-  if (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-    const long long t0 = clock64();
-    while (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-      __nanosleep(64);
-      if (*abort_flag) { ok = false; break; }
-      if (clock64() - t0 > p.timeout_cycles) { record_timeout(wc); ok = false; break; }
-    }
-  }
-  if (!__all_sync(0xffffffffu, ok)) return false;
-  float2 tot = __ldcg(wsrow);
-  float n_acc = (float)kBN;
-  for (int j = 1; j < p.tiles_n; ++j) {
-    tot = Stat<R>::merge(tot, __ldcg(wsrow + (size_t)j * kBM), n_acc);
-    n_acc += (float)kBN;
-  }
-  st = tot;
-  return true;
-}
-
-struct Work {
-  int i, step, end, rank, tiles_n;
-  __device__ bool valid() const { return i < end; }
-  __device__ void next() { i += step; }
-};
-
-template <int XMODE>
-__device__ __forceinline__ Work make_work(const GemmEpiParams& p) {
-  Work w;
-  w.tiles_n = p.tiles_n;
-  if (XMODE == X_CLUSTER) {
-    w.i = (int)cluster_id_x();
-    w.step = (int)num_clusters_x();
-    w.end = p.strips;
-    w.rank = (int)cluster_ctarank();
-  } else if (p.pair) {
-    // A pair of CTAs takes strips (2 sp, 2 sp + 1) of the same N tile.
-    w.i = (int)cluster_id_x();
-    w.step = (int)num_clusters_x();
-    w.end = p.pair_items;
-    w.rank = (int)cluster_ctarank();
-  } else {
-    w.i = blockIdx.x;
-    w.step = gridDim.x;
-    w.end = p.num_items;
-    w.rank = 0;
-  }
-  return w;
-}
-
-template <int XMODE>
-__device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& w, int& strip, int& tile) {
-  if (XMODE == X_CLUSTER) {
-    strip = w.i;
-    tile = w.rank;
-  } else if (p.pair) {
-    const int sp = w.i / w.tiles_n;
-    tile = w.i - sp * w.tiles_n;
-    if (sp & 1) tile = w.tiles_n - 1 - tile;  // serpentine, see below
-    strip = 2 * sp + w.rank;
-  } else {
-    strip = w.i / w.tiles_n;
-    tile = w.i - strip * w.tiles_n;
-    if (strip & 1) tile = w.tiles_n - 1 - tile;
-  }
-}
-// Serpentine tile order: consecutive (pairs of) strips walk the N tiles in
-// opposite directions, so a strip starts on the B tiles its predecessor read
-// last, while they are still in L2.  When B is about the size of L2 (the
-// 4096 x 16384 softmax head: 128 MB), a plain order re-reads all of B from
-// DRAM for every strip.  Items of a strip stay contiguous, so the row
-// statistics exchange keeps its strip-major schedule.
-
-// ROWOP0 != ROW_NONE: the program has two chained row reductions, ROWOP0
-// (LayerNorm or RMSNorm) then ROWOP; only the per-tile and workspace
-// exchanges are instantiated for it.
-template <int ROWOP, int XMODE, bool CTA2, int ROWOP0 = ROW_NONE>
-__global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmEpiParams p) {
-  using G = Geo<CTA2>;
-  constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kOffOut = G::kOffOut,
-                kOffSlots = G::kOffSlots, kOffBars = G::kOffBars, kOffMisc = G::kOffMisc;
-  constexpr int kOffStages = 0;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  // CTA2: rank 0 of the pair issues every MMA ("leader").
-  const uint32_t pair_rank = CTA2 ? cluster_ctarank() : 0u;
-  const bool leader = pair_rank == 0;
-
-  auto bar = [&](int idx) -> uint32_t { return sbase + kOffBars + 8 * idx; };
-  const int BAR_FULL = 0, BAR_EMPTY = kStages, BAR_TFULL = 2 * kStages, BAR_TEMPTY = 2 * kStages + 2;
-  const int BAR_SFULL = 2 * kStages + 4, BAR_SEMPTY = 2 * kStages + 12, BAR_DRAIN = 2 * kStages + 20;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
-
-  int cn = 1;
-  if (XMODE == X_CLUSTER) cn = p.tiles_n;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(bar(BAR_TFULL + a), 1);
-      // CTA2: the leader's barrier collects both CTAs' epilogue warps.
-      mbar_init(bar(BAR_TEMPTY + a), CTA2 ? 2 * kEpiWarps : kEpiWarps);
-    }
-    for (int k = 0; k < 8; ++k) {
-      mbar_init(bar(BAR_SFULL + k), cn);
-      mbar_init(bar(BAR_SEMPTY + k), cn);
-    }
-    mbar_init(bar(BAR_DRAIN), 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmB);
-    tma_prefetch_desc(&p.tmOut);
-  }
-  if (warp == 1) {
-    if (CTA2) {
-      tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-      tmem_relinquish();
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (XMODE == X_CLUSTER || CTA2) cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
-  const int kblocks = (p.K + kBK - 1) / kBK;  // the last block is zero-filled past K
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      // B tiles are reread by every strip: keep them in L2 ahead of the
-      // streamed output.
-      const uint64_t b_policy = l2_policy_evict_last();
-      for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next()) {
-        int strip, tile;
-        item_coords<XMODE>(p, w, strip, tile);
-        const int m0 = strip * kBM, n0 = tile * kBN;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1, wc)) { ok = false; break; }
-          const uint32_t sa = sbase + kOffStages + stage * kStageBytes;
-          const uint32_t sb = sa + kAStageBytes;
-          const uint32_t fb = bar(BAR_FULL + stage);
-          if (CTA2) {
-            // Both CTAs' bytes land on the leader's "full" barrier.
-            const uint32_t fbl = mapa_shared(fb, 0);
-            if (leader) mbar_arrive_expect_tx(fb, 2 * kStageBytes);
-            tma_load_2d_pair(sa, &p.tmA, fbl, kb * kBK, m0);
-            const int nb0 = n0 + (kBN / 2) * (int)pair_rank;  // this CTA's half of the B tile
-            if (p.b_mn_major) {
-              tma_load_2d_pair_hint(sb, &p.tmB, fbl, nb0, kb * kBK, b_policy);
-              tma_load_2d_pair_hint(sb + 64 * kBK * 2, &p.tmB, fbl, nb0 + 64, kb * kBK, b_policy);
-            } else {
-              tma_load_2d_pair_hint(sb, &p.tmB, fbl, kb * kBK, nb0, b_policy);
-            }
-          } else {
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            tma_load_2d(sa, &p.tmA, fb, kb * kBK, m0);
-            if (p.b_mn_major) {
-#pragma unroll
-              for (int i = 0; i < kBN / 64; ++i)
-                tma_load_2d(sb + i * (64 * kBK * 2), &p.tmB, fb, n0 + 64 * i, kb * kBK);
-            } else {
-              tma_load_2d(sb, &p.tmB, fb, kb * kBK, n0);
-            }
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-      }
-      if (CTA2) {
-        // The leader's MMA releases reach this CTA's barriers asynchronously:
-        // wait until every stage's last release has landed before exiting.
-        for (int s2 = 0; s2 < kStages; ++s2) {
-          mbar_wait<false, false>(bar(BAR_EMPTY + stage), phase ^ 1, wc);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(CTA2 ? 2 * kBM : kBM, kBN, (uint32_t)p.b_mn_major);
-      // Stage-0 descriptors; per 16 K elements A advances 32 bytes, B 32
-      // bytes (K-major) or 16 rows = 2048 bytes (MN-major: 64-column atoms
-      // 8 KB apart, 8-row groups 1 KB apart).
-      const SDesc da = sdesc_sw128(sbase + kOffStages, 16, 1024);
-      const SDesc db = sdesc_sw128(sbase + kOffStages + kAStageBytes, p.b_mn_major ? 64 * kBK * 2 : 16, 1024);
-      const uint32_t b_step = p.b_mn_major ? (2048u >> 4) : (32u >> 4);
-      uint32_t stage = 0, phase = 0;
-      int t = 0;
-      bool ok = true;
-      for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next(), ++t) {
-        const int acc = t & 1;
-        // CTA2: the peer's epilogue arrives remotely, so acquire at cluster scope.
-        if (!mbar_wait<CTA2>(bar(BAR_TEMPTY + acc), ((t >> 1) & 1) ^ 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(bar(BAR_FULL + stage), phase, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_lo = da.lo + stage * (kStageBytes >> 4);
-          const uint32_t b_lo = db.lo + stage * (kStageBytes >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            if (CTA2) mma_ss_pair(d, a_lo + kk * 2, da.hi, b_lo + kk * b_step, db.hi, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else mma_ss(d, a_lo + kk * 2, da.hi, b_lo + kk * b_step, db.hi, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          if (CTA2) mma_commit_pair(bar(BAR_EMPTY + stage), 0x3);  // frees the stage in both CTAs
-          else mma_commit(bar(BAR_EMPTY + stage));
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-        if (!ok) break;
-        if (CTA2) mma_commit_pair(bar(BAR_TFULL + acc), 0x3);
-        else mma_commit(bar(BAR_TFULL + acc));
-      }
-      // Drain: every MMA issued above has completed before TMEM is freed.
-      if (CTA2) mma_commit_pair(bar(BAR_DRAIN), 0x1);
-      else mma_commit(bar(BAR_DRAIN));
-      mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
-      if (CTA2 && ok) {
-        // Every remote "accumulator empty" arrival from the peer has landed.
-        for (int t2 = t; t2 < t + 2; ++t2)
-          mbar_wait<true, false>(bar(BAR_TEMPTY + (t2 & 1)), ((t2 >> 1) & 1) ^ 1, wc);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;             // TMEM lane quarter this warp may access
-    const int row = 32 * q + lane;      // row within the tile
-    const uint32_t out_buf = sbase + kOffOut + (warp - 2) * kOutStageBytes;
-    // The output is streamed out once: let it leave L2 first, keeping the
-    // operand tiles the next items reread.
-    const uint64_t out_policy = l2_policy_evict_first();
-    uint8_t* out_ptr = smem + kOffOut + (warp - 2) * kOutStageBytes;
-    float2* slots = reinterpret_cast<float2*>(smem + kOffSlots);
-    int t = 0;
-    for (Work w = make_work<XMODE>(p); w.valid(); w.next(), ++t) {
-      int strip, tile;
-      item_coords<XMODE>(p, w, strip, tile);
-      const int m0 = strip * kBM, n0 = tile * kBN;
-      const int acc = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_TFULL + acc), (t >> 1) & 1, wc))) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kBN);
-
-      // Chained programs: the first reduction stage.  Its elementwise ops
-      // [0, n_ops0) are applied and written back to TMEM, its statistics
-      // are merged across the strip (same exchange as the last stage), and
-      // pass 1 below normalises with (sc0, sh0) and its affine vectors
-      // before the ops that follow it.
-      float sc0 = 1.0f, sh0 = 0.0f;
-      if constexpr (ROWOP0 != ROW_NONE) {
-        float s1 = 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          tmem_wait_ld();
-          if (p.n_ops0 > 0) {
-            apply_program(p, v, n0 + c * 32, m0 + row, 0, p.n_ops0);
-            tmem_st32(taddr + c * 32, v);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s1 = (ROWOP0 == ROW_RMSNORM) ? fmaf(v[j], v[j], s1) : s1 + v[j];
-        }
-        if (p.n_ops0 > 0) tmem_wait_st();
-        float2 st0;
-        if (ROWOP0 == ROW_RMSNORM) {
-          st0 = make_float2(s1, 0.0f);
-        } else {
-          const float ref = s1 * (1.0f / kBN);
-          float s2 = 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = v[j] - ref;
-              s2 = fmaf(d, d, s2);
-            }
-          }
-          st0 = make_float2(ref, s2);
-        }
-        if (XMODE == X_GLOBAL &&
-            !global_exchange<ROWOP0>(p, p.ws_stats0, p.ws_count0, strip, tile, row, q, lane, abort_flag, wc, st0))
-          break;
-        if (ROWOP0 == ROW_RMSNORM) {
-          sc0 = rsqrtf(st0.x / (float)p.N + p.eps0);
-        } else {
-          sc0 = rsqrtf(st0.y / (float)p.N + p.eps0);
-          sh0 = -st0.x * sc0;
-        }
-      }
-
-      float2 st = Stat<ROWOP>::identity();
-      float scale_a = 1.0f, shift_a = 0.0f;  // y = gamma * (x * scale_a + shift_a) (+ beta)
-      if (ROWOP != ROW_NONE) {
-        // Pass 1: elementwise program, kept in TMEM; first local statistic.
-        float s1 = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          tmem_wait_ld();
-          if constexpr (ROWOP0 != ROW_NONE) {
-            const int n = n0 + c * 32;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
-            if (p.gamma0) {
-              const float4* g4 = reinterpret_cast<const float4*>(p.gamma0 + n);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 g = __ldg(g4 + j);
-                v[4 * j + 0] *= g.x;
-                v[4 * j + 1] *= g.y;
-                v[4 * j + 2] *= g.z;
-                v[4 * j + 3] *= g.w;
-              }
-            }
-            if (ROWOP0 == ROW_LAYERNORM && p.beta0) {
-              const float4* b4 = reinterpret_cast<const float4*>(p.beta0 + n);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 bb = __ldg(b4 + j);
-                v[4 * j + 0] += bb.x;
-                v[4 * j + 1] += bb.y;
-                v[4 * j + 2] += bb.z;
-                v[4 * j + 3] += bb.w;
-              }
-            }
-          }
-          if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
-            apply_program(p, v, n0 + c * 32, m0 + row, ROWOP0 != ROW_NONE ? p.n_ops0 : 0, p.n_ops);
-            tmem_st32(taddr + c * 32, v);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (ROWOP == ROW_RMSNORM) s1 = fmaf(v[j], v[j], s1);
-            else if (ROWOP == ROW_SOFTMAX) s1 = fmaxf(s1, v[j]);
-            else s1 += v[j];
-          }
-        }
-        if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
-        if (ROWOP == ROW_RMSNORM) {
-          st = make_float2(s1, 0.0f);
-        } else {
-          // Pass 2: second local statistic about the segment's own max/mean.
-          const float ref = (ROWOP == ROW_SOFTMAX) ? s1 : s1 * (1.0f / kBN);
-          float s2 = 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (ROWOP == ROW_SOFTMAX) s2 += ex2_approx((v[j] - ref) * kLog2e);
-              else { const float d = v[j] - ref; s2 = fmaf(d, d, s2); }
-            }
-          }
-          st = make_float2(ref, s2);
-        }
-
-        // Level 3: statistics of the whole row across the CTAs of the strip.
-        if (XMODE == X_CLUSTER) {
-          const int b = t & 1;
-          const uint32_t u = (uint32_t)(t >> 1);
-          const uint32_t slot_addr = smem_u32(slots + b * kBM + row);
-          if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_SEMPTY + b * 4 + q), (u & 1) ^ 1, wc))) break;
-          slots[b * kBM + row] = st;
-          __syncwarp();
-          if (lane == 0) {
-            fence_acq_rel_cluster();
-            for (int r = 0; r < cn; ++r) mbar_arrive_cluster(bar(BAR_SFULL + b * 4 + q), (uint32_t)r);
-          }
-          if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_SFULL + b * 4 + q), u & 1, wc))) break;
-          float2 tot = ld_shared_cluster_f2(mapa_shared(slot_addr, 0));
-          float n_acc = (float)kBN;
-          for (int r = 1; r < cn; ++r) {
-            tot = Stat<ROWOP>::merge(tot, ld_shared_cluster_f2(mapa_shared(slot_addr, (uint32_t)r)), n_acc);
-            n_acc += (float)kBN;
-          }
-          st = tot;
-          __syncwarp();
-          if (lane == 0) {
-            for (int r = 0; r < cn; ++r) mbar_arrive_cluster(bar(BAR_SEMPTY + b * 4 + q), (uint32_t)r);
-          }
-        } else if (XMODE == X_GLOBAL) {
-          float2* wsrow = p.ws_stats + (size_t)strip * p.tiles_n * kBM + row;
-          __stcg(wsrow + (size_t)tile * kBM, st);
-          __threadfence();
-          __syncwarp();
-          unsigned* cnt = p.ws_count + strip * 4 + q;
-          if (lane == 0) red_release_gpu_add(cnt, 1u);
-          bool ok = true;
-          if (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-            const long long t0 = clock64();
-            while (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-              __nanosleep(64);
-              if (*abort_flag) { ok = false; break; }
-              if (clock64() - t0 > p.timeout_cycles) { record_timeout(wc); ok = false; break; }
-            }
-          }
-          if (!__all_sync(0xffffffffu, ok)) break;
-          float2 tot = __ldcg(wsrow);
-          float n_acc = (float)kBN;
-          for (int j = 1; j < p.tiles_n; ++j) {
-            tot = Stat<ROWOP>::merge(tot, __ldcg(wsrow + (size_t)j * kBM), n_acc);
-            n_acc += (float)kBN;
-          }
-          st = tot;
-        }
-
-        // Row normalisation constants.
-        if (ROWOP == ROW_RMSNORM) {
-          scale_a = rsqrtf(st.x / (float)p.N + p.eps);
-        } else if (ROWOP == ROW_LAYERNORM) {
-          scale_a = rsqrtf(st.y / (float)p.N + p.eps);
-          shift_a = -st.x * scale_a;
-        } else {  // softmax: y = exp(x - max) / sum = exp2(x*log2e - max*log2e) / sum
-          scale_a = kLog2e;
-          shift_a = -st.x * kLog2e;
-        }
-      }
-      const float inv_sum = (ROWOP == ROW_SOFTMAX) ? 1.0f / st.y : 1.0f;
-
-      // Final pass: normalise, stage through swizzled smem, TMA store.
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        float v[32];
-        tmem_ld32(taddr + c * 32, v);
-        tmem_wait_ld();
-        const int n = n0 + c * 32;
-        if (ROWOP == ROW_NONE) {
-          apply_program(p, v, n, m0 + row, 0, p.n_ops);
-        } else if (ROWOP == ROW_SOFTMAX) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;
-        } else {
-          const float4* g4 = reinterpret_cast<const float4*>(p.gamma + n);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 g = __ldg(g4 + j);
-            v[4 * j + 0] = fmaf(v[4 * j + 0], scale_a, shift_a) * g.x;
-            v[4 * j + 1] = fmaf(v[4 * j + 1], scale_a, shift_a) * g.y;
-            v[4 * j + 2] = fmaf(v[4 * j + 2], scale_a, shift_a) * g.z;
-            v[4 * j + 3] = fmaf(v[4 * j + 3], scale_a, shift_a) * g.w;
-          }
-          if (ROWOP == ROW_LAYERNORM) {
-            const float4* b4 = reinterpret_cast<const float4*>(p.beta + n);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 bb = __ldg(b4 + j);
-              v[4 * j + 0] += bb.x;
-              v[4 * j + 1] += bb.y;
-              v[4 * j + 2] += bb.z;
-              v[4 * j + 3] += bb.w;
-            }
-          }
-        }
-        // The previous TMA store from this buffer must have read it.
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-        if (p.out_bf16) {
-          // bf16: 64-byte rows, unswizzled; lane l writes its 16-byte chunks
-          // starting at chunk l & 3 to spread them over the banks.
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = (jj + lane) & 3;
-            uint4 val;
-            switch (j) {  // constant register indices for each case
-              case 0: val = make_uint4(w[0], w[1], w[2], w[3]); break;
-              case 1: val = make_uint4(w[4], w[5], w[6], w[7]); break;
-              case 2: val = make_uint4(w[8], w[9], w[10], w[11]); break;
-              default: val = make_uint4(w[12], w[13], w[14], w[15]); break;
-            }
-            *reinterpret_cast<uint4*>(out_ptr + lane * 64 + j * 16) = val;
-          }
-        } else {
-          // 128-byte swizzle: 16-byte chunk j of row r lands at chunk j ^ (r & 7).
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4* dst = reinterpret_cast<float4*>(out_ptr + lane * 128 + ((j ^ (lane & 7)) * 16));
-            *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d_hint(&p.tmOut, out_buf, n, m0 + 32 * q, out_policy);
-          bulk_commit();
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (CTA2 && !leader) mbar_arrive_cluster(bar(BAR_TEMPTY + acc), 0);  // the leader issues the MMAs
-        else mbar_arrive(bar(BAR_TEMPTY + acc));
-      }
-    }
-    if (lane == 0) bulk_wait0();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (CTA2) {
-    cluster_sync_all();  // the peer's TMEM and smem are in use until the leader is done
-    if (warp == 1) {
-      tc_fence_after();
-      tmem_dealloc_pair(tmem_base, kTmemCols);
-    }
-  } else {
-    if (warp == 1) {
-      tc_fence_after();
-      tmem_dealloc(tmem_base, kTmemCols);
-    }
-    if (XMODE == X_CLUSTER) cluster_sync_all();
-  }
-}
-
-template <int R, int X, bool P, int R0 = ROW_NONE>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P, R0>);
-}
-
-const void* select_kernel(int rowop, int xmode, bool pair) {
-#define CF_CASE(R, X, P) \
-  if (rowop == R && xmode == X && pair == P) return kernel_ptr<R, X, P>();
-  CF_CASE(ROW_NONE, X_NONE, false)
-  CF_CASE(ROW_NONE, X_NONE, true)
-  CF_CASE(ROW_LAYERNORM, X_NONE, false)
-  CF_CASE(ROW_LAYERNORM, X_NONE, true)
-  CF_CASE(ROW_LAYERNORM, X_CLUSTER, false)
-  CF_CASE(ROW_LAYERNORM, X_GLOBAL, false)
-  CF_CASE(ROW_LAYERNORM, X_GLOBAL, true)
-  CF_CASE(ROW_RMSNORM, X_NONE, false)
-  CF_CASE(ROW_RMSNORM, X_NONE, true)
-  CF_CASE(ROW_RMSNORM, X_CLUSTER, false)
-  CF_CASE(ROW_RMSNORM, X_GLOBAL, false)
-  CF_CASE(ROW_RMSNORM, X_GLOBAL, true)
-  CF_CASE(ROW_SOFTMAX, X_NONE, false)
-  CF_CASE(ROW_SOFTMAX, X_NONE, true)
-  CF_CASE(ROW_SOFTMAX, X_CLUSTER, false)
-  CF_CASE(ROW_SOFTMAX, X_GLOBAL, false)
-  CF_CASE(ROW_SOFTMAX, X_GLOBAL, true)
-#undef CF_CASE
-  // Two chained reductions (per-tile or workspace exchange only).
-#define CF_CASE2(R0, R)                                                                            \
-  if (rowop == row_code(R0, R)) {                                                                  \
-    if (xmode == X_NONE) return pair ? kernel_ptr<R, X_NONE, true, R0>() : kernel_ptr<R, X_NONE, false, R0>();       \
-    if (xmode == X_GLOBAL) return pair ? kernel_ptr<R, X_GLOBAL, true, R0>() : kernel_ptr<R, X_GLOBAL, false, R0>(); \
-    return nullptr;                                                                                \
-  }
-  CF_CASE2(ROW_LAYERNORM, ROW_LAYERNORM)
-  CF_CASE2(ROW_LAYERNORM, ROW_RMSNORM)
-  CF_CASE2(ROW_LAYERNORM, ROW_SOFTMAX)
-  CF_CASE2(ROW_RMSNORM, ROW_LAYERNORM)
-  CF_CASE2(ROW_RMSNORM, ROW_RMSNORM)
-  CF_CASE2(ROW_RMSNORM, ROW_SOFTMAX)
-#undef CF_CASE2
-  return nullptr;
-}
-
-int smem_for(bool pair) { return pair ? Geo<true>::kSmemBytes : Geo<false>::kSmemBytes; }
-
 }  // namespace
 
 size_t gemm_epi_smem_bytes() { return (size_t)smem_for(false); }
 
-cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair) {
-  const void* k = select_kernel(rowop, xmode, pair);
+cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair, bool rag) {
+  const void* k = select_kernel(rowop, xmode, pair, rag);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for(pair));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int cluster, int* out) {
-  const void* k = select_kernel(rowop, xmode, pair);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, bool rag, int cluster, int* out) {
+  const void* k = select_kernel(rowop, xmode, pair, rag);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -794,14 +42,14 @@ cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int cluster, 
   return cudaOccupancyMaxActiveClusters(out, k, &cfg);
 }
 
-cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out) {
-  const void* k = select_kernel(rowop, xmode, false);
+cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, bool rag, int* out) {
+  const void* k = select_kernel(rowop, xmode, false, rag);
   if (!k) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, k, kThreads, smem_for(false));
 }
 
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
-  const void* k = select_kernel(L.rowop, L.xmode, L.p.pair != 0);
+  const void* k = select_kernel(L.rowop, L.xmode, L.p.pair != 0, L.p.N % kBN != 0);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

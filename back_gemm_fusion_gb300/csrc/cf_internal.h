@@ -30,7 +30,7 @@ struct GemmEpiParams {
   CUtensorMap tmB;    // B: K-major [N][K] box {64, 256} or MN-major [K][N] box {64, 64}
   CUtensorMap tmOut;  // out: fp32 [M][N], box {32, 32}, 128B swizzle; or bf16, box {32, 32}, no swizzle
   int M, N, K;
-  int tiles_n;        // N / kBN
+  int tiles_n;        // ceil(N / kBN); the last tile may be ragged
   int strips;         // M / kBM
   int num_items;      // strips * tiles_n
   int b_mn_major;     // 1: B stored K x N (N contiguous)
@@ -79,9 +79,10 @@ cf_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
 long long wait_timeout_cycles();
 
 size_t gemm_epi_smem_bytes();
-cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair);  // set function attributes
+// rag: N % kBN != 0 (the kernels whose last tile per row is ragged).
+cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair, bool rag);  // set function attributes
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);
-cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int cluster, int* out);
-cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int* out);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, bool rag, int cluster, int* out);
+cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, bool rag, int* out);
 
 }  // namespace cf

@@ -52,7 +52,7 @@ NCU_TRAFFIC = {
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("cf_gemm_epi.cu", "cf_b2b.cu", "cf_ptx.cuh", "cf_internal.h"):
+    for f in ("cf_gemm_epi_kernel.cuh", "cf_b2b.cu", "cf_ptx.cuh", "cf_internal.h"):
         with open(os.path.join(ROOT, "back_gemm_fusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

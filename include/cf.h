@@ -147,8 +147,11 @@ typedef struct {
  *          are scratch; concurrent calls must use distinct workspaces.
  *
  * Shape rules (this version): any M >= 0 (a ragged last 128-row strip is
- * handled), N % 256 == 0, K % 8 == 0 with K >= 64 (a ragged last 64-wide K
- * block reads zeros), all pointers and leading dims 16-byte aligned.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
+ * handled), any N >= 0 (a ragged last 256-column tile is handled: its
+ * columns past N stay out of the row statistics and are not stored), K % 8
+ * == 0 with K >= 64 (a ragged last 64-wide K block reads zeros), all
+ * pointers and leading dims 16-byte aligned; the cluster exchange takes rows
+ * of at most 16 tiles (N <= 4096).  Violations return CF_ERR_UNSUPPORTED_SHAPE /
  * CF_ERR_MISALIGNED without launching anything.  M == 0 or N == 0 returns
  * CF_OK without launching.
  */

@@ -74,7 +74,13 @@ def test_validation_errors(lib):
     A3, B3, O3 = _mats(M=200)
     assert _call(lib, A3, B3, O3, LN) in (0, 4, 8)          # ragged M is supported (device check follows)
     A4, B4, O4 = _mats(N=384)
-    assert _call(lib, A4, B4, O4, LN) == 2                  # N not a multiple of 256
+    assert _call(lib, A4, B4, O4, LN) in (0, 4, 8)          # ragged last N tile is supported
+    A4, B4, O4 = _mats(N=300)
+    assert _call(lib, A4, B4, O4, LN) == 3                  # N = ld = 300: rows not 16-byte aligned
+    B4.ld, O4.ld = 304, 304
+    assert _call(lib, A4, B4, O4, LN) in (0, 4, 8)          # N = 300 in padded rows
+    A4, B4, O4 = _mats(N=256 * 16 + 8)
+    assert _call(lib, A4, B4, O4, LN, exchange="cluster") == 2  # 17 tiles (last one ragged) > 16-CTA cluster
     A5, B5, O5 = _mats(K=96)
     assert _call(lib, A5, B5, O5, LN) in (0, 4, 8)          # ragged K (K % 8 == 0) is supported
     A6, B6, O6 = _mats(K=56)

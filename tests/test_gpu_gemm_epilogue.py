@@ -276,3 +276,90 @@ def test_bf16_output_strided_noalloc(cf):
     assert cf.cf_last_device_status() == 0
     bf16_out_gate(out.float().cpu().numpy(), _oracle(case), 2e-3, "bf16 out, padded ld")
     assert torch.all(buf[:, 1024:] == 7.0)
+
+
+RAGGED_N_PROGRAMS = {
+    "none": ([("bias",), ("gelu_tanh",)], 1e-4),
+    "layernorm": ([("bias",), ("layernorm", 1e-5)], 2e-3),
+    "rmsnorm": ([("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)], 2e-3),
+    "softmax": ([("scale", 0.125), ("softmax",)], 2e-3),
+}
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+@pytest.mark.parametrize("N", [8, 40, 264, 1000, 2056, 4104])
+@pytest.mark.parametrize("prog", sorted(RAGGED_N_PROGRAMS))
+def test_ragged_n(cf, prog, N, b_trans):
+    # N not a multiple of the 256-column tile: the last tile of each row holds
+    # N % 256 valid columns (one partial 32-column chunk, or a few whole
+    # ones); its B columns past N load as zeros, the row statistics skip
+    # them, the vectors are never read past N, and the stores clip them.
+    # 2056 takes the cluster exchange (9 tiles), 4104 the workspace (17).
+    ops, strict = RAGGED_N_PROGRAMS[prog]
+    case = I.gemm_epilogue_case("ragged_n", 200, N, 136, ops, seed=N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, b_trans), _oracle(case), strict=strict,
+                      what=f"ragged N={N} {prog} b_trans={b_trans}")
+
+
+@pytest.mark.parametrize("exchange", ["cluster", "global"])
+@pytest.mark.parametrize("rowop", ["layernorm", "softmax"])
+def test_ragged_n_exchanges(cf, rowop, exchange):
+    # Same row, both exchanges: tile counts 3 (the last with 8 columns).
+    ops = [("bias",), ("layernorm", 1e-5)] if rowop == "layernorm" else [("scale", 0.5), ("softmax",)]
+    case = I.gemm_epilogue_case("ragged_n_x", 384, 520, 64, ops, seed=7, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, exchange=exchange), _oracle(case), what=f"ragged N=520 {rowop} {exchange}")
+
+
+def test_ragged_n_padded_rows(cf):
+    # N = 300 (not a multiple of 8) inside 304-element rows: B, out and the
+    # residual are views of padded buffers; out's padding is never written.
+    M, N, K = 130, 300, 128
+    ops = [("bias",), ("residual",), ("rmsnorm", 1e-6)]
+    case = I.gemm_epilogue_case("ragged_n_ld", M, N, K, ops, seed=300, need_bias=True, need_gamma=True)
+    R = torch.from_numpy(np.random.default_rng(301).standard_normal((M, N)).astype(np.float32)).to(torch.bfloat16)
+    Bp = torch.zeros((K, 304), dtype=torch.bfloat16, device="cuda")
+    Bp[:, :N] = case.B.cuda()
+    Rp = torch.zeros((M, 304), dtype=torch.bfloat16, device="cuda")
+    Rp[:, :N] = R.cuda()
+    Op = torch.full((M, 304), 5.0, dtype=torch.float32, device="cuda")
+    cf.cf_gemm_epilogue(case.A.cuda(), Bp[:, :N], case.ops, _dev(case.bias), _dev(case.gamma), None,
+                        out=Op[:, :N], residual=Rp[:, :N])
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          None, residual=I.to_f64(R))
+    assert_rows_close(Op[:, :N].cpu().numpy(), ref, what="ragged N=300, padded rows")
+    assert torch.all(Op[:, N:] == 5.0)
+
+
+@pytest.mark.parametrize("N", [264, 1000, 4104])
+def test_ragged_n_chained(cf, N):
+    # Two reduction stages over a ragged row: both stages' statistics skip the
+    # columns past N (the first stage's affine output there is not zero).
+    ops = [("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)]
+    case = I.gemm_epilogue_case("ragged_n_chain", 256, N, 64, ops, seed=N + 5, need_bias=True, need_gamma=True)
+    rng = np.random.default_rng(N)
+    g0 = torch.from_numpy((1 + 0.3 * rng.standard_normal(N)).astype(np.float32))
+    b0 = torch.from_numpy((0.3 * rng.standard_normal(N)).astype(np.float32))
+    out = cf.cf_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma), None,
+                              stage0_gamma=g0.cuda(), stage0_beta=b0.cuda())
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          None, stage0_gamma=I.to_f64(g0), stage0_beta=I.to_f64(b0))
+    assert_rows_close(out.cpu().numpy(), ref, what=f"ragged N={N} chained")
+
+
+def test_ragged_n_bf16_output(cf):
+    ops, strict = BF16_PROGRAMS["layernorm"]
+    case = I.gemm_epilogue_case("ragged_n_bf16", 256, 1000, 128, ops, seed=11, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    args = (case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma), _dev(case.beta))
+    g = cf.cf_gemm_epilogue(*args, out_dtype=torch.bfloat16)
+    f = cf.cf_gemm_epilogue(*args)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16))
+    bf16_out_gate(g.float().cpu().numpy(), _oracle(case), strict, "ragged N=1000 bf16 out")

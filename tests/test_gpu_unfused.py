@@ -88,3 +88,15 @@ def test_unfused_mlp_bf16_output(cf):
     ref = O.b2bgemm(x, w1, w2, "relu")
     bound = 2.0 ** -7 * (np.abs(np.maximum(x @ w1, 0)) @ np.abs(w2)) + 2.0 ** -8 * np.abs(ref) * 1.01 + 1e-6
     assert np.all(np.abs(out.float().cpu().numpy() - ref) <= bound)
+
+
+@pytest.mark.parametrize("N", [264, 1000])
+def test_unfused_ragged_n(cf, N):
+    ops = [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)]
+    case = I.gemm_epilogue_case("ragged", 256, N, 128, ops, seed=N, need_bias=True, need_gamma=True)
+    vec = [None if t is None else t.cuda() for t in (case.bias, case.gamma, case.beta)]
+    out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, *vec)
+    torch.cuda.synchronize()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          None)
+    assert_rows_close(out.cpu().numpy(), ref, what=f"unfused ragged N={N}")
