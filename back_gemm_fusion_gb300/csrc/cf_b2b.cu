@@ -11,8 +11,9 @@
 //
 // Two sm_103a kernels:
 //
-// attn_kernel (W1 given as its transpose, K = N2 = 128; the attention shape
-// S = Q K^T):  one CTA owns a 128-row block of A for one batch entry and
+// attn_kernel (W1 given as its transpose, head dims K, N2 <= 128 computed
+// as 128 with zero padding, any N1; the attention shape S = Q K^T):  one CTA
+// owns a 128-row block of A for one batch entry and
 // walks the N1 dimension in 128-wide chunks.  Per chunk j: S_j = A . W1_j in
 // TMEM (two S buffers, so S_{j+1} is computed while F runs on S_j), F on
 // TMEM rows in registers, S'_j rounded to bf16 into a swizzled shared-memory
@@ -23,7 +24,7 @@
 // is divided by l at the end.  This is the C = 1 (single-CTA) case of the
 // review's Eq. (5) merge.
 //
-// mlp_kernel (general K, N1; N2 = 256 * C): a cluster of C CTAs shares one
+// mlp_kernel (general K, N1; N2 <= 256 * C): a cluster of C CTAs shares one
 // 128-row strip.  CTA c owns O[:, 256c .. 256c+255] in TMEM (the whole
 // 128 x N2 fp32 strip does not fit one SM's TMEM).  For each round of C
 // chunks of N1, CTA c computes the 128 x 128 chunk S_c = A . W1[:, chunk],
@@ -108,6 +109,20 @@ __device__ __forceinline__ void store_row(void* out, int bf16, long long off, co
   }
 }
 
+// store_row for an output row that ends inside these W columns: only the
+// first `valid` (< W) values are stored, one element at a time.
+template <int W>
+__device__ __forceinline__ void store_row_part(void* out, int bf16, long long off, const float* v, float s,
+                                               int valid) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    if (j < valid) {
+      if (bf16) static_cast<__nv_bfloat16*>(out)[off + j] = __float2bfloat16_rn(v[j] * s);
+      else static_cast<float*>(out)[off + j] = v[j] * s;
+    }
+  }
+}
+
 // ======================================================================
 // Attention-shaped B2BGEMM
 // ======================================================================
@@ -151,7 +166,9 @@ struct Params {
   int out_bf16;
   int M;             // rows of A per batch entry (the last 128-row block may be ragged)
   int batch, m_blocks, n1_blocks, items;
-  int softmax;       // 1: scaled softmax, 0: ReLU (optionally scaled)
+  int kv_last;       // valid columns of S in the last N1 chunk (1..128; < 128: ragged N1)
+  int n2;            // valid output columns (N2 <= 128)
+  int softmax;       // 1: scaled softmax (scale > 0), 0: ReLU (optionally scaled)
   float scale;       // multiplies S before F
   unsigned* status;
   long long timeout_cycles;
@@ -166,6 +183,12 @@ __device__ __forceinline__ float (&part32(float (&v)[128], int c))[32] {
 // single thread that also waits on barriers between GEMM1 and GEMM2 bursts
 // leaves the pipe idle for every wait.  With GEMM1 and GEMM2 issued from
 // different warps, one keeps the pipe fed while the other waits.
+// RAG: the softmax masks the last chunk's keys past N1 (N1 not a multiple
+// of 128), or the output has fewer than 128 columns; OBF16: bf16 output.
+// Both are compile-time so that the common instantiation (full chunks,
+// fp32 output) carries neither the masking nor a second store path in the F
+// warps, which bound the softmax variant.
+template <bool RAG, bool OBF16>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -356,6 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));  // S_sb may be overwritten now
         if (p.softmax) {
+          if (RAG && j == nb - 1 && p.kv_last < kTile) {
+            // Ragged N1: keys past N1 were loaded as zero rows; their logits
+            // leave the max and the sum (exp2(-inf) = 0).  The V rows past
+            // N1 are zero as well.
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if (e >= p.kv_last) v[e] = -INFINITY;
+          }
           float mx[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -473,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
         }
         if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
-          store_row<64>(p.out, p.out_bf16, orow + 64 * h, o, inv);
+          if (!RAG || p.n2 >= 64 * (h + 1)) store_row<64>(p.out, OBF16, orow + 64 * h, o, inv);
+          else if (p.n2 > 64 * h) store_row_part<64>(p.out, OBF16, orow + 64 * h, o, inv, p.n2 - 64 * h);
         }
       }
     }
@@ -525,16 +557,19 @@ struct Params {
   int out_bf16;
   int M;             // rows of A per batch entry (the last 128-row strip may be ragged)
   int w1_k_major;
-  int C;             // CTAs per cluster = N2 / 256
+  int C;             // CTAs per cluster = ceil(N2 / 256)
+  int n2;            // output columns (the last CTA's block may be ragged)
   int ring;          // ring stages (ring_for(C))
   int kblocks;       // ceil(K / 64): the last block's columns past K are zero-filled
-  int rounds;        // N1 / (128 C)
+  int rounds;        // ceil(N1 / (128 C)): chunks past N1 are zero (W1 and W2 zero-filled)
   int strips, items; // M / 128, batch * strips
   float scale;       // F(S) = max(scale S, 0)
   unsigned* status;
   long long timeout_cycles;
 };
 
+// OBF16: bf16 output (compile-time, one store path in the epilogue warps).
+template <bool OBF16>
 __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -775,8 +810,10 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         float v[32];
         tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
         tmem_wait_ld();
-        if (strip * 128 + row < p.M) {  // rows past M (ragged last strip) are not stored
-          store_row<32>(p.out, p.out_bf16, orow + c * 32, v, 1.0f);
+        const int col = (int)rank * 256 + c * 32;  // columns past N2 (ragged last block) are not stored
+        if (strip * 128 + row < p.M && col < p.n2) {  // nor rows past M (ragged last strip)
+          if (col + 32 <= p.n2) store_row<32>(p.out, OBF16, orow + c * 32, v, 1.0f);
+          else store_row_part<32>(p.out, OBF16, orow + c * 32, v, 1.0f, p.n2 - col);
         }
       }
       tc_fence_before();
@@ -797,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
 
 
 std::mutex g_mu;
-bool g_prepared[64][2] = {};
+bool g_prepared[64][6] = {};  // [device][MLP fp32 / bf16 out, attention variants 0..3]
 
 cf_status prepare(int slot, const void* fn, int smem) {
   int dev = 0;
@@ -862,18 +899,20 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
   p.C = (int)C;
+  p.n2 = (int)N2;
   p.ring = mlp::ring_for((int)C);
   p.kblocks = (int)((K + 63) / 64);
-  p.rounds = (int)(N1 / (128 * C));
+  p.rounds = (int)((N1 + 128 * C - 1) / (128 * C));
   p.M = (int)M;
   p.strips = (int)((M + 127) / 128);
   p.items = (int)(batch * p.strips);
   p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
   p.status = status;
   p.timeout_cycles = wait_timeout_cycles();
-  const void* fn = reinterpret_cast<const void*>(&mlp::mlp_kernel);
+  const void* fn = p.out_bf16 ? reinterpret_cast<const void*>(&mlp::mlp_kernel<true>)
+                              : reinterpret_cast<const void*>(&mlp::mlp_kernel<false>);
   const int smem = mlp::smem_for((int)C);
-  if ((s = prepare(1, fn, mlp::smem_for(1))) != CF_OK) return s;  // the largest layout
+  if ((s = prepare(p.out_bf16 ? 1 : 0, fn, mlp::smem_for(1))) != CF_OK) return s;  // the largest layout
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -911,6 +950,9 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   if (!d || d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
   if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX || !std::isfinite(d->mid_scale))
     return CF_ERR_INVALID_ARG;
+  // The softmax's running max is taken on the unscaled logits: its scale
+  // must be positive (a temperature).
+  if (d->mid_op == CF_MID_SCALE_SOFTMAX && !(d->mid_scale > 0.0f)) return CF_ERR_INVALID_ARG;
   if (d->out_dtype != CF_FP32 && d->out_dtype != CF_BF16) return CF_ERR_INVALID_ARG;
   if ((s = check_bf16_view(A, false)) != CF_OK) return s;
   if ((s = check_bf16_view(W1, true)) != CF_OK) return s;
@@ -927,12 +969,14 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
     return CF_ERR_MISALIGNED;
   if (M == 0 || N2 == 0) return CF_OK;
 
-  // Attention shape: W1 stored transposed (N1 x K), K = N2 = 128.
-  const bool attn_shape = W1->trans == 1 && K == 128 && N2 == 128 && N1 % 128 == 0 && N1 >= 128;
-  // MLP shape: N2 = 256 C with C <= 4 CTAs per cluster, elementwise F only.
-  const int64_t C = N2 / 256;
-  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 &&
-                         K >= 64 && N2 % 256 == 0 && C >= 1 && C <= mlp::kMaxC && N1 % (128 * C) == 0 && N1 > 0;
+  // Attention shape: W1 stored transposed (N1 x K), head dims K, N2 <= 128
+  // (K % 8 == 0), any N1 >= 1 (a ragged last 128-key chunk is masked).
+  const bool attn_shape = W1->trans == 1 && K % 8 == 0 && K >= 8 && K <= 128 && N2 >= 1 && N2 <= 128 && N1 >= 1;
+  // MLP shape: N2 <= 256 C with C <= 4 CTAs per cluster (the last CTA's
+  // block may be ragged), any N1 >= 1, elementwise F only.
+  const int64_t C = (N2 + 255) / 256;
+  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 64 && C >= 1 &&
+                         C <= mlp::kMaxC && N1 >= 1;
   if (!attn_shape && !mlp_shape) return CF_ERR_UNSUPPORTED_SHAPE;
 
   int sms = 0;
@@ -942,20 +986,23 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   attn::Params p;
   std::memset(&p, 0, sizeof(p));
   const uint64_t bs = (uint64_t)(batch > 1 ? batch : 1);
+  // K < 128 or N2 < 128 (head dims below 128): the columns past K of Q and
+  // K, and past N2 of V, load as zeros, adding nothing to S and giving O
+  // zero columns that are not stored; rows of K and V past N1 load as zeros.
   {
-    const uint64_t dims[3] = {128, (uint64_t)M, bs};
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)M, bs};
     const uint64_t st[2] = {(uint64_t)A->ld * 2, (uint64_t)(batch > 1 ? d->strideA : M * A->ld) * 2};
     const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A->ptr, dims, st, box)) != CF_OK) return s;
   }
   {
-    const uint64_t dims[3] = {128, (uint64_t)N1, bs};
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N1, bs};
     const uint64_t st[2] = {(uint64_t)W1->ld * 2, (uint64_t)(batch > 1 ? d->strideW1 : N1 * W1->ld) * 2};
     const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmW1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W1->ptr, dims, st, box)) != CF_OK) return s;
   }
   {
-    const uint64_t dims[3] = {128, (uint64_t)N1, bs};
+    const uint64_t dims[3] = {(uint64_t)N2, (uint64_t)N1, bs};
     const uint64_t st[2] = {(uint64_t)W2->ld * 2, (uint64_t)(batch > 1 ? d->strideW2 : N1 * W2->ld) * 2};
     const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W2->ptr, dims, st, box)) != CF_OK) return s;
@@ -967,15 +1014,28 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   p.batch = (int)bs;
   p.M = (int)M;
   p.m_blocks = (int)((M + 127) / 128);
-  p.n1_blocks = (int)(N1 / 128);
+  p.n1_blocks = (int)((N1 + 127) / 128);
+  p.kv_last = (int)(N1 - 128 * (p.n1_blocks - 1));
+  p.n2 = (int)N2;
   p.items = p.batch * p.m_blocks;
   p.softmax = d->mid_op == CF_MID_SCALE_SOFTMAX ? 1 : 0;
   p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
   p.status = status;
   p.timeout_cycles = wait_timeout_cycles();
-  if ((s = prepare(0, reinterpret_cast<const void*>(&attn::attn_kernel), attn::kSmemBytes)) != CF_OK) return s;
   const int grid = p.items < sms ? p.items : sms;
-  attn::attn_kernel<<<grid, attn::kThreads, attn::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+  const bool rag = (p.softmax && p.kv_last < attn::kTile) || p.n2 < attn::kTile;
+  const int variant = (rag ? 1 : 0) + (p.out_bf16 ? 2 : 0);
+  const void* fns[4] = {reinterpret_cast<const void*>(&attn::attn_kernel<false, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<false, true>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, true>)};
+  if ((s = prepare(2 + variant, fns[variant], attn::kSmemBytes)) != CF_OK) return s;
+  void* args[] = {&p};
+  if (cudaLaunchKernel(fns[variant], dim3(grid), dim3(attn::kThreads), args, attn::kSmemBytes,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
   if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
   return CF_OK;
 }

@@ -536,6 +536,7 @@ extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1,
   if (!A || !W1 || !W2 || !d || !out || !s_buf || !p_buf) return CF_ERR_INVALID_ARG;
   if (d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
   if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX) return CF_ERR_INVALID_ARG;
+  if (d->mid_op == CF_MID_SCALE_SOFTMAX && !(d->mid_scale > 0.0f)) return CF_ERR_INVALID_ARG;
   if ((d->out_dtype != CF_FP32 && d->out_dtype != CF_BF16) || out->dtype != d->out_dtype) return CF_ERR_INVALID_ARG;
   const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols;
   if (W1->rows != K || W2->rows != N1 || out->rows != M || out->cols != N2) return CF_ERR_INVALID_ARG;

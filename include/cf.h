@@ -229,10 +229,13 @@ typedef struct {
  *   The softmax mid op normalises each row of S over all N1 columns.
  *
  * Shape rules (this version), two kernels:
- *   attention shape: W1 given transposed (trans == 1), K == N2 == 128,
- *     N1 % 128 == 0; any mid op (the softmax normalises over all N1);
+ *   attention shape: W1 given transposed (trans == 1), head dims K <= 128
+ *     (K % 8 == 0) and N2 <= 128 (both computed as 128 with zero padding),
+ *     any N1 >= 1 (keys past N1 in the last 128-key chunk are masked); any
+ *     mid op (the softmax normalises over all N1);
  *   MLP shape: mid op ReLU or scaled ReLU, K % 8 == 0 with K >= 64,
- *     N2 == 256 C with C <= 4 CTAs per cluster, N1 % (128 C) == 0.
+ *     N2 <= 1024 (C = ceil(N2 / 256) CTAs per cluster), any N1 >= 1.
+ *   The softmax mid op needs mid_scale > 0 (CF_ERR_INVALID_ARG otherwise).
  *   Both: any M >= 0 (a ragged last 128-row block is handled), pointers and
  *   leading dims 16-byte aligned.  Other shapes return
  *   CF_ERR_UNSUPPORTED_SHAPE without launching anything.

@@ -218,3 +218,34 @@ def test_b2b_validation(lib):
 
     assert mlp(cf_matrix(0x40000, CF_BF16, 0, 256, 256, 256), CF_BF16) in (0, 4, 8)  # MLP shape, bf16 out
     assert mlp(cf_matrix(0x40000, CF_FP32, 0, 256, 256, 256), op="scale_softmax") == 2  # MLP: elementwise F only
+
+
+def test_b2b_shape_rules(lib):
+    # Attention shape: any N1 >= 1, head dims K, N2 <= 128; MLP shape: any
+    # N1, N2 <= 1024; the softmax needs a positive scale.
+    from back_gemm_fusion_gb300.binding import cf_matrix, b2b_desc, CF_FP32, CF_BF16
+
+    def call(M, K, N1, N2, op="scale_softmax", scale=0.125, trans=True):
+        A = cf_matrix(0x10000, CF_BF16, 0, M, K, K + (-K) % 8)
+        W1 = cf_matrix(0x20000, CF_BF16, 1, K, N1, K + (-K) % 8) if trans else \
+            cf_matrix(0x20000, CF_BF16, 0, K, N1, N1 + (-N1) % 8)
+        W2 = cf_matrix(0x30000, CF_BF16, 0, N1, N2, N2 + (-N2) % 8)
+        O = cf_matrix(0x40000, CF_FP32, 0, M, N2, N2 + (-N2) % 4)
+        d = b2b_desc(op, scale, 1)
+        return lib.cf_b2bgemm(ctypes.byref(A), ctypes.byref(W1), ctypes.byref(W2), ctypes.byref(d),
+                              ctypes.byref(O), None)
+
+    ok = (0, 4, 8)
+    assert call(256, 128, 100, 128) in ok                 # ragged keys
+    assert call(256, 128, 1, 128) in ok                   # a single key
+    assert call(256, 64, 200, 64) in ok                   # head dim 64
+    assert call(77, 96, 300, 32) in ok                    # head dims 96 / 32
+    assert call(256, 136, 256, 128) == 2                  # head dim above 128
+    assert call(256, 60, 256, 128) == 2                   # K % 8 != 0
+    assert call(256, 128, 0, 128) == 2                    # no keys
+    assert call(256, 128, 256, 128, scale=0.0) == 1       # softmax scale must be positive
+    assert call(256, 128, 256, 128, scale=-0.5) == 1
+    assert call(256, 128, 256, 128, op="scale_relu", scale=-0.5) in ok  # ReLU takes any finite scale
+    assert call(256, 256, 200, 300, op="relu", trans=False) in ok       # MLP, ragged N1 and N2
+    assert call(256, 256, 512, 1000, op="relu", trans=False) in ok      # MLP, C = 4, last block ragged
+    assert call(256, 256, 512, 1100, op="relu", trans=False) == 2       # MLP, C = 5 > 4

@@ -193,9 +193,15 @@ def test_mlp_full_size_sampled(cf):
 
 
 def test_b2b_rejects_unsupported(cf):
-    X, W1, W2 = _mlp_case(128, 64, 384, 1024, seed=1)  # N1 not a multiple of 128 * 4
+    X, W1, W2 = _mlp_case(128, 64, 384, 1280, seed=1)  # N2 = 1280: five CTAs per cluster
     with pytest.raises(cf.CFError):
         cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu")
+    X, W1, W2 = _mlp_case(128, 64, 384, 256, seed=1)   # softmax on the MLP shape (W1 not transposed)
+    with pytest.raises(cf.CFError):
+        cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "scale_softmax", 0.5)
+    Q = torch.zeros((128, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cf.CFError):                     # softmax with a non-positive scale
+        cf.cf_b2bgemm(Q, Q, Q, "scale_softmax", -1.0, w1_trans=True)
 
 
 def _bf16_gate(gpu, ref, absbound, what):
@@ -250,3 +256,77 @@ def test_mlp_bf16_output(cf, M, K, N1, N2):
     bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
     b2b_gate(f.cpu().numpy(), ref, bound, f"mlp fp32 {M}x{K}x{N1}x{N2}")
     _bf16_gate(g.float().cpu().numpy(), ref, bound, f"mlp bf16 {M}x{K}x{N1}x{N2}")
+
+
+def _bf16_t(a):
+    return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("Lq,N1", [(128, 1), (200, 77), (256, 200), (128, 1000)])
+def test_attention_ragged_keys(cf, Lq, N1, op):
+    # N1 not a multiple of the 128-key chunk: the last chunk's keys past N1
+    # load as zero rows and leave the softmax max and sum; V rows past N1
+    # are zero (target-attention-like short key sequences).
+    rng = np.random.default_rng(N1 + Lq)
+    Q = _bf16_t(rng.standard_normal((2, Lq, 128)))
+    K = _bf16_t(rng.standard_normal((2, N1, 128)))
+    V = _bf16_t(rng.standard_normal((2, N1, 128)))
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, op, scale)
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} Lq={Lq} N1={N1} b={b}")
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("d_qk,d_v,N1", [(64, 64, 256), (64, 64, 200), (128, 64, 384), (96, 32, 130),
+                                         (32, 128, 512)])
+def test_attention_head_dims(cf, d_qk, d_v, N1, op):
+    # Head dims below 128: Q/K columns past d_qk and V columns past d_v load
+    # as zeros; the output has d_v columns.
+    rng = np.random.default_rng(d_qk * 7 + d_v + N1)
+    Lq = 200
+    Q = _bf16_t(rng.standard_normal((2, Lq, d_qk)))
+    K = _bf16_t(rng.standard_normal((2, N1, d_qk)))
+    V = _bf16_t(rng.standard_normal((2, N1, d_v)))
+    scale = 1 / math.sqrt(d_qk)
+    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert out.shape == (2, Lq, d_v)
+    got = out.cpu().numpy()
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} d={d_qk}/{d_v} b={b}")
+
+
+@pytest.mark.parametrize("M,K,N1,N2", [(256, 128, 200, 256), (200, 64, 1000, 296), (128, 256, 384, 1000),
+                                       (64, 512, 104, 520), (300, 72, 136, 8)])
+def test_mlp_ragged_n(cf, M, K, N1, N2):
+    # N1 not a multiple of 128 C (chunks past N1 are zero) and N2 not a
+    # multiple of 256 (the last CTA's output block is clipped).
+    X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M + N1 + N2)
+    out = cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu")
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
+    b2b_gate(out.cpu().numpy(), ref, bound, f"mlp ragged N {M}x{K}x{N1}x{N2}")
+
+
+def test_mlp_ragged_n2_bf16_padded(cf):
+    # bf16 output of 296 columns inside 304-element rows: the padding stays.
+    X, W1, W2 = _mlp_case(256, 128, 256, 296, seed=3)
+    buf = torch.full((256, 304), 3.0, dtype=torch.bfloat16, device="cuda")
+    cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu", out=buf[:, :296])
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert torch.all(buf[:, 296:] == 3.0)
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
+    _bf16_gate(buf[:, :296].float().cpu().numpy(), ref, bound, "mlp N2=296 bf16")

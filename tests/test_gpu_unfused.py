@@ -100,3 +100,18 @@ def test_unfused_ragged_n(cf, N):
     ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
                           None)
     assert_rows_close(out.cpu().numpy(), ref, what=f"unfused ragged N={N}")
+
+
+def test_unfused_attention_ragged_keys(cf):
+    rng = np.random.default_rng(5)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    Q, K, V = t(rng.standard_normal((2, 256, 64))), t(rng.standard_normal((2, 200, 64))), \
+        t(rng.standard_normal((2, 200, 64)))
+    out = cf.cf_unfused_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), "scale_softmax", 0.125, w1_trans=True)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for h in range(2):
+        q, k, v = (I.to_f64(x[h]) for x in (Q, K, V))
+        ref = O.b2bgemm(q, k.T, v, "scale_softmax", 0.125)
+        bound = 2.0 ** -7 * (np.abs(O.mid_op(q @ k.T, "scale_softmax", 0.125)) @ np.abs(v)) + 1e-6
+        assert np.all(np.abs(got[h] - ref) <= bound)
