@@ -161,6 +161,19 @@ def attention_b2b(seed: int = 0, batch: int = 32, heads: int = 16, L: int = 2048
     return B2BCase(f"b2b_attention_{op}", bh, L, d, L, d, op, 1.0 / math.sqrt(d), True, Q, Kt, V)
 
 
+def target_attention(seed: int = 0, batch: int = 64, targets: int = 512, behaviours: int = 200, d: int = 128,
+                     op: str = "scale_softmax") -> B2BCase:
+    """Target-attention-like short key sequences: per batch entry, ``targets``
+    query rows attend over ``behaviours`` keys/values (a short behaviour
+    sequence, not a multiple of 128); Q, K, V ~ N(0, 1), scale 1/sqrt(d)."""
+    rng = np.random.default_rng(seed)
+    Q = _bf16(rng.standard_normal((batch, targets, d)))
+    Kt = _bf16(rng.standard_normal((batch, behaviours, d)))
+    V = _bf16(rng.standard_normal((batch, behaviours, d)))
+    return B2BCase(f"b2b_target_attention_{op}", batch, targets, d, behaviours, d, op, 1.0 / math.sqrt(d), True,
+                   Q, Kt, V)
+
+
 def to_f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     """Exact float64 copy of a bf16/fp32 CPU tensor (for the oracle)."""
     if t is None:

@@ -74,9 +74,11 @@ def load_peaks():
 class Workload:
     """A fused GEMM-epilogue or B2BGEMM problem with its accounting."""
 
-    def __init__(self, name: str, seed: int = 0, exchange: str = "auto", rows: int = 64):
+    def __init__(self, name: str, seed: int = 0, exchange: str = "auto", rows: int = 64, out_dtype: str = "fp32"):
         self.name = name
         self.exchange = exchange
+        self.out_dtype = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+        ob = 2.0 if out_dtype == "bf16" else 4.0
         if name == "gelu_rmsnorm":
             self.case = I.gelu_rmsnorm(seed)
         elif name == "layernorm_256":
@@ -91,23 +93,25 @@ class Workload:
             self.case = I.mlp_b2b(seed)
         elif name == "mlp_bottom":
             self.case = I.mlp_bottom(seed, rows=rows)
+        elif name == "target_attention":
+            self.case = I.target_attention(seed, batch=rows)
         elif name in ("attention_softmax", "attention_relu"):
             op = "scale_softmax" if name == "attention_softmax" else "scale_relu"
             self.case = I.attention_b2b(seed, op=op)
         else:
             raise ValueError(name)
-        self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu")
+        self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu", "target_attention")
         c = self.case
         if self.is_b2b:
             self.flops = 2.0 * c.batch * c.M * (c.K * c.N1 + c.N1 * c.N2)
-            self.out_bytes = 4.0 * c.batch * c.M * c.N2
+            self.out_bytes = ob * c.batch * c.M * c.N2
             self.bytes = 2.0 * (c.A.numel() + c.W1.numel() + c.W2.numel()) + self.out_bytes
             self.stat_bytes = 0.0
             self.rows = c.batch * c.M
         else:
             vec = sum(t.numel() for t in (c.bias, c.gamma, c.beta, c.stage0_gamma, c.stage0_beta) if t is not None)
             self.flops = 2.0 * c.M * c.N * c.K
-            self.out_bytes = 4.0 * c.M * c.N
+            self.out_bytes = ob * c.M * c.N
             res = 0.0 if c.residual is None else float(c.residual.numel() * c.residual.element_size())
             self.bytes = 2.0 * (c.M * c.K + c.K * c.N) + 4.0 * vec + res + self.out_bytes
             # Row statistics of rows wider than one 256-column tile: 8 bytes
@@ -118,11 +122,12 @@ class Workload:
 
     def config(self):
         c = self.case
+        out = "bf16" if self.out_dtype == torch.bfloat16 else "fp32"
         if self.is_b2b:
             return {"workload": self.name, "batch": c.batch, "M": c.M, "K": c.K, "N1": c.N1, "N2": c.N2,
-                    "mid_op": c.op, "intermediate": "bf16, on chip"}
+                    "mid_op": c.op, "intermediate": "bf16, on chip", "out": out}
         return {"workload": self.name, "M": c.M, "N": c.N, "K": c.K, "ops": [list(o) for o in c.ops],
-                "row_stat_exchange": self.exchange}
+                "row_stat_exchange": self.exchange, "out": out}
 
     # -- GPU side
     def to_device(self):
@@ -130,13 +135,13 @@ class Workload:
         dev = {}
         if self.is_b2b:
             dev["A"], dev["W1"], dev["W2"] = c.A.cuda(), c.W1.cuda(), c.W2.cuda()
-            dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=torch.float32, device="cuda")
+            dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=self.out_dtype, device="cuda")
         else:
             dev["A"], dev["B"] = c.A.cuda(), c.B.cuda()
             for k in ("bias", "gamma", "beta", "residual", "stage0_gamma", "stage0_beta"):
                 t = getattr(c, k)
                 dev[k] = None if t is None else t.cuda()
-            dev["out"] = torch.empty((c.M, c.N), dtype=torch.float32, device="cuda")
+            dev["out"] = torch.empty((c.M, c.N), dtype=self.out_dtype, device="cuda")
         return dev
 
     def fused_step(self, cf, dev, stream=None, workspace=None):
@@ -481,6 +486,24 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     except Exception as exc:  # the comparison path is optional for the headline
         unfused = {"error": str(exc)[:200]}
 
+    # The fused call captured once in a CUDA graph and replayed: the device
+    # time of a small problem is then not the host's marshalling and launch
+    # time (the graph holds the same launch, with the same arguments).
+    graph, launch_mode = None, "direct"
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                wl.fused_step(cf, dev, None, workspace)
+            g.replay()
+            torch.cuda.synchronize()
+            if cf.cf_last_device_status() != 0:
+                raise RuntimeError("device status reports a timeout in the graph replay")
+            graph, launch_mode = g, "cuda graph replay"
+        except Exception as exc:  # direct launches remain valid; say why
+            launch_mode = f"direct (graph capture failed: {str(exc)[:120]})"
+            torch.cuda.synchronize()
+
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk, NvmlSampler(torch.cuda.current_device()) as nv:
@@ -490,7 +513,10 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         for k in range(args.steps):
             flush.fill_(float(k))
             starts[k].record(stream)
-            step()
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
             ends[k].record(stream)
         torch.cuda.synchronize()
         barrier(dist)
@@ -515,9 +541,9 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         t = getattr(c, k)
         if t is not None:
             host_in.append((k, t.pin_memory()))
-    host_out = torch.empty(dev["out"].shape, dtype=torch.float32).pin_memory()
+    host_out = torch.empty(dev["out"].shape, dtype=dev["out"].dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for _, t in host_in)
-    d2h = host_out.numel() * 4
+    d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
     for k in range(max(3, args.steps)):
         torch.cuda.synchronize()
@@ -539,7 +565,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     ref_tflops, ref_rows, ref_s = time_oracle(wl, args.cpu_seconds)
     t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
     src = kernel_source_hash()
-    tr = NCU_TRAFFIC.get(wl.name)
+    tr = NCU_TRAFFIC.get(wl.name) if wl.out_dtype == torch.float32 else None  # counters taken with fp32 out
     tr = tr if tr and tr.get("src") == src else None
     traffic = (tr["read"] + tr["write"]) if tr else None
     # An intermediate that went to HBM would have to be written there: DRAM
@@ -549,7 +575,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**wl.config(), "l2": "flushed between timed steps (256 MB write)",
+        "config": {**wl.config(), "l2": "flushed between timed steps (256 MB write)", "launch": launch_mode,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": tflops / peaks["bf16_tflops"], "traffic": traffic,
@@ -580,18 +606,24 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
-                             "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms"])
-    ap.add_argument("--rows", type=int, default=64, help="batch rows of the mlp_bottom workload (1..64)")
+                             "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms",
+                             "target_attention"])
+    ap.add_argument("--rows", type=int, default=64,
+                    help="batch of the mlp_bottom (rows) and target_attention (users) workloads (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--ref-step-seconds", type=float, default=5.0, help="oracle seconds per reference step")
+    ap.add_argument("--out-dtype", default="fp32", choices=["fp32", "bf16"],
+                    help="output dtype of the fused call (the unfused GEMM-epilogue path is fp32-only)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct launches instead of replaying the fused call's CUDA graph")
     ap.add_argument("--once", action="store_true",
                     help="run the fused kernel of the workload once and exit (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     dist, rank, world, local = dist_setup(args)
-    wl = Workload(args.workload, exchange=args.exchange, rows=args.rows)
+    wl = Workload(args.workload, exchange=args.exchange, rows=args.rows, out_dtype=args.out_dtype)
     if args.impl == "reference":
         run_reference(args, wl, dist, rank, world)
     else:

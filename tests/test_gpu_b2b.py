@@ -330,3 +330,15 @@ def test_mlp_ragged_n2_bf16_padded(cf):
     ref = O.b2bgemm(x, w1, w2, "relu")
     bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
     _bf16_gate(buf[:, :296].float().cpu().numpy(), ref, bound, "mlp N2=296 bf16")
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+def test_target_attention_shape(cf, op):
+    # The target-attention bench shape (512 targets over 200 behaviours,
+    # d = 128) at batch 4, every row compared.
+    case = I.target_attention(batch=4, op=op)
+    got = _run_attention(cf, case.A, case.W1, case.W2, op, case.scale)
+    for b in range(case.batch):
+        q, k, v = (I.to_f64(t[b]) for t in (case.A, case.W1, case.W2))
+        ref = O.b2bgemm(q, k.T, v, op, case.scale)
+        b2b_gate(got[b], ref, _abs_bound(q, k, v, op, case.scale), f"target attention {op} b={b}")
