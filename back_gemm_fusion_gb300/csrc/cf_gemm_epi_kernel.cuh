@@ -49,6 +49,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kAStageBytes = kBM * kBK * 2;              // 16 KB
 constexpr int kOutStageBytes = 32 * 32 * 4;              // 4 KB per epilogue warp
 constexpr int kTmemCols = 2 * kBN;                       // two accumulators
+constexpr int kNumVec = 5;                               // staged vector slices per tile
 
 // Per-mode geometry.  CTA2: a CTA pair runs 256 x 256 MMAs (cta_group::2),
 // each CTA holding its 128 rows of A and half (128 columns) of the B tile,
@@ -60,14 +61,20 @@ struct Geo {
   static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr int kOffOut = kStages * kStageBytes;
   static constexpr int kOffSlots = kOffOut + kEpiWarps * kOutStageBytes;  // float2 [2][128]
-  static constexpr int kOffBars = kOffSlots + 2 * kBM * 8;
+  static constexpr int kOffVec = kOffSlots + 2 * kBM * 8;                 // float [kNumVec][kBN]
+  static constexpr int kOffBars = kOffVec + kNumVec * kBN * 4;
   // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[2][4], sempty[2][4], drain
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1;
+  // ..., vec_free, vec_full
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32)
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack for the 1024-byte alignment
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// The tile's slices of the epilogue vectors, staged in shared memory once per
+// tile: bias, gamma, beta, and the first reduction stage's gamma0, beta0.
+enum VecSlot : int { VEC_BIAS = 0, VEC_GAMMA = 1, VEC_BETA = 2, VEC_GAMMA0 = 3, VEC_BETA0 = 4 };
 
 enum OpKind : int { OP_BIAS = 1, OP_SCALE = 2, OP_RELU = 3, OP_GELU_TANH = 4, OP_ADD_RESIDUAL = 5 };
 
@@ -101,23 +108,24 @@ __device__ __forceinline__ void mask_tail(float (&v)[32], int cv, float fill) {
     if (j >= cv) v[j] = fill;
 }
 
-// v[j] *= x[n + j] and v[j] += x[n + j] over a 32-column chunk.
-template <bool GUARD>
-__device__ __forceinline__ void mul_vec(float (&v)[32], const float* x, int n, int N) {
+// v[j] *= x[j] and v[j] += x[j] over a 32-column chunk, x the chunk's slice
+// of a staged vector in shared memory (every lane reads the same address).
+__device__ __forceinline__ void mul_vec(float (&v)[32], const float* x) {
+  const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 g = ld4<GUARD>(x, n + 4 * j, N);
+    const float4 g = x4[j];
     v[4 * j + 0] *= g.x;
     v[4 * j + 1] *= g.y;
     v[4 * j + 2] *= g.z;
     v[4 * j + 3] *= g.w;
   }
 }
-template <bool GUARD>
-__device__ __forceinline__ void add_vec(float (&v)[32], const float* x, int n, int N) {
+__device__ __forceinline__ void add_vec(float (&v)[32], const float* x) {
+  const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 b = ld4<GUARD>(x, n + 4 * j, N);
+    const float4 b = x4[j];
     v[4 * j + 0] += b.x;
     v[4 * j + 1] += b.y;
     v[4 * j + 2] += b.z;
@@ -126,24 +134,27 @@ __device__ __forceinline__ void add_vec(float (&v)[32], const float* x, int n, i
 }
 
 // Normalisation with the affine vectors: v = gamma (v sa + sh) (+ beta).
-template <bool GUARD, bool BETA>
-__device__ __forceinline__ void norm_affine(float (&v)[32], const float* gamma, const float* beta, int n, int N,
-                                            float sa, float sh) {
+template <bool BETA>
+__device__ __forceinline__ void norm_affine(float (&v)[32], const float* gamma, const float* beta, float sa,
+                                            float sh) {
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 g = ld4<GUARD>(gamma, n + 4 * j, N);
+    const float4 g = g4[j];
     v[4 * j + 0] = fmaf(v[4 * j + 0], sa, sh) * g.x;
     v[4 * j + 1] = fmaf(v[4 * j + 1], sa, sh) * g.y;
     v[4 * j + 2] = fmaf(v[4 * j + 2], sa, sh) * g.z;
     v[4 * j + 3] = fmaf(v[4 * j + 3], sa, sh) * g.w;
   }
-  if (BETA) add_vec<GUARD>(v, beta, n, N);
+  if (BETA) add_vec(v, beta);
 }
 
 // Elementwise ops [o0, o1) of the program on 32 consecutive columns n.. of
-// row m of the tile.  GUARD: the chunk crosses column N (see ld4).
+// row m of the tile; bias_s: the chunk's slice of the staged bias.  GUARD:
+// the chunk crosses column N (see ld4; the staged slices hold zeros there).
 template <bool GUARD>
-__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m, int o0, int o1) {
+__device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m, int o0, int o1,
+                                              const float* bias_s) {
   for (int o = o0; o < o1; ++o) {
     const int kind = p.op_kind[o];
     if (kind == OP_ADD_RESIDUAL) {
@@ -193,14 +204,7 @@ __device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)
         }
       }
     } else if (kind == OP_BIAS) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 b = ld4<GUARD>(p.bias, n + 4 * j, p.N);
-        v[4 * j + 0] += b.x;
-        v[4 * j + 1] += b.y;
-        v[4 * j + 2] += b.z;
-        v[4 * j + 3] += b.w;
-      }
+      add_vec(v, bias_s);
     } else if (kind == OP_SCALE) {
       const float s = p.op_scalar[o];
 #pragma unroll
@@ -361,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   auto bar = [&](int idx) -> uint32_t { return sbase + kOffBars + 8 * idx; };
   const int BAR_FULL = 0, BAR_EMPTY = kStages, BAR_TFULL = 2 * kStages, BAR_TEMPTY = 2 * kStages + 2;
   const int BAR_SFULL = 2 * kStages + 4, BAR_SEMPTY = 2 * kStages + 12, BAR_DRAIN = 2 * kStages + 20;
+  const int BAR_VFREE = 2 * kStages + 21, BAR_VFULL = 2 * kStages + 22;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
@@ -383,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       mbar_init(bar(BAR_SEMPTY + k), cn);
     }
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_VFREE), kEpiWarps);
+    mbar_init(bar(BAR_VFULL), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -516,6 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const uint64_t out_policy = l2_policy_evict_first();
     uint8_t* out_ptr = smem + kOffOut + (warp - 2) * kOutStageBytes;
     float2* slots = reinterpret_cast<float2*>(smem + kOffSlots);
+    float* vsm = reinterpret_cast<float*>(smem + G::kOffVec);  // [kNumVec][kBN] this tile's vector slices
+    const bool stage_vec = p.bias || p.gamma || p.beta || p.gamma0 || p.beta0;
     int t = 0;
     for (Work w = make_work<XMODE>(p); w.valid(); w.next(), ++t) {
       int strip, tile;
@@ -524,6 +533,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       const int nv = RAG ? min(kBN, p.N - n0) : kBN;  // valid columns: fewer in a ragged last tile
       const int nch = RAG ? (nv + 31) >> 5 : kBN / 32;  // 32-column chunks holding them
       const int acc = t & 1;
+      // Stage the tile's vector slices (zeros past N) while its main loop
+      // runs: one round trip to L2 per tile instead of one per chunk and
+      // pass.  Every epilogue warp must be done with the previous tile's
+      // slices first (vec_free); all four fill, then wait for vec_full.
+      // (Programs without vectors, e.g. scale + softmax, skip all of it.)
+      if (stage_vec) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VFREE), (t & 1) ^ 1, wc))) break;
+        for (int i = lane + 32 * (warp - 2); i < kNumVec * (kBN / 4); i += 32 * kEpiWarps) {
+          const int vi = i / (kBN / 4), c4 = 4 * (i - vi * (kBN / 4));
+          const float* src = vi == VEC_BIAS ? p.bias : vi == VEC_GAMMA ? p.gamma : vi == VEC_BETA ? p.beta
+                           : vi == VEC_GAMMA0 ? p.gamma0 : p.beta0;
+          if (src) *reinterpret_cast<float4*>(vsm + vi * kBN + c4) = ld4<RAG>(src, n0 + c4, p.N);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_VFULL));
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VFULL), t & 1, wc))) break;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_TFULL + acc), (t >> 1) & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kBN);
@@ -544,8 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           const int n = n0 + c * 32;
           const bool tail = RAG && n + 32 > p.N;
           if (p.n_ops0 > 0) {
-            if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops0);
-            else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops0);
+            const float* bs = vsm + VEC_BIAS * kBN + c * 32;
+            if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops0, bs);
+            else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops0, bs);
             tmem_st32(taddr + c * 32, v);
           }
           if (tail) mask_tail(v, p.N - n, 0.0f);
@@ -599,19 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           if constexpr (ROWOP0 != ROW_NONE) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
-            if (p.gamma0) {
-              if (tail) mul_vec<true>(v, p.gamma0, n, p.N);
-              else mul_vec<false>(v, p.gamma0, n, p.N);
-            }
-            if (ROWOP0 == ROW_LAYERNORM && p.beta0) {
-              if (tail) add_vec<true>(v, p.beta0, n, p.N);
-              else add_vec<false>(v, p.beta0, n, p.N);
-            }
+            if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
+            if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
           }
           if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
             const int o0 = ROWOP0 != ROW_NONE ? p.n_ops0 : 0;
-            if (tail) apply_program<true>(p, v, n, m0 + row, o0, p.n_ops);
-            else apply_program<false>(p, v, n, m0 + row, o0, p.n_ops);
+            const float* bs = vsm + VEC_BIAS * kBN + c * 32;
+            if (tail) apply_program<true>(p, v, n, m0 + row, o0, p.n_ops, bs);
+            else apply_program<false>(p, v, n, m0 + row, o0, p.n_ops, bs);
             tmem_st32(taddr + c * 32, v);
           }
           if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
@@ -720,14 +742,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         const int n = n0 + c * 32;
         const bool tail = RAG && n + 32 > p.N;
         if (ROWOP == ROW_NONE) {
-          if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops);
-          else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops);
+          const float* bs = vsm + VEC_BIAS * kBN + c * 32;
+          if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops, bs);
+          else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops, bs);
         } else if (ROWOP == ROW_SOFTMAX) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;
         } else {
-          if (tail) norm_affine<true, ROWOP == ROW_LAYERNORM>(v, p.gamma, p.beta, n, p.N, scale_a, shift_a);
-          else norm_affine<false, ROWOP == ROW_LAYERNORM>(v, p.gamma, p.beta, n, p.N, scale_a, shift_a);
+          norm_affine<ROWOP == ROW_LAYERNORM>(v, vsm + VEC_GAMMA * kBN + c * 32, vsm + VEC_BETA * kBN + c * 32,
+                                              scale_a, shift_a);
         }
         // The previous TMA store from this buffer must have read it.
         if (lane == 0) bulk_wait_read0();
@@ -773,6 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       if (lane == 0) {
         if (CTA2 && !leader) mbar_arrive_cluster(bar(BAR_TEMPTY + acc), 0);  // the leader issues the MMAs
         else mbar_arrive(bar(BAR_TEMPTY + acc));
+        if (stage_vec) mbar_arrive(bar(BAR_VFREE));  // this warp no longer reads the tile's vector slices
       }
     }
     if (lane == 0) bulk_wait0();
