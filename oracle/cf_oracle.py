@@ -34,7 +34,9 @@ written out:
 3. Row reductions (LayerNorm, RMSNorm, softmax), each a stage boundary: a
    program is elementwise nodes, a reduction, and optionally more elementwise
    nodes and a second reduction that ends it (the Stage-Stream model's chain
-   of stages; the kernels support up to two).
+   of stages; the kernels support up to two).  The same reductions down the
+   columns of P (along its first dimension, the complementary strip of major
+   comment 1) are the ``col_*`` functions.
 4. For B2BGEMM the single rounding point is the intermediate S' = F(S), which
    is rounded to bfloat16 round-to-nearest-even before the second GEMM.
 
@@ -65,6 +67,9 @@ __all__ = [
     "row_layernorm",
     "row_rmsnorm",
     "row_softmax",
+    "col_layernorm",
+    "col_rmsnorm",
+    "col_softmax",
     "gemm_epilogue",
     "mid_op",
     "b2bgemm",
@@ -208,19 +213,56 @@ def row_softmax(x) -> np.ndarray:
     return e / e.sum(axis=1, keepdims=True)
 
 
+def col_layernorm(x, gamma, beta, eps: float) -> np.ndarray:
+    """LayerNorm down each column: the reduction along the first dimension of
+    P (referee report, major comment 1 [Sec. III, Eq. (1)]: such reductions
+    need the complementary strip, the column of tiles T_{m,n} over m).  Mean
+    and biased variance over m; the affine vectors stay indexed by the column
+    (a per-feature scale and shift, as for a batch normalisation):
+
+    y[m, n] = gamma[n] (x[m, n] - mu_n) / sqrt(var_n + eps) + beta[n].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=0, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=0, keepdims=True)
+    g = np.asarray(gamma, dtype=np.float64)[None, :]
+    b = np.asarray(beta, dtype=np.float64)[None, :]
+    return g * (x - mu) / np.sqrt(var + eps) + b
+
+
+def col_rmsnorm(x, gamma, eps: float) -> np.ndarray:
+    """RMSNorm down each column: y = gamma[n] x / sqrt(mean_m(x^2) + eps)."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = (x * x).mean(axis=0, keepdims=True)
+    return np.asarray(gamma, dtype=np.float64)[None, :] * x / np.sqrt(ms + eps)
+
+
+def col_softmax(x) -> np.ndarray:
+    """Softmax down each column: exp(x - max_m) / sum_m exp(x - max_m)."""
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(x - x.max(axis=0, keepdims=True))
+    return e / e.sum(axis=0, keepdims=True)
+
+
 _ROW_OPS = ("layernorm", "rmsnorm", "softmax")
 
 
 def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta, residual=None, stage0_gamma=None,
-                   stage0_beta=None) -> np.ndarray:
-    """Run an epilogue program: elementwise nodes and row reductions in order.
+                   stage0_beta=None, axis: str = "row") -> np.ndarray:
+    """Run an epilogue program: elementwise nodes and reductions in order.
 
     ``ops`` is a sequence of ``(name,)`` or ``(name, scalar)`` tuples; the
-    scalar is the scale for ``scale`` and eps for the norms.  At most two row
+    scalar is the scale for ``scale`` and eps for the norms.  At most two
     reductions, and if there is one the program ends with a reduction.  The
     last reduction uses ``gamma`` / ``beta``; an earlier one uses
     ``stage0_gamma`` / ``stage0_beta`` (None: 1 and 0, no affine transform).
+    ``axis="row"`` reduces along each row, ``axis="col"`` down each column
+    (every vector is indexed by the column in both cases).
     """
+    if axis not in ("row", "col"):
+        raise ValueError("axis is 'row' or 'col'")
+    norms = {"row": (row_layernorm, row_rmsnorm, row_softmax), "col": (col_layernorm, col_rmsnorm, col_softmax)}
+    layernorm, rmsnorm, softmax = norms[axis]
     names = [o[0] for o in ops]
     row_at = [i for i, n in enumerate(names) if n in _ROW_OPS]
     if len(row_at) > 2 or (row_at and row_at[-1] != len(names) - 1):
@@ -234,25 +276,26 @@ def _apply_program(x, ops: Sequence[tuple], bias, gamma, beta, residual=None, st
             g = gamma if last else (np.ones(N) if stage0_gamma is None else stage0_gamma)
             b = beta if last else (np.zeros(N) if stage0_beta is None else stage0_beta)
             if name == "layernorm":
-                x = row_layernorm(x, g, b, scalar)
+                x = layernorm(x, g, b, scalar)
             elif name == "rmsnorm":
-                x = row_rmsnorm(x, g, scalar)
+                x = rmsnorm(x, g, scalar)
             else:
-                x = row_softmax(x)
+                x = softmax(x)
         else:
             x = elementwise(x, name, scalar, bias, residual)
     return x
 
 
 def gemm_epilogue(A, B, ops: Iterable[tuple], bias=None, gamma=None, beta=None, residual=None,
-                  stage0_gamma=None, stage0_beta=None) -> np.ndarray:
+                  stage0_gamma=None, stage0_beta=None, axis: str = "row") -> np.ndarray:
     """GEMM followed by an epilogue program, all in float64.
 
     A: M x K, B: K x N (row-major, bf16 values as float64); ``residual``
     (M x N) is read by the ``residual`` op; ``stage0_gamma`` / ``stage0_beta``
-    are the affine vectors of the first of two row reductions.  Returns M x N.
+    are the affine vectors of the first of two reductions; ``axis`` picks
+    row reductions (over n) or column reductions (over m).  Returns M x N.
     """
-    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta, residual, stage0_gamma, stage0_beta)
+    return _apply_program(matmul(A, B), list(ops), bias, gamma, beta, residual, stage0_gamma, stage0_beta, axis)
 
 
 def mid_op(S, op: str, scale: float = 1.0) -> np.ndarray:

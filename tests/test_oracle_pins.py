@@ -113,6 +113,48 @@ def test_chained_reductions_rules():
                         beta=np.zeros(4))
 
 
+def test_hand_example_column_reductions():
+    # Reductions down the columns of P (two rows per column): closed forms
+    # from the golden file, including per-column affine vectors.
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    ones, zeros = np.ones(4), np.zeros(4)
+    for key, ops, g, b in (("col_layernorm_eps0", [("layernorm", 0.0)], ones, zeros),
+                           ("col_layernorm_affine", [("layernorm", 0.0)], np.array(h["col_layernorm_affine_gamma"]),
+                            np.array(h["col_layernorm_affine_beta"])),
+                           ("col_rmsnorm_eps0", [("rmsnorm", 0.0)], ones, zeros),
+                           ("col_softmax", [("softmax",)], ones, zeros)):
+        exp = np.array([[_closed(str(v)) for v in row] for row in h[key]], float)
+        got = O.gemm_epilogue(A, B, ops, gamma=g, beta=b, axis="col")
+        np.testing.assert_allclose(got, exp, rtol=0, atol=1e-12, err_msg=key)
+
+
+def test_column_reductions_invariants_and_library():
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((37, 9)) * 3 + 1
+    np.testing.assert_allclose(O.col_softmax(x).sum(axis=0), np.ones(9), rtol=0, atol=1e-14)
+    y = O.col_layernorm(x, np.ones(9), np.zeros(9), 0.0)
+    np.testing.assert_allclose(y.mean(axis=0), np.zeros(9), atol=1e-13)
+    np.testing.assert_allclose((y ** 2).mean(axis=0), np.ones(9), atol=1e-12)
+    r = O.col_rmsnorm(x, np.ones(9), 0.0)
+    np.testing.assert_allclose((r ** 2).mean(axis=0), np.ones(9), atol=1e-12)
+    # A single row: softmax down a column of one element is 1.
+    np.testing.assert_array_equal(O.col_softmax(x[:1]), np.ones((1, 9)))
+    # Library routines in float64: softmax along dim 0, and layer_norm of the
+    # transposed matrix followed by the per-column affine vectors.
+    g, b = rng.standard_normal(9), rng.standard_normal(9)
+    t = torch.from_numpy(x)
+    np.testing.assert_allclose(O.col_softmax(x), torch.softmax(t, dim=0).numpy(), rtol=1e-13, atol=1e-15)
+    ln = torch.nn.functional.layer_norm(t.T, (37,), eps=1e-5).T.numpy() * g[None] + b[None]
+    np.testing.assert_allclose(O.col_layernorm(x, g, b, 1e-5), ln, rtol=1e-10, atol=1e-12)
+    ms = (t * t).mean(dim=0, keepdim=True)
+    np.testing.assert_allclose(O.col_rmsnorm(x, g, 1e-6), (torch.from_numpy(g)[None] * t / torch.sqrt(ms + 1e-6)).numpy(),
+                               rtol=1e-13, atol=1e-14)
+    with pytest.raises(ValueError):
+        O.gemm_epilogue(x[:, :3], np.eye(3), [("softmax",)], axis="diagonal")
+
+
 def _closed(expr: str) -> float:
     """Evaluate a closed form written in the golden file (sqrt, exp, tanh only)."""
     return float(eval(expr, {"__builtins__": {}},
@@ -371,12 +413,18 @@ def test_oracle_mutations_are_caught(monkeypatch):
                                 if np.asarray(B).shape[0] == np.asarray(B).shape[1] else
                                 np.asarray(A, float) @ np.asarray(B, float) * 1.0000001),
         "bf16_truncation": ("bf16_round", lambda x: np.trunc(np.asarray(x, float) * 128) / 128),
+        "col_softmax_row_axis": ("col_softmax", lambda x: np.exp(x) / np.exp(x).sum(1, keepdims=True)),
+        "col_layernorm_gamma_by_row": ("col_layernorm", lambda x, g, b, eps: (
+            (x - x.mean(0, keepdims=True)) / np.sqrt(x.var(0, keepdims=True) + eps) * np.resize(g, (x.shape[0], 1))
+            + np.resize(b, (x.shape[0], 1)))),
+        "col_rmsnorm_unbiased": ("col_rmsnorm", lambda x, g, eps: (
+            np.asarray(g)[None] * x / np.sqrt((x * x).sum(0, keepdims=True) / (x.shape[0] - 1) + eps))),
     }
     checks = [test_hand_example_epilogues, test_layernorm_eps_inside_root_closed_form,
               test_rmsnorm_mean_square_one_and_scale_invariance, test_epilogues_match_torch_float64,
               test_softmax_rows_sum_to_one, test_hand_example_gemm_exact,
               test_matmul_brute_force_fraction, test_b2b_relu_brute_force_with_library_rounding,
-              test_bf16_round_matches_torch_on_float32_values]
+              test_bf16_round_matches_torch_on_float32_values, test_hand_example_column_reductions]
     for name, (attr, bad) in mutations.items():
         with monkeypatch.context() as mp:
             mp.setattr(O, attr, bad)
