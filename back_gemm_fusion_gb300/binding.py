@@ -43,7 +43,7 @@ class cf_op(ctypes.Structure):
 class cf_epi_desc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("n_ops", ctypes.c_uint32), ("ops", cf_op * EPI_MAX_OPS),
                 ("out_dtype", ctypes.c_int32), ("exchange", ctypes.c_int32), ("residual", cf_matrix),
-                ("stage0_gamma", ctypes.c_void_p), ("stage0_beta", ctypes.c_void_p)]
+                ("stage0_gamma", ctypes.c_void_p), ("stage0_beta", ctypes.c_void_p), ("axis", ctypes.c_int32)]
 
 
 class cf_b2b_desc(ctypes.Structure):
@@ -120,14 +120,19 @@ def matrix(t: torch.Tensor, trans: bool = False) -> cf_matrix:
     return cf_matrix(t.data_ptr(), _dtype_code(t), 1 if trans else 0, rows, cols, max(t.stride(0), 1))
 
 
+AXIS_CODES = {"row": 0, "col": 1}
+
+
 def epi_desc(ops: Sequence[Tuple], exchange: str = "auto", residual: Optional[torch.Tensor] = None,
              stage0_gamma: Optional[torch.Tensor] = None, stage0_beta: Optional[torch.Tensor] = None,
-             out_dtype: int = CF_FP32) -> cf_epi_desc:
-    """Descriptor (version 2); ``residual`` is the M x N matrix read by the
+             out_dtype: int = CF_FP32, axis: str = "row") -> cf_epi_desc:
+    """Descriptor (version 3); ``residual`` is the M x N matrix read by the
     ``residual`` op, ``stage0_gamma`` / ``stage0_beta`` the affine vectors of
-    the first of two row reductions, ``out_dtype`` CF_FP32 or CF_BF16."""
+    the first of two reductions, ``out_dtype`` CF_FP32 or CF_BF16, ``axis``
+    "row" (reductions along rows) or "col" (down columns)."""
     d = cf_epi_desc()
-    d.version = 2
+    d.version = 3
+    d.axis = AXIS_CODES[axis]
     d.n_ops = len(ops)
     if len(ops) > EPI_MAX_OPS:
         raise ValueError("too many epilogue ops")
@@ -160,9 +165,9 @@ def _check(status: int, where: str):
 
 # ----------------------------------------------------------------- wrappers
 def cf_workspace_size(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], b_trans: bool = False,
-                      exchange: str = "auto") -> int:
+                      exchange: str = "auto", axis: str = "row") -> int:
     lib = load_library()
-    a, b, d = matrix(A), matrix(B, b_trans), epi_desc(ops, exchange)
+    a, b, d = matrix(A), matrix(B, b_trans), epi_desc(ops, exchange, axis=axis)
     return int(lib.cf_workspace_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
 
 
@@ -171,18 +176,19 @@ def cf_gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tuple], bia
                      workspace: Optional[torch.Tensor] = None, stream=None,
                      residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
                      stage0_beta: Optional[torch.Tensor] = None,
-                     out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+                     out_dtype: torch.dtype = torch.float32, axis: str = "row") -> torch.Tensor:
     """out = epilogue(A @ B) in one fused kernel.  ``B`` is K x N, or N x K
     with ``b_trans=True``; ``residual`` (M x N, fp32 or bf16) feeds the
     ``residual`` op.  ``out`` is fp32 or bf16 (``out_dtype`` when it is
-    allocated here).  A workspace is allocated if needed and not given."""
+    allocated here).  ``axis="col"`` reduces down the columns (needs
+    ``b_trans=True``).  A workspace is allocated if needed and not given."""
     lib = load_library()
     M = A.shape[0]
     N = B.shape[0] if b_trans else B.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
-                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out)))
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out), axis))
     need = int(lib.cf_workspace_size(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
@@ -199,7 +205,7 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
                              exchange: str = "auto", stream=None,
                              residual: Optional[torch.Tensor] = None, stage0_gamma: Optional[torch.Tensor] = None,
                              stage0_beta: Optional[torch.Tensor] = None,
-                             out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+                             out_dtype: torch.dtype = torch.float32, axis: str = "row") -> torch.Tensor:
     """Same as cf_gemm_epilogue, but the library takes any scratch it needs
     from its own static device array: nothing is allocated by this call
     (``out`` must be given by callers that cannot allocate)."""
@@ -209,7 +215,7 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
         N = B.shape[0] if b_trans else B.shape[1]
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
-                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out)))
+                  epi_desc(ops, exchange, residual, stage0_gamma, stage0_beta, _dtype_code(out), axis))
     st = lib.cf_gemm_epilogue_noalloc(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _stream(stream))
     _check(st, "cf_gemm_epilogue_noalloc")

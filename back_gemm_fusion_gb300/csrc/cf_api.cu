@@ -28,11 +28,11 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   unsigned* status = nullptr;
   // Indexed by the kernel variant's row code (row_code(first, last row op)).
-  // Indexed [row code][ragged-N kernels][...].
-  bool prepared[kRowCodes][2][3][2] = {};
-  int max_clusters[kRowCodes][2][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit), 0 = unknown
-  int max_pairs[kRowCodes][2][3] = {};                        // resident 2-CTA clusters per (row code, xmode)
-  int blocks_per_sm[kRowCodes][2][3] = {};                    // 0 = unknown
+  // Indexed [row code][kernel variant][...].
+  bool prepared[kRowCodes][kNumVariants][3][2] = {};
+  int max_clusters[kRowCodes][kNumVariants][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit)
+  int max_pairs[kRowCodes][kNumVariants][3] = {};                        // resident 2-CTA clusters per xmode
+  int blocks_per_sm[kRowCodes][kNumVariants][3] = {};                    // 0 = unknown
 };
 
 std::mutex g_mu;
@@ -128,10 +128,11 @@ struct EpiPlan {
   int kinds[CF_EPI_MAX_OPS] = {};
   float scalars[CF_EPI_MAX_OPS] = {};
   bool need_bias = false, need_gamma = false, need_beta = false, need_residual = false;
+  bool cols = false;      // reductions down the columns (the kernel runs on P^T)
 };
 
 cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
-  if (!epi || (epi->version != 1 && epi->version != 2) || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if (!epi || epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
   if (epi->exchange < CF_XCHG_AUTO || epi->exchange > CF_XCHG_GLOBAL) return CF_ERR_INVALID_ARG;
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
     const cf_op& op = epi->ops[i];
@@ -167,6 +168,11 @@ cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
     plan->scalars[plan->n_elem] = op.scalar;
     plan->n_elem++;
   }
+  // The axis field exists from version 3 (never read from a shorter struct).
+  if (epi->version >= 3) {
+    if (epi->axis != CF_AXIS_ROWS && epi->axis != CF_AXIS_COLS) return CF_ERR_INVALID_ARG;
+    plan->cols = epi->axis == CF_AXIS_COLS && plan->rowop != ROW_NONE;
+  }
   return CF_OK;
 }
 
@@ -186,7 +192,8 @@ size_t ws_bytes_for(int64_t strips, int64_t tiles_n) {
 }
 
 struct GemmShape {
-  int64_t M, N, K;
+  int64_t M, N, K;   // the user's problem: P = A . B is M x N
+  int64_t kM, kN;    // the kernel's: M x N, or N x M for column reductions (P^T)
 };
 
 cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float* bias, const float* gamma,
@@ -204,7 +211,8 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
     return CF_ERR_INVALID_ARG;
   if ((bias && !aligned16(bias)) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)))
     return CF_ERR_MISALIGNED;
-  if (plan->rowop0 != ROW_NONE && epi->exchange == CF_XCHG_CLUSTER && N > kBN) return CF_ERR_UNSUPPORTED_SHAPE;
+  const int64_t kN = plan->cols ? M : N;  // the kernel's row length
+  if (plan->rowop0 != ROW_NONE && epi->exchange == CF_XCHG_CLUSTER && kN > kBN) return CF_ERR_UNSUPPORTED_SHAPE;
   if (plan->rowop0 != ROW_NONE &&
       ((epi->stage0_gamma && !aligned16(epi->stage0_gamma)) || (epi->stage0_beta && !aligned16(epi->stage0_beta))))
     return CF_ERR_MISALIGNED;
@@ -217,7 +225,12 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   sh->M = M;
   sh->N = N;
   sh->K = K;
+  sh->kM = plan->cols ? N : M;
+  sh->kN = kN;
   if (M == 0 || N == 0) return CF_OK;
+  // Column reductions run on P^T = B^T A^T: the kernel's A operand is B's
+  // N x K transpose (K-major), so B must be given that way.
+  if (plan->cols && B->trans != 1) return CF_ERR_UNSUPPORTED_SHAPE;
   // Any M >= 1: rows past M are zero-filled by the TMA loads and clipped by
   // the TMA stores of the last (ragged) 128-row strip; rows are independent.
   // K >= 64 with K % 8 == 0: the last 64-wide K block reads zeros past K
@@ -227,7 +240,7 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   // statistics and never reads a vector past N, and the TMA stores clip them.
   if (K % 8 != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
-  const int64_t tiles_n = (N + kBN - 1) / kBN;
+  const int64_t tiles_n = (kN + kBN - 1) / kBN;
   if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)
     return CF_ERR_UNSUPPORTED_SHAPE;
   return CF_OK;
@@ -297,7 +310,7 @@ size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf_epi_de
   if (!A || !B || !epi) return 0;
   EpiPlan plan;
   if (parse_epi(epi, &plan) != CF_OK) return 0;
-  const int64_t M = A->rows, N = B->cols;
+  const int64_t M = plan.cols ? B->cols : A->rows, N = plan.cols ? A->rows : B->cols;  // the kernel's
   if (M <= 0 || N <= 0) return 0;
   const int64_t tiles_n = (N + kBN - 1) / kBN;
   // The cluster path may fall back to the workspace path when no cluster of
@@ -316,7 +329,12 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   cf_status s = validate_gemm_epi(A, B, bias, gamma, beta, epi, out, &plan, &sh);
   if (s != CF_OK) return s;
   if (sh.M == 0 || sh.N == 0) return CF_OK;
-  const int64_t tiles_n = (sh.N + kBN - 1) / kBN, strips = (sh.M + kBM - 1) / kBM;
+  // The kernel's operands: P^T = B^T A^T for column reductions (B given as
+  // N x K is the K-major A operand, A the K-major B operand).
+  const cf_matrix* KA = plan.cols ? B : A;
+  const cf_matrix* KB = plan.cols ? A : B;
+  const bool kb_k_major = plan.cols || B->trans == 1;
+  const int64_t tiles_n = (sh.kN + kBN - 1) / kBN, strips = (sh.kM + kBM - 1) / kBM;
   int xmode = choose_xmode(plan, epi, tiles_n);
   const int code = plan.code();
   const size_t ws_stage = (plan.rowop != ROW_NONE && tiles_n > 1) ? ws_bytes_for(strips, tiles_n) : 0;
@@ -331,19 +349,21 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   GemmEpiLaunch L;
   std::memset(&L, 0, sizeof(L));
   GemmEpiParams& p = L.p;
-  if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A->ptr, sh.K, sh.M, A->ld * 2, kBK, kBM)) != CF_OK)
+  if ((s = encode_2d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KA->ptr, sh.K, sh.kM, KA->ld * 2, kBK, kBM)) != CF_OK)
     return s;
-  p.b_mn_major = B->trans == 0 ? 1 : 0;
+  p.b_mn_major = kb_k_major ? 0 : 1;
   // fp32 out: 32 x 32 blocks of 128-byte rows, 128-byte swizzle; bf16 out:
-  // 32 x 32 blocks of 64-byte rows, unswizzled.
+  // 32 x 32 blocks of 64-byte rows, unswizzled; column reductions stage
+  // transposed blocks, unswizzled.  The map always describes the user's
+  // M x N output.
   p.out_bf16 = epi->out_dtype == CF_BF16 ? 1 : 0;
   if ((s = p.out_bf16 ? encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out->ptr, sh.N, sh.M, out->ld * 2, 32,
                                   32, CU_TENSOR_MAP_SWIZZLE_NONE)
                       : encode_2d(&p.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out->ptr, sh.N, sh.M, out->ld * 4, 32,
-                                  32)) != CF_OK)
+                                  32, plan.cols ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != CF_OK)
     return s;
-  p.M = (int)sh.M;
-  p.N = (int)sh.N;
+  p.M = (int)sh.kM;
+  p.N = (int)sh.kN;
   p.K = (int)sh.K;
   p.tiles_n = (int)tiles_n;
   p.strips = (int)strips;
@@ -371,7 +391,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   p.status = dev->status;
   p.timeout_cycles = wait_timeout_cycles();
 
-  const int rag = sh.N % kBN != 0 ? 1 : 0;  // the last tile of each row is ragged
+  const int variant = (sh.kN % kBN != 0 ? 1 : 0) + (plan.cols ? 2 : 0);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int x = X_NONE; x <= X_GLOBAL; ++x) {
@@ -379,9 +399,9 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       if (plan.rowop0 != ROW_NONE && x == X_CLUSTER) continue;  // not instantiated for chained stages
       for (int pr = 0; pr < 2; ++pr) {
         if (pr == 1 && x == X_CLUSTER) continue;
-        if (!dev->prepared[code][rag][x][pr]) {
-          if (gemm_epi_prepare(code, x, pr == 1, rag != 0) != cudaSuccess) return CF_ERR_CUDA;
-          dev->prepared[code][rag][x][pr] = true;
+        if (!dev->prepared[code][variant][x][pr]) {
+          if (gemm_epi_prepare(code, x, pr == 1, variant) != cudaSuccess) return CF_ERR_CUDA;
+          dev->prepared[code][variant][x][pr] = true;
         }
       }
     }
@@ -391,10 +411,10 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int maxc = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_clusters[code][rag][tiles_n];
+      int& cached = dev->max_clusters[code][variant][tiles_n];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(code, X_CLUSTER, false, rag != 0, (int)tiles_n, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, X_CLUSTER, false, variant, (int)tiles_n, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -425,19 +445,19 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   // exchange keeps 1-CTA tiles.
   const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
   if (p.b_mn_major)
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.N, sh.K, B->ld * 2, 64, kBK);
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.kN, sh.K, KB->ld * 2, 64, kBK);
   else
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B->ptr, sh.K, sh.N, B->ld * 2, kBK,
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.K, sh.kN, KB->ld * 2, kBK,
                   want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
   if (s != CF_OK) return s;
   if (want_pair) {
     int maxp = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->max_pairs[code][rag][xmode];
+      int& cached = dev->max_pairs[code][variant][xmode];
       if (cached == 0) {
         int q = 0;
-        if (gemm_epi_max_clusters(code, xmode, true, rag != 0, 2, &q) != cudaSuccess) {
+        if (gemm_epi_max_clusters(code, xmode, true, variant, 2, &q) != cudaSuccess) {
           cudaGetLastError();
           q = 0;
         }
@@ -454,8 +474,8 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     int per_sm = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      int& cached = dev->blocks_per_sm[code][rag][xmode];
-      if (cached == 0 && gemm_epi_max_blocks_per_sm(code, xmode, rag != 0, &cached) != cudaSuccess) cached = 0;
+      int& cached = dev->blocks_per_sm[code][variant][xmode];
+      if (cached == 0 && gemm_epi_max_blocks_per_sm(code, xmode, variant, &cached) != cudaSuccess) cached = 0;
       per_sm = cached;
     }
     if (per_sm < 1) return CF_ERR_CUDA;
@@ -478,6 +498,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   }
   L.rowop = code;
   L.xmode = xmode;
+  L.variant = variant;
   if (gemm_epi_launch(L, st) != cudaSuccess) {
     cudaGetLastError();
     return CF_ERR_CUDA;

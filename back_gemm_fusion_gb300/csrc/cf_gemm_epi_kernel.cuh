@@ -152,12 +152,27 @@ __device__ __forceinline__ void norm_affine(float (&v)[32], const float* gamma, 
 // Elementwise ops [o0, o1) of the program on 32 consecutive columns n.. of
 // row m of the tile; bias_s: the chunk's slice of the staged bias.  GUARD:
 // the chunk crosses column N (see ld4; the staged slices hold zeros there).
-template <bool GUARD>
+// COLS: the tile is a tile of P^T (column reductions): row m is column m of
+// the output, the 32 columns are output rows n.., the bias is the row's own
+// scalar bias_r and the residual is read transposed (R[n + j][m]; the lanes
+// of a warp hold consecutive m, so each read is coalesced across the warp).
+template <bool GUARD, bool COLS>
 __device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)[32], int n, int m, int o0, int o1,
-                                              const float* bias_s) {
+                                              const float* bias_s, float bias_r) {
   for (int o = o0; o < o1; ++o) {
     const int kind = p.op_kind[o];
-    if (kind == OP_ADD_RESIDUAL) {
+    if (COLS && kind == OP_ADD_RESIDUAL) {
+      if (m < p.M) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (!GUARD || n + j < p.N) {
+            const long long idx = (long long)(n + j) * p.res_ld + m;
+            v[j] += p.res_bf16 ? __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(p.res) + idx) << 16)
+                               : __ldg(static_cast<const float*>(p.res) + idx);
+          }
+        }
+      }
+    } else if (kind == OP_ADD_RESIDUAL) {
       // Each thread owns one row: 128 (fp32) or 64 (bf16) contiguous bytes of
       // the residual row, read with 16-byte loads.  Rows past M (a ragged
       // last strip) are never stored, so they skip the read.
@@ -204,7 +219,12 @@ __device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)
         }
       }
     } else if (kind == OP_BIAS) {
-      add_vec(v, bias_s);
+      if (COLS) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += bias_r;
+      } else {
+        add_vec(v, bias_s);
+      }
     } else if (kind == OP_SCALE) {
       const float s = p.op_scalar[o];
 #pragma unroll
@@ -347,7 +367,13 @@ __device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& 
 //
 // RAG: N is not a multiple of kBN, so the last tile of each row is ragged.
 // The full-tile instantiations compile every ragged-column guard away.
-template <int ROWOP, int XMODE, bool CTA2, bool RAG, int ROWOP0 = ROW_NONE>
+//
+// COLS: column reductions (over the first dimension of the user's P).  The
+// host swaps the operands, so the kernel computes tiles of P^T = B^T A^T and
+// runs the same row machinery over them (the complementary strip: all tiles
+// of one column block of P share a row strip of P^T); the vectors become
+// per-row scalars and the output tiles are stored transposed.
+template <int ROWOP, int XMODE, bool CTA2, bool RAG, bool COLS, int ROWOP0 = ROW_NONE>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ GemmEpiParams p) {
   using G = Geo<CTA2>;
   constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kOffOut = G::kOffOut,
@@ -524,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     uint8_t* out_ptr = smem + kOffOut + (warp - 2) * kOutStageBytes;
     float2* slots = reinterpret_cast<float2*>(smem + kOffSlots);
     float* vsm = reinterpret_cast<float*>(smem + G::kOffVec);  // [kNumVec][kBN] this tile's vector slices
-    const bool stage_vec = p.bias || p.gamma || p.beta || p.gamma0 || p.beta0;
+    const bool stage_vec = !COLS && (p.bias || p.gamma || p.beta || p.gamma0 || p.beta0);
     int t = 0;
     for (Work w = make_work<XMODE>(p); w.valid(); w.next(), ++t) {
       int strip, tile;
@@ -550,6 +576,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(bar(BAR_VFULL));
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VFULL), t & 1, wc))) break;
       }
+      // COLS: this thread's row is one column of the output; its vector
+      // entries are scalars (rows past M keep the neutral values).
+      float r_bias = 0.0f, r_gamma = 1.0f, r_beta = 0.0f, r_gamma0 = 1.0f, r_beta0 = 0.0f;
+      if (COLS && m0 + row < p.M) {
+        const int i = m0 + row;
+        if (p.bias) r_bias = __ldg(p.bias + i);
+        if (p.gamma) r_gamma = __ldg(p.gamma + i);
+        if (p.beta) r_beta = __ldg(p.beta + i);
+        if (p.gamma0) r_gamma0 = __ldg(p.gamma0 + i);
+        if (p.beta0) r_beta0 = __ldg(p.beta0 + i);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_TFULL + acc), (t >> 1) & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kBN);
@@ -571,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           const bool tail = RAG && n + 32 > p.N;
           if (p.n_ops0 > 0) {
             const float* bs = vsm + VEC_BIAS * kBN + c * 32;
-            if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops0, bs);
-            else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops0, bs);
+            if (tail) apply_program<true, COLS>(p, v, n, m0 + row, 0, p.n_ops0, bs, r_bias);
+            else apply_program<false, COLS>(p, v, n, m0 + row, 0, p.n_ops0, bs, r_bias);
             tmem_st32(taddr + c * 32, v);
           }
           if (tail) mask_tail(v, p.N - n, 0.0f);
@@ -626,14 +663,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           if constexpr (ROWOP0 != ROW_NONE) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
-            if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
-            if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
+            if (COLS) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = v[j] * r_gamma0 + (ROWOP0 == ROW_LAYERNORM ? r_beta0 : 0.0f);
+            } else {
+              if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
+              if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
+            }
           }
           if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
             const int o0 = ROWOP0 != ROW_NONE ? p.n_ops0 : 0;
             const float* bs = vsm + VEC_BIAS * kBN + c * 32;
-            if (tail) apply_program<true>(p, v, n, m0 + row, o0, p.n_ops, bs);
-            else apply_program<false>(p, v, n, m0 + row, o0, p.n_ops, bs);
+            if (tail) apply_program<true, COLS>(p, v, n, m0 + row, o0, p.n_ops, bs, r_bias);
+            else apply_program<false, COLS>(p, v, n, m0 + row, o0, p.n_ops, bs, r_bias);
             tmem_st32(taddr + c * 32, v);
           }
           if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
@@ -743,19 +785,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         const bool tail = RAG && n + 32 > p.N;
         if (ROWOP == ROW_NONE) {
           const float* bs = vsm + VEC_BIAS * kBN + c * 32;
-          if (tail) apply_program<true>(p, v, n, m0 + row, 0, p.n_ops, bs);
-          else apply_program<false>(p, v, n, m0 + row, 0, p.n_ops, bs);
+          if (tail) apply_program<true, COLS>(p, v, n, m0 + row, 0, p.n_ops, bs, r_bias);
+          else apply_program<false, COLS>(p, v, n, m0 + row, 0, p.n_ops, bs, r_bias);
         } else if (ROWOP == ROW_SOFTMAX) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;
         } else {
-          norm_affine<ROWOP == ROW_LAYERNORM>(v, vsm + VEC_GAMMA * kBN + c * 32, vsm + VEC_BETA * kBN + c * 32,
-                                              scale_a, shift_a);
+          if (COLS) {
+            const float b = ROWOP == ROW_LAYERNORM ? r_beta : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], scale_a, shift_a) * r_gamma + b;
+          } else {
+            norm_affine<ROWOP == ROW_LAYERNORM>(v, vsm + VEC_GAMMA * kBN + c * 32, vsm + VEC_BETA * kBN + c * 32,
+                                                scale_a, shift_a);
+          }
         }
         // The previous TMA store from this buffer must have read it.
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
-        if (p.out_bf16) {
+        if (COLS) {
+          // Transposed block: staging row j holds output row n + j, whose 32
+          // columns are this warp's 32 tile rows (one per lane), unswizzled;
+          // the lanes write consecutive elements of a row.
+          if (p.out_bf16) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              reinterpret_cast<__nv_bfloat16*>(out_ptr)[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) reinterpret_cast<float*>(out_ptr)[j * 32 + lane] = v[j];
+          }
+        } else if (p.out_bf16) {
           // bf16: 64-byte rows, unswizzled; lane l writes its 16-byte chunks
           // starting at chunk l & 3 to spread them over the banks.
           uint32_t w[16];
@@ -787,7 +847,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d_hint(&p.tmOut, out_buf, n, m0 + 32 * q, out_policy);
+          if (COLS) tma_store_2d_hint(&p.tmOut, out_buf, m0 + 32 * q, n, out_policy);
+          else tma_store_2d_hint(&p.tmOut, out_buf, n, m0 + 32 * q, out_policy);
           bulk_commit();
         }
       }
@@ -819,20 +880,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   }
 }
 
-template <int R, int X, bool P, bool RAG, int R0 = ROW_NONE>
+template <int R, int X, bool P, bool RAG, bool COLS, int R0 = ROW_NONE>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P, RAG, R0>);
+  return reinterpret_cast<const void*>(&gemm_epi_kernel<R, X, P, RAG, COLS, R0>);
 }
 
-// The instantiations one translation unit holds: full tiles (RAG = false)
-// in cf_gemm_epi.cu, ragged last tiles in cf_gemm_epi_ragged.cu, compiled in
-// parallel.
-template <bool RAG>
+// The instantiations one translation unit holds, one (RAG, COLS) variant per
+// unit: cf_gemm_epi.cu (full tiles), cf_gemm_epi_ragged.cu (ragged last
+// tile), cf_gemm_epi_cols.cu and cf_gemm_epi_cols_ragged.cu (column
+// reductions), compiled in parallel.  Column variants exist for programs with
+// a reduction only (without one the two axes are the same program).
+template <bool RAG, bool COLS>
 const void* select_kernel_t(int rowop, int xmode, bool pair) {
 #define CF_CASE(R, X, P) \
-  if (rowop == R && xmode == X && pair == P) return kernel_ptr<R, X, P, RAG>();
-  CF_CASE(ROW_NONE, X_NONE, false)
-  CF_CASE(ROW_NONE, X_NONE, true)
+  if (rowop == R && xmode == X && pair == P) return kernel_ptr<R, X, P, RAG, COLS>();
+  if constexpr (!COLS) {
+    CF_CASE(ROW_NONE, X_NONE, false)
+    CF_CASE(ROW_NONE, X_NONE, true)
+  }
   CF_CASE(ROW_LAYERNORM, X_NONE, false)
   CF_CASE(ROW_LAYERNORM, X_NONE, true)
   CF_CASE(ROW_LAYERNORM, X_CLUSTER, false)
@@ -850,12 +915,14 @@ const void* select_kernel_t(int rowop, int xmode, bool pair) {
   CF_CASE(ROW_SOFTMAX, X_GLOBAL, true)
 #undef CF_CASE
   // Two chained reductions (per-tile or workspace exchange only).
-#define CF_CASE2(R0, R)                                                                            \
-  if (rowop == row_code(R0, R)) {                                                                  \
-    if (xmode == X_NONE) return pair ? kernel_ptr<R, X_NONE, true, RAG, R0>() : kernel_ptr<R, X_NONE, false, RAG, R0>(); \
-    if (xmode == X_GLOBAL)                                                                         \
-      return pair ? kernel_ptr<R, X_GLOBAL, true, RAG, R0>() : kernel_ptr<R, X_GLOBAL, false, RAG, R0>();              \
-    return nullptr;                                                                                \
+#define CF_CASE2(R0, R)                                                                                   \
+  if (rowop == row_code(R0, R)) {                                                                         \
+    if (xmode == X_NONE)                                                                                  \
+      return pair ? kernel_ptr<R, X_NONE, true, RAG, COLS, R0>() : kernel_ptr<R, X_NONE, false, RAG, COLS, R0>(); \
+    if (xmode == X_GLOBAL)                                                                                \
+      return pair ? kernel_ptr<R, X_GLOBAL, true, RAG, COLS, R0>()                                        \
+                  : kernel_ptr<R, X_GLOBAL, false, RAG, COLS, R0>();                                      \
+    return nullptr;                                                                                       \
   }
   CF_CASE2(ROW_LAYERNORM, ROW_LAYERNORM)
   CF_CASE2(ROW_LAYERNORM, ROW_RMSNORM)

@@ -5,6 +5,8 @@
 
 namespace cf {
 
-const void* gemm_epi_select_ragged(int rowop, int xmode, bool pair) { return select_kernel_t<true>(rowop, xmode, pair); }
+const void* gemm_epi_select_variant1(int rowop, int xmode, bool pair) {
+  return select_kernel_t<true, false>(rowop, xmode, pair);
+}
 
 }  // namespace cf

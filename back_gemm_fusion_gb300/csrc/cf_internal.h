@@ -67,6 +67,7 @@ struct GemmEpiLaunch {
   int xmode;
   int grid;          // CTAs
   int cluster;       // CTAs per cluster (X_CLUSTER: tiles_n; pair mode: 2), else 1
+  int variant;       // kernel variant: ragged last tile (+1), column reductions (+2)
 };
 
 // Host helpers implemented in cf_api.cu and shared by the kernel launchers.
@@ -79,10 +80,12 @@ cf_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, void* 
 long long wait_timeout_cycles();
 
 size_t gemm_epi_smem_bytes();
-// rag: N % kBN != 0 (the kernels whose last tile per row is ragged).
-cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair, bool rag);  // set function attributes
+// variant: 1 if the kernel's N % kBN != 0 (its last tile per row is ragged),
+// + 2 for column reductions (the kernel runs on P^T).
+constexpr int kNumVariants = 4;
+cudaError_t gemm_epi_prepare(int rowop, int xmode, bool pair, int variant);  // set function attributes
 cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s);
-cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, bool rag, int cluster, int* out);
-cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, bool rag, int* out);
+cudaError_t gemm_epi_max_clusters(int rowop, int xmode, bool pair, int variant, int cluster, int* out);
+cudaError_t gemm_epi_max_blocks_per_sm(int rowop, int xmode, int variant, int* out);
 
 }  // namespace cf

@@ -455,7 +455,13 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   if (!A || !B || !epi || !out || !intermediate || !A->ptr || !B->ptr || !out->ptr) return CF_ERR_INVALID_ARG;
   if (A->dtype != CF_BF16 || B->dtype != CF_BF16 || out->dtype != CF_FP32 || A->trans || out->trans)
     return CF_ERR_INVALID_ARG;
-  if ((epi->version != 1 && epi->version != 2) || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if (epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  // Column reductions have no unfused counterpart here.
+  if (epi->version >= 3 && epi->axis != CF_AXIS_ROWS) {
+    for (uint32_t i = 0; i < epi->n_ops; ++i)
+      if (epi->ops[i].kind >= CF_OP_ROW_LAYERNORM && epi->ops[i].kind <= CF_OP_ROW_SOFTMAX)
+        return CF_ERR_UNSUPPORTED_SHAPE;
+  }
   const int64_t M = A->rows, K = A->cols, N = B->cols;
   if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return CF_OK;

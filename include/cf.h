@@ -100,7 +100,13 @@ typedef struct {
   float scalar;  /* the scale for CF_OP_SCALE, eps for the norms, unused otherwise */
 } cf_op;
 
-#define CF_EPI_VERSION 2  /* version 1 (no residual field) is still accepted */
+#define CF_EPI_VERSION 3  /* versions 1 (no residual) and 2 (no axis) are still accepted */
+
+/* Axis of an epilogue program's reductions (descriptor version 3). */
+typedef enum {
+  CF_AXIS_ROWS = 0, /* along each row of P = A.B (over n) */
+  CF_AXIS_COLS = 1  /* down each column of P (over m): the complementary strip */
+} cf_axis;
 #define CF_EPI_MAX_OPS 8
 
 /* Row-statistics exchange used when a row spans several CTAs. */
@@ -129,6 +135,14 @@ typedef struct {
    * row reductions; NULL means gamma = 1 / beta = 0 (no affine transform). */
   const float* stage0_gamma;
   const float* stage0_beta;
+  /* Version 3: cf_axis of the program's reductions.  CF_AXIS_COLS reduces
+   * down each column of P (LayerNorm / RMSNorm / softmax over m, e.g. a
+   * batch normalisation); every vector (bias, gamma, beta, stage0_*) stays
+   * indexed by the column n, so for columns gamma/beta are constant along
+   * the reduction.  CF_AXIS_COLS needs B given as its N x K transpose
+   * (trans == 1); the cluster exchange then takes M <= 4096.  Programs
+   * without a reduction ignore the axis. */
+  int32_t axis;
 } cf_epi_desc;
 
 /*

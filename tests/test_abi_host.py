@@ -249,3 +249,44 @@ def test_b2b_shape_rules(lib):
     assert call(256, 256, 200, 300, op="relu", trans=False) in ok       # MLP, ragged N1 and N2
     assert call(256, 256, 512, 1000, op="relu", trans=False) in ok      # MLP, C = 4, last block ragged
     assert call(256, 256, 512, 1100, op="relu", trans=False) == 2       # MLP, C = 5 > 4
+
+
+def test_column_axis_rules(lib):
+    # Column reductions: descriptor version 3, B given as N x K, the kernel
+    # runs on P^T (so the workspace follows the swapped shape).
+    from back_gemm_fusion_gb300.binding import cf_matrix, epi_desc, CF_BF16, CF_FP32
+    M, N, K = 4096, 512, 256
+    A = cf_matrix(0x10000, CF_BF16, 0, M, K, K)
+    Bt = cf_matrix(0x20000, CF_BF16, 1, K, N, K)     # stored N x K
+    Bn = cf_matrix(0x20000, CF_BF16, 0, K, N, N)     # stored K x N
+    O = cf_matrix(0x30000, CF_FP32, 0, M, N, N)
+
+    def call(B, ops, axis="col", exchange="auto", ws=0x80000, ws_bytes=1 << 24):
+        d = epi_desc(ops, exchange, axis=axis)
+        return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                    ctypes.byref(O), ws, ws_bytes, None)
+
+    assert call(Bt, LN) in (0, 4, 8)                          # B as N x K: supported
+    assert call(Bn, LN) == 2                                  # B as K x N: the kernel needs it K-major
+    assert call(Bn, [("bias",), ("relu",)]) in (0, 4, 8)      # no reduction: the axis is ignored
+    assert call(Bt, LN, exchange="cluster") in (0, 4, 8)      # the reduced dim M = 4096: 16 tiles fit a cluster
+    A17 = cf_matrix(0x10000, CF_BF16, 0, 4352, K, K)
+    O17 = cf_matrix(0x30000, CF_FP32, 0, 4352, N, N)
+    d17 = epi_desc(LN, "cluster", axis="col")
+    assert lib.cf_gemm_epilogue(ctypes.byref(A17), ctypes.byref(Bt), 0x40000, 0x50000, 0x60000, ctypes.byref(d17),
+                                ctypes.byref(O17), 0x80000, 1 << 24, None) == 2  # 17 tiles down a column
+    d = epi_desc(LN, axis="col")
+    d.axis = 2
+    assert lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(Bt), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                ctypes.byref(O), 0x80000, 1 << 24, None) == 1  # unknown axis
+    # Workspace: strips of P^T (N / 128 = 4) x tiles along M (4096 / 256 = 16).
+    ws_col = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(Bt), ctypes.byref(epi_desc(LN, axis="col")))
+    ws_row = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(Bt), ctypes.byref(epi_desc(LN, axis="row")))
+    # Statistics (strips x tiles x 128 rows x 8 bytes) then 16 bytes of
+    # counters per strip, each region padded to 256 bytes.
+    assert ws_col == 4 * 16 * 128 * 8 + 256      # 4 strips of P^T, 16 tiles along M
+    assert ws_row == 32 * 2 * 128 * 8 + 512      # 32 strips of P, 2 tiles along N
+    # The unfused comparison path has no column reductions.
+    dd = epi_desc(LN, axis="col")
+    assert lib.cf_unfused_gemm_epilogue(ctypes.byref(A), ctypes.byref(Bt), 0x40000, 0x50000, 0x60000,
+                                        ctypes.byref(dd), ctypes.byref(O), 0x90000, None) == 2

@@ -363,3 +363,80 @@ def test_ragged_n_bf16_output(cf):
     assert cf.cf_last_device_status() == 0
     assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16))
     bf16_out_gate(g.float().cpu().numpy(), _oracle(case), strict, "ragged N=1000 bf16 out")
+
+
+COL_PROGRAMS = {
+    "layernorm": [("bias",), ("layernorm", 1e-5)],
+    "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+    "softmax": [("scale", 0.5), ("softmax",)],
+}
+
+
+def _run_col(cf, case, exchange="auto", out_dtype=torch.float32, residual=None, stage0=None):
+    Bt = case.B.t().contiguous().cuda()  # stored N x K
+    kw = {}
+    if stage0 is not None:
+        kw = {"stage0_gamma": stage0[0].cuda(), "stage0_beta": stage0[1].cuda()}
+    out = cf.cf_gemm_epilogue(case.A.cuda(), Bt, case.ops, _dev(case.bias), _dev(case.gamma), _dev(case.beta),
+                              b_trans=True, exchange=exchange, out_dtype=out_dtype, axis="col",
+                              residual=None if residual is None else residual.cuda(), **kw)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    return out
+
+
+def _col_gate(gpu, ref, strict, what):
+    # The per-row gate applied to the columns (the reduction's own axis).
+    assert_rows_close(np.ascontiguousarray(gpu.T), np.ascontiguousarray(ref.T), strict=strict, what=what)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 384, 128), (1000, 520, 72), (4104, 256, 64),
+                                   (77, 136, 64)])
+@pytest.mark.parametrize("prog", sorted(COL_PROGRAMS))
+def test_column_reductions(cf, prog, M, N, K):
+    # Reductions down the columns of P (over m): the kernel runs on P^T with
+    # the strip machinery (cluster or workspace exchange across the M tiles),
+    # per-column vectors as per-row scalars, and transposed output tiles.
+    # Shapes: one tile; 2 tiles down a column with an odd strip count; ragged
+    # in both dims; 17 tiles (workspace exchange); a single partial tile.
+    case = I.gemm_epilogue_case("col", M, N, K, COL_PROGRAMS[prog], seed=M + N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    got = _run_col(cf, case).cpu().numpy()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), axis="col")
+    _col_gate(got, ref, 2e-3, f"columns {prog} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("exchange", ["cluster", "global"])
+def test_column_reductions_exchanges(cf, exchange):
+    case = I.gemm_epilogue_case("col_x", 768, 256, 64, COL_PROGRAMS["layernorm"], seed=3, need_bias=True,
+                                need_gamma=True, need_beta=True)
+    got = _run_col(cf, case, exchange=exchange).cpu().numpy()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), axis="col")
+    _col_gate(got, ref, 2e-3, f"columns layernorm {exchange}")
+
+
+@pytest.mark.parametrize("res_dtype", [torch.float32, torch.bfloat16])
+def test_column_residual_and_bf16_output(cf, res_dtype):
+    ops = [("bias",), ("residual",), ("rmsnorm", 1e-6)]
+    case = I.gemm_epilogue_case("col_res", 600, 264, 128, ops, seed=9, need_bias=True, need_gamma=True)
+    R = torch.from_numpy(np.random.default_rng(10).standard_normal((600, 264)).astype(np.float32)).to(res_dtype)
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          None, residual=I.to_f64(R), axis="col")
+    f = _run_col(cf, case, residual=R)
+    g = _run_col(cf, case, residual=R, out_dtype=torch.bfloat16)
+    _col_gate(f.cpu().numpy(), ref, 2e-3, f"columns residual {res_dtype}")
+    assert torch.equal(g.cpu(), f.cpu().to(torch.bfloat16))
+
+
+def test_column_chained(cf):
+    ops = [("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)]
+    case = I.gemm_epilogue_case("col_chain", 520, 256, 64, ops, seed=13, need_bias=True, need_gamma=True)
+    rng = np.random.default_rng(14)
+    g0 = torch.from_numpy((1 + 0.3 * rng.standard_normal(256)).astype(np.float32))
+    b0 = torch.from_numpy((0.3 * rng.standard_normal(256)).astype(np.float32))
+    got = _run_col(cf, case, stage0=(g0, b0)).cpu().numpy()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          None, stage0_gamma=I.to_f64(g0), stage0_beta=I.to_f64(b0), axis="col")
+    _col_gate(got, ref, 2e-3, "columns chained")
