@@ -80,6 +80,16 @@ def postnorm_layernorm(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 409
     return c
 
 
+def column_layernorm(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 4096) -> GemmEpilogueCase:
+    """Column reductions: GEMM + bias + LayerNorm down each column (over the
+    M = 8192 rows, a batch normalisation of every output feature, eps 1e-5),
+    fp32 out; same draws as the GELU + RMSNorm workload's shapes."""
+    c = gemm_epilogue_case("gemm_bias_column_layernorm", M, N, K, [("bias",), ("layernorm", 1e-5)], seed,
+                           need_bias=True, need_gamma=True, need_beta=True)
+    c.meta["axis"] = "col"
+    return c
+
+
 def chained_ln_gelu_rms(seed: int = 0, M: int = 8192, N: int = 4096, K: int = 4096) -> GemmEpilogueCase:
     """Two reduction stages in one epilogue: GEMM + bias + LayerNorm (its own
     gamma0/beta0) + tanh-GELU + RMSNorm (gamma), fp32 out; the first stage's

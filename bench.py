@@ -89,6 +89,8 @@ class Workload:
             self.case = I.postnorm_layernorm(seed)
         elif name == "chained_ln_gelu_rms":
             self.case = I.chained_ln_gelu_rms(seed)
+        elif name == "column_layernorm":
+            self.case = I.column_layernorm(seed)
         elif name == "mlp_b2b":
             self.case = I.mlp_b2b(seed)
         elif name == "mlp_bottom":
@@ -100,8 +102,11 @@ class Workload:
             self.case = I.attention_b2b(seed, op=op)
         else:
             raise ValueError(name)
+        self.axis = "row"
         self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu", "target_attention")
         c = self.case
+        if not self.is_b2b:
+            self.axis = c.meta.get("axis", "row")
         if self.is_b2b:
             self.flops = 2.0 * c.batch * c.M * (c.K * c.N1 + c.N1 * c.N2)
             self.out_bytes = ob * c.batch * c.M * c.N2
@@ -117,8 +122,10 @@ class Workload:
             # Row statistics of rows wider than one 256-column tile: 8 bytes
             # per row per tile in the workspace (written once, read per tile).
             n_row = sum(o[0] in ("layernorm", "rmsnorm", "softmax") for o in c.ops)
-            self.stat_bytes = 8.0 * n_row * c.M * (c.N // 256) if c.N > 256 else 0.0
-            self.rows = c.M
+            # Column reductions: per column per 256-row tile.
+            lines, length = (c.N, c.M) if self.axis == "col" else (c.M, c.N)
+            self.stat_bytes = 8.0 * n_row * lines * (length // 256) if length > 256 else 0.0
+            self.rows = c.N if self.axis == "col" else c.M  # oracle sample units
 
     def config(self):
         c = self.case
@@ -127,7 +134,7 @@ class Workload:
             return {"workload": self.name, "batch": c.batch, "M": c.M, "K": c.K, "N1": c.N1, "N2": c.N2,
                     "mid_op": c.op, "intermediate": "bf16, on chip", "out": out}
         return {"workload": self.name, "M": c.M, "N": c.N, "K": c.K, "ops": [list(o) for o in c.ops],
-                "row_stat_exchange": self.exchange, "out": out}
+                "axis": self.axis, "row_stat_exchange": self.exchange, "out": out}
 
     # -- GPU side
     def to_device(self):
@@ -137,7 +144,9 @@ class Workload:
             dev["A"], dev["W1"], dev["W2"] = c.A.cuda(), c.W1.cuda(), c.W2.cuda()
             dev["out"] = torch.empty((c.batch, c.M, c.N2), dtype=self.out_dtype, device="cuda")
         else:
-            dev["A"], dev["B"] = c.A.cuda(), c.B.cuda()
+            dev["A"] = c.A.cuda()
+            # Column reductions take B as its N x K transpose.
+            dev["B"] = c.B.t().contiguous().cuda() if self.axis == "col" else c.B.cuda()
             for k in ("bias", "gamma", "beta", "residual", "stage0_gamma", "stage0_beta"):
                 t = getattr(c, k)
                 dev[k] = None if t is None else t.cuda()
@@ -156,10 +165,12 @@ class Workload:
             cf.cf_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
                                 out=dev["out"], workspace=workspace, stream=stream, exchange=self.exchange,
                                 residual=dev["residual"], stage0_gamma=dev["stage0_gamma"],
-                                stage0_beta=dev["stage0_beta"])
+                                stage0_beta=dev["stage0_beta"], b_trans=self.axis == "col", axis=self.axis)
 
     def unfused_step(self, cf, dev, scratch, stream=None):
         c = self.case
+        if self.axis == "col":
+            raise NotImplementedError("the unfused comparison path has no column reductions")
         if self.is_b2b:
             A = dev["A"] if c.batch > 1 else dev["A"][0]
             W1 = dev["W1"] if c.batch > 1 else dev["W1"][0]
@@ -204,6 +215,16 @@ class Workload:
                 W1 = W1.T if c.w1_k_major else W1
                 O.b2bgemm(A, W1, I.to_f64(c.W2[b]), c.op, c.scale)
             return 2.0 * len(rows) * (c.K * c.N1 + c.N1 * c.N2)
+        if self.axis == "col":
+            # Column reductions: the sampled units are output columns (each
+            # needs all M rows).
+            def cols(key):
+                v = self._f64(key)
+                return None if v is None else v[..., rows]
+            R = None if c.residual is None else self._f64("residual")[:, rows]
+            O.gemm_epilogue(self._f64("A"), self._f64("B")[:, rows], c.ops, cols("bias"), cols("gamma"), cols("beta"),
+                            residual=R, stage0_gamma=cols("stage0_gamma"), stage0_beta=cols("stage0_beta"), axis="col")
+            return 2.0 * len(rows) * c.M * c.K
         A = self._f64("A")[rows]
         R = None if c.residual is None else self._f64("residual")[rows]
         O.gemm_epilogue(A, self._f64("B"), c.ops, self._f64("bias"), self._f64("gamma"), self._f64("beta"),
@@ -388,7 +409,8 @@ def run_reference(args, wl: Workload, dist, rank, world):
         vals.append(v)
         secs += dt
     value = statistics.mean(vals)
-    sample = f"{rows_used} of {wl.rows} output rows (seeded), float64 numpy oracle, extrapolated per row"
+    unit = "columns" if getattr(wl, "axis", "row") == "col" else "rows"
+    sample = f"{rows_used} of {wl.rows} output {unit} (seeded), float64 numpy oracle, extrapolated per {unit[:-1]}"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -409,7 +431,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     workspace = None
     if not wl.is_b2b:
         c = wl.case
-        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops, exchange=args.exchange)
+        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops, exchange=args.exchange, b_trans=wl.axis == "col",
+                                    axis=wl.axis)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
     flush = torch.empty(256 * 2 ** 20 // 4, dtype=torch.float32, device="cuda")
@@ -444,7 +467,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
                 wv.exchange = xch
                 ws = workspace
                 if ws is None:
-                    need = cf.cf_workspace_size(dev["A"], dev["B"], wl.case.ops, exchange=xch)
+                    need = cf.cf_workspace_size(dev["A"], dev["B"], wl.case.ops, exchange=xch,
+                                                b_trans=wl.axis == "col", axis=wl.axis)
                     ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
                 for _ in range(2):
                     wv.fused_step(cf, dev, stream, ws)
@@ -540,6 +564,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     for k in names:
         t = getattr(c, k)
         if t is not None:
+            if k == "B" and wl.axis == "col":
+                t = t.t().contiguous()  # the device copy is B's N x K transpose
             host_in.append((k, t.pin_memory()))
     host_out = torch.empty(dev["out"].shape, dtype=dev["out"].dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for _, t in host_in)
@@ -585,7 +611,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         "dram_bytes": ({"read": tr["read"], "write": tr["write"], "source": "ncu, one launch"} if tr else None),
         "compulsory_bytes": wl.bytes,
         "cpu_baseline": {"value": ref_tflops, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{ref_rows} of {wl.rows} output rows (seeded), {ref_s:.1f} s"},
+                         "sample": f"{ref_rows} of {wl.rows} output {'columns' if wl.axis == 'col' else 'rows'} "
+                                   f"(seeded), {ref_s:.1f} s"},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step},
         "unfused": unfused,
@@ -607,7 +634,7 @@ def main():
     ap.add_argument("--workload", default="gelu_rmsnorm",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
                              "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms",
-                             "target_attention"])
+                             "target_attention", "column_layernorm"])
     ap.add_argument("--rows", type=int, default=64,
                     help="batch of the mlp_bottom (rows) and target_attention (users) workloads (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],

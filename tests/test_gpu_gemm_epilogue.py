@@ -440,3 +440,16 @@ def test_column_chained(cf):
     ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
                           None, stage0_gamma=I.to_f64(g0), stage0_beta=I.to_f64(b0), axis="col")
     _col_gate(got, ref, 2e-3, "columns chained")
+
+
+def test_column_layernorm_full_size_sampled(cf):
+    # The column-reduction bench workload at full size (M = 8192 rows reduced
+    # per column, 32 tiles down each column: workspace exchange); 64 sampled
+    # columns against the oracle, each over all rows.
+    case = I.column_layernorm()
+    got = _run_col(cf, case).cpu().numpy()
+    cols = sample_rows(case.N, 64, seed=5)
+    B = I.to_f64(case.B)[:, cols]
+    ref = O.gemm_epilogue(I.to_f64(case.A), B, case.ops, I.to_f64(case.bias)[cols], I.to_f64(case.gamma)[cols],
+                          I.to_f64(case.beta)[cols], axis="col")
+    _col_gate(got[:, cols], ref, 2e-3, "column layernorm 8192x4096x4096")
