@@ -126,6 +126,13 @@ __device__ __forceinline__ float res_at(const void* res, long long ld, int bf16,
               : static_cast<const float*>(res)[(long long)m * ld + n];
 }
 
+// tanh-GELU as 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)), u = sqrt(2/pi) (x +
+// 0.044715 x^3), with the fast exponential (the fused kernel's arithmetic).
+__device__ __forceinline__ float gelu_fast(float x) {
+  const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+  return __fdividef(x, 1.0f + __expf(-2.0f * u));
+}
+
 // Elementwise program for element (m, n); `r` is residual[m][n].
 __device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* bias, int n, float r) {
   for (int o = 0; o < pg.n_ops; ++o) {
@@ -134,7 +141,7 @@ __device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* 
       case CF_OP_ADD_RESIDUAL: x += r; break;
       case CF_OP_SCALE: x *= pg.scalar[o]; break;
       case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
-      case CF_OP_GELU_TANH: x = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x))); break;
+      case CF_OP_GELU_TANH: x = gelu_fast(x); break;
     }
   }
   return x;
@@ -149,7 +156,7 @@ __device__ __forceinline__ float ew_range(const RowProgram& pg, float x, const f
       case CF_OP_ADD_RESIDUAL: x += r; break;
       case CF_OP_SCALE: x *= pg.scalar[o]; break;
       case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
-      case CF_OP_GELU_TANH: x = 0.5f * x * (1.0f + tanhf(0.7978845608028654f * (x + 0.044715f * x * x * x))); break;
+      case CF_OP_GELU_TANH: x = gelu_fast(x); break;
     }
   }
   return x;
@@ -313,14 +320,39 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
   float4* o = reinterpret_cast<float4*>(out + (int64_t)blockIdx.x * ldo);
   float4 v[VPT];
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int c = i * 256 + threadIdx.x;  // float4 index
-    float4 x = p[c];
-    x.x = ew(pg, x.x, bias, 4 * c, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c));
-    x.y = ew(pg, x.y, bias, 4 * c + 1, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 1));
-    x.z = ew(pg, x.z, bias, 4 * c + 2, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 2));
-    x.w = ew(pg, x.w, bias, 4 * c + 3, res_at(res, res_ld, res_bf16, (int)blockIdx.x, 4 * c + 3));
-    v[i] = x;
+  for (int i = 0; i < VPT; ++i) v[i] = p[i * 256 + threadIdx.x];
+  // The program op by op over the thread's vectors (one dispatch per op,
+  // 16-byte loads of the bias and the residual).
+  for (int op = 0; op < pg.n_ops; ++op) {
+    const int kind = pg.kind[op];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = i * 256 + threadIdx.x;  // float4 index
+      float4 x = v[i];
+      if (kind == CF_OP_BIAS) {
+        const float4 b = reinterpret_cast<const float4*>(bias)[c];
+        x = make_float4(x.x + b.x, x.y + b.y, x.z + b.z, x.w + b.w);
+      } else if (kind == CF_OP_ADD_RESIDUAL) {
+        float4 r;
+        if (res_bf16) {
+          const uint2 w = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(res) +
+                                                         (long long)blockIdx.x * res_ld)[c];
+          r = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                          __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        } else {
+          r = reinterpret_cast<const float4*>(static_cast<const float*>(res) + (long long)blockIdx.x * res_ld)[c];
+        }
+        x = make_float4(x.x + r.x, x.y + r.y, x.z + r.z, x.w + r.w);
+      } else if (kind == CF_OP_SCALE) {
+        const float sc = pg.scalar[op];
+        x = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
+      } else if (kind == CF_OP_RELU) {
+        x = make_float4(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f), fmaxf(x.z, 0.0f), fmaxf(x.w, 0.0f));
+      } else if (kind == CF_OP_GELU_TANH) {
+        x = make_float4(gelu_fast(x.x), gelu_fast(x.y), gelu_fast(x.z), gelu_fast(x.w));
+      }
+      v[i] = x;
+    }
   }
   float mul = 1.0f, add = 0.0f;  // y = (x * mul + add) [* gamma + beta]
   if (pg.rowop == CF_OP_ROW_LAYERNORM) {

@@ -279,6 +279,48 @@ CF_API cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1, con
                              const cf_b2b_desc* desc, cf_matrix* out,
                              float* s_buf, void* p_buf, void* stream);
 
+/*
+ * Cost model (host only, no device access): predicts whether fusing pays.
+ *
+ * The ComFuse review's suggested extension ("If this is right", third
+ * bullet): compare the predicted GEMM time with the predicted epilogue time
+ * and fuse only when the GEMM is heavy enough to hide the epilogue.  The
+ * fused kernel's main loop and epilogue overlap tile by tile (two TMEM
+ * accumulators), so a fused tile costs max(main loop, epilogue + exchange);
+ * the unfused path pays the GEMM, then a second kernel that reads the
+ * intermediate back from HBM.  Efficiencies are calibrated on a GB300 (the
+ * fused kernels' measured fractions of the tensor peak, cuBLASLt's, and the
+ * copy bandwidth); the numbers are estimates, not guarantees.
+ */
+typedef struct {
+  double tensor_tflops; /* dense bf16 tensor peak (TFLOP/s); <= 0: 1908 (a measured GB300 burst) */
+  double hbm_gbs;       /* HBM copy bandwidth (GB/s); <= 0: 7000 */
+  int32_t sms;          /* streaming multiprocessors; <= 0: 152 */
+  double clock_ghz;     /* SM clock (GHz); <= 0: 2.07 */
+  double launch_us;     /* fixed cost of one kernel launch on the device (us); < 0: 4 */
+} cf_device_model;
+
+typedef struct {
+  double flops;            /* algorithmic flops: 2 M N K per GEMM */
+  double fused_bytes;      /* compulsory HBM bytes of the fused call */
+  double unfused_bytes;    /* HBM bytes of the unfused path (the intermediate written and read back) */
+  double mainloop_us;      /* fused: predicted main-loop time of one tile */
+  double epilogue_us;      /* fused: predicted epilogue (+ statistics exchange) time of one tile */
+  double fused_us;         /* predicted time of the fused call */
+  double unfused_us;       /* predicted time of the unfused path (< 0: it has no counterpart) */
+  int32_t fused_preferred; /* 1 when fused_us <= unfused_us (or there is no unfused path) */
+  int32_t epilogue_hidden; /* 1 when a tile's epilogue fits inside a tile's main loop */
+} cf_cost;
+
+/* Same validation as cf_gemm_epilogue / cf_b2bgemm (pointers are not
+ * dereferenced; NULL data pointers are allowed here).  `dev` may be NULL
+ * (GB300 defaults).  Returns CF_ERR_UNSUPPORTED_SHAPE where the fused call
+ * would. */
+CF_API cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const cf_epi_desc* epi,
+                                       const cf_device_model* dev, cf_cost* out);
+CF_API cf_status cf_cost_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
+                                 const cf_b2b_desc* desc, const cf_device_model* dev, cf_cost* out);
+
 /* Reads and clears the device status word written by bounded waits
  * (synchronises the stream first).  CF_OK or CF_ERR_TIMEOUT. */
 CF_API cf_status cf_last_device_status(void* stream);
