@@ -46,6 +46,18 @@ class cf_epi_desc(ctypes.Structure):
                 ("stage0_gamma", ctypes.c_void_p), ("stage0_beta", ctypes.c_void_p), ("axis", ctypes.c_int32)]
 
 
+class cf_device_model(ctypes.Structure):
+    _fields_ = [("tensor_tflops", ctypes.c_double), ("hbm_gbs", ctypes.c_double), ("sms", ctypes.c_int32),
+                ("clock_ghz", ctypes.c_double), ("launch_us", ctypes.c_double)]
+
+
+class cf_cost(ctypes.Structure):
+    _fields_ = [("flops", ctypes.c_double), ("fused_bytes", ctypes.c_double), ("unfused_bytes", ctypes.c_double),
+                ("mainloop_us", ctypes.c_double), ("epilogue_us", ctypes.c_double), ("fused_us", ctypes.c_double),
+                ("unfused_us", ctypes.c_double), ("fused_preferred", ctypes.c_int32),
+                ("epilogue_hidden", ctypes.c_int32)]
+
+
 class cf_b2b_desc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("mid_op", ctypes.c_int32), ("mid_scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int32), ("batch", ctypes.c_int64), ("strideA", ctypes.c_int64),
@@ -73,6 +85,10 @@ _SIGNATURES = {
                                                 ctypes.c_void_p]),
     "cf_unfused_b2bgemm": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), _P(cf_matrix), _P(cf_b2b_desc),
                                           _P(cf_matrix), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "cf_cost_gemm_epilogue": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), _P(cf_epi_desc), _P(cf_device_model),
+                                             _P(cf_cost)]),
+    "cf_cost_b2bgemm": (ctypes.c_int, [_P(cf_matrix), _P(cf_matrix), _P(cf_matrix), _P(cf_b2b_desc),
+                                       _P(cf_device_model), _P(cf_cost)]),
     "cf_last_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "cf_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "cf_abi_version": (ctypes.c_int, []),
@@ -296,6 +312,43 @@ def cf_unfused_b2bgemm(A, W1, W2, op, scale=1.0, w1_trans=False, out=None, s_buf
                                 ctypes.byref(o), _ptr(s_buf), _ptr(p_buf), _stream(stream))
     _check(st, "cf_unfused_b2bgemm")
     return out
+
+
+def _device_model(device: Optional[dict]) -> cf_device_model:
+    dm = cf_device_model(0.0, 0.0, 0, 0.0, -1.0)  # library defaults (a GB300)
+    for k, v in (device or {}).items():
+        setattr(dm, k, v)
+    return dm
+
+
+def _cost_dict(c: cf_cost) -> dict:
+    return {name: getattr(c, name) for name, _ in cf_cost._fields_}
+
+
+def cf_cost_gemm_epilogue(M: int, N: int, K: int, ops: Sequence[Tuple], b_trans: bool = False,
+                          axis: str = "row", device: Optional[dict] = None) -> dict:
+    """Predicted fused and unfused times of a GEMM + epilogue of this shape
+    (host only; ``device`` overrides cf_device_model fields)."""
+    lib = load_library()
+    a = cf_matrix(0, CF_BF16, 0, M, K, K)
+    b = cf_matrix(0, CF_BF16, 1, K, N, K) if b_trans else cf_matrix(0, CF_BF16, 0, K, N, N)
+    d, c, dm = epi_desc(ops, axis=axis), cf_cost(), _device_model(device)
+    _check(lib.cf_cost_gemm_epilogue(ctypes.byref(a), ctypes.byref(b), ctypes.byref(d), ctypes.byref(dm),
+                                     ctypes.byref(c)), "cf_cost_gemm_epilogue")
+    return _cost_dict(c)
+
+
+def cf_cost_b2bgemm(M: int, K: int, N1: int, N2: int, op: str, scale: float = 1.0, batch: int = 1,
+                    w1_trans: bool = False, device: Optional[dict] = None) -> dict:
+    """Predicted fused and unfused times of a B2BGEMM of this shape (host only)."""
+    lib = load_library()
+    a = cf_matrix(0, CF_BF16, 0, M, K, K)
+    w1 = cf_matrix(0, CF_BF16, 1, K, N1, K) if w1_trans else cf_matrix(0, CF_BF16, 0, K, N1, N1)
+    w2 = cf_matrix(0, CF_BF16, 0, N1, N2, N2)
+    d, c, dm = b2b_desc(op, scale, batch), cf_cost(), _device_model(device)
+    _check(lib.cf_cost_b2bgemm(ctypes.byref(a), ctypes.byref(w1), ctypes.byref(w2), ctypes.byref(d), ctypes.byref(dm),
+                               ctypes.byref(c)), "cf_cost_b2bgemm")
+    return _cost_dict(c)
 
 
 def cf_last_device_status(stream=None) -> int:

@@ -21,7 +21,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libcf_gb300.so")
 
 SOURCES = ["cf_api.cu", "cf_gemm_epi.cu", "cf_gemm_epi_ragged.cu", "cf_gemm_epi_cols.cu", "cf_gemm_epi_cols_ragged.cu",
-           "cf_b2b.cu", "cf_unfused.cu", "cf_noalloc.cu"]
+           "cf_b2b.cu", "cf_unfused.cu", "cf_noalloc.cu", "cf_cost.cu"]
 HEADERS = ["cf_ptx.cuh", "cf_internal.h", "cf_gemm_epi_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -1,0 +1,199 @@
+// cf_cost.cu -- host-only cost model: predicted time of the fused kernels and
+// of the unfused path (GEMM, then a kernel that reads the intermediate back).
+//
+// The ComFuse review, "If this is right" (third bullet): fuse only when the
+// GEMM is heavy enough to hide the epilogue.  The fused GEMM-epilogue kernel
+// overlaps tile t's epilogue with tile t+1's main loop (two TMEM
+// accumulators), so in steady state a tile costs max(main loop, epilogue +
+// statistics exchange); the last tile's epilogue is exposed.  The unfused
+// path costs the GEMM (its output written to HBM) plus a bandwidth-bound
+// epilogue kernel that reads it back.
+//
+// Calibration (one GB300, 2.07 GHz, L2 flushed between steps, against the
+// 1908 TFLOP/s measured bf16 burst): the fused main loop runs a tile at 0.92
+// of the per-SM peak; cuBLASLt's GEMMs at the full measured figure; the
+// row-epilogue and mid-op kernels at 0.85 of the copy bandwidth; the fused
+// epilogue costs ~1.5 cycles per instruction per thread (one warp per SM
+// sub-partition), with the per-element instruction counts below; per work
+// item the fused B2B kernels reach 0.634 (attention, softmax), 0.742
+// (attention, ReLU) and 0.51 (MLP, per cluster strip) of the per-SM peak.
+// Fixed costs: a launch (4 us), the fused kernel's pipeline fill (4 us), a
+// library GEMM's (3 us), an epilogue kernel's (2 us).  Operand re-reads of
+// the strip-major schedule are added when B exceeds half of the 129 MB L2.
+#include <cmath>
+#include <cstdint>
+
+#include "cf.h"
+
+namespace cf {
+namespace {
+
+struct Dev {
+  double peak, bw, ghz, launch;  // flop/s, byte/s, GHz, s
+  int sms;
+};
+
+Dev dev_model(const cf_device_model* d) {
+  Dev v;
+  v.peak = (d && d->tensor_tflops > 0 ? d->tensor_tflops : 1908.0) * 1e12;
+  v.bw = (d && d->hbm_gbs > 0 ? d->hbm_gbs : 7000.0) * 1e9;
+  v.sms = d && d->sms > 0 ? d->sms : 152;
+  v.ghz = d && d->clock_ghz > 0 ? d->clock_ghz : 2.07;
+  v.launch = (d && d->launch_us >= 0 ? d->launch_us : 4.0) * 1e-6;
+  return v;
+}
+
+constexpr double kMainloopEff = 0.92, kLibGemmEff = 1.0, kBwEff = 0.85, kCpi = 1.5;
+constexpr double kL2Bytes = 129e6;
+constexpr double kFusedFill = 4e-6, kLibGemmFill = 3e-6, kEpiKernelFill = 2e-6;
+constexpr double kAttnSoftmaxEff = 0.634, kAttnReluEff = 0.742, kMlpEff = 0.51;
+// A second (chained) reduction couples the strip's tiles once more through
+// the workspace: a serial cost per tile that the main loop does not hide.
+constexpr double kChainCoupling = 8e-6;
+
+// Imperfect overlap of a compute-bound and a memory-bound estimate.
+double overlap(double tc, double tm) { return std::fmax(tc, tm) + 0.25 * std::fmin(tc, tm); }
+
+// A library GEMM (batch x) M x N x K writing `out_bytes` per element, one
+// strided-batched launch.
+double lib_gemm_s(const Dev& d, double M, double N, double K, double out_bytes, double batch = 1.0) {
+  const double tc = batch * 2.0 * M * N * K / (d.peak * kLibGemmEff);
+  const double tm = batch * (2.0 * (M * K + K * N) + out_bytes * M * N) / d.bw;
+  return std::fmax(tc, tm) + d.launch + kLibGemmFill;
+}
+
+bool is_reduction(int kind) { return kind >= CF_OP_ROW_LAYERNORM && kind <= CF_OP_ROW_SOFTMAX; }
+
+// Instructions per element and thread of one epilogue op (fused kernel).
+double op_instr(int kind) {
+  switch (kind) {
+    case CF_OP_BIAS: return 2;
+    case CF_OP_SCALE: return 1;
+    case CF_OP_RELU: return 1;
+    case CF_OP_GELU_TANH: return 9;
+    case CF_OP_ADD_RESIDUAL: return 4;
+    case CF_OP_ROW_LAYERNORM: return 8;  // two statistic passes + the affine
+    case CF_OP_ROW_RMSNORM: return 4;
+    case CF_OP_ROW_SOFTMAX: return 9;    // two passes with exp2
+    default: return 0;
+  }
+}
+
+}  // namespace
+}  // namespace cf
+
+using namespace cf;
+
+extern "C" cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const cf_epi_desc* epi,
+                                           const cf_device_model* dm, cf_cost* out) {
+  if (!A || !B || !epi || !out) return CF_ERR_INVALID_ARG;
+  if (epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
+  if (A->trans != 0 || A->cols != B->rows || A->rows < 0 || B->cols < 0) return CF_ERR_INVALID_ARG;
+  const double M = (double)A->rows, N = (double)B->cols, K = (double)A->cols;
+  if ((A->cols % 8) != 0 || A->cols < 64) return CF_ERR_UNSUPPORTED_SHAPE;
+  int n_red = 0, has_res = 0, n_vec = 0;
+  double instr = 6.0;  // TMEM load, statistics and the final store per element
+  for (uint32_t i = 0; i < epi->n_ops; ++i) {
+    const int k = epi->ops[i].kind;
+    instr += op_instr(k);
+    n_red += is_reduction(k);
+    has_res |= k == CF_OP_ADD_RESIDUAL;
+    n_vec += k == CF_OP_BIAS || k == CF_OP_ROW_LAYERNORM || k == CF_OP_ROW_RMSNORM;
+  }
+  const bool cols = epi->version >= 3 && epi->axis == CF_AXIS_COLS && n_red > 0;
+  if (cols && B->trans != 1) return CF_ERR_UNSUPPORTED_SHAPE;
+  const Dev d = dev_model(dm);
+  const double kM = cols ? N : M, kN = cols ? M : N;  // the kernel runs on P^T for columns
+  cf_cost c = {};
+  c.flops = 2.0 * M * N * K;
+  const double res_bytes = has_res ? 2.0 * M * N : 0.0;  // a bf16 residual
+  c.fused_bytes = 2.0 * (M * K + K * N) + 4.0 * M * N + res_bytes;
+  c.unfused_bytes = c.fused_bytes + 8.0 * M * N;  // the fp32 intermediate written and read back
+  if (M == 0 || N == 0) {
+    c.fused_preferred = 1;
+    c.epilogue_hidden = 1;
+    *out = c;
+    return CF_OK;
+  }
+  // Fused: persistent tiles of 128 x 256 (CTA pairs take 256 x 256 on two SMs).
+  const double Kp = std::ceil(K / 64.0) * 64.0;
+  const double strips = std::ceil(kM / 128.0), tiles_n = std::ceil(kN / 256.0);
+  const double tiles = strips * tiles_n;
+  const double per_sm = d.peak / d.sms;
+  c.mainloop_us = 1e6 * 2.0 * 128.0 * 256.0 * Kp / (per_sm * kMainloopEff);
+  const double xchg = (n_red > 0 && tiles_n > 1) ? (tiles_n <= 16 ? 1.0e-6 : 2.0e-6) * n_red : 0.0;
+  c.epilogue_us = 1e6 * (256.0 * instr * kCpi / (d.ghz * 1e9) + xchg);
+  const double waves = std::ceil(tiles / d.sms);
+  const double t_tile = std::fmax(c.mainloop_us, c.epilogue_us) * 1e-6 + (n_red > 1 ? kChainCoupling : 0.0);
+  const double tc = waves * t_tile + c.epilogue_us * 1e-6;  // the last epilogue is exposed
+  // B re-read by every strip pair once it no longer fits in L2 (strip-major
+  // order; the serpentine walk keeps about half of it).
+  const double b_bytes = 2.0 * K * kN;
+  const double reread = b_bytes > 0.5 * kL2Bytes ? 0.5 * b_bytes * (strips / 2.0 - 1.0) : 0.0;
+  c.fused_us = 1e6 * (overlap(tc, (c.fused_bytes + std::fmax(reread, 0.0)) / d.bw) + d.launch + kFusedFill);
+  c.epilogue_hidden = c.epilogue_us <= c.mainloop_us ? 1 : 0;
+  // Unfused: library GEMM to fp32, then a bandwidth-bound epilogue kernel.
+  if (cols) {
+    c.unfused_us = -1.0;  // no unfused column-reduction path
+    c.fused_preferred = 1;
+  } else {
+    const double epi_bytes = 8.0 * M * N + res_bytes + 4.0 * N * n_vec;
+    c.unfused_us = 1e6 * (lib_gemm_s(d, M, N, K, 4.0) + epi_bytes / (d.bw * kBwEff) + d.launch + kEpiKernelFill);
+    c.fused_preferred = c.fused_us <= c.unfused_us ? 1 : 0;
+  }
+  *out = c;
+  return CF_OK;
+}
+
+extern "C" cf_status cf_cost_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
+                                     const cf_b2b_desc* desc, const cf_device_model* dm, cf_cost* out) {
+  if (!A || !W1 || !W2 || !desc || !out) return CF_ERR_INVALID_ARG;
+  if (desc->version != CF_B2B_VERSION || desc->batch < 1) return CF_ERR_INVALID_ARG;
+  if (desc->mid_op < CF_MID_RELU || desc->mid_op > CF_MID_SCALE_SOFTMAX) return CF_ERR_INVALID_ARG;
+  const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols;
+  if (W1->rows != K || W2->rows != N1) return CF_ERR_INVALID_ARG;
+  const bool attn = W1->trans == 1 && K % 8 == 0 && K >= 8 && K <= 128 && N2 >= 1 && N2 <= 128 && N1 >= 1;
+  const int64_t C = (N2 + 255) / 256;
+  const bool mlp = !attn && desc->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 64 && C >= 1 && C <= 4 &&
+                   N1 >= 1;
+  if (!attn && !mlp) return CF_ERR_UNSUPPORTED_SHAPE;
+  const Dev d = dev_model(dm);
+  const double b = (double)desc->batch, m = (double)M, k = (double)K, n1 = (double)N1, n2 = (double)N2;
+  cf_cost c = {};
+  c.flops = 2.0 * b * m * (k * n1 + n1 * n2);
+  c.fused_bytes = b * (2.0 * (m * k + k * n1 + n1 * n2) + 4.0 * m * n2);
+  c.unfused_bytes = c.fused_bytes + b * m * n1 * (4.0 + 4.0 + 2.0 + 2.0);  // S written, read; S' written, read
+  if (M == 0 || N2 == 0) {
+    c.fused_preferred = 1;
+    c.epilogue_hidden = 1;
+    *out = c;
+    return CF_OK;
+  }
+  // Fused: the measured full-size efficiency of each kernel, applied to the
+  // padded work (head dims and key chunks of 128, 128-row blocks) with the
+  // wave quantisation of a persistent grid.
+  double eff, per_item, slots;
+  const double work_items = b * std::ceil(m / 128.0);  // 128-row blocks (MLP: one per cluster of C CTAs)
+  if (attn) {
+    eff = desc->mid_op == CF_MID_SCALE_SOFTMAX ? kAttnSoftmaxEff : kAttnReluEff;
+    per_item = 2.0 * 128.0 * 128.0 * std::ceil(n1 / 128.0) * 128.0 * 2.0;  // head dims computed as 128
+    slots = d.sms;
+  } else {
+    eff = kMlpEff;
+    const double n1p = std::ceil(n1 / (128.0 * C)) * 128.0 * C;
+    per_item = 2.0 * 128.0 * (k * n1p / C + n1p * 256.0);  // per CTA: its S chunks, then its 256 O columns
+    slots = std::floor(d.sms / (double)C);                  // resident clusters
+  }
+  const double per_sm = d.peak / d.sms;
+  const double t_item = per_item / (per_sm * eff);
+  const double waves = std::ceil(work_items / slots);
+  c.mainloop_us = 1e6 * t_item;
+  c.fused_us = 1e6 * (overlap(waves * t_item, c.fused_bytes / d.bw) + d.launch + kFusedFill);
+  c.epilogue_hidden = 1;
+  // Unfused: GEMM1 to fp32, the mid op (S read, bf16 S' written), GEMM2.
+  const double mid = b * m * n1 * 6.0 / (d.bw * kBwEff) + d.launch + kEpiKernelFill;
+  c.unfused_us = 1e6 * (lib_gemm_s(d, m, n1, k, 4.0, b) + mid + lib_gemm_s(d, m, n2, n1, 4.0, b));
+  c.fused_preferred = c.fused_us <= c.unfused_us ? 1 : 0;
+  *out = c;
+  return CF_OK;
+}
