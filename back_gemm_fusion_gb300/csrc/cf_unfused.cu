@@ -133,35 +133,6 @@ __device__ __forceinline__ float gelu_fast(float x) {
   return __fdividef(x, 1.0f + __expf(-2.0f * u));
 }
 
-// Elementwise program for element (m, n); `r` is residual[m][n].
-__device__ __forceinline__ float ew(const RowProgram& pg, float x, const float* bias, int n, float r) {
-  for (int o = 0; o < pg.n_ops; ++o) {
-    switch (pg.kind[o]) {
-      case CF_OP_BIAS: x += bias[n]; break;
-      case CF_OP_ADD_RESIDUAL: x += r; break;
-      case CF_OP_SCALE: x *= pg.scalar[o]; break;
-      case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
-      case CF_OP_GELU_TANH: x = gelu_fast(x); break;
-    }
-  }
-  return x;
-}
-
-// Elementwise ops [o0, o1) of the program for element (m, n); `r` is residual[m][n].
-__device__ __forceinline__ float ew_range(const RowProgram& pg, float x, const float* bias, int n, float r, int o0,
-                                          int o1) {
-  for (int o = o0; o < o1; ++o) {
-    switch (pg.kind[o]) {
-      case CF_OP_BIAS: x += bias[n]; break;
-      case CF_OP_ADD_RESIDUAL: x += r; break;
-      case CF_OP_SCALE: x *= pg.scalar[o]; break;
-      case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
-      case CF_OP_GELU_TANH: x = gelu_fast(x); break;
-    }
-  }
-  return x;
-}
-
 // The first of two chained row reductions of a program (LayerNorm or
 // RMSNorm); ops [0, n_ops0) precede it.
 struct ChainStage {
@@ -188,6 +159,28 @@ __device__ float block_reduce(float v, float* red) {
   return r;
 }
 
+// Ops [o0, o1) of the program over this thread's elements of row m (held in
+// shared memory; every pass visits the same elements with the same thread,
+// so no barrier is needed between passes), one dispatch per op.
+__device__ __forceinline__ void apply_ops_smem(const RowProgram& pg, float* row, int N, const float* bias,
+                                               const ResView& rv, int m, int o0, int o1) {
+  for (int op = o0; op < o1; ++op) {
+    const int kind = pg.kind[op];
+    const float sc = pg.scalar[op];
+    if (kind == CF_OP_BIAS) {
+      for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] += bias[n];
+    } else if (kind == CF_OP_ADD_RESIDUAL) {
+      for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] += res_at(rv.ptr, rv.ld, rv.bf16, m, n);
+    } else if (kind == CF_OP_SCALE) {
+      for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] *= sc;
+    } else if (kind == CF_OP_RELU) {
+      for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = fmaxf(row[n], 0.0f);
+    } else if (kind == CF_OP_GELU_TANH) {
+      for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = gelu_fast(row[n]);
+    }
+  }
+}
+
 // One CTA per row: read P back from HBM, elementwise program, row statistic,
 // normalise, write out.  The activated row is kept in shared memory.
 __global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restrict__ P, int64_t ldp,
@@ -197,15 +190,13 @@ __global__ void __launch_bounds__(256) row_epilogue_kernel(const float* __restri
                                                            const float* __restrict__ beta, ResView rv) {
   extern __shared__ float row[];
   __shared__ float red[32];
-  const void* res = rv.ptr;
-  const long long res_ld = rv.ld;
-  const int res_bf16 = rv.bf16;
   const float* p = P + (int64_t)blockIdx.x * ldp;
   float* o = out + (int64_t)blockIdx.x * ldo;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = p[n];
+  apply_ops_smem(pg, row, N, bias, rv, (int)blockIdx.x, 0, pg.n_ops);
   float acc = 0.0f, mx = -INFINITY;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const float x = ew(pg, p[n], bias, n, res_at(res, res_ld, res_bf16, (int)blockIdx.x, n));
-    row[n] = x;
+    const float x = row[n];
     acc += x;
     mx = fmaxf(mx, x);
   }
@@ -250,10 +241,11 @@ __global__ void __launch_bounds__(256) row_epilogue_chain_kernel(const float* __
   const int m = (int)blockIdx.x;
   const float* p = P + (int64_t)m * ldp;
   float* o = out + (int64_t)m * ldo;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) row[n] = p[n];
+  apply_ops_smem(pg, row, N, bias, rv, m, 0, c0.n_ops0);
   float acc = 0.0f;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const float x = ew_range(pg, p[n], bias, n, res_at(rv.ptr, rv.ld, rv.bf16, m, n), 0, c0.n_ops0);
-    row[n] = x;
+    const float x = row[n];
     acc += (c0.rowop == CF_OP_ROW_RMSNORM) ? x * x : x;
   }
   float sc, sh = 0.0f;
@@ -269,14 +261,17 @@ __global__ void __launch_bounds__(256) row_epilogue_chain_kernel(const float* __
   } else {
     sc = rsqrtf(block_reduce<false>(acc, red) / N + c0.eps);
   }
-  acc = 0.0f;
-  float mx = -INFINITY;
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
     float x = row[n] * sc + sh;
     if (c0.gamma) x *= c0.gamma[n];
     if (c0.rowop == CF_OP_ROW_LAYERNORM && c0.beta) x += c0.beta[n];
-    x = ew_range(pg, x, bias, n, res_at(rv.ptr, rv.ld, rv.bf16, m, n), c0.n_ops0, pg.n_ops);
     row[n] = x;
+  }
+  apply_ops_smem(pg, row, N, bias, rv, m, c0.n_ops0, pg.n_ops);
+  acc = 0.0f;
+  float mx = -INFINITY;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    const float x = row[n];
     acc += x;
     mx = fmaxf(mx, x);
   }

@@ -36,17 +36,22 @@ from back_gemm_fusion_gb300 import inputs as I  # noqa: E402
 METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)"
 
 # DRAM traffic of one fused launch (dram__bytes_read.sum, dram__bytes_write.sum)
-# from an ncu --set full capture of `bench.py --workload W --once` on a GB300,
-# keyed by workload; valid only while the kernel source hash matches the one
-# the counters were taken with (profiles/ has the summaries and commands).
+# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k <fused
+# kernel> -c 1 bench.py --workload W --once` on a GB300 (fp32 output), keyed
+# by workload; valid only while the kernel source hash matches the one the
+# counters were taken with (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "gelu_rmsnorm": {"read": 110362880, "write": 91411712, "src": "f9cc6d4cb667d654"},
-    "scaled_softmax": {"read": 1396333568, "write": 239146752, "src": "f9cc6d4cb667d654"},
-    "mlp_b2b": {"read": 50470400, "write": 14872576, "src": "f9cc6d4cb667d654"},
-    "attention_softmax": {"read": 805418496, "write": 497545984, "src": "f9cc6d4cb667d654"},
-    "attention_relu": {"read": 805729280, "write": 495820800, "src": "f9cc6d4cb667d654"},
-    "postnorm_layernorm": {"read": 193516288, "write": 95745024, "src": "f9cc6d4cb667d654"},
-    "chained_ln_gelu_rms": {"read": 109929216, "write": 88441088, "src": "f9cc6d4cb667d654"},
+    "attention_relu": {"read": 805990912, "write": 494909440, "src": "ef34b4774b3dcf83"},
+    "attention_softmax": {"read": 805394176, "write": 497605632, "src": "ef34b4774b3dcf83"},
+    "chained_ln_gelu_rms": {"read": 116142848, "write": 87649024, "src": "ef34b4774b3dcf83"},
+    "column_layernorm": {"read": 305788928, "write": 99484672, "src": "ef34b4774b3dcf83"},
+    "gelu_rmsnorm": {"read": 116979712, "write": 89708544, "src": "ef34b4774b3dcf83"},
+    "layernorm_256": {"read": 312832, "write": 0, "src": "ef34b4774b3dcf83"},
+    "mlp_b2b": {"read": 50451968, "write": 14731520, "src": "ef34b4774b3dcf83"},
+    "mlp_bottom": {"read": 316928, "write": 0, "src": "ef34b4774b3dcf83"},
+    "postnorm_layernorm": {"read": 200069376, "write": 93125120, "src": "ef34b4774b3dcf83"},
+    "scaled_softmax": {"read": 1385517312, "write": 238905088, "src": "ef34b4774b3dcf83"},
+    "target_attention": {"read": 15006976, "write": 256, "src": "ef34b4774b3dcf83"},
 }
 
 
