@@ -298,27 +298,13 @@ __global__ void __launch_bounds__(256) row_epilogue_chain_kernel(const float* __
   }
 }
 
-// Bandwidth-oriented row epilogue for N = 1024 * VPT: each of 256 threads
-// keeps VPT float4 vectors of the row in registers, so P is read once and
-// the output written once.
+// Ops [o0, o1) of the program over a thread's VPT float4 vectors of row m
+// (float4 index c = i * 256 + threadIdx.x), one dispatch per op, 16-byte
+// loads of the bias and the residual.
 template <int VPT>
-__global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __restrict__ P, int64_t ldp,
-                                                               float* __restrict__ out, int64_t ldo, int N,
-                                                               RowProgram pg, const float* __restrict__ bias,
-                                                               const float* __restrict__ gamma,
-                                                               const float* __restrict__ beta, ResView rv) {
-  __shared__ float red[32];
-  const void* res = rv.ptr;
-  const long long res_ld = rv.ld;
-  const int res_bf16 = rv.bf16;
-  const float4* p = reinterpret_cast<const float4*>(P + (int64_t)blockIdx.x * ldp);
-  float4* o = reinterpret_cast<float4*>(out + (int64_t)blockIdx.x * ldo);
-  float4 v[VPT];
-#pragma unroll
-  for (int i = 0; i < VPT; ++i) v[i] = p[i * 256 + threadIdx.x];
-  // The program op by op over the thread's vectors (one dispatch per op,
-  // 16-byte loads of the bias and the residual).
-  for (int op = 0; op < pg.n_ops; ++op) {
+__device__ __forceinline__ void apply_ops_vec(const RowProgram& pg, float4 (&v)[VPT], const float* bias,
+                                              const ResView& rv, int m, int o0, int o1) {
+  for (int op = o0; op < o1; ++op) {
     const int kind = pg.kind[op];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -329,13 +315,13 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
         x = make_float4(x.x + b.x, x.y + b.y, x.z + b.z, x.w + b.w);
       } else if (kind == CF_OP_ADD_RESIDUAL) {
         float4 r;
-        if (res_bf16) {
-          const uint2 w = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(res) +
-                                                         (long long)blockIdx.x * res_ld)[c];
+        if (rv.bf16) {
+          const uint2 w = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(rv.ptr) +
+                                                         (long long)m * rv.ld)[c];
           r = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
         } else {
-          r = reinterpret_cast<const float4*>(static_cast<const float*>(res) + (long long)blockIdx.x * res_ld)[c];
+          r = reinterpret_cast<const float4*>(static_cast<const float*>(rv.ptr) + (long long)m * rv.ld)[c];
         }
         x = make_float4(x.x + r.x, x.y + r.y, x.z + r.z, x.w + r.w);
       } else if (kind == CF_OP_SCALE) {
@@ -348,6 +334,77 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
       }
       v[i] = x;
     }
+  }
+}
+
+// Normalisation constants (y = x * mul + add) of a LayerNorm or RMSNorm over
+// the row held in the block's vectors.
+template <int VPT>
+__device__ __forceinline__ void norm_consts_vec(int rowop, float eps, const float4 (&v)[VPT], int N, float* red,
+                                                float& mul, float& add) {
+  add = 0.0f;
+  if (rowop == CF_OP_ROW_LAYERNORM) {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) s += v[i].x + v[i].y + v[i].z + v[i].w;
+    const float mean = block_reduce<false>(s, red) / N;
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+      ss += a * a + b * b + c * c + d * d;
+    }
+    mul = rsqrtf(block_reduce<false>(ss, red) / N + eps);
+    add = -mean * mul;
+  } else {
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    mul = rsqrtf(block_reduce<false>(ss, red) / N + eps);
+  }
+}
+
+// Bandwidth-oriented row epilogue for N = 1024 * VPT: each of 256 threads
+// keeps VPT float4 vectors of the row in registers, so P is read once and
+// the output written once; chained programs (c0.rowop != 0) run both stages
+// on the same registers.
+template <int VPT>
+__global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __restrict__ P, int64_t ldp,
+                                                               float* __restrict__ out, int64_t ldo, int N,
+                                                               RowProgram pg, ChainStage c0,
+                                                               const float* __restrict__ bias,
+                                                               const float* __restrict__ gamma,
+                                                               const float* __restrict__ beta, ResView rv) {
+  __shared__ float red[32];
+  const float4* p = reinterpret_cast<const float4*>(P + (int64_t)blockIdx.x * ldp);
+  float4* o = reinterpret_cast<float4*>(out + (int64_t)blockIdx.x * ldo);
+  float4 v[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) v[i] = p[i * 256 + threadIdx.x];
+  if (c0.rowop != 0) {
+    // A first (chained) reduction: its ops, its normalisation and affine
+    // vectors, then the ops that follow it.
+    apply_ops_vec<VPT>(pg, v, bias, rv, (int)blockIdx.x, 0, c0.n_ops0);
+    float mul0, add0;
+    norm_consts_vec<VPT>(c0.rowop, c0.eps, v, N, red, mul0, add0);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = i * 256 + threadIdx.x;
+      float4 x = make_float4(fmaf(v[i].x, mul0, add0), fmaf(v[i].y, mul0, add0), fmaf(v[i].z, mul0, add0),
+                             fmaf(v[i].w, mul0, add0));
+      if (c0.gamma) {
+        const float4 g = reinterpret_cast<const float4*>(c0.gamma)[c];
+        x = make_float4(x.x * g.x, x.y * g.y, x.z * g.z, x.w * g.w);
+      }
+      if (c0.rowop == CF_OP_ROW_LAYERNORM && c0.beta) {
+        const float4 b = reinterpret_cast<const float4*>(c0.beta)[c];
+        x = make_float4(x.x + b.x, x.y + b.y, x.z + b.z, x.w + b.w);
+      }
+      v[i] = x;
+    }
+    apply_ops_vec<VPT>(pg, v, bias, rv, (int)blockIdx.x, c0.n_ops0, pg.n_ops);
+  } else {
+    apply_ops_vec<VPT>(pg, v, bias, rv, (int)blockIdx.x, 0, pg.n_ops);
   }
   float mul = 1.0f, add = 0.0f;  // y = (x * mul + add) [* gamma + beta]
   if (pg.rowop == CF_OP_ROW_LAYERNORM) {
@@ -535,7 +592,8 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   float* o = static_cast<float*>(out->ptr);
   const bool vec = N % 1024 == 0 && (out->ld % 4) == 0 && aligned16(out->ptr) && (!bias || aligned16(bias)) &&
                    (!gamma || aligned16(gamma)) && (!beta || aligned16(beta));
-  if (c0.rowop != 0) {
+  const bool vec_chain = vec && (!c0.gamma || aligned16(c0.gamma)) && (!c0.beta || aligned16(c0.beta));
+  if (c0.rowop != 0 && !vec_chain) {
     const size_t smem = (size_t)N * sizeof(float);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(row_epilogue_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -546,11 +604,11 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
     return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
   }
   switch (vec ? N / 1024 : 0) {
-    case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
-    case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
-    case 4: row_epilogue_reg_kernel<4><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
-    case 8: row_epilogue_reg_kernel<8><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
-    case 16: row_epilogue_reg_kernel<16><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, bias, gamma, beta, rv); break;
+    case 1: row_epilogue_reg_kernel<1><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias, gamma, beta, rv); break;
+    case 2: row_epilogue_reg_kernel<2><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias, gamma, beta, rv); break;
+    case 4: row_epilogue_reg_kernel<4><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias, gamma, beta, rv); break;
+    case 8: row_epilogue_reg_kernel<8><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias, gamma, beta, rv); break;
+    case 16: row_epilogue_reg_kernel<16><<<(unsigned)M, 256, 0, st>>>(intermediate, N, o, out->ld, (int)N, pg, c0, bias, gamma, beta, rv); break;
     default: {
       const size_t smem = (size_t)N * sizeof(float);
       if (smem > 48 * 1024 &&

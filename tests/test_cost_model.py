@@ -18,6 +18,7 @@ MEASURED = {
     "mlp_b2b": (334.0, 240.0),
     "attention_softmax": (910.0, 4200.0),
     "column_layernorm": (209.0, None),
+    "chained_ln_gelu_rms": (229.0, 217.5),
 }
 
 
@@ -45,6 +46,15 @@ def test_gemm_epilogue_calibration_and_decisions(lib):
     assert c2["epilogue_hidden"] == 1 and c1["epilogue_hidden"] == 0
     assert c2["flops"] == 2.0 * 8192 * 4096 * 4096
     assert c2["unfused_bytes"] - c2["fused_bytes"] == 8.0 * 8192 * 4096  # the intermediate written and read back
+
+
+def test_chained_program_prefers_unfused(lib):
+    # Two strip-wide exchanges per tile: measured slower fused than unfused.
+    c = B.cf_cost_gemm_epilogue(8192, 4096, 4096, [("bias",), ("layernorm", 1e-5), ("gelu_tanh",),
+                                                   ("rmsnorm", 1e-6)])
+    fm, um = MEASURED["chained_ln_gelu_rms"]
+    assert _within(c["fused_us"], fm, 0.25) and _within(c["unfused_us"], um, 0.25)
+    assert c["fused_preferred"] == 0
 
 
 def test_column_reductions_have_no_unfused_path(lib):

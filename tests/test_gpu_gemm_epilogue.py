@@ -173,17 +173,26 @@ def test_chained_reductions(cf, chain, M, N, affine0):
     assert_rows_close(out.cpu().numpy(), ref, what=f"chain {chain} {M}x{N} affine0={affine0}")
 
 
-def test_chained_reductions_unfused(cf):
-    ops = CHAINS["ln_gelu_rms"]
-    case = I.gemm_epilogue_case("chain_unfused", 256, 2048, 128, ops, seed=7, need_bias=True, need_gamma=True,
+@pytest.mark.parametrize("N", [2048, 1000])
+@pytest.mark.parametrize("chain", sorted(CHAINS))
+def test_chained_reductions_unfused(cf, chain, N):
+    # The unfused comparison path: register-resident rows (N a multiple of
+    # 1024) or the shared-memory kernel (other N), first-stage affine vectors.
+    ops = CHAINS[chain]
+    case = I.gemm_epilogue_case("chain_unfused", 256, N, 128, ops, seed=7, need_bias=True, need_gamma=True,
                                 need_beta=True)
-    g0 = torch.from_numpy((1.0 + 0.3 * np.random.default_rng(3).standard_normal(2048)).astype(np.float32))
+    rng = np.random.default_rng(3)
+    g0 = torch.from_numpy((1.0 + 0.3 * rng.standard_normal(N)).astype(np.float32))
+    b0 = torch.from_numpy((0.3 * rng.standard_normal(N)).astype(np.float32))
+    R = torch.from_numpy(rng.standard_normal((256, N)).astype(np.float32)).to(torch.bfloat16)
     out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), case.B.cuda(), case.ops, _dev(case.bias), _dev(case.gamma),
-                                      _dev(case.beta), stage0_gamma=g0.cuda())
+                                      _dev(case.beta), stage0_gamma=g0.cuda(), stage0_beta=b0.cuda(),
+                                      residual=R.cuda())
     torch.cuda.synchronize()
     ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
-                          I.to_f64(case.beta), stage0_gamma=I.to_f64(g0))
-    assert_rows_close(out.cpu().numpy(), ref, what="unfused chain ln_gelu_rms")
+                          I.to_f64(case.beta), residual=I.to_f64(R), stage0_gamma=I.to_f64(g0),
+                          stage0_beta=I.to_f64(b0))
+    assert_rows_close(out.cpu().numpy(), ref, what=f"unfused chain {chain} N={N}")
 
 
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
