@@ -60,16 +60,47 @@ __device__ __forceinline__ void pack_bf16(const float (&v)[32], uint32_t (&w)[16
   }
 }
 
-// Sum of the 32 bf16 values held in 16 packed words (exact widening).
-__device__ __forceinline__ float sum_packed_bf16(const uint32_t (&w)[16]) {
-  float t[16];
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// v[e] = v[e] * s + t for 32 values, two per packed fp32x2 FMA; s2 and t2
+// hold {s, s} and {t, t}.
+__device__ __forceinline__ void fma2_32(float (&v)[32], uint64_t s2, uint64_t t2) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xffff0000u);
+  for (int e = 0; e < 32; e += 2) {
+    asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%0, %1};\n\tfma.rn.f32x2 x, x, %2, %3;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(v[e]), "+f"(v[e + 1])
+        : "l"(s2), "l"(t2));
+  }
+}
+
+__device__ __forceinline__ uint64_t pack2f(float a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(a));
+  return r;
+}
+
+// Sum of the 32 bf16 values held in 16 packed words (exact widening).
+// Each word widens to an fp32 pair {low, high}; the 16 pairs are summed as
+// packed fp32x2 in a log-depth tree, then the two halves.
+__device__ __forceinline__ float sum_packed_bf16(const uint32_t (&w)[16]) {
+  uint64_t t[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint32_t lo = w[e] << 16, hi = w[e] & 0xffff0000u;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(t[e]) : "r"(lo), "r"(hi));
+  }
 #pragma unroll
   for (int h = 8; h >= 1; h >>= 1)
 #pragma unroll
-    for (int e = 0; e < h; ++e) t[e] += t[e + h];  // pairwise: log-depth dependency chain
-  return t[0];
+    for (int e = 0; e < h; ++e) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(t[e]) : "l"(t[e + h]));
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(t[0]));
+  return a + b;
 }
 
 // Write 32 packed bf16 values of row `r` (columns c0..c0+31 of a 128-column
@@ -387,16 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             for (int e = 0; e < 128; ++e)
               if (e >= p.kv_last) v[e] = -INFINITY;
           }
+          // Row max with three-input max instructions: 128 -> 16 -> 1.
           float mx[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            mx[e] = fmaxf(fmaxf(fmaxf(v[e], v[e + 16]), fmaxf(v[e + 32], v[e + 48])),
-                          fmaxf(fmaxf(v[e + 64], v[e + 80]), fmaxf(v[e + 96], v[e + 112])));
-#pragma unroll
-          for (int h = 8; h >= 1; h >>= 1)
-#pragma unroll
-            for (int e = 0; e < h; ++e) mx[e] = fmaxf(mx[e], mx[e + h]);
-          const float bmax = mx[0] * sl2;
+            mx[e] = max3f(max3f(v[e], v[e + 16], v[e + 32]), max3f(v[e + 48], v[e + 64], v[e + 80]),
+                          fmaxf(v[e + 96], v[e + 112]));
+          const float mxa = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), max3f(mx[6], mx[7], mx[8]));
+          const float mxb = max3f(max3f(mx[9], mx[10], mx[11]), max3f(mx[12], mx[13], mx[14]), mx[15]);
+          const float bmax = fmaxf(mxa, mxb) * sl2;
           // Max in use after chunk gg-1 (every chunk but the CTA's first
           // waits, so hand-offs alternate strictly between the groups).
           float m_prev = -INFINITY;
@@ -449,7 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           uint32_t w[16];
           if (p.softmax) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) vc[e] = ex2_approx(fmaf(vc[e], sl2, -m_last));
+            fma2_32(vc, pack2f(sl2), pack2f(-m_last));  // the exp2 arguments, two per instruction
+#pragma unroll
+            for (int e = 0; e < 32; ++e) vc[e] = ex2_approx(vc[e]);
             pack_bf16(vc, w);
             l += sum_packed_bf16(w);
           } else {
