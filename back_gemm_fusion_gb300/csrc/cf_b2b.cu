@@ -485,9 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             pack_bf16(vc, w);
             l += sum_packed_bf16(w);
           } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) vc[e] = fmaxf(vc[e] * p.scale, 0.0f);
+            // relu(bf16(scale s)) == bf16(relu(scale s)) (rounding is monotonic
+            // and keeps 0): scale two per packed FMA, round, then a bf16x2 max.
+            fma2_32(vc, pack2f(p.scale), pack2f(0.0f));
             pack_bf16(vc, w);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) asm("max.bf16x2 %0, %0, %1;" : "+r"(w[e]) : "r"(0u));
           }
           tmem_st16(tmem_base + lane_off + kTmemP + 64 * sb + 16 * c, *reinterpret_cast<float(*)[16]>(&w[0]));
         }
