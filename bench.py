@@ -38,26 +38,28 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # DRAM traffic of one fused launch (dram__bytes_read.sum, dram__bytes_write.sum)
 # from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k <fused
 # kernel> -c 1 bench.py --workload W --once` on a GB300 (fp32 output), keyed
-# by workload; valid only while the kernel source hash matches the one the
-# counters were taken with (profiles/ has the summaries and commands).
+# by workload; valid only while the hash of the workload's kernel family
+# sources (kernel_source_hash) matches the one the counters were taken with
+# (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "attention_relu": {"read": 805990912, "write": 494909440, "src": "ef34b4774b3dcf83"},
-    "attention_softmax": {"read": 805394176, "write": 497605632, "src": "ef34b4774b3dcf83"},
-    "chained_ln_gelu_rms": {"read": 116142848, "write": 87649024, "src": "ef34b4774b3dcf83"},
-    "column_layernorm": {"read": 305788928, "write": 99484672, "src": "ef34b4774b3dcf83"},
-    "gelu_rmsnorm": {"read": 116979712, "write": 89708544, "src": "ef34b4774b3dcf83"},
-    "layernorm_256": {"read": 312832, "write": 0, "src": "ef34b4774b3dcf83"},
-    "mlp_b2b": {"read": 50451968, "write": 14731520, "src": "ef34b4774b3dcf83"},
-    "mlp_bottom": {"read": 316928, "write": 0, "src": "ef34b4774b3dcf83"},
-    "postnorm_layernorm": {"read": 200069376, "write": 93125120, "src": "ef34b4774b3dcf83"},
-    "scaled_softmax": {"read": 1385517312, "write": 238905088, "src": "ef34b4774b3dcf83"},
-    "target_attention": {"read": 15006976, "write": 256, "src": "ef34b4774b3dcf83"},
+    "attention_relu": {"read": 805553152, "write": 494316288, "src": "586c6da1657d2165"},
+    "attention_softmax": {"read": 805414400, "write": 495480832, "src": "586c6da1657d2165"},
+    "chained_ln_gelu_rms": {"read": 116142848, "write": 87649024, "src": "80d4303150507d8f"},
+    "column_layernorm": {"read": 305788928, "write": 99484672, "src": "80d4303150507d8f"},
+    "gelu_rmsnorm": {"read": 116979712, "write": 89708544, "src": "80d4303150507d8f"},
+    "layernorm_256": {"read": 312832, "write": 0, "src": "80d4303150507d8f"},
+    "mlp_b2b": {"read": 50479104, "write": 14797056, "src": "586c6da1657d2165"},
+    "mlp_bottom": {"read": 317184, "write": 0, "src": "586c6da1657d2165"},
+    "postnorm_layernorm": {"read": 200069376, "write": 93125120, "src": "80d4303150507d8f"},
+    "scaled_softmax": {"read": 1385517312, "write": 238905088, "src": "80d4303150507d8f"},
+    "target_attention": {"read": 15001600, "write": 512, "src": "586c6da1657d2165"},
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(b2b: bool) -> str:
+    """Hash of the sources of the fused kernel family a workload runs."""
     h = hashlib.sha256()
-    for f in ("cf_gemm_epi_kernel.cuh", "cf_b2b.cu", "cf_ptx.cuh", "cf_internal.h"):
+    for f in (("cf_b2b.cu" if b2b else "cf_gemm_epi_kernel.cuh"), "cf_ptx.cuh", "cf_internal.h"):
         with open(os.path.join(ROOT, "back_gemm_fusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -595,7 +597,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     # CPU baseline: the oracle on the host cores, bounded sample.
     ref_tflops, ref_rows, ref_s = time_oracle(wl, args.cpu_seconds)
     t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
-    src = kernel_source_hash()
+    src = kernel_source_hash(wl.is_b2b)
     tr = NCU_TRAFFIC.get(wl.name) if wl.out_dtype == torch.float32 else None  # counters taken with fp32 out
     tr = tr if tr and tr.get("src") == src else None
     traffic = (tr["read"] + tr["write"]) if tr else None
