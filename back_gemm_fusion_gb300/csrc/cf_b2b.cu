@@ -85,22 +85,21 @@ __device__ __forceinline__ uint64_t pack2f(float a) {
 }
 
 // Sum of the 32 bf16 values held in 16 packed words (exact widening).
-// Each word widens to an fp32 pair {low, high}; the 16 pairs are summed as
-// packed fp32x2 in a log-depth tree, then the two halves.
+// Sum of the 32 bf16 values held in 16 packed words: mixed-precision adds
+// (each bf16 half widens exactly into an fp32 accumulator), four independent
+// accumulators to keep the dependency chains short.
 __device__ __forceinline__ float sum_packed_bf16(const uint32_t (&w)[16]) {
-  uint64_t t[16];
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const uint32_t lo = w[e] << 16, hi = w[e] & 0xffff0000u;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(t[e]) : "r"(lo), "r"(hi));
+    float& a = acc[(e & 1) * 2];
+    float& b = acc[(e & 1) * 2 + 1];
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w[e]));
   }
-#pragma unroll
-  for (int h = 8; h >= 1; h >>= 1)
-#pragma unroll
-    for (int e = 0; e < h; ++e) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(t[e]) : "l"(t[e + h]));
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(t[0]));
-  return a + b;
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // Write 32 packed bf16 values of row `r` (columns c0..c0+31 of a 128-column
