@@ -15,7 +15,7 @@
 // row-epilogue and mid-op kernels at 0.85 of the copy bandwidth; the fused
 // epilogue costs ~1.5 cycles per instruction per thread (one warp per SM
 // sub-partition), with the per-element instruction counts below; per work
-// item the fused B2B kernels reach 0.634 (attention, softmax), 0.742
+// item the fused B2B kernels reach 0.683 (attention, softmax), 0.759
 // (attention, ReLU) and 0.51 (MLP, per cluster strip) of the per-SM peak.
 // Fixed costs: a launch (4 us), the fused kernel's pipeline fill (4 us), a
 // library GEMM's (3 us), an epilogue kernel's (2 us).  Operand re-reads of
@@ -46,7 +46,7 @@ Dev dev_model(const cf_device_model* d) {
 constexpr double kMainloopEff = 0.92, kLibGemmEff = 1.0, kBwEff = 0.85, kCpi = 1.5;
 constexpr double kL2Bytes = 129e6;
 constexpr double kFusedFill = 4e-6, kLibGemmFill = 3e-6, kEpiKernelFill = 2e-6;
-constexpr double kAttnSoftmaxEff = 0.634, kAttnReluEff = 0.742, kMlpEff = 0.51;
+constexpr double kAttnSoftmaxEff = 0.683, kAttnReluEff = 0.759, kMlpEff = 0.51;
 // A second (chained) reduction couples the strip's tiles once more through
 // the workspace: a serial cost per tile that the main loop does not hide.
 constexpr double kChainCoupling = 8e-6;

@@ -16,7 +16,7 @@ MEASURED = {
     "scaled_softmax": (386.0, 415.0),
     "layernorm_256": (17.1, 15.2),
     "mlp_b2b": (334.0, 240.0),
-    "attention_softmax": (910.0, 4200.0),
+    "attention_softmax": (845.0, 4229.0),
     "column_layernorm": (209.0, None),
     "chained_ln_gelu_rms": (229.0, 217.5),
 }
