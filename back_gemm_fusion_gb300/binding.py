@@ -279,8 +279,10 @@ def cf_b2bgemm(A: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, op: str, sca
 
 
 def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=None, b_trans=False,
-                             intermediate=None, stream=None, residual=None, stage0_gamma=None, stage0_beta=None):
-    """Comparison path: cuBLASLt GEMM to an fp32 intermediate, then a separate epilogue kernel."""
+                             intermediate=None, stream=None, residual=None, stage0_gamma=None, stage0_beta=None,
+                             axis: str = "row"):
+    """Comparison path: cuBLASLt GEMM to an fp32 intermediate, then a separate
+    epilogue kernel (row or column reductions)."""
     lib = load_library()
     M = A.shape[0]
     N = B.shape[0] if b_trans else B.shape[1]
@@ -288,7 +290,8 @@ def cf_unfused_gemm_epilogue(A, B, ops, bias=None, gamma=None, beta=None, out=No
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if intermediate is None:
         intermediate = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    a, b, o, d = matrix(A), matrix(B, b_trans), matrix(out), epi_desc(ops, residual=residual, stage0_gamma=stage0_gamma, stage0_beta=stage0_beta)
+    a, b, o, d = (matrix(A), matrix(B, b_trans), matrix(out),
+                  epi_desc(ops, residual=residual, stage0_gamma=stage0_gamma, stage0_beta=stage0_beta, axis=axis))
     st = lib.cf_unfused_gemm_epilogue(ctypes.byref(a), ctypes.byref(b), _ptr(bias), _ptr(gamma), _ptr(beta),
                                       ctypes.byref(d), ctypes.byref(o), _ptr(intermediate), _stream(stream))
     _check(st, "cf_unfused_gemm_epilogue")

@@ -44,6 +44,10 @@ Dev dev_model(const cf_device_model* d) {
 }
 
 constexpr double kMainloopEff = 0.92, kLibGemmEff = 1.0, kBwEff = 0.85, kCpi = 1.5;
+// The unfused column epilogue (three small kernels per reduction stage,
+// recomputing the elementwise program on each pass) reaches about a third
+// of the copy bandwidth.
+constexpr double kColBwEff = 0.35;
 constexpr double kL2Bytes = 129e6;
 constexpr double kFusedFill = 4e-6, kLibGemmFill = 3e-6, kEpiKernelFill = 2e-6;
 constexpr double kAttnSoftmaxEff = 0.683, kAttnReluEff = 0.759, kMlpEff = 0.51;
@@ -132,15 +136,14 @@ extern "C" cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* 
   const double reread = b_bytes > 0.5 * kL2Bytes ? 0.5 * b_bytes * (strips / 2.0 - 1.0) : 0.0;
   c.fused_us = 1e6 * (overlap(tc, (c.fused_bytes + std::fmax(reread, 0.0)) / d.bw) + d.launch + kFusedFill);
   c.epilogue_hidden = c.epilogue_us <= c.mainloop_us ? 1 : 0;
-  // Unfused: library GEMM to fp32, then a bandwidth-bound epilogue kernel.
-  if (cols) {
-    c.unfused_us = -1.0;  // no unfused column-reduction path
-    c.fused_preferred = 1;
-  } else {
-    const double epi_bytes = 8.0 * M * N + res_bytes + 4.0 * N * n_vec;
-    c.unfused_us = 1e6 * (lib_gemm_s(d, M, N, K, 4.0) + epi_bytes / (d.bw * kBwEff) + d.launch + kEpiKernelFill);
-    c.fused_preferred = c.fused_us <= c.unfused_us ? 1 : 0;
-  }
+  // Unfused: library GEMM to fp32, then a bandwidth-bound epilogue kernel
+  // (for columns, one read of the intermediate per statistics pass plus the
+  // writing pass).
+  const double reads = cols ? (double)n_red + 1.0 : 1.0;
+  const double epi_bytes = (4.0 * reads + 4.0) * M * N + res_bytes * reads + 4.0 * N * n_vec;
+  c.unfused_us = 1e6 * (lib_gemm_s(d, M, N, K, 4.0) + epi_bytes / (d.bw * (cols ? kColBwEff : kBwEff)) + d.launch +
+                        kEpiKernelFill);
+  c.fused_preferred = c.fused_us <= c.unfused_us ? 1 : 0;
   *out = c;
   return CF_OK;
 }

@@ -458,6 +458,151 @@ __global__ void __launch_bounds__(256) row_epilogue_reg_kernel(const float* __re
   }
 }
 
+// Column reductions for the unfused comparison path, three kinds of
+// kernels over a grid of (32-column block, row chunk) CTAs of 32 x 16
+// threads (lane x = column, y = row group: every row read is a coalesced
+// 128-byte segment):
+//   col_stats_kernel     per-chunk statistics of one reduction stage,
+//   col_finalize_kernel  per-column merge of the chunks -> (mul, add),
+//   col_write_kernel     the normalised output.
+// The elementwise stages are recomputed from P on every pass.  Norm
+// statistics are sums shifted by the column's row-0 value (robust to large
+// means, identical in every chunk); softmax keeps an online (max, sum) pair.
+// Scratch (partials and constants) is a static device array of the library.
+constexpr int kColGroups = 16;
+constexpr int kColMaxN = 65536;
+constexpr size_t kColPartCap = (size_t)6 << 17;  // ColStat entries (6 MB)
+
+struct ColStat {
+  float a, b;  // norms: shifted sum, shifted sum of squares; softmax: max, sum exp
+};
+
+__device__ ColStat g_col_part[kColPartCap];   // [chunk][column]
+__device__ float2 g_col_consts[2][kColMaxN];  // [stage][column]: y = x * mul + add
+
+struct ColArgs {
+  const float* P;
+  int M, N, rows_per, chunks;
+  RowProgram pg;
+  ChainStage c0;
+  const float* bias;
+  ResView rv;
+};
+
+__device__ __forceinline__ float col_ops(const RowProgram& pg, float x, const float* bias, const ResView& rv, int m,
+                                         int n, int o0, int o1) {
+  for (int op = o0; op < o1; ++op) {
+    switch (pg.kind[op]) {
+      case CF_OP_BIAS: x += bias[n]; break;
+      case CF_OP_ADD_RESIDUAL: x += res_at(rv.ptr, rv.ld, rv.bf16, m, n); break;
+      case CF_OP_SCALE: x *= pg.scalar[op]; break;
+      case CF_OP_RELU: x = fmaxf(x, 0.0f); break;
+      case CF_OP_GELU_TANH: x = gelu_fast(x); break;
+    }
+  }
+  return x;
+}
+
+// Value of element (m, n) at the input of reduction stage `second` (0: the
+// first or only reduction, 1: the second of a chain).
+__device__ __forceinline__ float col_stage(const ColArgs& a, int m, int n, bool second) {
+  const bool chain = a.c0.rowop != 0;
+  float x = col_ops(a.pg, a.P[(int64_t)m * a.N + n], a.bias, a.rv, m, n, 0, chain ? a.c0.n_ops0 : a.pg.n_ops);
+  if (!second) return x;
+  const float2 k0 = g_col_consts[0][n];
+  x = fmaf(x, k0.x, k0.y);
+  if (a.c0.gamma) x *= a.c0.gamma[n];
+  if (a.c0.rowop == CF_OP_ROW_LAYERNORM && a.c0.beta) x += a.c0.beta[n];
+  return col_ops(a.pg, x, a.bias, a.rv, m, n, a.c0.n_ops0, a.pg.n_ops);
+}
+
+__global__ void __launch_bounds__(32 * kColGroups) col_stats_kernel(ColArgs a, int rowop, int second) {
+  __shared__ ColStat sh[kColGroups][32];
+  const int n = blockIdx.x * 32 + threadIdx.x;
+  const int nn = n < a.N ? n : a.N - 1;
+  const float shift = col_stage(a, 0, nn, second);
+  ColStat st = rowop == CF_OP_ROW_SOFTMAX ? ColStat{-INFINITY, 0.0f} : ColStat{0.0f, 0.0f};
+  const int r0 = blockIdx.y * a.rows_per, r1 = min(a.M, r0 + a.rows_per);
+  for (int m = r0 + threadIdx.y; m < r1; m += kColGroups) {
+    const float x = col_stage(a, m, nn, second);
+    if (rowop == CF_OP_ROW_SOFTMAX) {
+      const float mm = fmaxf(st.a, x);
+      st.b = st.b * __expf(st.a - mm) + __expf(x - mm);
+      st.a = mm;
+    } else {
+      const float d = x - shift;
+      st.a += d;
+      st.b = fmaf(d, d, st.b);
+    }
+  }
+  sh[threadIdx.y][threadIdx.x] = st;
+  __syncthreads();
+  if (threadIdx.y != 0 || n >= a.N) return;
+  for (int g = 1; g < kColGroups; ++g) {
+    const ColStat u = sh[g][threadIdx.x];
+    if (rowop == CF_OP_ROW_SOFTMAX) {
+      const float mm = fmaxf(st.a, u.a);
+      st.b = (st.b == 0.0f ? 0.0f : st.b * __expf(st.a - mm)) + (u.b == 0.0f ? 0.0f : u.b * __expf(u.a - mm));
+      st.a = mm;
+    } else {
+      st.a += u.a;
+      st.b += u.b;
+    }
+  }
+  g_col_part[(size_t)blockIdx.y * a.N + n] = st;
+}
+
+// Constants of the stage whose input is col_stage(second) into slot `slot`.
+__global__ void col_finalize_kernel(ColArgs a, int rowop, float eps, int second, int slot) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= a.N) return;
+  ColStat t = g_col_part[n];
+  for (int r = 1; r < a.chunks; ++r) {
+    const ColStat u = g_col_part[(size_t)r * a.N + n];
+    if (rowop == CF_OP_ROW_SOFTMAX) {
+      const float mm = fmaxf(t.a, u.a);
+      t.b = (t.b == 0.0f ? 0.0f : t.b * __expf(t.a - mm)) + (u.b == 0.0f ? 0.0f : u.b * __expf(u.a - mm));
+      t.a = mm;
+    } else {
+      t.a += u.a;
+      t.b += u.b;
+    }
+  }
+  float mul, add;
+  if (rowop == CF_OP_ROW_SOFTMAX) {  // y = exp(x - max) / sum: kept as (1 / sum, max)
+    mul = 1.0f / t.b;
+    add = t.a;
+  } else {
+    const float shift = col_stage(a, 0, n, second);
+    const float m1 = t.a / a.M, m2 = t.b / a.M;
+    if (rowop == CF_OP_ROW_LAYERNORM) {
+      mul = rsqrtf(fmaxf(m2 - m1 * m1, 0.0f) + eps);
+      add = -(shift + m1) * mul;
+    } else {  // mean of x^2 = mean of (d + shift)^2 with d = x - shift
+      mul = rsqrtf(m2 + 2.0f * shift * m1 + shift * shift + eps);
+      add = 0.0f;
+    }
+  }
+  g_col_consts[slot][n] = make_float2(mul, add);
+}
+
+__global__ void __launch_bounds__(32 * kColGroups) col_write_kernel(ColArgs a, float* __restrict__ out, int64_t ldo,
+                                                                     const float* __restrict__ gamma,
+                                                                     const float* __restrict__ beta) {
+  const int n = blockIdx.x * 32 + threadIdx.x;
+  if (n >= a.N) return;
+  const bool chain = a.c0.rowop != 0;
+  const int rowop = a.pg.rowop;
+  const float2 k = g_col_consts[1][n];
+  const float g = rowop == CF_OP_ROW_SOFTMAX ? 1.0f : gamma[n];
+  const float b = rowop == CF_OP_ROW_LAYERNORM ? beta[n] : 0.0f;
+  const int r0 = blockIdx.y * a.rows_per, r1 = min(a.M, r0 + a.rows_per);
+  for (int m = r0 + threadIdx.y; m < r1; m += kColGroups) {
+    const float x = col_stage(a, m, n, chain);
+    out[(int64_t)m * ldo + n] = rowop == CF_OP_ROW_SOFTMAX ? __expf(x - k.y) * k.x : fmaf(x, k.x, k.y) * g + b;
+  }
+}
+
 // Register-resident mid op for N1 = 1024 * VPT (one CTA of 256 threads per row).
 template <int VPT>
 __global__ void __launch_bounds__(256) mid_op_reg_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ Pout,
@@ -540,11 +685,12 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
   if (A->dtype != CF_BF16 || B->dtype != CF_BF16 || out->dtype != CF_FP32 || A->trans || out->trans)
     return CF_ERR_INVALID_ARG;
   if (epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
-  // Column reductions have no unfused counterpart here.
-  if (epi->version >= 3 && epi->axis != CF_AXIS_ROWS) {
+  bool cols = false;  // reductions down the columns (col_epilogue_kernel)
+  if (epi->version >= 3) {
+    if (epi->axis != CF_AXIS_ROWS && epi->axis != CF_AXIS_COLS) return CF_ERR_INVALID_ARG;
     for (uint32_t i = 0; i < epi->n_ops; ++i)
       if (epi->ops[i].kind >= CF_OP_ROW_LAYERNORM && epi->ops[i].kind <= CF_OP_ROW_SOFTMAX)
-        return CF_ERR_UNSUPPORTED_SHAPE;
+        cols = epi->axis == CF_AXIS_COLS;
   }
   const int64_t M = A->rows, K = A->cols, N = B->cols;
   if (B->rows != K || out->rows != M || out->cols != N) return CF_ERR_INVALID_ARG;
@@ -590,6 +736,36 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
                         0, 0, st);
   if (s != CF_OK) return s;
   float* o = static_cast<float*>(out->ptr);
+  if (cols) {
+    if (N > kColMaxN) return CF_ERR_UNSUPPORTED_SHAPE;
+    ColArgs ca;
+    ca.P = intermediate;
+    ca.M = (int)M;
+    ca.N = (int)N;
+    // Row chunks of >= 256 rows, as many as the partial-statistics array holds.
+    const int64_t max_chunks = (int64_t)(kColPartCap / (size_t)N);
+    int64_t rows_per = 256;
+    while ((M + rows_per - 1) / rows_per > max_chunks) rows_per *= 2;
+    ca.rows_per = (int)rows_per;
+    ca.chunks = (int)((M + rows_per - 1) / rows_per);
+    ca.pg = pg;
+    ca.c0 = c0;
+    ca.bias = bias;
+    ca.rv = rv;
+    const dim3 grid((unsigned)((N + 31) / 32), (unsigned)ca.chunks), block(32, kColGroups);
+    const unsigned fin_grid = (unsigned)((N + 255) / 256);
+    // Slot 0: a chain's first reduction (read by col_stage for the second);
+    // slot 1: the last reduction (read by the write kernel).
+    if (c0.rowop != 0) {
+      col_stats_kernel<<<grid, block, 0, st>>>(ca, c0.rowop, 0);
+      col_finalize_kernel<<<fin_grid, 256, 0, st>>>(ca, c0.rowop, c0.eps, 0, 0);
+    }
+    const int second = c0.rowop != 0 ? 1 : 0;
+    col_stats_kernel<<<grid, block, 0, st>>>(ca, pg.rowop, second);
+    col_finalize_kernel<<<fin_grid, 256, 0, st>>>(ca, pg.rowop, pg.eps, second, 1);
+    col_write_kernel<<<grid, block, 0, st>>>(ca, o, out->ld, gamma, beta);
+    return cudaGetLastError() == cudaSuccess ? CF_OK : CF_ERR_CUDA;
+  }
   const bool vec = N % 1024 == 0 && (out->ld % 4) == 0 && aligned16(out->ptr) && (!bias || aligned16(bias)) &&
                    (!gamma || aligned16(gamma)) && (!beta || aligned16(beta));
   const bool vec_chain = vec && (!c0.gamma || aligned16(c0.gamma)) && (!c0.beta || aligned16(c0.beta));

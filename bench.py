@@ -176,8 +176,6 @@ class Workload:
 
     def unfused_step(self, cf, dev, scratch, stream=None):
         c = self.case
-        if self.axis == "col":
-            raise NotImplementedError("the unfused comparison path has no column reductions")
         if self.is_b2b:
             A = dev["A"] if c.batch > 1 else dev["A"][0]
             W1 = dev["W1"] if c.batch > 1 else dev["W1"][0]
@@ -191,7 +189,7 @@ class Workload:
             cf.cf_unfused_gemm_epilogue(dev["A"], dev["B"], c.ops, dev["bias"], dev["gamma"], dev["beta"],
                                         out=dev["out"], intermediate=scratch, stream=stream,
                                         residual=dev["residual"], stage0_gamma=dev["stage0_gamma"],
-                                        stage0_beta=dev["stage0_beta"])
+                                        stage0_beta=dev["stage0_beta"], b_trans=self.axis == "col", axis=self.axis)
 
     def unfused_scratch(self):
         c = self.case

@@ -261,8 +261,8 @@ CF_API cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_ma
  * cf_unfused_gemm_epilogue -- the unfused comparison path: a cuBLASLt GEMM
  * writes P (M x N fp32) to `intermediate`, then a separate row-epilogue
  * kernel reads it back and writes `out`.  Same program semantics as
- * cf_gemm_epilogue, fp32 `out` only.  `intermediate` is caller-owned
- * device memory of M * N * 4 bytes.
+ * cf_gemm_epilogue (row or column reductions), fp32 `out` only.
+ * `intermediate` is caller-owned device memory of M * N * 4 bytes.
  */
 CF_API cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
                                    const float* bias, const float* gamma, const float* beta,
@@ -307,8 +307,8 @@ typedef struct {
   double mainloop_us;      /* fused: predicted main-loop time of one tile */
   double epilogue_us;      /* fused: predicted epilogue (+ statistics exchange) time of one tile */
   double fused_us;         /* predicted time of the fused call */
-  double unfused_us;       /* predicted time of the unfused path (< 0: it has no counterpart) */
-  int32_t fused_preferred; /* 1 when fused_us <= unfused_us (or there is no unfused path) */
+  double unfused_us;       /* predicted time of the unfused path */
+  int32_t fused_preferred; /* 1 when fused_us <= unfused_us */
   int32_t epilogue_hidden; /* 1 when a tile's epilogue fits inside a tile's main loop */
 } cf_cost;
 

@@ -286,7 +286,8 @@ def test_column_axis_rules(lib):
     # counters per strip, each region padded to 256 bytes.
     assert ws_col == 4 * 16 * 128 * 8 + 256      # 4 strips of P^T, 16 tiles along M
     assert ws_row == 32 * 2 * 128 * 8 + 512      # 32 strips of P, 2 tiles along N
-    # The unfused comparison path has no column reductions.
+    # An unknown axis is rejected by the unfused path too.
     dd = epi_desc(LN, axis="col")
+    dd.axis = 5
     assert lib.cf_unfused_gemm_epilogue(ctypes.byref(A), ctypes.byref(Bt), 0x40000, 0x50000, 0x60000,
-                                        ctypes.byref(dd), ctypes.byref(O), 0x90000, None) == 2
+                                        ctypes.byref(dd), ctypes.byref(O), 0x90000, None) == 1

@@ -115,3 +115,33 @@ def test_unfused_attention_ragged_keys(cf):
         ref = O.b2bgemm(q, k.T, v, "scale_softmax", 0.125)
         bound = 2.0 ** -7 * (np.abs(O.mid_op(q @ k.T, "scale_softmax", 0.125)) @ np.abs(v)) + 1e-6
         assert np.all(np.abs(got[h] - ref) <= bound)
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+@pytest.mark.parametrize("M,N", [(512, 256), (1000, 200), (4104, 64)])
+@pytest.mark.parametrize("prog", ["layernorm", "rmsnorm", "softmax", "chained"])
+def test_unfused_column_reductions(cf, prog, M, N, b_trans):
+    # The unfused column path: cuBLASLt GEMM, then one CTA per 32 columns
+    # (ragged N, long columns, either B layout, chained stages).
+    ops = {"layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("residual",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.5), ("softmax",)],
+           "chained": [("bias",), ("layernorm", 1e-5), ("gelu_tanh",), ("rmsnorm", 1e-6)]}[prog]
+    case = I.gemm_epilogue_case("col_unfused", M, N, 128, ops, seed=M + N, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    rng = np.random.default_rng(M)
+    R = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to(torch.bfloat16)
+    g0 = torch.from_numpy((1 + 0.3 * rng.standard_normal(N)).astype(np.float32))
+    b0 = torch.from_numpy((0.3 * rng.standard_normal(N)).astype(np.float32))
+    B = case.B.t().contiguous() if b_trans else case.B
+    vec = [None if t is None else t.cuda() for t in (case.bias, case.gamma, case.beta)]
+    kw = {"stage0_gamma": g0.cuda(), "stage0_beta": b0.cuda()} if prog == "chained" else {}
+    out = cf.cf_unfused_gemm_epilogue(case.A.cuda(), B.cuda(), case.ops, *vec, b_trans=b_trans, axis="col",
+                                      residual=R.cuda() if prog == "rmsnorm" else None, **kw)
+    torch.cuda.synchronize()
+    ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
+                          I.to_f64(case.beta), residual=I.to_f64(R) if prog == "rmsnorm" else None,
+                          stage0_gamma=I.to_f64(g0) if prog == "chained" else None,
+                          stage0_beta=I.to_f64(b0) if prog == "chained" else None, axis="col")
+    assert_rows_close(np.ascontiguousarray(out.cpu().numpy().T), np.ascontiguousarray(ref.T),
+                      what=f"unfused columns {prog} {M}x{N}")
