@@ -56,6 +56,12 @@ NCU_TRAFFIC = {
 }
 
 
+def percentile(xs, q: float) -> float:
+    """Nearest-rank percentile (q in [0, 1]) of a non-empty list."""
+    v = sorted(xs)
+    return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+
+
 def kernel_source_hash(b2b: bool) -> str:
     """Hash of the sources of the fused kernel family a workload runs."""
     h = hashlib.sha256()
@@ -605,6 +611,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step_dist": {"p10": percentile(ms, 0.1), "median": statistics.median(ms), "p90": percentile(ms, 0.9),
+                             "mean": statistics.mean(ms), "rank": rank},
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**wl.config(), "l2": "flushed between timed steps (256 MB write)", "launch": launch_mode,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
