@@ -262,7 +262,11 @@ CF_API cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_ma
  * writes P (M x N fp32) to `intermediate`, then a separate row-epilogue
  * kernel reads it back and writes `out`.  Same program semantics as
  * cf_gemm_epilogue (row or column reductions), fp32 `out` only.
- * `intermediate` is caller-owned device memory of M * N * 4 bytes.
+ * `intermediate` is caller-owned device memory of M * N * 4 bytes.  Column
+ * reductions (N <= 65536) keep per-chunk statistics in a static device array
+ * of the library (6 MB + 0.5 MB per device, held until the process exits):
+ * column calls whose executions overlap on the GPU race on it and must be
+ * serialised by the caller.
  */
 CF_API cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matrix* B,
                                    const float* bias, const float* gamma, const float* beta,
