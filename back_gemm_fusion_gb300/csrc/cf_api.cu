@@ -27,8 +27,7 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   unsigned* status = nullptr;
-  // Indexed by the kernel variant's row code (row_code(first, last row op)).
-  // Indexed [row code][kernel variant][...].
+  // Indexed [row code (row_code(first, last row op))][kernel variant][...].
   bool prepared[kRowCodes][kNumVariants][3][2] = {};
   int max_clusters[kRowCodes][kNumVariants][kMaxClusterCtas + 1] = {};  // resident clusters per size (-1: none fit)
   int max_pairs[kRowCodes][kNumVariants][3] = {};                        // resident 2-CTA clusters per xmode

@@ -78,12 +78,14 @@ typedef struct {
 } cf_matrix;
 
 /* Epilogue operations.  Elementwise ops (kind < 16) are applied in order to
- * every element of P = A.B; row reductions (kind >= 16) are stage
- * boundaries.  A program has at most two reductions, and if it has any it
- * ends with one: [elementwise...] [R0 [elementwise...]] R1.  A first
- * reduction R0 (descriptor version 2) must be LayerNorm or RMSNorm; its
- * affine vectors are stage0_gamma / stage0_beta, the last reduction's are the
- * gamma / beta arguments. */
+ * every element of P = A.B; reductions (kind >= 16) are stage boundaries,
+ * along each row (over n) or, with descriptor version 3 and CF_AXIS_COLS,
+ * down each column (over m; the formulas below then reduce over m and the
+ * vectors stay indexed by n).  A program has at most two reductions, and if
+ * it has any it ends with one: [elementwise...] [R0 [elementwise...]] R1.  A
+ * first reduction R0 (descriptor version 2) must be LayerNorm or RMSNorm;
+ * its affine vectors are stage0_gamma / stage0_beta, the last reduction's
+ * are the gamma / beta arguments. */
 typedef enum {
   CF_OP_BIAS = 1,            /* x += bias[n]                                        */
   CF_OP_SCALE = 2,           /* x *= scalar                                         */
@@ -119,7 +121,8 @@ typedef enum {
 /* A tiny epilogue program: a linear chain of ops (the Stage-Stream model with
  * one trailing reduction stage). */
 typedef struct {
-  uint32_t version;  /* 1 or 2 (CF_EPI_VERSION); version 1 ends after `exchange` */
+  uint32_t version;  /* 1, 2 or 3 (CF_EPI_VERSION); version 1 ends after `exchange`,
+                        version 2 after `stage0_beta` */
   uint32_t n_ops;    /* 0..CF_EPI_MAX_OPS */
   cf_op ops[CF_EPI_MAX_OPS];
   int32_t out_dtype; /* cf_dtype of `out`: CF_FP32, or CF_BF16 (each value
