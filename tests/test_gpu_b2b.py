@@ -9,7 +9,7 @@ import torch
 
 from oracle import cf_oracle as O
 from back_gemm_fusion_gb300 import inputs as I
-from tests.parity import assert_rows_close, sample_rows
+from tests.parity import sample_rows
 
 pytestmark = pytest.mark.gpu
 

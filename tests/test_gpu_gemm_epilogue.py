@@ -1,6 +1,5 @@
 """GPU parity: fused GEMM + epilogue (cf_gemm_epilogue through the C ABI)
 against the float64 oracle on the same seeded bf16/fp32 inputs."""
-import math
 
 import numpy as np
 import pytest

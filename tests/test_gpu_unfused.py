@@ -1,7 +1,6 @@
 """GPU parity of the unfused comparison path (cuBLASLt GEMM -> HBM
 intermediate -> separate epilogue / mid-op kernel), so the fused-vs-unfused
 numbers compare two correct implementations."""
-import math
 
 import numpy as np
 import pytest

@@ -5,7 +5,6 @@ partial row statistics from the library's own static device array instead
 of a caller workspace.  This file is collected last on purpose."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
