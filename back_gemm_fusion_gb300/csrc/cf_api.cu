@@ -442,15 +442,16 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   // loads its A rows and half of the B tile, halving per-SM shared-memory
   // traffic per MMA.  Needs an even number of strips; the cluster (DSMEM)
   // exchange keeps 1-CTA tiles.
-  const bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
-  if (p.b_mn_major)
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.kN, sh.K, KB->ld * 2, 64, kBK);
-  else
-    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.K, sh.kN, KB->ld * 2, kBK,
-                  want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
-  if (s != CF_OK) return s;
+  //
+  // The workspace exchange makes every tile of a strip (pair) wait for all of
+  // its strip-mates, and each worker (a CTA pair, or a CTA) holds two tiles at
+  // a time (two TMEM accumulators), so a strip's tiles must fit in twice the
+  // resident workers; otherwise its last tiles could never start.  Strips too
+  // wide for the pairs run on 1-CTA tiles (twice the workers); wider still
+  // they are refused below.
+  bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
+  int maxp = 0;
   if (want_pair) {
-    int maxp = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
       int& cached = dev->max_pairs[code][variant][xmode];
@@ -464,7 +465,17 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
       }
       maxp = cached > 0 ? cached : 0;
     }
-    if (maxp <= 0) return CF_ERR_CUDA;  // the B box was encoded for pair mode
+    const int64_t pair_items = strips / 2 * tiles_n;
+    const int64_t pairs = pair_items < maxp ? pair_items : maxp;
+    if (maxp <= 0 || (xmode == X_GLOBAL && tiles_n > 2 * pairs)) want_pair = false;
+  }
+  if (p.b_mn_major)
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.kN, sh.K, KB->ld * 2, 64, kBK);
+  else
+    s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.K, sh.kN, KB->ld * 2, kBK,
+                  want_pair ? kBN / 2 : kBN);  // pair mode: each CTA loads 128 of the 256 N rows
+  if (s != CF_OK) return s;
+  if (want_pair) {
     p.pair = 1;
     p.pair_items = (int)(strips / 2 * tiles_n);
     L.grid = 2 * (p.pair_items < maxp ? p.pair_items : maxp);
@@ -481,6 +492,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     const int64_t cap = (int64_t)per_sm * dev->sms;
     L.grid = (int)(p.num_items < cap ? p.num_items : cap);
     L.cluster = 1;
+    if (xmode == X_GLOBAL && tiles_n > 2 * (int64_t)L.grid) return CF_ERR_UNSUPPORTED_SHAPE;  // see above
   }
   if (xmode == X_GLOBAL) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);

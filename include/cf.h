@@ -168,7 +168,11 @@ typedef struct {
  * columns past N stay out of the row statistics and are not stored), K % 8
  * == 0 with K >= 64 (a ragged last 64-wide K block reads zeros), all
  * pointers and leading dims 16-byte aligned; the cluster exchange takes rows
- * of at most 16 tiles (N <= 4096).  Violations return CF_ERR_UNSUPPORTED_SHAPE /
+ * of at most 16 tiles (N <= 4096).  Through the workspace every tile of a
+ * row strip waits for its strip-mates and each resident CTA holds two tiles,
+ * so a row may span at most twice the resident CTAs: N <= 77,824 on a
+ * 152-SM GB300 (CTA pairs up to N <= 38,912, wider rows on 1-CTA tiles);
+ * wider rows return CF_ERR_UNSUPPORTED_SHAPE.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
  * CF_ERR_MISALIGNED without launching anything.  M == 0 or N == 0 returns
  * CF_OK without launching.
  */
