@@ -998,6 +998,9 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols, batch = d->batch;
   if (W1->rows != K || W2->rows != N1 || out->rows != M || out->cols != N2) return CF_ERR_INVALID_ARG;
   if (d->strideA < 0 || d->strideW1 < 0 || d->strideW2 < 0 || d->strideOut < 0) return CF_ERR_INVALID_ARG;
+  // Inputs may overlap between batch entries (they are only read); outputs
+  // must not, or the entries' stores would race.
+  if (batch > 1 && M > 0 && d->strideOut < (M - 1) * out->ld + N2) return CF_ERR_INVALID_ARG;
   if (batch > 1 && ((d->strideA * 2) % 16 || (d->strideW1 * 2) % 16 || (d->strideW2 * 2) % 16 ||
                     (d->strideOut * out_elem) % 16))
     return CF_ERR_MISALIGNED;

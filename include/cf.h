@@ -235,7 +235,9 @@ typedef struct {
                         nearest even from the fp32 accumulator; cf_b2bgemm
                         only) */
   int64_t batch;     /* number of independent problems (>= 1) */
-  int64_t strideA, strideW1, strideW2, strideOut; /* elements between problems */
+  int64_t strideA, strideW1, strideW2, strideOut; /* elements between problems; inputs may
+                                                     overlap (read only), outputs must not:
+                                                     strideOut >= (M - 1) * ld + N2 */
 } cf_b2b_desc;
 
 /*

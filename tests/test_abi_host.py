@@ -291,3 +291,21 @@ def test_column_axis_rules(lib):
     dd.axis = 5
     assert lib.cf_unfused_gemm_epilogue(ctypes.byref(A), ctypes.byref(Bt), 0x40000, 0x50000, 0x60000,
                                         ctypes.byref(dd), ctypes.byref(O), 0x90000, None) == 1
+
+
+def test_b2b_batch_output_must_not_overlap(lib):
+    from back_gemm_fusion_gb300.binding import cf_matrix, b2b_desc, CF_FP32, CF_BF16
+    Q = cf_matrix(0x10000, CF_BF16, 0, 256, 128, 128)
+    K = cf_matrix(0x20000, CF_BF16, 1, 128, 512, 128)
+    V = cf_matrix(0x30000, CF_BF16, 0, 512, 128, 128)
+    O = cf_matrix(0x40000, CF_FP32, 0, 256, 128, 128)
+
+    def call(stride_out, stride_in=256 * 128):
+        d = b2b_desc("scale_softmax", 0.125, 4, strides=(stride_in, 512 * 128, 512 * 128, stride_out))
+        return lib.cf_b2bgemm(ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V), ctypes.byref(d),
+                              ctypes.byref(O), None)
+
+    assert call(256 * 128) in (0, 4, 8)          # contiguous batch of outputs
+    assert call(0) == 1                           # every entry writes the same output
+    assert call(255 * 128) == 1                   # entries overlap by one row
+    assert call(256 * 128, stride_in=0) in (0, 4, 8)  # a broadcast input is fine
