@@ -92,3 +92,8 @@ def test_monotonic_and_device_overrides(lib):
     assert fast["fused_us"] < base["fused_us"]
     with pytest.raises(B.CFError):               # K below one 64-wide block
         B.cf_cost_gemm_epilogue(256, 256, 56, LN)
+    # Rows up to twice the resident CTAs in tiles (304 x 256 = 77,824) are
+    # accepted, wider ones refused like the fused call refuses them.
+    assert B.cf_cost_gemm_epilogue(1024, 77824, 256, SOFTMAX)["fused_us"] > 0
+    with pytest.raises(B.CFError):
+        B.cf_cost_gemm_epilogue(1024, 77824 + 256, 256, SOFTMAX)
