@@ -717,6 +717,9 @@ extern "C" cf_status cf_unfused_gemm_epilogue(const cf_matrix* A, const cf_matri
       if (epi->version < 2 || !r.ptr || r.trans || r.rows != M || r.cols != N || r.ld < N ||
           (r.dtype != CF_FP32 && r.dtype != CF_BF16))
         return CF_ERR_INVALID_ARG;
+      // The row kernels read the residual with vector loads (same rule as
+      // the fused call).
+      if (!aligned16(r.ptr) || (r.ld * (r.dtype == CF_FP32 ? 4 : 2)) % 16 != 0) return CF_ERR_MISALIGNED;
       rv.ptr = r.ptr;
       rv.ld = r.ld;
       rv.bf16 = r.dtype == CF_BF16;
@@ -815,7 +818,7 @@ extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1,
   if (s != CF_OK) return s;
   __nv_bfloat16* pb = static_cast<__nv_bfloat16*>(p_buf);
   const unsigned rows = (unsigned)(M * batch);
-  switch (N1 % 1024 == 0 && aligned16(p_buf) ? N1 / 1024 : 0) {
+  switch (N1 % 1024 == 0 && aligned16(p_buf) && aligned16(s_buf) ? N1 / 1024 : 0) {
     case 1: mid_op_reg_kernel<1><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
     case 2: mid_op_reg_kernel<2><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;
     case 4: mid_op_reg_kernel<4><<<rows, 256, 0, st>>>(s_buf, pb, (int)N1, d->mid_op, d->mid_scale); break;

@@ -309,3 +309,17 @@ def test_b2b_batch_output_must_not_overlap(lib):
     assert call(0) == 1                           # every entry writes the same output
     assert call(255 * 128) == 1                   # entries overlap by one row
     assert call(256 * 128, stride_in=0) in (0, 4, 8)  # a broadcast input is fine
+
+
+def test_unfused_residual_alignment(lib):
+    # The unfused row kernels read the residual with vector loads: the same
+    # alignment rule as the fused call, checked before anything is enqueued.
+    from back_gemm_fusion_gb300.binding import cf_matrix, epi_desc, CF_FP32, CF_BF16
+    A, B, O = _mats()
+    d = epi_desc([("bias",), ("residual",), ("layernorm", 1e-5)])
+    d.residual = cf_matrix(0x70008, CF_FP32, 0, 256, 256, 256)      # misaligned pointer
+    assert lib.cf_unfused_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000,
+                                        ctypes.byref(d), ctypes.byref(O), 0x90000, None) == 3
+    d.residual = cf_matrix(0x70000, CF_BF16, 0, 256, 256, 260)      # 520-byte rows
+    assert lib.cf_unfused_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000,
+                                        ctypes.byref(d), ctypes.byref(O), 0x90000, None) == 3

@@ -32,6 +32,6 @@ def test_two_rank_replica_plumbing():
     if torch.cuda.is_available():
         pytest.skip("CPU (gloo) test")
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork after threads exist
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] == out[1] == 2.5
