@@ -46,6 +46,46 @@ def test_hand_example_epilogues():
         np.testing.assert_allclose(got[: exp.shape[0]], exp, rtol=0, atol=1e-12, err_msg=key)
 
 
+def test_hand_example_bias_and_scale():
+    # Bias along the column index and a non-power-of-two scale: exact dyadic
+    # values written by hand.  The square 4 x 4 product makes a bias indexed
+    # by the row broadcast silently instead of failing, so it must fail here.
+    h = _hand()
+    A = np.array(h["A"], float)
+    B = np.array(h["B"], float)
+    bias = np.array(h["bias"], float)
+    assert O.gemm_epilogue(A, B, [("bias",)], bias=bias).tolist() == h["P_plus_bias"]
+    A_sq = np.array(h["A_sq"], float)
+    assert O.matmul(A_sq, B).tolist() == h["P_sq"]
+    assert O.gemm_epilogue(A_sq, B, [("bias",)], bias=bias).tolist() == h["P_sq_plus_bias"]
+    assert O.gemm_epilogue(A, B, [("scale", h["scale"])]).tolist() == h["P_times_scale"]
+    # Bias then LayerNorm, scale then softmax: closed forms in the golden file.
+    for key, ops in (("bias_layernorm_eps0", [("bias",), ("layernorm", 0.0)]),
+                     ("scale_softmax", [("scale", h["scale"]), ("softmax",)])):
+        exp = np.array([[_closed(v) for v in row] for row in h[key]], float)
+        got = O.gemm_epilogue(A, B, ops, bias=bias, gamma=np.ones(4), beta=np.zeros(4))
+        np.testing.assert_allclose(got, exp, rtol=0, atol=1e-12, err_msg=key)
+
+
+def test_bias_scale_brute_force_fraction():
+    # Exact rational evaluation of (P + bias[n]) * s on a small non-square
+    # shape with dyadic inputs: every value is exact in float64.
+    rng = np.random.default_rng(11)
+    M, K, N = 5, 4, 6
+    A = rng.integers(-9, 10, (M, K)) / 4.0
+    B = rng.integers(-9, 10, (K, N)) / 8.0
+    bias = rng.integers(-9, 10, N) / 2.0
+    s = Fraction(3, 8)
+    P = _frac_matmul(A.tolist(), B.tolist())
+    exact = [[(P[m][n] + Fraction(bias[n])) * s for n in range(N)] for m in range(M)]
+    got = O.gemm_epilogue(A, B, [("bias",), ("scale", float(s))], bias=bias)
+    assert got.tolist() == [[float(v) for v in row] for row in exact]
+    # Node order matters: scaling first leaves the bias unscaled.
+    exact2 = [[P[m][n] * s + Fraction(bias[n]) for n in range(N)] for m in range(M)]
+    got2 = O.gemm_epilogue(A, B, [("scale", float(s)), ("bias",)], bias=bias)
+    assert got2.tolist() == [[float(v) for v in row] for row in exact2]
+
+
 def test_hand_example_b2b_relu_exact():
     h = _hand()
     O_ = O.b2bgemm(np.array(h["A"], float), np.array(h["B"], float),
@@ -241,6 +281,13 @@ def test_epilogues_match_torch_float64():
     np.testing.assert_allclose(O.elementwise(x, "gelu_tanh"),
                                F.gelu(tx, approximate="tanh").numpy(), rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(O.elementwise(x, "relu"), F.relu(tx).numpy(), atol=0)
+    # Bias along the last (column) dimension, as torch broadcasts a vector;
+    # a scale by a non-power-of-two multiplies.
+    np.testing.assert_allclose(O.elementwise(x, "bias", bias=b), torch.add(tx, tb).numpy(), rtol=0, atol=0)
+    np.testing.assert_allclose(O.elementwise(x, "scale", 0.3), torch.mul(tx, 0.3).numpy(), rtol=0, atol=0)
+    sq = x[:, :31]
+    np.testing.assert_allclose(O.elementwise(sq, "bias", bias=b[:31]), torch.add(tx[:, :31], tb[:31]).numpy(),
+                               rtol=0, atol=0)
 
 
 def test_attention_unrounded_matches_sdpa():
@@ -396,6 +443,18 @@ def test_bf16_round_matches_torch_on_float32_values():
 
 
 # ------------------------------------------------------------- planted mistakes
+_ORIG_ELEMENTWISE = O.elementwise
+
+
+def _wrap_elementwise(which, bad):
+    """The oracle's elementwise node with one op replaced by a planted mistake."""
+    def f(x, op, scalar=0.0, bias=None, residual=None):
+        if op == which:
+            return bad(np.asarray(x, float), scalar, bias)
+        return _ORIG_ELEMENTWISE(x, op, scalar, bias, residual)
+    return f
+
+
 def test_oracle_mutations_are_caught(monkeypatch):
     """Plant plausible mistakes in the oracle and check that a pin fails."""
     mutations = {
@@ -419,12 +478,17 @@ def test_oracle_mutations_are_caught(monkeypatch):
             + np.resize(b, (x.shape[0], 1)))),
         "col_rmsnorm_unbiased": ("col_rmsnorm", lambda x, g, eps: (
             np.asarray(g)[None] * x / np.sqrt((x * x).sum(0, keepdims=True) / (x.shape[0] - 1) + eps))),
+        "bias_by_row": ("elementwise", _wrap_elementwise(
+            "bias", lambda x, scalar, bias: x + np.resize(np.asarray(bias, float), (x.shape[0], 1)))),
+        "scale_divides": ("elementwise", _wrap_elementwise("scale", lambda x, scalar, bias: x / float(scalar))),
+        "bias_dropped": ("elementwise", _wrap_elementwise("bias", lambda x, scalar, bias: x)),
     }
     checks = [test_hand_example_epilogues, test_layernorm_eps_inside_root_closed_form,
               test_rmsnorm_mean_square_one_and_scale_invariance, test_epilogues_match_torch_float64,
               test_softmax_rows_sum_to_one, test_hand_example_gemm_exact,
               test_matmul_brute_force_fraction, test_b2b_relu_brute_force_with_library_rounding,
-              test_bf16_round_matches_torch_on_float32_values, test_hand_example_column_reductions]
+              test_bf16_round_matches_torch_on_float32_values, test_hand_example_column_reductions,
+              test_hand_example_bias_and_scale]
     for name, (attr, bad) in mutations.items():
         with monkeypatch.context() as mp:
             mp.setattr(O, attr, bad)
