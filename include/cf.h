@@ -32,8 +32,17 @@
  *   - There is no CPU fallback: without an sm_103 device every compute entry
  *     point returns CF_ERR_UNSUPPORTED_DEVICE (or CF_ERR_NO_DEVICE).
  *   - Entry points are thread-safe for distinct streams; tensor-map encoding
- *     is done per call on the host (no global mutable state beyond a
- *     per-device attribute cache).
+ *     is done per call on the host.  Host-side state: a per-device cache
+ *     (device properties, kernel attributes, occupancy answers and the
+ *     device addresses of the library's __device__ variables).  Device-side
+ *     state: the status word (all entry points), the 4 MiB scratch array of
+ *     cf_gemm_epilogue_noalloc, and the per-chunk statistics arrays of the
+ *     unfused column path; each of the last two is shared by every call of
+ *     its entry point (see there).
+ *   - The cache assumes a device's context lives as long as the process:
+ *     after cudaDeviceReset() on a device, the library must not be used on
+ *     that device again in the same process (its cached device addresses
+ *     would point into the destroyed context).
  */
 #ifndef CF_GB300_H
 #define CF_GB300_H
@@ -56,7 +65,7 @@ extern "C" {
 typedef enum {
   CF_OK = 0,
   CF_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, inconsistent dims     */
-  CF_ERR_UNSUPPORTED_SHAPE = 2,  /* dims not multiples of the tile sizes listed  */
+  CF_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside a call's shape rules (below)   */
   CF_ERR_MISALIGNED = 3,         /* pointer or leading dim not 16-byte aligned   */
   CF_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
   CF_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed            */
@@ -118,8 +127,9 @@ typedef enum {
   CF_XCHG_GLOBAL = 2   /* force per-tile partial statistics through the workspace    */
 } cf_exchange;
 
-/* A tiny epilogue program: a linear chain of ops (the Stage-Stream model with
- * one trailing reduction stage). */
+/* A tiny epilogue program: a linear chain of ops (the Stage-Stream model:
+ * elementwise nodes, then up to two reduction stages, the last one ending
+ * the program; see cf_op_kind). */
 typedef struct {
   uint32_t version;  /* 1, 2 or 3 (CF_EPI_VERSION); version 1 ends after `exchange`,
                         version 2 after `stage0_beta` */
@@ -150,6 +160,14 @@ typedef struct {
 
 /*
  * cf_gemm_epilogue -- out = epilogue(A . B), fused in one kernel.
+ *
+ * Passages: the Stage-Stream Execution Model (ComFuse review, "What carries
+ * the argument": accumulator tiles stream on chip through elementwise nodes,
+ * each reduction is a stage boundary aggregated hierarchically) and the
+ * tile-strip locality of a row reduction (referee report, major comment 1
+ * [Sec. III, Eq. (1)]: a row depends only on its strip {T_{m,n}}_n, and a
+ * strip wider than one cluster needs a multi-cluster fallback; column
+ * reductions use the complementary strip).
  *
  *   A    : M x K, bf16, trans == 0 (K contiguous).
  *   B    : K x N, bf16; trans == 0 (stored K x N, N contiguous) or
@@ -203,8 +221,10 @@ CF_API size_t cf_workspace_size(const cf_matrix* A, const cf_matrix* B, const cf
  *
  * Arguments and results are those of cf_gemm_epilogue without the workspace.
  * Problems needing more scratch than the array holds (cf_workspace_size >
- * CF_NOALLOC_WORKSPACE_BYTES, i.e. roughly M * N > 2^27 with a row op)
- * return CF_ERR_WORKSPACE and enqueue nothing.
+ * CF_NOALLOC_WORKSPACE_BYTES: roughly M * N > 2^27 with one reduction
+ * stage, M * N > 2^26 with two chained stages, which need one statistics
+ * region each; cf_workspace_size is the exact test) return
+ * CF_ERR_WORKSPACE and enqueue nothing.
  *
  * Sharing: all calls in the process share the one array per device, which
  * keeps the last call's contents; each call clears the part that must start
@@ -243,6 +263,13 @@ typedef struct {
 /*
  * cf_b2bgemm -- out = bf16_rne(F(A . W1)) . W2 per batch entry, fused: the
  * intermediate S' never reaches global memory.
+ *
+ * Passages: the B2BGEMM schedule (ComFuse review, "What carries the
+ * argument": the post-processed intermediate tile stays on chip and the
+ * second GEMM's output accumulation is distributed across the cluster) and
+ * referee report, major comment 2 [Sec. IV-A, Eqs. (3)-(5)] (S = A W1, the
+ * tile transform F, O accumulated over the set C of co-scheduled CTAs, with
+ * partial results aggregated across C).
  *
  *   A   : M x K bf16, trans == 0.
  *   W1  : K x N1 bf16; trans == 0 (stored K x N1) or trans == 1 (stored

@@ -61,7 +61,9 @@ def test_layernorm_256(cf, b_trans):
 
 @pytest.mark.parametrize("b_trans", [False, True])
 def test_layernorm_pairs_wide(cf, b_trans):
-    # 32 tiles per row with an even number of strips: 2-CTA pairs multicast B.
+    # 32 tiles per row with an even number of strips: CTA pairs run 256 x 256
+    # tiles, each CTA of a pair loading its own half of the B tile
+    # (cta_group::2 MMAs read both halves).
     case = I.gemm_epilogue_case("ln_wide", 256, 8192, 128, [("bias",), ("layernorm", 1e-5)], seed=9,
                                 need_bias=True, need_gamma=True, need_beta=True)
     assert_rows_close(_run(cf, case, b_trans), _oracle(case), what="layernorm 32 tiles, pairs")
@@ -196,17 +198,40 @@ def test_chained_reductions_unfused(cf, chain, N):
 
 @pytest.mark.parametrize("N", [4096, 4352, 8192])
 def test_softmax_wide_rows(cf, N):
-    # 16 tiles: cluster of 16; 17 tiles: wider than a cluster -> workspace path;
-    # 32 tiles: workspace path with 2-CTA pairs sharing B.
+    # AUTO picks the workspace exchange at all three widths on a 152-SM GB300:
+    # 16 tiles (only 7 clusters of 16 CTAs are resident, too few to fill the
+    # GPU), 17 tiles (wider than a cluster), 32 tiles (CTA pairs).  The forced
+    # 16-CTA cluster exchange is tested below.
     case = I.gemm_epilogue_case("sm", 256, N, 128, [("scale", 0.25), ("softmax",)], seed=5)
     assert_rows_close(_run(cf, case), _oracle(case), what=f"softmax N={N}")
 
 
-def test_gelu_rmsnorm_full_size_sampled(cf):
+@pytest.mark.parametrize("b_trans", [False, True])
+@pytest.mark.parametrize("rowop", ["layernorm", "rmsnorm", "softmax"])
+def test_cluster_exchange_16_ctas(cf, rowop, b_trans):
+    # N = 4096 with the DSMEM exchange forced: 16 tiles per row, one
+    # non-portable 16-CTA cluster per row strip (AUTO does not pick it on a
+    # 152-SM GB300, where only 7 such clusters are resident at once).  Three
+    # strips: the persistent clusters take more than one strip when fewer
+    # are resident.
+    ops = {"layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.25), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case("cluster16", 384, 4096, 128, ops, seed=16, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, b_trans, exchange="cluster"), _oracle(case),
+                      what=f"{rowop} N=4096 16-CTA cluster b_trans={b_trans}")
+
+
+@pytest.mark.parametrize("exchange", ["auto", "cluster"])
+def test_gelu_rmsnorm_full_size_sampled(cf, exchange):
+    # The GELU + RMSNorm workload at full size with AUTO (workspace exchange,
+    # CTA pairs) and with the 16-CTA DSMEM exchange forced (64 strips over the
+    # resident 16-CTA clusters).
     case = I.gelu_rmsnorm()
-    gpu = _run(cf, case)
+    gpu = _run(cf, case, exchange=exchange)
     rows = sample_rows(case.M)
-    assert_rows_close(gpu[rows], _oracle(case, rows), what="gemm+bias+gelu+rmsnorm 8192x4096x4096")
+    assert_rows_close(gpu[rows], _oracle(case, rows), what=f"gemm+bias+gelu+rmsnorm 8192x4096x4096 {exchange}")
 
 
 def test_scaled_softmax_full_size_sampled(cf):
