@@ -4,8 +4,13 @@
 
 A step is one call of the fused kernel over one batch of synthetic inputs
 that are already resident in HBM; L2 is flushed (a 256 MB write) between
-timed steps.  The default workload is GEMM + bias + tanh-GELU + row RMSNorm
-at M=8192, N=4096, K=4096.  Rank 0 prints ONE JSON line.
+timed steps.  The default workload, the one on the top level of the line, is
+the largest configuration: the attention-shaped B2BGEMM (32 x 16 heads,
+L = 2048, d = 128, softmax).  The line's ``configs`` object carries every
+other configuration of the metric measured in the same run (GEMM + bias +
+LayerNorm 256^3, GEMM + bias + tanh-GELU + RMSNorm 8192x4096x4096, the
+scaled-softmax logit head 4096x16384x4096, the MLP B2BGEMM and the ReLU
+attention variant), each with the same fields.  Rank 0 prints ONE JSON line.
 
 ``--impl reference`` times the float64 CPU oracle (the reference arm of this
 build, a deliberately slow plain implementation) on the host cores instead.
@@ -52,6 +57,15 @@ NCU_TRAFFIC = {
     "postnorm_layernorm": {"read": 200069376, "write": 93125120, "src": "80d4303150507d8f"},
     "scaled_softmax": {"read": 1385517312, "write": 238905088, "src": "80d4303150507d8f"},
     "target_attention": {"read": 15000832, "write": 0, "src": "e3aaae959dc1d804"},
+}
+
+
+# Global store bytes of one fused launch, from the L2-side store counters
+# (`ncu --metrics l1tex__m_l1tex2xbar_write_bytes_mem_global_op_tma_st.sum,
+# l1tex__m_l1tex2xbar_write_bytes_mem_lg_op_st.sum,...` on the fused kernel,
+# fp32 output): the sum over TMA stores, plain global stores, reductions and
+# atomics.  Keyed and validated like NCU_TRAFFIC.
+NCU_STORES = {
 }
 
 
@@ -430,18 +444,18 @@ def run_reference(args, wl: Workload, dist, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, wl: Workload, dist, rank, world, local):
-    import back_gemm_fusion_gb300 as cf
-    from back_gemm_fusion_gb300 import build
-    build.build()
-    cf.load_library()
-    peaks = load_peaks()
+def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int, warmup: int,
+            cpu_seconds: float, variants: bool = True):
+    """Time one workload: the fused call (CUDA events over `steps` steps, L2
+    flushed between them), the unfused path and the other exchanges in the
+    same run, the end-to-end call with host buffers, and the oracle on a
+    bounded host sample.  Returns the per-workload record (rank 0)."""
     dev = wl.to_device()
     stream = torch.cuda.current_stream()
     workspace = None
     if not wl.is_b2b:
         c = wl.case
-        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops, exchange=args.exchange, b_trans=wl.axis == "col",
+        need = cf.cf_workspace_size(dev["A"], dev["B"], c.ops, exchange=wl.exchange, b_trans=wl.axis == "col",
                                     axis=wl.axis)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
@@ -450,26 +464,17 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     def step():
         wl.fused_step(cf, dev, stream, workspace)
 
-    if args.once:
-        # One fused launch and nothing else (for a profiler's kernel filter).
-        step()
-        torch.cuda.synchronize()
-        st = cf.cf_last_device_status()
-        print(json.dumps({"workload": wl.name, "once": True, "device_status": st}), flush=True)
-        if st != 0:
-            raise RuntimeError("device status reports a timeout")
-        return
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.fill_(1.0)
         step()
     torch.cuda.synchronize()
     if cf.cf_last_device_status() != 0:
-        raise RuntimeError("device status reports a timeout after warm-up")
+        raise RuntimeError(f"{wl.name}: device status reports a timeout after warm-up")
     # Other row-statistics exchanges of the same fused kernel, same run.
-    variants = {}
-    if not wl.is_b2b and any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in wl.case.ops):
+    xvar = {}
+    if variants and not wl.is_b2b and any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in wl.case.ops):
         for xch in ("cluster", "global"):
-            if xch == args.exchange:
+            if xch == wl.exchange:
                 continue
             try:
                 wv = Workload.__new__(Workload)
@@ -484,7 +489,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
                     wv.fused_step(cf, dev, stream, ws)
                 torch.cuda.synchronize()
                 vm = []
-                for k in range(max(3, args.steps)):
+                for k in range(max(3, steps)):
                     flush.fill_(float(k))
                     s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     s0.record(stream)
@@ -493,9 +498,9 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
                     torch.cuda.synchronize()
                     vm.append(s0.elapsed_time(e0))
                 v = statistics.mean(vm)
-                variants[xch] = {"ms_per_step": v, "tflops": wl.flops / (v * 1e-3) / 1e12}
+                xvar[xch] = {"ms_per_step": v, "tflops": wl.flops / (v * 1e-3) / 1e12}
             except Exception as exc:
-                variants[xch] = {"error": str(exc)[:200]}
+                xvar[xch] = {"error": str(exc)[:200]}
 
     # Unfused comparison (cuBLASLt GEMM + separate epilogue kernel), same run.
     unfused = None
@@ -505,7 +510,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
             wl.unfused_step(cf, dev, scratch, stream)
         torch.cuda.synchronize()
         um = []
-        for k in range(max(3, args.steps)):
+        for k in range(max(3, steps)):
             flush.fill_(float(k))
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
@@ -515,7 +520,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
             um.append(s.elapsed_time(e))
         u = statistics.mean(um)
         unfused = {"ms_per_step": u, "tflops": wl.flops / (u * 1e-3) / 1e12,
-                   "path": "cuBLASLt GEMM -> HBM intermediate -> separate epilogue kernel"}
+                   "path": ("cuBLASLt GEMM1 -> HBM S -> mid-op kernel -> HBM bf16 S' -> cuBLASLt GEMM2"
+                            if wl.is_b2b else "cuBLASLt GEMM -> HBM intermediate -> separate epilogue kernel")}
         del scratch
     except Exception as exc:  # the comparison path is optional for the headline
         unfused = {"error": str(exc)[:200]}
@@ -538,13 +544,13 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
             launch_mode = f"direct (graph capture failed: {str(exc)[:120]})"
             torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with ClockSampler(local) as clk, NvmlSampler(torch.cuda.current_device()) as nv:
         barrier(dist)
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        for k in range(args.steps):
+        for k in range(steps):
             flush.fill_(float(k))
             starts[k].record(stream)
             if graph is not None:
@@ -557,13 +563,14 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         t_wall = time.perf_counter() - t_wall
     clocks = nv.summary() or clk.summary()
     if cf.cf_last_device_status() != 0:
-        raise RuntimeError("device status reports a timeout in the timed region")
+        raise RuntimeError(f"{wl.name}: device status reports a timeout in the timed region")
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_step = max_over_ranks(dist, statistics.mean(ms))
     tflops = wl.flops / (ms_step * 1e-3) / 1e12
     value = tflops * world
     if unfused and "ms_per_step" in unfused:
         unfused["fused_speedup"] = unfused["ms_per_step"] / ms_step
+    del graph
 
     # End to end through the public API: pinned host inputs -> device, fused
     # call, device -> pinned host output, all inside the timed region.
@@ -581,7 +588,7 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for _, t in host_in)
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
-    for k in range(max(3, args.steps)):
+    for k in range(max(3, steps)):
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
@@ -594,25 +601,32 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         e2e_ms.append(s.elapsed_time(e))
     e2e_step = max_over_ranks(dist, statistics.mean(e2e_ms))
     e2e_val = wl.flops / (e2e_step * 1e-3) / 1e12 * world
+    if cf.cf_last_device_status() != 0:
+        raise RuntimeError(f"{wl.name}: device status reports a timeout in the end-to-end steps")
+    del dev, workspace, flush, host_in, host_out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     if rank != 0:
-        return
+        return None
     # CPU baseline: the oracle on the host cores, bounded sample.
-    ref_tflops, ref_rows, ref_s = time_oracle(wl, args.cpu_seconds)
+    ref_tflops, ref_rows, ref_s = time_oracle(wl, cpu_seconds)
     t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
     src = kernel_source_hash(wl.is_b2b)
-    tr = NCU_TRAFFIC.get(wl.name) if wl.out_dtype == torch.float32 else None  # counters taken with fp32 out
+    fp32 = wl.out_dtype == torch.float32  # counters taken with fp32 out
+    tr = NCU_TRAFFIC.get(wl.name) if fp32 else None
     tr = tr if tr and tr.get("src") == src else None
     traffic = (tr["read"] + tr["write"]) if tr else None
-    # An intermediate that went to HBM would have to be written there: DRAM
-    # writes beyond the output and the row-statistics workspace.
-    inter = max(0.0, tr["write"] - wl.out_bytes - wl.stat_bytes) if tr else None
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+    # The page's own test: global store bytes of one launch beyond the
+    # output and the row-statistics workspace (an intermediate would have
+    # to be stored), from the L2-side store counters.
+    stc = NCU_STORES.get(wl.name) if fp32 else None
+    stc = stc if stc and stc.get("src") == src else None
+    inter = (stc["stores"] - wl.out_bytes - wl.stat_bytes) if stc else None
+    return {
+        "workload": wl.name, "value": value, "ms_per_step": ms_step, "tflops": tflops,
         "ms_per_step_dist": {"p10": percentile(ms, 0.1), "median": statistics.median(ms), "p90": percentile(ms, 0.9),
                              "mean": statistics.mean(ms), "rank": rank},
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**wl.config(), "l2": "flushed between timed steps (256 MB write)", "launch": launch_mode,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -620,6 +634,8 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
                      "peak_source": f"{peaks['source']} bf16 burst",
                      "roofline_frac": (t_roof * 1e3) / ms_step},
         "intermediate_hbm_bytes": inter,
+        "global_store_bytes": ({"stores": stc["stores"], "output": wl.out_bytes, "row_stats": wl.stat_bytes,
+                                "source": "ncu L2-side store counters, one launch"} if stc else None),
         "dram_bytes": ({"read": tr["read"], "write": tr["write"], "source": "ncu, one launch"} if tr else None),
         "compulsory_bytes": wl.bytes,
         "cpu_baseline": {"value": ref_tflops, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -628,11 +644,80 @@ def run_ours(args, wl: Workload, dist, rank, world, local):
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step},
         "unfused": unfused,
-        "exchange_variants": variants or None,
-        "gpu_launches": args.steps,
+        "exchange_variants": xvar or None,
+        "gpu_launches": steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
         "kernel_src": src,
+    }
+
+
+# The configurations the metric is quoted on, by workload name: the GEMM +
+# bias + LayerNorm latency case, GELU + RMSNorm, the softmax logit head, the
+# MLP B2BGEMM and both attention variants.
+CONFIG_WORKLOADS = ["layernorm_256", "gelu_rmsnorm", "scaled_softmax", "mlp_b2b", "attention_softmax",
+                    "attention_relu"]
+
+
+def run_ours(args, wl: Workload, dist, rank, world, local):
+    import back_gemm_fusion_gb300 as cf
+    from back_gemm_fusion_gb300 import build
+    build.build()
+    cf.load_library()
+    peaks = load_peaks()
+    if args.once:
+        # One fused launch and nothing else (for a profiler's kernel filter).
+        dev = wl.to_device()
+        workspace = None
+        if not wl.is_b2b:
+            need = cf.cf_workspace_size(dev["A"], dev["B"], wl.case.ops, exchange=wl.exchange,
+                                        b_trans=wl.axis == "col", axis=wl.axis)
+            workspace = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+        wl.fused_step(cf, dev, torch.cuda.current_stream(), workspace)
+        torch.cuda.synchronize()
+        st = cf.cf_last_device_status()
+        print(json.dumps({"workload": wl.name, "once": True, "device_status": st}), flush=True)
+        if st != 0:
+            raise RuntimeError("device status reports a timeout")
+        return
+    head = measure(args, wl, cf, peaks, dist, rank, world, local, args.steps, args.warmup, args.cpu_seconds)
+    configs = {}
+    if args.configs == "all":
+        for name in CONFIG_WORKLOADS:
+            if name == wl.name and wl.out_dtype == torch.float32 and wl.exchange == "auto":
+                continue
+            w2 = Workload(name, exchange="auto", rows=args.rows)
+            r = measure(args, w2, cf, peaks, dist, rank, world, local, args.config_steps, 3, args.config_cpu_seconds,
+                        variants=False)
+            del w2
+            if r is not None:
+                configs[name] = {k: r[k] for k in ("value", "ms_per_step", "ms_per_step_dist", "config", "roofline",
+                                                   "intermediate_hbm_bytes", "global_store_bytes", "dram_bytes",
+                                                   "compulsory_bytes", "cpu_baseline", "e2e", "unfused",
+                                                   "gpu_launches", "clocks")}
+                configs[name]["steps"] = args.config_steps
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "ms_per_step_dist": head["ms_per_step_dist"],
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": head["config"],
+        "roofline": head["roofline"],
+        "intermediate_hbm_bytes": head["intermediate_hbm_bytes"],
+        "global_store_bytes": head["global_store_bytes"],
+        "dram_bytes": head["dram_bytes"],
+        "compulsory_bytes": head["compulsory_bytes"],
+        "cpu_baseline": head["cpu_baseline"],
+        "e2e": head["e2e"],
+        "unfused": head["unfused"],
+        "exchange_variants": head["exchange_variants"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
+        "kernel_src": head["kernel_src"],
+        "configs": configs or None,
     }
     print(json.dumps(line), flush=True)
 
@@ -643,7 +728,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gelu_rmsnorm",
+    ap.add_argument("--workload", default="attention_softmax",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
                              "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms",
                              "target_attention", "column_layernorm"])
@@ -657,6 +742,11 @@ def main():
                     help="output dtype of the fused call (the unfused GEMM-epilogue path is fp32-only)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct launches instead of replaying the fused call's CUDA graph")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="also measure every other configuration of the metric (the 'configs' object)")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps per extra configuration")
+    ap.add_argument("--config-cpu-seconds", type=float, default=4.0,
+                    help="oracle sample budget per extra configuration")
     ap.add_argument("--once", action="store_true",
                     help="run the fused kernel of the workload once and exit (profiling captures)")
     args = ap.parse_args()
