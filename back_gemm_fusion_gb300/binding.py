@@ -61,7 +61,8 @@ class cf_cost(ctypes.Structure):
 class cf_b2b_desc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("mid_op", ctypes.c_int32), ("mid_scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int32), ("batch", ctypes.c_int64), ("strideA", ctypes.c_int64),
-                ("strideW1", ctypes.c_int64), ("strideW2", ctypes.c_int64), ("strideOut", ctypes.c_int64)]
+                ("strideW1", ctypes.c_int64), ("strideW2", ctypes.c_int64), ("strideOut", ctypes.c_int64),
+                ("key_split", ctypes.c_int32)]
 
 
 class CFError(RuntimeError):
@@ -238,9 +239,13 @@ def cf_gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence[Tup
     return out
 
 
-def b2b_desc(op: str, scale: float, batch: int, strides=(0, 0, 0, 0), out_dtype: int = CF_FP32) -> cf_b2b_desc:
+def b2b_desc(op: str, scale: float, batch: int, strides=(0, 0, 0, 0), out_dtype: int = CF_FP32,
+             key_split: int = 0) -> cf_b2b_desc:
+    """B2BGEMM descriptor (version 2); ``key_split`` 0 = chosen per shape,
+    1 = off, 2..8 = CTAs per query block (attention shape)."""
     d = cf_b2b_desc()
-    d.version = 1
+    d.version = 2
+    d.key_split = key_split
     d.mid_op = MID_CODES[op]
     d.mid_scale = float(scale)
     d.out_dtype = out_dtype
@@ -263,15 +268,17 @@ def _b2b_views(A, W1, W2, w1_trans, out):
 
 def cf_b2bgemm(A: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, op: str, scale: float = 1.0,
                w1_trans: bool = False, out: Optional[torch.Tensor] = None, stream=None,
-               out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+               out_dtype: torch.dtype = torch.float32, key_split: int = 0) -> torch.Tensor:
     """out = bf16(F(A @ W1)) @ W2, fused; tensors may carry a leading batch
-    dim.  ``out`` is fp32 or bf16 (``out_dtype`` when it is allocated here)."""
+    dim.  ``out`` is fp32 or bf16 (``out_dtype`` when it is allocated here).
+    ``key_split`` (attention shape): 0 = chosen per shape, 1 = one CTA per
+    query block, 2..8 = CTAs of a cluster sharing a block's key range."""
     lib = load_library()
     if out is None:
         shape = A.shape[:-1] + (W2.shape[-1],)
         out = torch.empty(shape, dtype=out_dtype, device=A.device)
     batch, (a, w1, w2, o), strides = _b2b_views(A, W1, W2, w1_trans, out)
-    d = b2b_desc(op, scale, batch, strides, _dtype_code(out))
+    d = b2b_desc(op, scale, batch, strides, _dtype_code(out), key_split)
     st = lib.cf_b2bgemm(ctypes.byref(a), ctypes.byref(w1), ctypes.byref(w2), ctypes.byref(d), ctypes.byref(o),
                         _stream(stream))
     _check(st, "cf_b2bgemm")

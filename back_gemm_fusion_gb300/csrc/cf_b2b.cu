@@ -177,11 +177,13 @@ constexpr int kOffBars = kOffL + 2 * 128 * 8;
 // b (= chunk parity = F group): s_full, s_free (group b holds S_b in
 // registers), p_full, pv_done; then o_full, o_empty, one drain barrier per
 // MMA issuer, running-max hand-off [2 chunk parities][4 quarters], (l, m)
-// hand-off [2 item parities][4 quarters].
+// hand-off [2 item parities][4 quarters]; key split only: the cluster's
+// published row statistics [4 quarters] and staged output rows [4 quarters].
 constexpr int BAR_QF = 0, BAR_QE = 1, BAR_RF1 = 2, BAR_RE1 = BAR_RF1 + kRing1, BAR_RF2 = BAR_RE1 + kRing1,
               BAR_RE2 = BAR_RF2 + kRing2, BAR_SF = BAR_RE2 + kRing2, BAR_SFREE = BAR_SF + 2, BAR_PF = BAR_SFREE + 2,
               BAR_PV = BAR_PF + 2, BAR_OF = BAR_PV + 2, BAR_OE = BAR_OF + 1, BAR_DRAIN1 = BAR_OE + 1,
-              BAR_DRAIN2 = BAR_DRAIN1 + 1, BAR_MB = BAR_DRAIN2 + 1, BAR_XL = BAR_MB + 8, kNumBars = BAR_XL + 8;
+              BAR_DRAIN2 = BAR_DRAIN1 + 1, BAR_MB = BAR_DRAIN2 + 1, BAR_XL = BAR_MB + 8, BAR_MLF = BAR_XL + 8,
+              BAR_STG = BAR_MLF + 4, kNumBars = BAR_STG + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), S'0 [384,448), S'1 [448,512)
@@ -200,9 +202,36 @@ struct Params {
   int n2;            // valid output columns (N2 <= 128)
   int softmax;       // 1: scaled softmax (scale > 0), 0: ReLU (optionally scaled)
   float scale;       // multiplies S before F
+  int split;         // key split: CTAs per query block (the cluster size); 1 without the split
+  int nb_per;        // key split: 128-key chunks per CTA (the last CTA's range may be shorter)
   unsigned* status;
   long long timeout_cycles;
 };
+
+// Four output values of one row at element offset `off`: fp32 (one 16-byte
+// store) or bf16 rounded to nearest even (one 8-byte store); only the first
+// `valid` are stored when the row ends inside them.
+template <bool OBF16>
+__device__ __forceinline__ void store4(void* out, long long off, float4 v, int valid) {
+  if (valid >= 4) {
+    if (OBF16) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + off) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + off) = v;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    if (j < valid) {
+      const float e = j == 0 ? v.x : j == 1 ? v.y : v.z;
+      if (OBF16) static_cast<__nv_bfloat16*>(out)[off + j] = __float2bfloat16_rn(e);
+      else static_cast<float*>(out)[off + j] = e;
+    }
+  }
+}
 
 __device__ __forceinline__ float (&part32(float (&v)[128], int c))[32] {
   return *reinterpret_cast<float(*)[32]>(&v[32 * c]);
@@ -218,7 +247,18 @@ __device__ __forceinline__ float (&part32(float (&v)[128], int c))[32] {
 // Both are compile-time so that the common instantiation (full chunks,
 // fp32 output) carries neither the masking nor a second store path in the F
 // warps, which bound the softmax variant.
-template <bool RAG, bool OBF16>
+//
+// SPLIT: the key range of each query block is split across the CTAs of a
+// thread-block cluster (the co-scheduled CTA set C of the review's Eq. (5)):
+// CTA r of the cluster runs the same pipeline over its own chunks
+// [r nb_per, min(N1 chunks, (r + 1) nb_per)) and keeps its running
+// (m_r, l_r, O_r); at the end the cluster merges them through distributed
+// shared memory, m = max_r m_r, l = sum_r l_r 2^(m_r - m),
+// O = sum_r O_r 2^(m_r - m) / l (for ReLU, O = sum_r O_r).  Each cluster takes
+// exactly one query block (no persistence), so the key rings are idle when
+// the merge stages O in them.  Used when there are fewer query blocks than
+// SMs, where one CTA per block would leave most of the GPU idle.
+template <bool RAG, bool OBF16, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,6 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
   const int nb = p.n1_blocks;
+  // Items (query blocks) of this CTA and its key chunks [j0, j1) of each.
+  int item0 = blockIdx.x, istep = gridDim.x, j0 = 0, j1 = nb;
+  uint32_t crank = 0;
+  if constexpr (SPLIT) {
+    crank = cluster_ctarank();
+    item0 = (int)cluster_id_x();
+    istep = (int)num_clusters_x();
+    j0 = (int)crank * p.nb_per;
+    j1 = min(nb, j0 + p.nb_per);
+  }
+  const int nbl = j1 - j0;  // >= 1: the host sizes the split so that no range is empty
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_QF), 1);
@@ -252,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     mbar_init(bar(BAR_DRAIN1), 1);
     mbar_init(bar(BAR_DRAIN2), 1);
     for (int i = 0; i < 16; ++i) mbar_init(bar(BAR_MB + i), 1);  // MB[8] then XL[8]: one publishing warp
+    for (int i = 0; i < 8; ++i) mbar_init(bar(BAR_MLF + i), SPLIT ? p.split : 1);  // one warp of each CTA
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -282,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       uint32_t rs = 0, rph = 0;
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+      for (int item = item0; ok && item < p.items; item += istep, ++it) {
         const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
         if (w1) {
           if (!mbar_wait(bar(BAR_QE), (it & 1) ^ 1, wc)) break;
@@ -290,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           tma_load_3d(sbase + kOffQ, &p.tmA, bar(BAR_QF), 0, mb * kTile, b);
           tma_load_3d(sbase + kOffQ + 16384, &p.tmA, bar(BAR_QF), 64, mb * kTile, b);
         }
-        for (int j = 0; j < nb; ++j) {
+        for (int j = j0; j < j1; ++j) {
           if (!mbar_wait(bar(re + rs), rph ^ 1, wc)) { ok = false; break; }
           const uint32_t dst = sbase + off + rs * kTileBytes;
           mbar_arrive_expect_tx(bar(rf + rs), kTileBytes);
@@ -311,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       uint32_t g = 0;  // global chunk counter (S buffer and F group = g & 1)
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+      for (int item = item0; ok && item < p.items; item += istep, ++it) {
         if (!mbar_wait(bar(BAR_QF), it & 1, wc)) break;
-        for (int j = 0; j < nb; ++j, ++g) {
+        for (int j = j0; j < j1; ++j, ++g) {
           // S buffer g & 1 is free once F group g & 1 holds S_{g-2} in registers.
           if (g >= 2 && !mbar_wait(bar(BAR_SFREE + (g & 1)), ((g - 2) >> 1) & 1, wc)) { ok = false; break; }
           if (!mbar_wait(bar(BAR_RF1 + rs), rph, wc)) { ok = false; break; }
@@ -345,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
-        for (int j = 0; j < nb; ++j, ++g) {
+      for (int item = item0; ok && item < p.items; item += istep, ++it) {
+        for (int j = j0; j < j1; ++j, ++g) {
           if (!mbar_wait(bar(BAR_PF + (g & 1)), (g >> 1) & 1, wc)) { ok = false; break; }
-          if (j == 0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
+          if (j == j0 && !mbar_wait(bar(BAR_OE), (it & 1) ^ 1, wc)) { ok = false; break; }
           if (!mbar_wait(bar(BAR_RF2 + rs), rph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint32_t v_lo = dv.lo + rs * kTileStep;
@@ -358,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             // A = S' from TMEM (16 K elements = 8 packed columns per step);
             // B = W2 rows 16 kk .. 16 kk + 15 (2048 bytes per step).
             mma_ts(tmem_base + kTmemO, p_col + 8 * kk, v_lo + kk * (2048 >> 4), dv.hi, id_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+                   (j > j0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(BAR_RE2 + rs));
           mma_commit(bar(BAR_PV + (g & 1)));
@@ -391,10 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x, ++it) {
+    for (int item = item0; ok && item < p.items; item += istep, ++it) {
       const int b = item / p.m_blocks, mb = item - b * p.m_blocks;
       const uint32_t g0 = g;
-      const uint32_t g_last = g0 + (uint32_t)nb - 1;
+      const uint32_t g_last = g0 + (uint32_t)nbl - 1;
       float l = 0.0f, m_last = -INFINITY;   // this group's sum, and the max it is scaled to
       for (uint32_t gg = g0 + ((g0 & 1) != (uint32_t)grp ? 1u : 0u); gg <= g_last; gg += 2) {
         const int j = (int)(gg - g0);
@@ -409,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));  // S_sb may be overwritten now
         if (p.softmax) {
-          if (RAG && j == nb - 1 && p.kv_last < kTile) {
+          if (RAG && j0 + j == nb - 1 && p.kv_last < kTile) {
             // Ragged N1: keys past N1 were loaded as zero rows; their logits
             // leave the max and the sum (exp2(-inf) = 0).  The V rows past
             // N1 are zero as well.
@@ -477,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           float(&vc)[32] = part32(v, c);
           uint32_t w[16];
           if (p.softmax) {
-#pragma unroll
             fma2_32(vc, pack2f(sl2), pack2f(-m_last));  // the exp2 arguments, two per instruction
 #pragma unroll
             for (int e = 0; e < 32; ++e) vc[e] = ex2_approx(vc[e]);
@@ -504,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const uint32_t xl = (uint32_t)(it & 1);
       if (!writer) {
         // Hand this group's (l, max) to the writer of the item's output.
-        if (p.softmax && nb >= 2) {
+        if (p.softmax && nbl >= 2) {
           lm[xl * 128 + row] = make_float2(l, m_last);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(BAR_XL + xl * 4 + q));
@@ -512,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         continue;
       }
       // Writer: O / l -> fp32 output rows (all 128 columns of its rows).
-      float inv = 1.0f;
+      float inv = 1.0f, lt = 1.0f;
       if (p.softmax) {
-        float lt = l;
-        if (nb >= 2) {
+        lt = l;
+        if (nbl >= 2) {
           if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_XL + xl * 4 + q), (it >> 1) & 1, wc))) break;
           const float2 o = lm[xl * 128 + row];
           // m_last is the final max (the max in use never decreases).
@@ -526,26 +577,98 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), it & 1, wc))) break;
       tc_fence_after();
       const long long orow = (long long)b * p.stride_out + (long long)(mb * kTile + row) * p.ldo;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float o[64];
-        tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h, *reinterpret_cast<float(*)[32]>(&o[0]));
-        tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
-        tmem_wait_ld();
-        if (h == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
+      if constexpr (SPLIT) {
+        // The review's Eq. (5) over the cluster.  Each CTA publishes its
+        // rows' (m_r, l_r), derives the block's (m, l) from all of them in
+        // rank order, stages O_r 2^(m_r - m) / l in shared memory, and sums
+        // its own slice of the 32 four-column chunks of every CTA's staged
+        // row, in rank order, into the output.  Only this CTA's warp of the
+        // same TMEM quarter reads a row, so the barriers are per quarter.
+        const int C = p.split;
+        float2* mlx = lm + 128;  // one item per CTA: the second item slot is free
+        mlx[row] = make_float2(m_last, lt);
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          for (int r = 0; r < C; ++r) mbar_arrive_cluster(bar(BAR_MLF + q), (uint32_t)r);
         }
-        if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
-          if (!RAG || p.n2 >= 64 * (h + 1)) store_row<64>(p.out, OBF16, orow + 64 * h, o, inv);
-          else if (p.n2 > 64 * h) store_row_part<64>(p.out, OBF16, orow + 64 * h, o, inv, p.n2 - 64 * h);
+        if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_MLF + q), 0, wc))) break;
+        float f = 1.0f;
+        if (p.softmax) {
+          const uint32_t a = smem_u32(mlx + row);
+          float mx = -INFINITY;
+          for (int r = 0; r < C; ++r) mx = fmaxf(mx, ld_shared_cluster_f2(mapa_shared(a, (uint32_t)r)).x);
+          float lsum = 0.0f;
+          for (int r = 0; r < C; ++r) {
+            const float2 v = ld_shared_cluster_f2(mapa_shared(a, (uint32_t)r));
+            lsum += v.y * ex2_approx(v.x - mx);
+          }
+          f = ex2_approx(m_last - mx) / lsum;
+        }
+        // Stage the scaled O rows in the W1 ring: its last tile was consumed
+        // by a GEMM1 that completed before this item's last GEMM2.  Row r is
+        // 512 bytes; its 16-byte chunk k sits at chunk k ^ (r & 31), so a
+        // warp's 32 rows hit distinct bank groups.
+        fence_proxy_async_smem();
+        uint8_t* srow = smem + kOffW1 + row * 512;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          float o[32];
+          tmem_ld32(tmem_base + lane_off + kTmemO + 32 * h, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const int k = 8 * h + k4;
+            *reinterpret_cast<float4*>(srow + ((k ^ (row & 31)) << 4)) =
+                make_float4(o[4 * k4] * f, o[4 * k4 + 1] * f, o[4 * k4 + 2] * f, o[4 * k4 + 3] * f);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_cluster();
+          for (int r = 0; r < C; ++r) mbar_arrive_cluster(bar(BAR_STG + q), (uint32_t)r);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_STG + q), 0, wc))) break;
+        const int kb = (32 * (int)crank) / C, ke = (32 * ((int)crank + 1)) / C;
+        const uint32_t srow_addr = sbase + kOffW1 + row * 512;
+        const bool live = mb * kTile + row < p.M;  // rows past M (ragged last block) are not stored
+#pragma unroll 1
+        for (int k = kb; k < ke; ++k) {
+          const uint32_t a = srow_addr + ((uint32_t)(k ^ (row & 31)) << 4);
+          float4 acc = ld_shared_cluster_f4(mapa_shared(a, 0));
+          for (int r = 1; r < C; ++r) {
+            const float4 v = ld_shared_cluster_f4(mapa_shared(a, (uint32_t)r));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          if (live && 4 * k < p.n2) store4<OBF16>(p.out, orow + 4 * k, acc, p.n2 - 4 * k);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float o[64];
+          tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h, *reinterpret_cast<float(*)[32]>(&o[0]));
+          tmem_ld32(tmem_base + lane_off + kTmemO + 64 * h + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
+          tmem_wait_ld();
+          if (h == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
+          }
+          if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
+            if (!RAG || p.n2 >= 64 * (h + 1)) store_row<64>(p.out, OBF16, orow + 64 * h, o, inv);
+            else if (p.n2 > 64 * h) store_row_part<64>(p.out, OBF16, orow + 64 * h, o, inv, p.n2 - 64 * h);
+          }
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  // Key split: no CTA leaves while a peer may still read its shared memory.
+  if constexpr (SPLIT) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -868,7 +991,42 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
 
 
 std::mutex g_mu;
-bool g_prepared[64][6] = {};  // [device][MLP fp32 / bf16 out, attention variants 0..3]
+bool g_prepared[64][10] = {};  // [device][MLP fp32 / bf16 out, attention variants 0..7]
+// Resident clusters of C CTAs of the key-split attention kernel, by device,
+// kernel variant and C (0: not queried yet, -1: none fit).
+int g_attn_clusters[64][8][CF_MAX_KEY_SPLIT + 1] = {};
+
+// Clusters of C CTAs of `fn` (a key-split attention variant) that fit on
+// the current device at once; 0 if none (cached per device and variant).
+int attn_max_clusters(const void* fn, int variant, int C) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& cached = g_attn_clusters[dev][variant][C];
+  if (cached == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(attn::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = attn::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int q = 0;
+    if (cudaOccupancyMaxActiveClusters(&q, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      q = 0;
+    }
+    cached = q > 0 ? q : -1;
+  }
+  return cached > 0 ? cached : 0;
+}
 
 cf_status prepare(int slot, const void* fn, int smem) {
   int dev = 0;
@@ -981,9 +1139,12 @@ using namespace cf;
 extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2, const cf_b2b_desc* d,
                                 cf_matrix* out, void* stream) {
   cf_status s;
-  if (!d || d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
+  if (!d || d->version < 1 || d->version > CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
   if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX || !std::isfinite(d->mid_scale))
     return CF_ERR_INVALID_ARG;
+  // The key_split field exists from version 2 (never read from a version-1 struct).
+  const int key_split = d->version >= 2 ? d->key_split : 0;
+  if (key_split < 0 || key_split > CF_MAX_KEY_SPLIT) return CF_ERR_INVALID_ARG;
   // The softmax's running max is taken on the unscaled logits: its scale
   // must be positive (a temperature).
   if (d->mid_op == CF_MID_SCALE_SOFTMAX && !(d->mid_scale > 0.0f)) return CF_ERR_INVALID_ARG;
@@ -1059,20 +1220,71 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
   p.status = status;
   p.timeout_cycles = wait_timeout_cycles();
-  const int grid = p.items < sms ? p.items : sms;
+  // Key split (the review's Eq. (5) over a cluster).  AUTO splits only
+  // when the query blocks are fewer than the SMs (one CTA per block would
+  // leave SMs idle), every CTA keeps at least kSplitMinChunks 128-key
+  // chunks (measured on GB300: the merge and the cluster launch cost about
+  // as much as 6-7 chunks of one CTA's pipeline, so a 2-chunk row loses
+  // 13.5 -> 19.6 us when split), and all the clusters are resident at once
+  // (a second wave of clusters doubles the time); it takes the largest such
+  // cluster.  Otherwise one CTA per block walks all keys (the C = 1 online
+  // form).  The chunk count per CTA is rounded up and the CTA count
+  // recomputed from it, so that no CTA's key range is empty.
+  constexpr int kSplitMinChunks = 8;
   const bool rag = (p.softmax && p.kv_last < attn::kTile) || p.n2 < attn::kTile;
-  const int variant = (rag ? 1 : 0) + (p.out_bf16 ? 2 : 0);
-  const void* fns[4] = {reinterpret_cast<const void*>(&attn::attn_kernel<false, false>),
-                        reinterpret_cast<const void*>(&attn::attn_kernel<true, false>),
-                        reinterpret_cast<const void*>(&attn::attn_kernel<false, true>),
-                        reinterpret_cast<const void*>(&attn::attn_kernel<true, true>)};
+  const int base_variant = (rag ? 1 : 0) + (p.out_bf16 ? 2 : 0);
+  const void* fns[8] = {reinterpret_cast<const void*>(&attn::attn_kernel<false, false, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, false, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<false, true, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, true, false>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<false, false, true>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, false, true>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<false, true, true>),
+                        reinterpret_cast<const void*>(&attn::attn_kernel<true, true, true>)};
+  int split = key_split == 0 ? 1 : key_split;
+  if (key_split == 0 && p.items < sms && p.n1_blocks >= 2 * kSplitMinChunks) {
+    if ((s = prepare(2 + base_variant + 4, fns[base_variant + 4], attn::kSmemBytes)) != CF_OK) return s;
+    int cmax = p.n1_blocks / kSplitMinChunks;
+    if (cmax > CF_MAX_KEY_SPLIT) cmax = CF_MAX_KEY_SPLIT;
+    for (int c = cmax; c >= 2; --c) {
+      if (p.items <= attn_max_clusters(fns[base_variant + 4], base_variant + 4, c)) {
+        split = c;
+        break;
+      }
+    }
+  }
+  if (split > p.n1_blocks) split = p.n1_blocks;
+  if (split >= 2) {
+    p.nb_per = (p.n1_blocks + split - 1) / split;
+    split = (p.n1_blocks + p.nb_per - 1) / p.nb_per;
+  }
+  p.split = split >= 2 ? split : 1;
+  const int variant = base_variant + (p.split > 1 ? 4 : 0);
   if ((s = prepare(2 + variant, fns[variant], attn::kSmemBytes)) != CF_OK) return s;
   void* args[] = {&p};
-  if (cudaLaunchKernel(fns[variant], dim3(grid), dim3(attn::kThreads), args, attn::kSmemBytes,
-                       static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(attn::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = attn::kSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  if (p.split > 1) {
+    // One cluster of `split` CTAs per query block, not persistent: clusters
+    // do not wait on each other, so any number of them may queue.
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (attn_max_clusters(fns[variant], variant, p.split) < 1) return CF_ERR_UNSUPPORTED_SHAPE;  // none fits
+    if ((int64_t)p.items * p.split > INT32_MAX) return CF_ERR_UNSUPPORTED_SHAPE;
+    cfg.gridDim = dim3((unsigned)(p.items * p.split), 1, 1);
+  } else {
+    cfg.gridDim = dim3((unsigned)(p.items < sms ? p.items : sms), 1, 1);  // persistent
+  }
+  if (cudaLaunchKernelExC(&cfg, fns[variant], args) != cudaSuccess) {
     cudaGetLastError();
     return CF_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
   return CF_OK;
 }

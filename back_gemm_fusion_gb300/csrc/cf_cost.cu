@@ -154,7 +154,7 @@ extern "C" cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* 
 extern "C" cf_status cf_cost_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W2,
                                      const cf_b2b_desc* desc, const cf_device_model* dm, cf_cost* out) {
   if (!A || !W1 || !W2 || !desc || !out) return CF_ERR_INVALID_ARG;
-  if (desc->version != CF_B2B_VERSION || desc->batch < 1) return CF_ERR_INVALID_ARG;
+  if (desc->version < 1 || desc->version > CF_B2B_VERSION || desc->batch < 1) return CF_ERR_INVALID_ARG;
   if (desc->mid_op < CF_MID_RELU || desc->mid_op > CF_MID_SCALE_SOFTMAX) return CF_ERR_INVALID_ARG;
   const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols;
   if (W1->rows != K || W2->rows != N1) return CF_ERR_INVALID_ARG;

@@ -804,7 +804,7 @@ extern "C" cf_status cf_unfused_b2bgemm(const cf_matrix* A, const cf_matrix* W1,
                                         const cf_b2b_desc* d, cf_matrix* out, float* s_buf, void* p_buf,
                                         void* stream) {
   if (!A || !W1 || !W2 || !d || !out || !s_buf || !p_buf) return CF_ERR_INVALID_ARG;
-  if (d->version != CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
+  if (d->version < 1 || d->version > CF_B2B_VERSION || d->batch < 1) return CF_ERR_INVALID_ARG;
   if (d->mid_op < CF_MID_RELU || d->mid_op > CF_MID_SCALE_SOFTMAX) return CF_ERR_INVALID_ARG;
   if (d->mid_op == CF_MID_SCALE_SOFTMAX && !(d->mid_scale > 0.0f)) return CF_ERR_INVALID_ARG;
   if ((d->out_dtype != CF_FP32 && d->out_dtype != CF_BF16) || out->dtype != d->out_dtype) return CF_ERR_INVALID_ARG;

@@ -245,10 +245,13 @@ typedef enum {
   CF_MID_SCALE_SOFTMAX = 3  /* S' = row softmax of (scale S)     */
 } cf_mid_op;
 
-#define CF_B2B_VERSION 1
+#define CF_B2B_VERSION 2  /* version 1 (no key_split) is still accepted */
+
+/* Largest key split (CTAs per query block) of the attention shape. */
+#define CF_MAX_KEY_SPLIT 8
 
 typedef struct {
-  uint32_t version;  /* must be CF_B2B_VERSION */
+  uint32_t version;  /* 1 or 2 (CF_B2B_VERSION); version 1 ends after strideOut */
   int32_t mid_op;    /* cf_mid_op */
   float mid_scale;   /* scale for the SCALE_* ops */
   int32_t out_dtype; /* cf_dtype of `out`: CF_FP32, or CF_BF16 (rounded to
@@ -258,6 +261,15 @@ typedef struct {
   int64_t strideA, strideW1, strideW2, strideOut; /* elements between problems; inputs may
                                                      overlap (read only), outputs must not:
                                                      strideOut >= (M - 1) * ld + N2 */
+  /* Version 2, attention shape only (ignored by the MLP shape): how many
+   * CTAs share the N1 (key) range of one 128-row block of A.  0: chosen per
+   * shape (split only when the row blocks are fewer than the SMs, into as
+   * many CTAs as keep every SM busy); 1: one CTA walks all of N1;
+   * 2..CF_MAX_KEY_SPLIT: that many CTAs of a thread-block cluster (fewer
+   * when N1 has fewer 128-key chunks, or when the count must shrink so that
+   * every CTA gets at least one chunk), each over its own key range,
+   * merged on chip (see cf_b2bgemm).  Other values: CF_ERR_INVALID_ARG. */
+  int32_t key_split;
 } cf_b2b_desc;
 
 /*
@@ -277,6 +289,15 @@ typedef struct {
  *   W2  : N1 x N2 bf16, trans == 0 (stored N1 x N2, e.g. the value matrix).
  *   out : M x N2, trans == 0, dtype == desc->out_dtype (fp32 or bf16).
  *   The softmax mid op normalises each row of S over all N1 columns.
+ *
+ * Attention shape, key split (desc->key_split): the CTAs of a cluster each
+ * run GEMM1 -> F -> GEMM2 over their own key range with the online softmax
+ * statistics (m_c, l_c) and partial output O_c, then merge them through
+ * distributed shared memory as in Eq. (5): m = max_c m_c,
+ * l = sum_c l_c exp(m_c - m), O = sum_c O_c exp(m_c - m) / l (for ReLU,
+ * O = sum_c O_c), summed in cluster-rank order.  Nothing of S, S' or the
+ * partial outputs reaches global memory.  A forced split whose cluster
+ * cannot be resident returns CF_ERR_UNSUPPORTED_SHAPE.
  *
  * Shape rules (this version), two kernels:
  *   attention shape: W1 given transposed (trans == 1), head dims K <= 128

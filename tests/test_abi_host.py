@@ -251,6 +251,31 @@ def test_b2b_shape_rules(lib):
     assert call(256, 256, 512, 1100, op="relu", trans=False) == 2       # MLP, C = 5 > 4
 
 
+def test_b2b_key_split_rules(lib):
+    # Descriptor version 2 carries key_split (0 auto, 1 off, 2..8 CTAs per
+    # query block); out-of-range values are argument errors found on the
+    # host; version-1 descriptors (no key_split field) are still accepted.
+    from back_gemm_fusion_gb300.binding import cf_matrix, b2b_desc, CF_BF16, CF_FP32
+    Q = cf_matrix(0x10000, CF_BF16, 0, 128, 128, 128)
+    K = cf_matrix(0x20000, CF_BF16, 1, 128, 2048, 128)
+    V = cf_matrix(0x30000, CF_BF16, 0, 2048, 128, 128)
+    O = cf_matrix(0x40000, CF_FP32, 0, 128, 128, 128)
+
+    def call(ks, version=2):
+        d = b2b_desc("scale_softmax", 0.125, 1, key_split=ks)
+        d.version = version
+        return lib.cf_b2bgemm(ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V), ctypes.byref(d), ctypes.byref(O),
+                              None)
+
+    ok = (0, 4, 8)
+    for ks in (0, 1, 2, 3, 8):
+        assert call(ks) in ok
+    assert call(-1) == 1
+    assert call(9) == 1
+    assert call(9, version=1) in ok      # version 1 never reads the field
+    assert call(0, version=3) == 1       # unknown version
+
+
 def test_column_axis_rules(lib):
     # Column reductions: descriptor version 3, B given as N x K, the kernel
     # runs on P^T (so the workspace follows the swapped shape).

@@ -58,32 +58,39 @@ def _attention_case(batch, L, op, seed, growth=None):
     return t(q), t(k), t(v)
 
 
-def _run_attention(cf, Q, K, V, op, scale):
-    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+def _run_attention(cf, Q, K, V, op, scale, key_split=0):
+    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, key_split=key_split)
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == 0
     return out.cpu().numpy()
 
 
+# key_split: 1 = one CTA walks all keys of a query block (the online C = 1
+# form); 2 = two CTAs of a cluster split each block's keys (for these short
+# key ranges AUTO keeps one CTA: too few chunks to pay for the merge).
+@pytest.mark.parametrize("key_split", [1, 2])
 @pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
 @pytest.mark.parametrize("batch,L", [(1, 128), (2, 256), (3, 384), (2, 1024)])
-def test_attention_small(cf, batch, L, op):
+def test_attention_small(cf, batch, L, op, key_split):
     Q, K, V = _attention_case(batch, L, op, seed=L + batch)
     scale = 1 / math.sqrt(128)
-    got = _run_attention(cf, Q, K, V, op, scale)
+    got = _run_attention(cf, Q, K, V, op, scale, key_split)
     q, k, v = (I.to_f64(t) for t in (Q, K, V))
     for b in range(batch):
         ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
         b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} b={b} L={L}")
 
 
+@pytest.mark.parametrize("key_split", [1, 4])
 @pytest.mark.parametrize("growth", [2.0, 6.0])
-def test_attention_softmax_rescales(cf, growth):
+def test_attention_softmax_rescales(cf, growth, key_split):
     # Logits grow block by block, so the running max increases by more than
-    # 2^8 in exp2 units several times: exercises the O rescale path.
+    # 2^8 in exp2 units several times: exercises the O rescale path.  With
+    # the key split each CTA rescales on its own range and the merge meets
+    # maxima that differ by far more than 2^8 between the CTAs.
     Q, K, V = _attention_case(2, 1024, "scale_softmax", seed=11, growth=growth)
     scale = 1 / math.sqrt(128)
-    got = _run_attention(cf, Q, K, V, "scale_softmax", scale)
+    got = _run_attention(cf, Q, K, V, "scale_softmax", scale, key_split)
     q, k, v = (I.to_f64(t) for t in (Q, K, V))
     for b in range(2):
         ref = O.b2bgemm(q[b], k[b].T, v[b], "scale_softmax", scale)
@@ -220,15 +227,17 @@ def _bf16_gate(gpu, ref, absbound, what):
     assert worst <= 1.0, f"{what}: bf16-output bound exceeded ({worst:.3g} x)"
 
 
+@pytest.mark.parametrize("key_split", [1, 2])
 @pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
 @pytest.mark.parametrize("batch,Lq,L", [(2, 256, 256), (2, 77, 384), (1, 128, 1024)])
-def test_attention_bf16_output(cf, batch, Lq, L, op):
+def test_attention_bf16_output(cf, batch, Lq, L, op, key_split):
     rng = np.random.default_rng(Lq + L)
     t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
     Q, K, V = (t(rng.standard_normal((batch, n, 128))) for n in (Lq, L, L))
     scale = 1 / math.sqrt(128)
-    g = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, out_dtype=torch.bfloat16)
-    f = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+    g = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, out_dtype=torch.bfloat16,
+                      key_split=key_split)
+    f = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, key_split=key_split)
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == 0
     assert g.dtype == torch.bfloat16 and g.shape == (batch, Lq, 128)
@@ -262,9 +271,10 @@ def _bf16_t(a):
     return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
 
 
+@pytest.mark.parametrize("key_split", [1, 2])
 @pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
 @pytest.mark.parametrize("Lq,N1", [(128, 1), (200, 77), (256, 200), (128, 1000)])
-def test_attention_ragged_keys(cf, Lq, N1, op):
+def test_attention_ragged_keys(cf, Lq, N1, op, key_split):
     # N1 not a multiple of the 128-key chunk: the last chunk's keys past N1
     # load as zero rows and leave the softmax max and sum; V rows past N1
     # are zero (target-attention-like short key sequences).
@@ -273,17 +283,18 @@ def test_attention_ragged_keys(cf, Lq, N1, op):
     K = _bf16_t(rng.standard_normal((2, N1, 128)))
     V = _bf16_t(rng.standard_normal((2, N1, 128)))
     scale = 1 / math.sqrt(128)
-    got = _run_attention(cf, Q, K, V, op, scale)
+    got = _run_attention(cf, Q, K, V, op, scale, key_split)
     q, k, v = (I.to_f64(x) for x in (Q, K, V))
     for b in range(2):
         ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
         b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"attention {op} Lq={Lq} N1={N1} b={b}")
 
 
+@pytest.mark.parametrize("key_split", [1, 2])
 @pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
 @pytest.mark.parametrize("d_qk,d_v,N1", [(64, 64, 256), (64, 64, 200), (128, 64, 384), (96, 32, 130),
                                          (32, 128, 512)])
-def test_attention_head_dims(cf, d_qk, d_v, N1, op):
+def test_attention_head_dims(cf, d_qk, d_v, N1, op, key_split):
     # Head dims below 128: Q/K columns past d_qk and V columns past d_v load
     # as zeros; the output has d_v columns.
     rng = np.random.default_rng(d_qk * 7 + d_v + N1)
@@ -292,7 +303,7 @@ def test_attention_head_dims(cf, d_qk, d_v, N1, op):
     K = _bf16_t(rng.standard_normal((2, N1, d_qk)))
     V = _bf16_t(rng.standard_normal((2, N1, d_v)))
     scale = 1 / math.sqrt(d_qk)
-    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True)
+    out = cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), op, scale, w1_trans=True, key_split=key_split)
     torch.cuda.synchronize()
     assert cf.cf_last_device_status() == 0
     assert out.shape == (2, Lq, d_v)
@@ -342,3 +353,70 @@ def test_target_attention_shape(cf, op):
         q, k, v = (I.to_f64(t[b]) for t in (case.A, case.W1, case.W2))
         ref = O.b2bgemm(q, k.T, v, op, case.scale)
         b2b_gate(got[b], ref, _abs_bound(q, k, v, op, case.scale), f"target attention {op} b={b}")
+
+
+# ------------------------------------------------------------ key split (Eq. 5)
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+@pytest.mark.parametrize("key_split", [2, 3, 5, 8, 0])
+def test_attention_key_split(cf, key_split, op):
+    # One query block over 2048 keys (16 chunks) split across a cluster:
+    # 3 CTAs take 6 + 6 + 4 chunks, a request of 5 becomes 4 CTAs of 4
+    # chunks, 8 CTAs take 2 each, and AUTO picks 2 (at least 8 chunks per
+    # CTA).  The merged (m, l, O) must match the oracle like the one-CTA
+    # form does.
+    Q, K, V = _attention_case(2, 2048, op, seed=40 + key_split)
+    Q = Q[:, :128].contiguous()
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, op, scale, key_split)
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        b2b_gate(got[b], ref, _abs_bound(q[b], k[b], v[b], op, scale), f"key split {key_split} {op} b={b}")
+
+
+@pytest.mark.parametrize("op", ["scale_softmax", "scale_relu"])
+def test_attention_key_split_decode_shape(cf, op):
+    # Few query rows over a long key sequence (4 heads x 77 queries x 8192
+    # keys, ragged query block): AUTO splits each block over 8 CTAs.
+    rng = np.random.default_rng(5)
+    Q = _bf16_t(rng.standard_normal((4, 77, 128)))
+    K = _bf16_t(rng.standard_normal((4, 8192, 128)))
+    V = _bf16_t(rng.standard_normal((4, 8192, 128)))
+    scale = 1 / math.sqrt(128)
+    got = _run_attention(cf, Q, K, V, op, scale, 0)
+    one = _run_attention(cf, Q, K, V, op, scale, 1)
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for b in range(4):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], op, scale)
+        bound = _abs_bound(q[b], k[b], v[b], op, scale)
+        b2b_gate(got[b], ref, bound, f"decode shape split {op} b={b}")
+        b2b_gate(one[b], ref, bound, f"decode shape one CTA {op} b={b}")
+
+
+def test_attention_key_split_ragged_head_dim_bf16(cf):
+    # Split with ragged keys (N1 = 1000: 8 chunks, the last with 104 keys),
+    # a value head dim of 30 written into 32-element rows (the last
+    # four-column group of each row is partial), fp32 and bf16 outputs.
+    rng = np.random.default_rng(6)
+    Q = _bf16_t(rng.standard_normal((2, 200, 64)))
+    K = _bf16_t(rng.standard_normal((2, 1000, 64)))
+    V = _bf16_t(rng.standard_normal((2, 1000, 30)))
+    Vp = torch.zeros((2, 1000, 32), dtype=torch.bfloat16, device="cuda")  # 16-byte row pitch
+    Vp[:, :, :30] = V.cuda()
+    scale = 1 / 8.0
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    for dt in (torch.float32, torch.bfloat16):
+        buf = torch.full((2, 200, 32), 9.0, dtype=dt, device="cuda")
+        cf.cf_b2bgemm(Q.cuda(), K.cuda(), Vp[:, :, :30], "scale_softmax", scale, w1_trans=True, out=buf[:, :, :30],
+                      key_split=3)
+        torch.cuda.synchronize()
+        assert cf.cf_last_device_status() == 0
+        assert torch.all(buf[:, :, 30:] == 9.0)
+        got = buf[:, :, :30].float().cpu().numpy()
+        for b in range(2):
+            ref = O.b2bgemm(q[b], k[b].T, v[b], "scale_softmax", scale)
+            bound = _abs_bound(q[b], k[b], v[b], "scale_softmax", scale)
+            if dt == torch.float32:
+                b2b_gate(got[b], ref, bound, f"split ragged fp32 b={b}")
+            else:
+                _bf16_gate(got[b], ref, bound, f"split ragged bf16 b={b}")
