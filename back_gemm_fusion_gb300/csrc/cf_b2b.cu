@@ -114,12 +114,45 @@ __device__ __forceinline__ void store_row_packed_sw128(uint8_t* tile, int r, int
   }
 }
 
+// One 32-byte store (a whole 32-byte sector of the memory system).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Store W values v[i] * s of one output row at element offset `off` of
-// `out`: fp32 (16-byte vector stores) or bf16 rounded to nearest even
-// (8 values per 16-byte store). W is a multiple of 8; `off` keeps each store
-// 16-byte aligned (row pitch and column offsets are checked on the host).
+// `out`: fp32 or bf16 rounded to nearest even.  W is a multiple of 16.
+// V8: `out + off` is 32-byte aligned, so every store writes one whole
+// 32-byte sector (8 fp32 or 16 bf16 values); otherwise 16-byte stores (row
+// pitch and column offsets keep those aligned; checked on the host).  Each
+// thread writes its own row, so 16-byte stores would leave every sector
+// half-written per request.
 template <int W>
-__device__ __forceinline__ void store_row(void* out, int bf16, long long off, const float* v, float s) {
+__device__ __forceinline__ void store_row(void* out, int bf16, long long off, const float* v, float s, bool v8) {
+  if (v8) {
+    if (bf16) {
+#pragma unroll
+      for (int j = 0; j < W / 16; ++j) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[16 * j + 2 * e] * s, v[16 * j + 2 * e + 1] * s);
+          w[e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        st_global_v8(static_cast<uint16_t*>(out) + off + 16 * j, w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < W / 8; ++j) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[8 * j + e] * s);
+        st_global_v8(static_cast<float*>(out) + off + 8 * j, w);
+      }
+    }
+    return;
+  }
   if (bf16) {
     uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
 #pragma unroll
@@ -202,6 +235,7 @@ struct Params {
   int n2;            // valid output columns (N2 <= 128)
   int softmax;       // 1: scaled softmax (scale > 0), 0: ReLU (optionally scaled)
   float scale;       // multiplies S before F
+  int out_v8;        // the output base, row pitch and batch stride are 32-byte aligned
   int split;         // key split: CTAs per query block (the cluster size); 1 without the split
   int nb_per;        // key split: 128-key chunks per CTA (the last CTA's range may be shorter)
   unsigned* status;
@@ -331,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       const int off = w1 ? kOffW1 : kOffW2;
       const int rf = w1 ? BAR_RF1 : BAR_RF2, re = w1 ? BAR_RE1 : BAR_RE2;
       const CUtensorMap* m = w1 ? &p.tmW1 : &p.tmW2;
-      uint32_t rs = 0, rph = 0;
+      uint32_t rs = 0, rph = 0, issued = 0, q_issued = 0;
       int it = 0;
       bool ok = true;
       for (int item = item0; ok && item < p.items; item += istep, ++it) {
@@ -341,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           mbar_arrive_expect_tx(bar(BAR_QF), kTileBytes);
           tma_load_3d(sbase + kOffQ, &p.tmA, bar(BAR_QF), 0, mb * kTile, b);
           tma_load_3d(sbase + kOffQ + 16384, &p.tmA, bar(BAR_QF), 64, mb * kTile, b);
+          ++q_issued;
         }
         for (int j = j0; j < j1; ++j) {
           if (!mbar_wait(bar(re + rs), rph ^ 1, wc)) { ok = false; break; }
@@ -348,9 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           mbar_arrive_expect_tx(bar(rf + rs), kTileBytes);
           tma_load_3d(dst, m, bar(rf + rs), 0, j * kTile, b);
           tma_load_3d(dst + 16384, m, bar(rf + rs), 64, j * kTile, b);
+          ++issued;
           if (++rs == (uint32_t)depth) { rs = 0; rph ^= 1; }
         }
       }
+      // No load of this CTA is still in flight when it exits.
+      drain_ring(bar(rf), (uint32_t)depth, issued, wc);
+      if (w1) drain_ring(bar(BAR_QF), 1u, q_issued, wc);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- GEMM1 issuer
@@ -658,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (lane == 0) mbar_arrive(bar(BAR_OE));  // O may be overwritten by the next item
           }
           if (mb * kTile + row < p.M) {  // rows past M (ragged last block) are not stored
-            if (!RAG || p.n2 >= 64 * (h + 1)) store_row<64>(p.out, OBF16, orow + 64 * h, o, inv);
+            if (!RAG || p.n2 >= 64 * (h + 1)) store_row<64>(p.out, OBF16, orow + 64 * h, o, inv, p.out_v8);
             else if (p.n2 > 64 * h) store_row_part<64>(p.out, OBF16, orow + 64 * h, o, inv, p.n2 - 64 * h);
           }
         }
@@ -717,6 +756,7 @@ struct Params {
   int C;             // CTAs per cluster = ceil(N2 / 256)
   int n2;            // output columns (the last CTA's block may be ragged)
   int ring;          // ring stages (ring_for(C))
+  int out_v8;        // the output base, row pitch and batch stride are 32-byte aligned
   int kblocks;       // ceil(K / 64): the last block's columns past K are zero-filled
   int rounds;        // ceil(N1 / (128 C)): chunks past N1 are zero (W1 and W2 zero-filled)
   int strips, items; // M / 128, batch * strips
@@ -782,13 +822,16 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t rs = 0, rph = 0;
+      uint32_t rs = 0, rph = 0, issued = 0;
       bool ok = true;
       auto acquire = [&]() -> uint32_t {
         if (!mbar_wait(bar(BAR_RE + rs), rph ^ 1, wc)) return 0;
         return 1;
       };
-      auto advance = [&]() { if (++rs == kRing) { rs = 0; rph ^= 1; } };
+      auto advance = [&]() {
+        ++issued;
+        if (++rs == kRing) { rs = 0; rph ^= 1; }
+      };
       auto load_g1 = [&](int strip, int b, int r) -> bool {
         const int h = r * C + (int)rank;  // this CTA's N1 chunk
         for (int kb = 0; kb < p.kblocks; ++kb) {
@@ -830,6 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
           if (ok) ok = load_g2(b, r);
         }
       }
+      drain_ring(bar(BAR_RF), (uint32_t)kRing, issued, wc);  // no load of this CTA is still in flight
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -900,8 +944,9 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       }
       mma_commit(bar(BAR_DRAIN));
       mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
-      // All peers' multicast arrivals for the last round have landed here.
-      if (ok && g > 0) mbar_wait<false, false>(bar(BAR_SLE), (g - 1) & 1, wc);
+      // All peers' multicast arrivals for the last round have landed here
+      // (after an abort they may never come: stop at the abort flag).
+      if (ok && g > 0) mbar_wait<false, true>(bar(BAR_SLE), (g - 1) & 1, wc);
     }
   } else {
     // ------------------------------------------------ F warps and epilogue
@@ -969,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         tmem_wait_ld();
         const int col = (int)rank * 256 + c * 32;  // columns past N2 (ragged last block) are not stored
         if (strip * 128 + row < p.M && col < p.n2) {  // nor rows past M (ragged last strip)
-          if (col + 32 <= p.n2) store_row<32>(p.out, OBF16, orow + c * 32, v, 1.0f);
+          if (col + 32 <= p.n2) store_row<32>(p.out, OBF16, orow + c * 32, v, 1.0f, p.out_v8);
           else store_row_part<32>(p.out, OBF16, orow + c * 32, v, 1.0f, p.n2 - col);
         }
       }
@@ -985,6 +1030,12 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     tmem_dealloc(tmem_base, kTmemCols);
   }
   cluster_sync_all();
+  // S' slots travel between the CTAs as bulk copies that complete on the
+  // receiver's barrier.  After an abort (any bounded wait gave up: the
+  // status word is set) some may still be in flight; every CTA has stopped
+  // issuing them at the cluster barrier above, so all wait here before
+  // leaving (the copies' sources and destinations both stay allocated).
+  if (C > 1 && threadIdx.x == 0 && *reinterpret_cast<volatile unsigned*>(p.status) != 0u) settle_after_abort();
 }
 
 }  // namespace mlp
@@ -1044,6 +1095,12 @@ cf_status prepare(int slot, const void* fn, int smem) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every output row (and batch entry) starts on a 32-byte boundary.
+bool out_aligned32(const cf_matrix* out, long long stride_out) {
+  const long long es = out->dtype == CF_BF16 ? 2 : 4;
+  return (reinterpret_cast<uintptr_t>(out->ptr) & 31u) == 0 && (out->ld * es) % 32 == 0 && (stride_out * es) % 32 == 0;
+}
+
 cf_status check_bf16_view(const cf_matrix* m, bool allow_trans) {
   if (!m || !m->ptr || m->dtype != CF_BF16) return CF_ERR_INVALID_ARG;
   if (m->trans != 0 && !(allow_trans && m->trans == 1)) return CF_ERR_INVALID_ARG;
@@ -1090,6 +1147,7 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.out_bf16 = out->dtype == CF_BF16 ? 1 : 0;
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
+  p.out_v8 = out_aligned32(out, p.stride_out) ? 1 : 0;
   p.C = (int)C;
   p.n2 = (int)N2;
   p.ring = mlp::ring_for((int)C);
@@ -1209,6 +1267,7 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   p.out_bf16 = out->dtype == CF_BF16 ? 1 : 0;
   p.ldo = out->ld;
   p.stride_out = batch > 1 ? d->strideOut : 0;
+  p.out_v8 = out_aligned32(out, p.stride_out) ? 1 : 0;
   p.batch = (int)bs;
   p.M = (int)M;
   p.m_blocks = (int)((M + 127) / 128);

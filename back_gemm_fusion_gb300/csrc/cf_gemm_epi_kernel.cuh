@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
+      uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       // B tiles are reread by every strip: keep them in L2 ahead of the
       // streamed output.
@@ -480,16 +480,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
               tma_load_2d(sb, &p.tmB, fb, kb * kBK, n0);
             }
           }
+          ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
       if (CTA2) {
         // The leader's MMA releases reach this CTA's barriers asynchronously:
-        // wait until every stage's last release has landed before exiting.
+        // wait until every stage's last release has landed before exiting
+        // (after an abort they may never come: stop at the abort flag).
         for (int s2 = 0; s2 < kStages; ++s2) {
-          mbar_wait<false, false>(bar(BAR_EMPTY + stage), phase ^ 1, wc);
+          if (!mbar_wait<false, true>(bar(BAR_EMPTY + stage), phase ^ 1, wc)) break;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        // A pair's loads complete on the leader's barrier only, so after an
+        // abort they are waited for at the end of the kernel (settle).
+      } else {
+        drain_ring(bar(BAR_FULL), kStages, issued, wc);  // no load of this CTA is still in flight
       }
     }
   } else if (warp == 1) {
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       if (CTA2 && ok) {
         // Every remote "accumulator empty" arrival from the peer has landed.
         for (int t2 = t; t2 < t + 2; ++t2)
-          mbar_wait<true, false>(bar(BAR_TEMPTY + (t2 & 1)), ((t2 >> 1) & 1) ^ 1, wc);
+          if (!mbar_wait<true, true>(bar(BAR_TEMPTY + (t2 & 1)), ((t2 >> 1) & 1) ^ 1, wc)) break;
       }
     }
   } else {
@@ -871,6 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       tc_fence_after();
       tmem_dealloc_pair(tmem_base, kTmemCols);
     }
+    // After an abort (any bounded wait gave up: the status word is set),
+    // loads of the pair may still be in flight into this CTA's shared
+    // memory or onto the leader's barrier; both CTAs stop issuing before
+    // the cluster barrier above, so both wait here before leaving.
+    if (threadIdx.x == 0 && *reinterpret_cast<volatile unsigned*>(p.status) != 0u) settle_after_abort();
   } else {
     if (warp == 1) {
       tc_fence_after();

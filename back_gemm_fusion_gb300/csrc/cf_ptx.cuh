@@ -82,24 +82,55 @@ __device__ __forceinline__ void record_timeout(const WaitCtx& w) {
   *w.abort_flag = 1;
 }
 
+// Budget of the waits that drain work already in flight before a CTA
+// frees what that work uses (MMAs before TMEM is freed, TMA loads before
+// the CTA exits).  That work completes on its own, so these waits get about
+// two seconds however short the wait budget of the call is.
+constexpr long long kDrainCycles = 4000000000LL;
+
 // Bounded wait for phase `parity` of a CTA-local barrier.  Returns false
 // (and records a timeout) if the budget runs out or another role aborted.
-// kCheckAbort = false keeps waiting (still bounded) after another role gave
-// up; used to drain work already in flight before freeing resources.
+// kCheckAbort = false is a drain: it keeps waiting after another role gave
+// up, with the drain budget (the larger of kDrainCycles and the call's).
 template <bool kCluster = false, bool kCheckAbort = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const long long budget = kCheckAbort ? w.timeout_cycles
+                                       : (w.timeout_cycles > kDrainCycles ? w.timeout_cycles : kDrainCycles);
+  // try_wait itself suspends the thread for a while before it reports an
+  // incomplete phase, so the budget and the abort flag are checked after
+  // every poll.
   const long long t0 = clock64();
-  for (uint32_t it = 0;; ++it) {
+  for (;;) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (kCheckAbort && *w.abort_flag) return false;
-      if (clock64() - t0 > w.timeout_cycles) {
-        record_timeout(w);
-        return false;
-      }
+    if (kCheckAbort && *w.abort_flag) return false;
+    if (clock64() - t0 > budget) {
+      record_timeout(w);
+      return false;
     }
   }
+}
+
+// Before a producer's CTA exits: wait until every TMA load this thread
+// armed on a ring of `depth` "full" barriers (8 bytes apart from
+// `full_bar0`) has landed.  Uses are numbered 0 .. issued-1 in ring order:
+// use i went to slot i % depth with phase parity (i / depth) & 1.  Only the
+// last armed use of each slot can still be pending, and no later phase of
+// that slot was armed, so the phase waited for is exact.  On the normal
+// path every one has completed already (the consumer waited for it).
+__device__ __forceinline__ void drain_ring(uint32_t full_bar0, uint32_t depth, uint32_t issued, const WaitCtx& w) {
+  const uint32_t first = issued > depth ? issued - depth : 0u;
+  for (uint32_t i = first; i < issued; ++i) mbar_wait<false, false>(full_bar0 + 8u * (i % depth), (i / depth) & 1u, w);
+}
+
+// After an abort, a CTA whose loads or copies complete on another CTA's
+// barrier (a CTA pair's shared "full" barrier, bulk copies between the CTAs
+// of a cluster) cannot wait for them exactly: it waits about 50 us (at the
+// GB300's 2 GHz clock) before leaving, far longer than a load or copy that
+// is already in flight takes to land.
+__device__ __forceinline__ void settle_after_abort() {
+  const long long t0 = clock64();
+  while (clock64() - t0 < 100000) __nanosleep(1000);
 }
 
 // -------------------------------------------------------------------- TMA

@@ -420,3 +420,34 @@ def test_attention_key_split_ragged_head_dim_bf16(cf):
                 b2b_gate(got[b], ref, bound, f"split ragged fp32 b={b}")
             else:
                 _bf16_gate(got[b], ref, bound, f"split ragged bf16 b={b}")
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_b2b_output_rows_16_byte_aligned(cf, dt):
+    # Output rows that start on 16-byte but not 32-byte boundaries take the
+    # 16-byte store path (32-byte aligned rows are written a whole 32-byte
+    # sector per store); the padding past each row stays untouched.
+    rng = np.random.default_rng(8)
+    scale = 1 / math.sqrt(128)
+    Q = _bf16_t(rng.standard_normal((2, 200, 128)))
+    K = _bf16_t(rng.standard_normal((2, 384, 128)))
+    V = _bf16_t(rng.standard_normal((2, 384, 128)))
+    pitch = 132 if dt == torch.float32 else 136
+    buf = torch.full((2, 200, pitch), 5.0, dtype=dt, device="cuda")
+    cf.cf_b2bgemm(Q.cuda(), K.cuda(), V.cuda(), "scale_softmax", scale, w1_trans=True, out=buf[:, :, :128])
+    X, W1, W2 = _mlp_case(200, 128, 512, 256, seed=9)
+    mpitch = 260 if dt == torch.float32 else 264
+    mbuf = torch.full((200, mpitch), 5.0, dtype=dt, device="cuda")
+    cf.cf_b2bgemm(X.cuda(), W1.cuda(), W2.cuda(), "relu", out=mbuf[:, :256])
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    assert torch.all(buf[:, :, 128:] == 5.0) and torch.all(mbuf[:, 256:] == 5.0)
+    gate = b2b_gate if dt == torch.float32 else _bf16_gate
+    q, k, v = (I.to_f64(x) for x in (Q, K, V))
+    got = buf[:, :, :128].float().cpu().numpy()
+    for b in range(2):
+        ref = O.b2bgemm(q[b], k[b].T, v[b], "scale_softmax", scale)
+        gate(got[b], ref, _abs_bound(q[b], k[b], v[b], "scale_softmax", scale), f"attention 16-byte rows b={b}")
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu")
+    gate(mbuf[:, :256].float().cpu().numpy(), ref, np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2), "mlp 16-byte rows")
