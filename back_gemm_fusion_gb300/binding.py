@@ -27,7 +27,7 @@ CF_BF16, CF_FP32 = 0, 1
 OP_CODES = {"bias": 1, "scale": 2, "relu": 3, "gelu_tanh": 4, "residual": 5, "layernorm": 16, "rmsnorm": 17,
             "softmax": 18}
 MID_CODES = {"relu": 1, "scale_relu": 2, "scale_softmax": 3}
-EXCHANGE_CODES = {"auto": 0, "cluster": 1, "global": 2}
+EXCHANGE_CODES = {"auto": 0, "cluster": 1, "global": 2, "global_dynamic": 3}
 EPI_MAX_OPS = 8
 
 

@@ -132,7 +132,7 @@ struct EpiPlan {
 
 cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
   if (!epi || epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
-  if (epi->exchange < CF_XCHG_AUTO || epi->exchange > CF_XCHG_GLOBAL) return CF_ERR_INVALID_ARG;
+  if (epi->exchange < CF_XCHG_AUTO || epi->exchange > CF_XCHG_GLOBAL_DYNAMIC) return CF_ERR_INVALID_ARG;
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
     const cf_op& op = epi->ops[i];
     if (!std::isfinite(op.scalar)) return CF_ERR_INVALID_ARG;
@@ -179,14 +179,16 @@ cf_status parse_epi(const cf_epi_desc* epi, EpiPlan* plan) {
 int choose_xmode(const EpiPlan& plan, const cf_epi_desc* epi, int64_t tiles_n) {
   if (plan.rowop == ROW_NONE || tiles_n == 1) return X_NONE;
   if (plan.rowop0 != ROW_NONE) return X_GLOBAL;  // chained stages: workspace exchange only
-  if (epi->exchange == CF_XCHG_GLOBAL) return X_GLOBAL;
+  if (epi->exchange == CF_XCHG_GLOBAL || epi->exchange == CF_XCHG_GLOBAL_DYNAMIC) return X_GLOBAL;
   if (epi->exchange == CF_XCHG_CLUSTER) return X_CLUSTER;
   return tiles_n <= kMaxClusterCtas ? X_CLUSTER : X_GLOBAL;
 }
 
+// Workspace of one reduction stage: per-tile partial statistics, then the
+// per-(strip, quarter) arrival counters and the work-item ticket counter.
 size_t ws_bytes_for(int64_t strips, int64_t tiles_n) {
   const size_t stats = (size_t)strips * (size_t)tiles_n * kBM * sizeof(float2);
-  const size_t counters = (size_t)strips * 4 * sizeof(unsigned);
+  const size_t counters = ((size_t)strips * 4 + 1) * sizeof(unsigned);
   return ((stats + 255) & ~size_t(255)) + ((counters + 255) & ~size_t(255));
 }
 
@@ -212,6 +214,8 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
     return CF_ERR_MISALIGNED;
   const int64_t kN = plan->cols ? M : N;  // the kernel's row length
   if (plan->rowop0 != ROW_NONE && epi->exchange == CF_XCHG_CLUSTER && kN > kBN) return CF_ERR_UNSUPPORTED_SHAPE;
+  // Chained stages keep the static order (no claimed work items).
+  if (plan->rowop0 != ROW_NONE && epi->exchange == CF_XCHG_GLOBAL_DYNAMIC) return CF_ERR_UNSUPPORTED_SHAPE;
   if (plan->rowop0 != ROW_NONE &&
       ((epi->stage0_gamma && !aligned16(epi->stage0_gamma)) || (epi->stage0_beta && !aligned16(epi->stage0_beta))))
     return CF_ERR_MISALIGNED;
@@ -445,10 +449,17 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
   //
   // The workspace exchange makes every tile of a strip (pair) wait for all of
   // its strip-mates, and each worker (a CTA pair, or a CTA) holds two tiles at
-  // a time (two TMEM accumulators), so a strip's tiles must fit in twice the
-  // resident workers; otherwise its last tiles could never start.  Strips too
-  // wide for the pairs run on 1-CTA tiles (twice the workers); wider still
-  // they are refused below.
+  // a time (two TMEM accumulators).  In the static order a worker's epilogue
+  // publishes its tiles' statistics one after another, so a worker holding
+  // two tiles of one strip would wait for itself: a strip's tiles must not
+  // outnumber the workers.  Single-stage programs may instead claim tiles
+  // as tickets and publish a worker's next tile while the current one waits
+  // (see the kernel): then a strip's tiles must fit in twice the workers
+  // that run.  Tickets are used for strips wider than the workers and when
+  // the caller asks for them (CF_XCHG_GLOBAL_DYNAMIC); the static order is
+  // faster on a GPU of its own.  Strips too wide for the pairs run on 1-CTA
+  // tiles (twice the workers); wider still they are refused below.
+  const int64_t per_worker = plan.rowop0 != ROW_NONE ? 1 : 2;
   bool want_pair = xmode != X_CLUSTER && strips % 2 == 0;
   int maxp = 0;
   if (want_pair) {
@@ -467,7 +478,7 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     }
     const int64_t pair_items = strips / 2 * tiles_n;
     const int64_t pairs = pair_items < maxp ? pair_items : maxp;
-    if (maxp <= 0 || (xmode == X_GLOBAL && tiles_n > 2 * pairs)) want_pair = false;
+    if (maxp <= 0 || (xmode == X_GLOBAL && tiles_n > per_worker * pairs)) want_pair = false;
   }
   if (p.b_mn_major)
     s = encode_2d(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, KB->ptr, sh.kN, sh.K, KB->ld * 2, 64, kBK);
@@ -492,14 +503,18 @@ cf_status cf_gemm_epilogue(const cf_matrix* A, const cf_matrix* B, const float* 
     const int64_t cap = (int64_t)per_sm * dev->sms;
     L.grid = (int)(p.num_items < cap ? p.num_items : cap);
     L.cluster = 1;
-    if (xmode == X_GLOBAL && tiles_n > 2 * (int64_t)L.grid) return CF_ERR_UNSUPPORTED_SHAPE;  // see above
+    if (xmode == X_GLOBAL && tiles_n > per_worker * (int64_t)L.grid) return CF_ERR_UNSUPPORTED_SHAPE;  // see above
   }
   if (xmode == X_GLOBAL) {
+    const int64_t workers = p.pair ? L.grid / 2 : L.grid;
+    p.tickets = (plan.rowop0 == ROW_NONE && (epi->exchange == CF_XCHG_GLOBAL_DYNAMIC || tiles_n > workers)) ? 1 : 0;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const size_t stats = ((size_t)strips * tiles_n * kBM * sizeof(float2) + 255) & ~size_t(255);
     p.ws_stats = reinterpret_cast<float2*>(ws);
     p.ws_count = reinterpret_cast<unsigned*>(ws + stats);
-    if (cudaMemsetAsync(p.ws_count, 0, (size_t)strips * 4 * sizeof(unsigned), st) != cudaSuccess) return CF_ERR_CUDA;
+    p.ws_ticket = p.ws_count + strips * 4;
+    if (cudaMemsetAsync(p.ws_count, 0, ((size_t)strips * 4 + 1) * sizeof(unsigned), st) != cudaSuccess)
+      return CF_ERR_CUDA;
     if (plan.rowop0 != ROW_NONE) {  // the first stage's region follows the last stage's
       p.ws_stats0 = reinterpret_cast<float2*>(ws + ws_stage);
       p.ws_count0 = reinterpret_cast<unsigned*>(ws + ws_stage + stats);

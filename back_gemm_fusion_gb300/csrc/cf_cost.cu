@@ -123,8 +123,9 @@ extern "C" cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* 
   const double Kp = std::ceil(K / 64.0) * 64.0;
   const double strips = std::ceil(kM / 128.0), tiles_n = std::ceil(kN / 256.0);
   // The fused call refuses rows whose tiles exceed twice the resident CTAs
-  // (the workspace exchange's launch rule).
-  if (n_red > 0 && tiles_n > 16.0 && tiles_n > 2.0 * d.sms) return CF_ERR_UNSUPPORTED_SHAPE;
+  // (once the CTAs with two reduction stages: the workspace exchange's
+  // launch rules).
+  if (n_red > 0 && tiles_n > 16.0 && tiles_n > (n_red > 1 ? 1.0 : 2.0) * d.sms) return CF_ERR_UNSUPPORTED_SHAPE;
   const double tiles = strips * tiles_n;
   const double per_sm = d.peak / d.sms;
   c.mainloop_us = 1e6 * 2.0 * 128.0 * 256.0 * Kp / (per_sm * kMainloopEff);

@@ -61,7 +61,7 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
   const void* k = select_kernel(L.rowop, L.xmode, L.p.pair != 0, L.variant);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   int na = 0;
   if (L.cluster > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -70,15 +70,9 @@ cudaError_t gemm_epi_launch(const GemmEpiLaunch& L, cudaStream_t s) {
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (L.xmode == X_GLOBAL && L.cluster == 1) {
-    // All CTAs must be co-resident: tiles of a strip wait for one another.
-    // The grid never exceeds the resident capacity (for clustered grids,
-    // the resident-cluster count from the occupancy query); for plain grids
-    // the cooperative attribute additionally asks the driver to guarantee it.
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na].val.cooperative = 1;
-    ++na;
-  }
+  // The workspace exchange needs no co-residency guarantee: tiles of a strip
+  // wait for one another, but items are claimed as tickets by running CTAs
+  // only (see the kernel), so CTAs that start late find the work taken.
   cfg.gridDim = dim3(L.grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_for(L.p.pair != 0);

@@ -62,12 +62,13 @@ struct Geo {
   static constexpr int kOffOut = kStages * kStageBytes;
   static constexpr int kOffSlots = kOffOut + kEpiWarps * kOutStageBytes;  // float2 [2][128]
   static constexpr int kOffVec = kOffSlots + 2 * kBM * 8;                 // float [kNumVec][kBN]
-  static constexpr int kOffBars = kOffVec + kNumVec * kBN * 4;
+  static constexpr int kOffEarly = kOffVec + kNumVec * kBN * 4;           // float [kEpiWarps][kBN]: early bias slices
+  static constexpr int kOffBars = kOffEarly + kEpiWarps * kBN * 4;
   // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[2][4], sempty[2][4], drain
-  // ..., vec_free, vec_full
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1 + 2;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32)
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + slack for the 1024-byte alignment
+  // ..., vec_free, vec_full, item[4], xdone[2]
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 8 + 8 + 1 + 2 + 4 + 2;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;  // tmem base (u32), abort flag (i32), item slots (i32 [4])
+  static constexpr int kSmemBytes = kOffMisc + 32 + 1024;   // + slack for the 1024-byte alignment
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -308,6 +309,78 @@ __device__ __forceinline__ bool global_exchange(const GemmEpiParams& p, float2* 
   return true;
 }
 
+// Pass 1 (the elementwise program applied and written back to TMEM, the
+// first local statistic) and pass 2 (the second statistic about the
+// segment's own mean or max) over one tile row segment: the tile's row
+// statistics.  vsm: the tile's staged vector slices [kNumVec][kBN] (only the
+// bias slice, VEC_BIAS = 0, is read when ROWOP0 == ROW_NONE); m: the row of
+// P (of P^T with COLS).  Chained programs (ROWOP0) first normalise with the
+// first stage's (sc0, sh0) and affine vectors.
+template <int ROWOP, bool RAG, bool COLS, int ROWOP0>
+__device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t taddr, int nch, int nv, int n0, int m,
+                                             const float* vsm, float r_bias, float r_gamma0, float r_beta0,
+                                             float sc0, float sh0) {
+  float2 st;
+  // Pass 1: elementwise program, kept in TMEM; first local statistic.
+  float s1 = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    float v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_wait_ld();
+    const int n = n0 + c * 32;
+    const bool tail = RAG && n + 32 > p.N;
+    if constexpr (ROWOP0 != ROW_NONE) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
+      if (COLS) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = v[j] * r_gamma0 + (ROWOP0 == ROW_LAYERNORM ? r_beta0 : 0.0f);
+      } else {
+        if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
+        if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
+      }
+    }
+    if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
+      const int o0 = ROWOP0 != ROW_NONE ? p.n_ops0 : 0;
+      const float* bs = vsm + VEC_BIAS * kBN + c * 32;
+      if (tail) apply_program<true, COLS>(p, v, n, m, o0, p.n_ops, bs, r_bias);
+      else apply_program<false, COLS>(p, v, n, m, o0, p.n_ops, bs, r_bias);
+      tmem_st32(taddr + c * 32, v);
+    }
+    if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (ROWOP == ROW_RMSNORM) s1 = fmaf(v[j], v[j], s1);
+      else if (ROWOP == ROW_SOFTMAX) s1 = fmaxf(s1, v[j]);
+      else s1 += v[j];
+    }
+  }
+  if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
+  if (ROWOP == ROW_RMSNORM) {
+    st = make_float2(s1, 0.0f);
+  } else {
+    // Pass 2: second local statistic about the segment's own max/mean.
+    const float ref = (ROWOP == ROW_SOFTMAX) ? s1 : RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
+    float s2 = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      tmem_wait_ld();
+      if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ROWOP == ROW_SOFTMAX ? -INFINITY : ref);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (ROWOP == ROW_SOFTMAX) s2 += ex2_approx((v[j] - ref) * kLog2e);
+        else { const float d = v[j] - ref; s2 = fmaf(d, d, s2); }
+      }
+    }
+    st = make_float2(ref, s2);
+  }
+
+  return st;
+}
+
 struct Work {
   int i, step, end, rank, tiles_n;
   __device__ bool valid() const { return i < end; }
@@ -361,6 +434,27 @@ __device__ __forceinline__ void item_coords(const GemmEpiParams& p, const Work& 
 // DRAM for every strip.  Items of a strip stay contiguous, so the row
 // statistics exchange keeps its strip-major schedule.
 
+// Workspace exchange (single-stage programs), when the host asks for it:
+// work items are claimed in the strip-major order above as tickets from a
+// global counter, so only CTAs that are running ever hold items (a
+// statically assigned item of a CTA that is not resident -- another kernel
+// holds its SM -- stalls its strip-mates until that CTA starts, or until
+// the bounded waits give up).  The static assignment is faster on a GPU of
+// its own (its rounds keep the tiles of a strip in lockstep; claims made as
+// strips complete drift off the strip boundaries), so it stays the default.  A worker claims an item
+// once its item two back has finished its strip exchange, and while an item
+// waits for its strip the epilogue publishes the statistics of the worker's
+// next item (see the epilogue), so a worker holding two tiles of one strip
+// never waits for itself; a strip's tiles then fit in twice the workers
+// that run, whatever the launched grid.
+__device__ __forceinline__ void ticket_coords(const GemmEpiParams& p, int idx, int rank, int& strip, int& tile) {
+  const int T = p.tiles_n;
+  const int u = idx / T;  // row-strip unit: a strip, or a strip pair with CTA pairs
+  tile = idx - u * T;
+  if (u & 1) tile = T - 1 - tile;
+  strip = p.pair ? 2 * u + rank : u;
+}
+
 // ROWOP0 != ROW_NONE: the program has two chained row reductions, ROWOP0
 // (LayerNorm or RMSNorm) then ROWOP; only the per-tile and workspace
 // exchanges are instantiated for it.
@@ -391,9 +485,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   auto bar = [&](int idx) -> uint32_t { return sbase + kOffBars + 8 * idx; };
   const int BAR_FULL = 0, BAR_EMPTY = kStages, BAR_TFULL = 2 * kStages, BAR_TEMPTY = 2 * kStages + 2;
   const int BAR_SFULL = 2 * kStages + 4, BAR_SEMPTY = 2 * kStages + 12, BAR_DRAIN = 2 * kStages + 20;
-  const int BAR_VFREE = 2 * kStages + 21, BAR_VFULL = 2 * kStages + 22;
+  const int BAR_VFREE = 2 * kStages + 21, BAR_VFULL = 2 * kStages + 22, BAR_ITEM = 2 * kStages + 23,
+            BAR_XDONE = 2 * kStages + 27;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  // Tickets: the claimed ticket of local item t sits in slot t & 3 (filled
+  // when item t - 2 has finished its exchange, read by every role of both
+  // CTAs of a pair before item t - 2 releases its accumulator).
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  const int sched_items = p.pair ? p.pair_items : p.num_items;
+  const Work w0 = make_work<XMODE>(p);
+  // Work items from tickets (the workspace exchange of single-stage
+  // programs, when the host asks for them: see its launch rules); otherwise
+  // the static strip-major assignment.
+  constexpr bool kTicketsOk = XMODE == X_GLOBAL && ROWOP0 == ROW_NONE;
+  const bool tickets = kTicketsOk && p.tickets != 0;
   const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
 
   int cn = 1;
@@ -416,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_VFREE), kEpiWarps);
     mbar_init(bar(BAR_VFULL), kEpiWarps);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(BAR_ITEM + i), 1);
+    mbar_init(bar(BAR_XDONE), kEpiWarps);  // this CTA's epilogue warps
+    mbar_init(bar(BAR_XDONE + 1), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -448,9 +557,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       // B tiles are reread by every strip: keep them in L2 ahead of the
       // streamed output.
       const uint64_t b_policy = l2_policy_evict_last();
-      for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next()) {
+      // Tickets (the leader of a pair claims for both CTAs): claim local item
+      // tn once item tn - 2 (the last item on accumulator tn & 1) has
+      // finished its strip exchange -- every tile of its strip has been
+      // claimed by then, so item tn belongs to another strip and item tn - 2
+      // never waits for it -- and hand it to this CTA's MMA and epilogue
+      // roles (and to the pair's peer).  Claims are made as late as that:
+      // claiming earlier spreads the start of a strip's tiles over time and
+      // lengthens the exchange waits (measured: claiming the next item while
+      // the current one's stages were still being issued cut GELU + RMSNorm
+      // 8192 x 4096 x 4096 from ~1490 to ~1020 TFLOP/s).
+      int claimed = -1;  // the last local item claimed
+      auto claim = [&](int tn) {
+        int v = (int)atomicAdd(p.ws_ticket, 1u);
+        if (v >= sched_items) v = -1;  // no work left
+        item_slot[tn & 3] = v;
+        if (CTA2) {
+          st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(item_slot) + (tn & 3)), 1u), (uint32_t)v);
+          mbar_arrive_cluster(bar(BAR_ITEM + (tn & 3)), 1u);
+        }
+        mbar_arrive(bar(BAR_ITEM + (tn & 3)));
+        claimed = tn;
+      };
+      for (int t = 0; ok; ++t) {
         int strip, tile;
-        item_coords<XMODE>(p, w, strip, tile);
+        if (tickets) {
+          int idx;
+          if (leader) {
+            if (claimed < t) {
+              if (!mbar_wait(bar(BAR_XDONE + (t & 1)), ((t >> 1) & 1) ^ 1, wc)) { ok = false; break; }
+              claim(t);
+            }
+            idx = item_slot[t & 3];
+          } else {
+            if (!mbar_wait<true>(bar(BAR_ITEM + (t & 3)), (t >> 2) & 1, wc)) { ok = false; break; }
+            idx = item_slot[t & 3];
+          }
+          if (idx < 0) break;
+          ticket_coords(p, idx, (int)pair_rank, strip, tile);
+        } else {
+          Work w = w0;
+          w.i += t * w.step;
+          if (!w.valid()) break;
+          item_coords<XMODE>(p, w, strip, tile);
+        }
         const int m0 = strip * kBM, n0 = tile * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1, wc)) { ok = false; break; }
@@ -511,10 +661,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0;
       int t = 0;
       bool ok = true;
-      for (Work w = make_work<XMODE>(p); ok && w.valid(); w.next(), ++t) {
+      for (;; ++t) {
         const int acc = t & 1;
         // CTA2: the peer's epilogue arrives remotely, so acquire at cluster scope.
         if (!mbar_wait<CTA2>(bar(BAR_TEMPTY + acc), ((t >> 1) & 1) ^ 1, wc)) { ok = false; break; }
+        if (tickets) {
+          if (!mbar_wait(bar(BAR_ITEM + (t & 3)), (t >> 2) & 1, wc)) { ok = false; break; }
+          if (item_slot[t & 3] < 0) break;  // no work left
+        } else {
+          if (w0.i + t * w0.step >= w0.end) break;
+        }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -557,10 +713,79 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     float2* slots = reinterpret_cast<float2*>(smem + kOffSlots);
     float* vsm = reinterpret_cast<float*>(smem + G::kOffVec);  // [kNumVec][kBN] this tile's vector slices
     const bool stage_vec = !COLS && (p.bias || p.gamma || p.beta || p.gamma0 || p.beta0);
+    // Workspace exchange: publishing an item's statistics to its strip.
+    auto publish = [&](int strip_, int tile_, float2 st_) {
+      float2* wsr = p.ws_stats + (size_t)strip_ * p.tiles_n * kBM + row;
+      __stcg(wsr + (size_t)tile_ * kBM, st_);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(p.ws_count + strip_ * 4 + q, 1u);
+    };
+    // Tickets: while item t waits for its strip, this warp publishes the
+    // statistics of its next item t + 1 as soon as that item's main loop is
+    // done, when t + 1 is a tile of the same strip.  The epilogue handles a
+    // worker's items in order: without this the first tile would wait for
+    // the second's statistics, which are published only after the first
+    // finishes.  Item t + 1's main loop needs only the accumulator that
+    // item t - 1 has released, so its statistics never wait on an exchange.
+    // (A next item of another strip is never needed: along any chain of
+    // waits between different strips the strips only go down in the
+    // strip-major ticket order, and the lowest incomplete strip waits for
+    // nobody.)  The bias slice comes from the global vector into this warp's
+    // own buffer (the shared staging belongs to item t).  The barriers are
+    // probed without blocking (test_wait), so the wait keeps watching its
+    // strip's counter.
+    int early_t = -1;
+    float2 early_st = make_float2(0.0f, 0.0f);
+    int checked_t = -1;  // the next item was looked at and needs no early statistics
+    float* ebuf = reinterpret_cast<float*>(smem + G::kOffEarly) + (warp - 2) * kBN;
+    auto try_early = [&](int tn, int strip_now) {
+      const int an = tn & 1;
+      const uint32_t par = (uint32_t)((tn >> 1) & 1), ipar = (uint32_t)((tn >> 2) & 1);
+      if (!__all_sync(0xffffffffu, CTA2 ? mbar_test_wait_cluster(bar(BAR_ITEM + (tn & 3)), ipar)
+                                        : mbar_test_wait(bar(BAR_ITEM + (tn & 3)), ipar)))
+        return;
+      const int idx = item_slot[tn & 3];
+      int strip1, tile1;
+      if (idx >= 0) ticket_coords(p, idx, (int)pair_rank, strip1, tile1);
+      if (idx < 0 || strip1 != strip_now) {
+        checked_t = tn;  // no next item, or one of another strip
+        return;
+      }
+      if (!__all_sync(0xffffffffu, mbar_test_wait(bar(BAR_TFULL + an), par))) return;
+      tc_fence_after();
+      const int m1 = strip1 * kBM, n1 = tile1 * kBN;
+      const int nv1 = RAG ? min(kBN, p.N - n1) : kBN;
+      const int nch1 = RAG ? (nv1 + 31) >> 5 : kBN / 32;
+      float rb = 0.0f;
+      if (COLS) {
+        if (p.bias && m1 + row < p.M) rb = __ldg(p.bias + m1 + row);
+      } else if (p.bias) {
+        for (int c4 = 4 * lane; c4 < kBN; c4 += 128) *reinterpret_cast<float4*>(ebuf + c4) = ld4<RAG>(p.bias, n1 + c4, p.N);
+        __syncwarp();
+      }
+      const uint32_t taddr1 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(an * kBN);
+      const float2 st1 = tile_stats<ROWOP, RAG, COLS, ROW_NONE>(p, taddr1, nch1, nv1, n1, m1 + row, ebuf, rb, 1.0f,
+                                                                0.0f, 1.0f, 0.0f);
+      publish(strip1, tile1, st1);
+      early_t = tn;
+      early_st = st1;
+    };
     int t = 0;
-    for (Work w = make_work<XMODE>(p); w.valid(); w.next(), ++t) {
+    for (;; ++t) {
       int strip, tile;
-      item_coords<XMODE>(p, w, strip, tile);
+      if (tickets) {
+        // CTA2: the leader fills the peer's slot remotely (cluster scope).
+        if (!__all_sync(0xffffffffu, mbar_wait<CTA2>(bar(BAR_ITEM + (t & 3)), (t >> 2) & 1, wc))) break;
+        const int idx = item_slot[t & 3];
+        if (idx < 0) break;
+        ticket_coords(p, idx, (int)pair_rank, strip, tile);
+      } else {
+        Work w = w0;
+        w.i += t * w.step;
+        if (!w.valid()) break;
+        item_coords<XMODE>(p, w, strip, tile);
+      }
       const int m0 = strip * kBM, n0 = tile * kBN;
       const int nv = RAG ? min(kBN, p.N - n0) : kBN;  // valid columns: fewer in a ragged last tile
       const int nch = RAG ? (nv + 31) >> 5 : kBN / 32;  // 32-column chunks holding them
@@ -657,62 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       float2 st = Stat<ROWOP>::identity();
       float scale_a = 1.0f, shift_a = 0.0f;  // y = gamma * (x * scale_a + shift_a) (+ beta)
       if (ROWOP != ROW_NONE) {
-        // Pass 1: elementwise program, kept in TMEM; first local statistic.
-        float s1 = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          tmem_wait_ld();
-          const int n = n0 + c * 32;
-          const bool tail = RAG && n + 32 > p.N;
-          if constexpr (ROWOP0 != ROW_NONE) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
-            if (COLS) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = v[j] * r_gamma0 + (ROWOP0 == ROW_LAYERNORM ? r_beta0 : 0.0f);
-            } else {
-              if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
-              if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
-            }
-          }
-          if (ROWOP0 != ROW_NONE || p.n_ops > 0) {
-            const int o0 = ROWOP0 != ROW_NONE ? p.n_ops0 : 0;
-            const float* bs = vsm + VEC_BIAS * kBN + c * 32;
-            if (tail) apply_program<true, COLS>(p, v, n, m0 + row, o0, p.n_ops, bs, r_bias);
-            else apply_program<false, COLS>(p, v, n, m0 + row, o0, p.n_ops, bs, r_bias);
-            tmem_st32(taddr + c * 32, v);
-          }
-          if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (ROWOP == ROW_RMSNORM) s1 = fmaf(v[j], v[j], s1);
-            else if (ROWOP == ROW_SOFTMAX) s1 = fmaxf(s1, v[j]);
-            else s1 += v[j];
-          }
-        }
-        if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
-        if (ROWOP == ROW_RMSNORM) {
-          st = make_float2(s1, 0.0f);
-        } else {
-          // Pass 2: second local statistic about the segment's own max/mean.
-          const float ref = (ROWOP == ROW_SOFTMAX) ? s1 : RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
-          float s2 = 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < nch; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            tmem_wait_ld();
-            if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ROWOP == ROW_SOFTMAX ? -INFINITY : ref);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (ROWOP == ROW_SOFTMAX) s2 += ex2_approx((v[j] - ref) * kLog2e);
-              else { const float d = v[j] - ref; s2 = fmaf(d, d, s2); }
-            }
-          }
-          st = make_float2(ref, s2);
-        }
+        const bool pre = tickets && early_t == t;  // published while the previous item waited
+        if (pre) st = early_st;
+        else st = tile_stats<ROWOP, RAG, COLS, ROWOP0>(p, taddr, nch, nv, n0, m0 + row, vsm, r_bias, r_gamma0, r_beta0,
+                                                       sc0, sh0);
 
         // Level 3: statistics of the whole row across the CTAs of the strip.
         if (XMODE == X_CLUSTER) {
@@ -740,22 +913,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             for (int r = 0; r < cn; ++r) mbar_arrive_cluster(bar(BAR_SEMPTY + b * 4 + q), (uint32_t)r);
           }
         } else if (XMODE == X_GLOBAL) {
-          float2* wsrow = p.ws_stats + (size_t)strip * p.tiles_n * kBM + row;
-          __stcg(wsrow + (size_t)tile * kBM, st);
-          __threadfence();
-          __syncwarp();
-          unsigned* cnt = p.ws_count + strip * 4 + q;
-          if (lane == 0) red_release_gpu_add(cnt, 1u);
+          if (!pre) publish(strip, tile, st);
+          // Wait (bounded, acquire) until every tile of the strip has
+          // published; the loop's control flow is uniform across the warp.
+          const unsigned* cnt = p.ws_count + strip * 4 + q;
           bool ok = true;
-          if (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-            const long long t0 = clock64();
-            while (ld_acquire_gpu(cnt) < (unsigned)p.tiles_n) {
-              __nanosleep(64);
-              if (*abort_flag) { ok = false; break; }
-              if (clock64() - t0 > p.timeout_cycles) { record_timeout(wc); ok = false; break; }
+          const long long t0 = clock64();
+          while (!__all_sync(0xffffffffu, ld_acquire_gpu(cnt) >= (unsigned)p.tiles_n)) {
+            if constexpr (kTicketsOk) {
+              if (tickets && early_t != t + 1 && checked_t != t + 1) try_early(t + 1, strip);
+            }
+            __nanosleep(64);
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, clock64() - t0 > p.timeout_cycles)) {
+              if (lane == 0) record_timeout(wc);
+              ok = false;
+              break;
             }
           }
-          if (!__all_sync(0xffffffffu, ok)) break;
+          if (!ok) break;
+          // The strip is complete: the producer may claim this warp's item
+          // t + 2 (the leader's warps signal for a CTA pair).
+          if (tickets) {
+            __syncwarp();
+            if (lane == 0 && leader) mbar_arrive(bar(BAR_XDONE + (t & 1)));
+          }
+          const float2* wsrow = p.ws_stats + (size_t)strip * p.tiles_n * kBM + row;
           float2 tot = __ldcg(wsrow);
           float n_acc = tile_cols<RAG>(p, 0);
           for (int j = 1; j < p.tiles_n; ++j) {

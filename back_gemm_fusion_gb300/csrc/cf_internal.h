@@ -57,6 +57,8 @@ struct GemmEpiParams {
   int out_bf16;           // 1: bf16 output (rounded to nearest even), 0: fp32
   float2* ws_stats;       // [strips][tiles_n][kBM] partial row statistics
   unsigned* ws_count;     // [strips][4] arrival counters (cleared by the host)
+  unsigned* ws_ticket;    // workspace exchange: the next work item to claim (cleared by the host)
+  int tickets;            // 1: work items from ws_ticket (single-stage programs), 0: static assignment
   unsigned* status;       // device status word
   long long timeout_cycles;
 };

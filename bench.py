@@ -473,7 +473,7 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
     # Other row-statistics exchanges of the same fused kernel, same run.
     xvar = {}
     if variants and not wl.is_b2b and any(o[0] in ("layernorm", "rmsnorm", "softmax") for o in wl.case.ops):
-        for xch in ("cluster", "global"):
+        for xch in ("cluster", "global", "global_dynamic"):
             if xch == wl.exchange:
                 continue
             try:
@@ -734,7 +734,7 @@ def main():
                              "target_attention", "column_layernorm"])
     ap.add_argument("--rows", type=int, default=64,
                     help="batch of the mlp_bottom (rows) and target_attention (users) workloads (1..64)")
-    ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global"],
+    ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global", "global_dynamic"],
                     help="row-statistics exchange of the fused GEMM-epilogue kernel")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--ref-step-seconds", type=float, default=5.0, help="oracle seconds per reference step")

@@ -124,7 +124,13 @@ typedef enum {
 typedef enum {
   CF_XCHG_AUTO = 0,    /* cluster DSMEM when the strip fits one cluster, else workspace */
   CF_XCHG_CLUSTER = 1, /* force the thread-block-cluster DSMEM exchange (<= 16 CTAs)  */
-  CF_XCHG_GLOBAL = 2   /* force per-tile partial statistics through the workspace    */
+  CF_XCHG_GLOBAL = 2,  /* force per-tile partial statistics through the workspace    */
+  /* The workspace exchange with work items claimed from a counter by the
+   * CTAs that run (one reduction stage only): for a GPU shared with other
+   * work (other streams, MPS), where not every CTA of the launch may become
+   * resident.  Slower on a GPU of its own (about 4-25% on the measured
+   * shapes). */
+  CF_XCHG_GLOBAL_DYNAMIC = 3
 } cf_exchange;
 
 /* A tiny epilogue program: a linear chain of ops (the Stage-Stream model:
@@ -187,10 +193,19 @@ typedef struct {
  * == 0 with K >= 64 (a ragged last 64-wide K block reads zeros), all
  * pointers and leading dims 16-byte aligned; the cluster exchange takes rows
  * of at most 16 tiles (N <= 4096).  Through the workspace every tile of a
- * row strip waits for its strip-mates and each resident CTA holds two tiles,
- * so a row may span at most twice the resident CTAs: N <= 77,824 on a
- * 152-SM GB300 (CTA pairs up to N <= 38,912, wider rows on 1-CTA tiles);
- * wider rows return CF_ERR_UNSUPPORTED_SHAPE.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
+ * row strip waits for its strip-mates and each CTA (or CTA pair) holds two
+ * tiles.  By default a CTA takes fixed tiles in a strip-major order, which
+ * needs every CTA of the launch to become resident (the grid never exceeds
+ * what fits on the device; kernels running beside it only delay it) and a
+ * row of at most as many tiles as CTAs: a CTA must not hold two tiles of
+ * one row.  With one reduction stage, wider rows (up to twice the CTAs) and
+ * CF_XCHG_GLOBAL_DYNAMIC take tiles from a counter in the workspace instead,
+ * claimed by the CTAs that run, so a row may span at most twice the CTAs
+ * that run: N <= 77,824 on a 152-SM GB300 (CTA pairs up to N <= 38,912,
+ * wider rows on 1-CTA tiles).  With two chained stages rows are limited to
+ * N <= 38,912 (CTA pairs up to N <= 19,456) and CF_XCHG_GLOBAL_DYNAMIC
+ * returns CF_ERR_UNSUPPORTED_SHAPE.  Wider rows return
+ * CF_ERR_UNSUPPORTED_SHAPE.  Violations return CF_ERR_UNSUPPORTED_SHAPE /
  * CF_ERR_MISALIGNED without launching anything.  M == 0 or N == 0 returns
  * CF_OK without launching.
  */

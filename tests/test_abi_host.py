@@ -251,6 +251,24 @@ def test_b2b_shape_rules(lib):
     assert call(256, 256, 512, 1100, op="relu", trans=False) == 2       # MLP, C = 5 > 4
 
 
+def test_dynamic_exchange_rules(lib):
+    # CF_XCHG_GLOBAL_DYNAMIC (3) is accepted for single-stage programs and
+    # refused for chained ones; larger values are argument errors.
+    from back_gemm_fusion_gb300.binding import epi_desc
+    A, B, O = _mats()
+    ok = (0, 4, 8)
+
+    def call(ops, exchange):
+        d = epi_desc(ops)
+        d.exchange = exchange
+        return lib.cf_gemm_epilogue(ctypes.byref(A), ctypes.byref(B), 0x40000, 0x50000, 0x60000, ctypes.byref(d),
+                                    ctypes.byref(O), 0x80000, 1 << 24, None)
+
+    assert call([("bias",), ("layernorm", 1e-5)], 3) in ok
+    assert call([("bias",), ("layernorm", 1e-5), ("rmsnorm", 1e-6)], 3) == 2
+    assert call([("bias",), ("layernorm", 1e-5)], 4) == 1
+
+
 def test_b2b_key_split_rules(lib):
     # Descriptor version 2 carries key_split (0 auto, 1 off, 2..8 CTAs per
     # query block); out-of-range values are argument errors found on the
@@ -308,9 +326,10 @@ def test_column_axis_rules(lib):
     ws_col = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(Bt), ctypes.byref(epi_desc(LN, axis="col")))
     ws_row = lib.cf_workspace_size(ctypes.byref(A), ctypes.byref(Bt), ctypes.byref(epi_desc(LN, axis="row")))
     # Statistics (strips x tiles x 128 rows x 8 bytes) then 16 bytes of
-    # counters per strip, each region padded to 256 bytes.
+    # counters per strip and a 4-byte ticket counter, each region padded to
+    # 256 bytes.
     assert ws_col == 4 * 16 * 128 * 8 + 256      # 4 strips of P^T, 16 tiles along M
-    assert ws_row == 32 * 2 * 128 * 8 + 512      # 32 strips of P, 2 tiles along N
+    assert ws_row == 32 * 2 * 128 * 8 + 768      # 32 strips of P, 2 tiles along N (516 -> 768)
     # An unknown axis is rejected by the unfused path too.
     dd = epi_desc(LN, axis="col")
     dd.axis = 5
