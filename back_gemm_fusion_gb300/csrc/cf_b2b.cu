@@ -730,10 +730,11 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Shared memory: the C slots, the barriers, then as many ring stages as fit
 // (C = 1: 6, C = 2: 5, C = 4: 3); the host computes the ring depth.
-// ring_full[6], ring_empty[6], s_full[2], s_free[2], slot_full, slot_empty, o_full, o_empty, drain,
-// slot_written (the F warps finished writing this CTA's S' chunk)
-constexpr int BAR_RF = 0, BAR_RE = 6, BAR_SF = 12, BAR_SFREE = 14, BAR_SLF = 16, BAR_SLE = 17, BAR_OF = 18,
-              BAR_OE = 19, BAR_DRAIN = 20, BAR_SLW = 21, kNumBars = 22;
+// ring_full[6], ring_empty[6], s_full[2], s_free[2], slot_full[4] (slot k holds CTA k's chunk;
+// a peer's slot fills with its bulk copy), slot_empty (this CTA's own slot is free: every CTA
+// consumed it), o_full, o_empty, drain, slot_written (the F warps finished writing this CTA's S' chunk)
+constexpr int BAR_RF = 0, BAR_RE = 6, BAR_SF = 12, BAR_SFREE = 14, BAR_SLF = 16, BAR_SLE = 20, BAR_OF = 21,
+              BAR_OE = 22, BAR_DRAIN = 23, BAR_SLW = 24, kNumBars = 25;
 constexpr int kSmemLimit = 232448;
 constexpr int kFixedBytes = 1024 + kNumBars * 8 + 16;  // alignment slack, barriers, misc
 __host__ __device__ constexpr int ring_for(int C) {
@@ -795,8 +796,13 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       mbar_init(bar(BAR_SF + i), 1);
       mbar_init(bar(BAR_SFREE + i), kEpiWarps);
     }
-    mbar_init(bar(BAR_SLF), 1);   // one local arrive (+ the peers' bytes)
-    mbar_init(bar(BAR_SLE), C);   // one multicast commit from every CTA's second GEMM
+    // A peer's slot: one arrival by this CTA's GEMM2 issuer (expecting the
+    // copy's bytes) per round, armed for the first round here.
+    for (int k = 0; k < C; ++k) {
+      mbar_init(bar(BAR_SLF + k), 1);
+      if (k != (int)rank) mbar_arrive_expect_tx(bar(BAR_SLF + k), kSlotBytes);
+    }
+    mbar_init(bar(BAR_SLE), C);   // one commit from every CTA's second GEMM on this CTA's chunk
     mbar_init(bar(BAR_OF), 1);
     mbar_init(bar(BAR_OE), kEpiWarps);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -851,7 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         return true;
       };
       auto load_g2 = [&](int b, int r) -> bool {
-        for (int c2 = 0; c2 < C; ++c2) {
+        for (int i2 = 0; i2 < C; ++i2) {
+          const int c2 = ((int)rank + i2) % C;  // the MMA issuer's chunk order: its own chunk first
           for (int kh = 0; kh < 2; ++kh) {
             if (!acquire()) return false;
             const uint32_t dst = sbase + kOffRing + rs * kStageBytes;
@@ -880,7 +887,6 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 128, p.w1_k_major ? 0u : 1u);
       const uint32_t id_o = idesc_bf16_f32(128, 256, 1u);
-      const uint16_t all = (uint16_t)((1u << C) - 1u);
       uint32_t rs = 0, rph = 0;
       uint32_t g = 0;  // global round counter
       int t = 0;
@@ -918,10 +924,19 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
           // The next-but-one S chunk only needs the F warps to have read S(r):
           // issue it first so it overlaps the S' exchange of round r.
           if (r + 2 < R && !(ok = g1(g + 2))) break;
-          if (!mbar_wait(bar(BAR_SLF), g & 1, wc)) { ok = false; break; }
           if (r == 0 && !mbar_wait(bar(BAR_OE), (t & 1) ^ 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          for (int c2 = 0; ok && c2 < C; ++c2) {
+          // The round's chunks, this CTA's own first (its F warps wrote it
+          // locally), then the peers' in turn as their copies land, so the
+          // second GEMM starts before the whole exchange is done.
+          for (int i2 = 0; ok && i2 < C; ++i2) {
+            const int c2 = ((int)rank + i2) % C;
+            if (c2 == (int)rank) {
+              if (!mbar_wait(bar(BAR_SLW), g & 1, wc)) { ok = false; break; }
+            } else {
+              if (!mbar_wait(bar(BAR_SLF + c2), g & 1, wc)) { ok = false; break; }
+              mbar_arrive_expect_tx(bar(BAR_SLF + c2), kSlotBytes);  // arm the next round's copy
+            }
+            tc_fence_after();
             for (int kh = 0; kh < 2; ++kh) {
               if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
               tc_fence_after();
@@ -930,14 +945,14 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_ss(tmem_base + 256, a_lo + kk * (32u >> 4), dsl.hi, w_lo + kk * (2048u >> 4), dw2.hi, id_o,
-                       (r | c2 | kh | kk) ? 1u : 0u);
+                       (r | i2 | kh | kk) ? 1u : 0u);
               mma_commit(bar(BAR_RE + rs));
               if (++rs == kRing) { rs = 0; rph ^= 1; }
             }
+            // CTA c2 may refill its slot once every CTA has consumed it.
+            if (ok) mma_commit_multicast(bar(BAR_SLE), (uint16_t)(1u << c2));
           }
           if (!ok) break;
-          // Every CTA of the cluster may refill its slot once all have consumed it.
-          mma_commit_multicast(bar(BAR_SLE), all);
         }
         if (!ok) break;
         mma_commit(bar(BAR_OF));
@@ -983,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
-        // The slots may be overwritten once every CTA finished the previous round.
+        // This CTA's slot may be overwritten once every CTA consumed its previous chunk.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLE), (g & 1) ^ 1, wc))) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < 4; ++c) store_row_packed_sw128(my_slot, row, c * 32, w[c]);
@@ -994,10 +1009,10 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
           // The whole chunk is in this CTA's slot: publish it to the peers.
           if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLW), g & 1, wc))) { ok = false; break; }
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar(BAR_SLF), (uint32_t)(C - 1) * kSlotBytes);
+            // Each copy completes on the peer's barrier for this CTA's slot.
             for (int pr = 1; pr < C; ++pr) {
               const uint32_t peer = (rank + pr) % C;
-              bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF), peer);
+              bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF + (int)rank), peer);
             }
           }
         }
