@@ -668,21 +668,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int r = 0; r < C; ++r) mbar_arrive_cluster(bar(BAR_STG + q), (uint32_t)r);
         }
         if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_STG + q), 0, wc))) break;
-        const int kb = (32 * (int)crank) / C, ke = (32 * ((int)crank + 1)) / C;
+        // This CTA's slice: eight-column units (32 bytes of fp32 output, one
+        // whole sector per store when the rows are 32-byte aligned).
+        const int ub = (16 * (int)crank) / C, ue = (16 * ((int)crank + 1)) / C;
         const uint32_t srow_addr = sbase + kOffW1 + row * 512;
         const bool live = mb * kTile + row < p.M;  // rows past M (ragged last block) are not stored
 #pragma unroll 1
-        for (int k = kb; k < ke; ++k) {
-          const uint32_t a = srow_addr + ((uint32_t)(k ^ (row & 31)) << 4);
-          float4 acc = ld_shared_cluster_f4(mapa_shared(a, 0));
-          for (int r = 1; r < C; ++r) {
-            const float4 v = ld_shared_cluster_f4(mapa_shared(a, (uint32_t)r));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        for (int u8 = ub; u8 < ue; ++u8) {
+          float4 acc[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int k = 2 * u8 + h;
+            const uint32_t a = srow_addr + ((uint32_t)(k ^ (row & 31)) << 4);
+            acc[h] = ld_shared_cluster_f4(mapa_shared(a, 0));
+            for (int r = 1; r < C; ++r) {
+              const float4 v = ld_shared_cluster_f4(mapa_shared(a, (uint32_t)r));
+              acc[h].x += v.x;
+              acc[h].y += v.y;
+              acc[h].z += v.z;
+              acc[h].w += v.w;
+            }
           }
-          if (live && 4 * k < p.n2) store4<OBF16>(p.out, orow + 4 * k, acc, p.n2 - 4 * k);
+          const int col = 8 * u8;
+          if (!live || col >= p.n2) continue;
+          if (p.out_v8 && col + 8 <= p.n2) {
+            uint32_t w[8];
+            if (OBF16) {
+              // 8 bf16 values: half a sector (16 bytes), still one store.
+              const float e[8] = {acc[0].x, acc[0].y, acc[0].z, acc[0].w, acc[1].x, acc[1].y, acc[1].z, acc[1].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * j], e[2 * j + 1]);
+                w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              w[0] = __float_as_uint(acc[0].x); w[1] = __float_as_uint(acc[0].y);
+              w[2] = __float_as_uint(acc[0].z); w[3] = __float_as_uint(acc[0].w);
+              w[4] = __float_as_uint(acc[1].x); w[5] = __float_as_uint(acc[1].y);
+              w[6] = __float_as_uint(acc[1].z); w[7] = __float_as_uint(acc[1].w);
+              st_global_v8(static_cast<float*>(p.out) + orow + col, w);
+            }
+          } else {
+            store4<OBF16>(p.out, orow + col, acc[0], p.n2 - col);
+            if (col + 4 < p.n2) store4<OBF16>(p.out, orow + col + 4, acc[1], p.n2 - col - 4);
+          }
         }
       } else {
 #pragma unroll

@@ -184,6 +184,20 @@ def target_attention(seed: int = 0, batch: int = 64, targets: int = 512, behavio
                    Q, Kt, V)
 
 
+def attention_long_keys(seed: int = 0, heads: int = 8, queries: int = 128, keys: int = 16384, d: int = 128,
+                        op: str = "scale_softmax") -> B2BCase:
+    """Few query rows over a long key sequence (one 128-query block per head,
+    a prefill chunk or decode batch against a long context): Q, K, V ~ N(0, 1),
+    scale 1/sqrt(d).  With fewer query blocks than SMs this is the shape the
+    key-range split across a cluster is for."""
+    rng = np.random.default_rng(seed)
+    Q = _bf16(rng.standard_normal((heads, queries, d)))
+    Kt = _bf16(rng.standard_normal((heads, keys, d)))
+    V = _bf16(rng.standard_normal((heads, keys, d)))
+    return B2BCase(f"b2b_attention_long_keys_{op}", heads, queries, d, keys, d, op, 1.0 / math.sqrt(d), True,
+                   Q, Kt, V)
+
+
 def to_f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     """Exact float64 copy of a bf16/fp32 CPU tensor (for the oracle)."""
     if t is None:

@@ -46,26 +46,40 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # sources (kernel_source_hash) matches the one the counters were taken with
 # (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "attention_relu": {"read": 805367552, "write": 494812416, "src": "e3aaae959dc1d804"},
-    "attention_softmax": {"read": 805390848, "write": 495150336, "src": "e3aaae959dc1d804"},
-    "chained_ln_gelu_rms": {"read": 116142848, "write": 87649024, "src": "80d4303150507d8f"},
-    "column_layernorm": {"read": 305788928, "write": 99484672, "src": "80d4303150507d8f"},
-    "gelu_rmsnorm": {"read": 116979712, "write": 89708544, "src": "80d4303150507d8f"},
-    "layernorm_256": {"read": 312832, "write": 0, "src": "80d4303150507d8f"},
-    "mlp_b2b": {"read": 50433280, "write": 15155968, "src": "e3aaae959dc1d804"},
-    "mlp_bottom": {"read": 317184, "write": 0, "src": "e3aaae959dc1d804"},
-    "postnorm_layernorm": {"read": 200069376, "write": 93125120, "src": "80d4303150507d8f"},
-    "scaled_softmax": {"read": 1385517312, "write": 238905088, "src": "80d4303150507d8f"},
-    "target_attention": {"read": 15000832, "write": 0, "src": "e3aaae959dc1d804"},
+    "attention_long_keys": {"read": 67438080, "write": 244480, "src": "6417a31d5978b06b"},
+    "attention_relu": {"read": 805384960, "write": 500814592, "src": "6417a31d5978b06b"},
+    "attention_softmax": {"read": 805946880, "write": 501840384, "src": "6417a31d5978b06b"},
+    "chained_ln_gelu_rms": {"read": 110306816, "write": 88747008, "src": "c8fb2f7ceaf75b55"},
+    "column_layernorm": {"read": 362330880, "write": 101095936, "src": "c8fb2f7ceaf75b55"},
+    "gelu_rmsnorm": {"read": 110800640, "write": 92438016, "src": "c8fb2f7ceaf75b55"},
+    "layernorm_256": {"read": 309248, "write": 0, "src": "c8fb2f7ceaf75b55"},
+    "mlp_b2b": {"read": 50394624, "write": 23421696, "src": "6417a31d5978b06b"},
+    "mlp_bottom": {"read": 316416, "write": 0, "src": "6417a31d5978b06b"},
+    "postnorm_layernorm": {"read": 194507008, "write": 96028672, "src": "c8fb2f7ceaf75b55"},
+    "scaled_softmax": {"read": 1396701184, "write": 239538688, "src": "c8fb2f7ceaf75b55"},
+    "target_attention": {"read": 15001856, "write": 0, "src": "6417a31d5978b06b"},
 }
 
 
-# Global store bytes of one fused launch, from the L2-side store counters
+# Global store bytes of one fused launch, from the SM-to-L2 store counters
 # (`ncu --metrics l1tex__m_l1tex2xbar_write_bytes_mem_global_op_tma_st.sum,
-# l1tex__m_l1tex2xbar_write_bytes_mem_lg_op_st.sum,...` on the fused kernel,
-# fp32 output): the sum over TMA stores, plain global stores, reductions and
-# atomics.  Keyed and validated like NCU_TRAFFIC.
+# ..._mem_lg_op_st.sum, ..._mem_global_op_red.sum, ..._mem_global_op_atom.sum`
+# on the fused kernel, fp32 output): TMA stores, plain global stores, and the
+# 4-byte reductions and atomics on the workspace's arrival counters (counted
+# per 32-byte sector).  Keyed and validated like NCU_TRAFFIC.
 NCU_STORES = {
+    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
+    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
+    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
+    "chained_ln_gelu_rms": {"tma": 134217728, "st": 2097152, "red": 262144, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "column_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "gelu_rmsnorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "layernorm_256": {"tma": 262144, "st": 0, "red": 0, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
+    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
+    "postnorm_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "scaled_softmax": {"tma": 268435456, "st": 2097152, "red": 262144, "atom": 0, "src": "c8fb2f7ceaf75b55"},
+    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "6417a31d5978b06b"},
 }
 
 
@@ -123,13 +137,16 @@ class Workload:
             self.case = I.mlp_bottom(seed, rows=rows)
         elif name == "target_attention":
             self.case = I.target_attention(seed, batch=rows)
+        elif name == "attention_long_keys":
+            self.case = I.attention_long_keys(seed)
         elif name in ("attention_softmax", "attention_relu"):
             op = "scale_softmax" if name == "attention_softmax" else "scale_relu"
             self.case = I.attention_b2b(seed, op=op)
         else:
             raise ValueError(name)
         self.axis = "row"
-        self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu", "target_attention")
+        self.is_b2b = name in ("mlp_b2b", "mlp_bottom", "attention_softmax", "attention_relu", "target_attention",
+                               "attention_long_keys")
         c = self.case
         if not self.is_b2b:
             self.axis = c.meta.get("axis", "row")
@@ -619,10 +636,11 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
     traffic = (tr["read"] + tr["write"]) if tr else None
     # The page's own test: global store bytes of one launch beyond the
     # output and the row-statistics workspace (an intermediate would have
-    # to be stored), from the L2-side store counters.
+    # to be stored), from the store counters; the counter updates are
+    # listed apart.
     stc = NCU_STORES.get(wl.name) if fp32 else None
     stc = stc if stc and stc.get("src") == src else None
-    inter = (stc["stores"] - wl.out_bytes - wl.stat_bytes) if stc else None
+    inter = (stc["tma"] + stc["st"] - wl.out_bytes - wl.stat_bytes) if stc else None
     return {
         "workload": wl.name, "value": value, "ms_per_step": ms_step, "tflops": tflops,
         "ms_per_step_dist": {"p10": percentile(ms, 0.1), "median": statistics.median(ms), "p90": percentile(ms, 0.9),
@@ -634,8 +652,9 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
                      "peak_source": f"{peaks['source']} bf16 burst",
                      "roofline_frac": (t_roof * 1e3) / ms_step},
         "intermediate_hbm_bytes": inter,
-        "global_store_bytes": ({"stores": stc["stores"], "output": wl.out_bytes, "row_stats": wl.stat_bytes,
-                                "source": "ncu L2-side store counters, one launch"} if stc else None),
+        "global_store_bytes": ({"tma_stores": stc["tma"], "stores": stc["st"], "counter_updates": stc["red"] + stc["atom"],
+                                "output": wl.out_bytes, "row_stats": wl.stat_bytes,
+                                "source": "ncu SM-to-L2 store counters, one launch"} if stc else None),
         "dram_bytes": ({"read": tr["read"], "write": tr["write"], "source": "ncu, one launch"} if tr else None),
         "compulsory_bytes": wl.bytes,
         "cpu_baseline": {"value": ref_tflops, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -731,7 +750,7 @@ def main():
     ap.add_argument("--workload", default="attention_softmax",
                     choices=["gelu_rmsnorm", "layernorm_256", "scaled_softmax", "mlp_b2b", "attention_softmax",
                              "attention_relu", "mlp_bottom", "postnorm_layernorm", "chained_ln_gelu_rms",
-                             "target_attention", "column_layernorm"])
+                             "target_attention", "column_layernorm", "attention_long_keys"])
     ap.add_argument("--rows", type=int, default=64,
                     help="batch of the mlp_bottom (rows) and target_attention (users) workloads (1..64)")
     ap.add_argument("--exchange", default="auto", choices=["auto", "cluster", "global", "global_dynamic"],
