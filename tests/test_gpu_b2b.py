@@ -187,6 +187,29 @@ def test_mlp_ragged(cf, M, K, N1, N2, w1_trans):
     b2b_gate(out.cpu().numpy(), ref, bound, f"mlp ragged {M}x{K}x{N1}x{N2} trans={w1_trans}")
 
 
+@pytest.mark.parametrize("batch,M,K,N1,N2,w1_trans", [(1, 384, 128, 640, 600, False), (2, 257, 64, 384, 1024, True),
+                                                       (3, 512, 96, 256, 256, False)])
+def test_mlp_pairs_batched(cf, batch, M, K, N1, N2, w1_trans):
+    # More than 128 rows: CTA pairs over 256-row strips.  Three pairs per
+    # cluster (N2 = 600), a last strip holding one row (M = 257), and batch
+    # entries.
+    rng = np.random.default_rng(batch * 1000 + M)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    X = t(rng.standard_normal((batch, M, K)))
+    W1 = t(rng.standard_normal((batch, K, N1)) / math.sqrt(K))
+    W2 = t(rng.standard_normal((batch, N1, N2)) / math.sqrt(N1))
+    W1d = W1.transpose(1, 2).contiguous().cuda() if w1_trans else W1.cuda()
+    out = cf.cf_b2bgemm(X.cuda(), W1d, W2.cuda(), "relu", w1_trans=w1_trans)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    got = out.cpu().numpy()
+    for b in range(batch):
+        x, w1, w2 = (I.to_f64(a[b]) for a in (X, W1, W2))
+        ref = O.b2bgemm(x, w1, w2, "relu")
+        bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
+        b2b_gate(got[b], ref, bound, f"mlp pairs batch {b} {M}x{K}x{N1}x{N2}")
+
+
 def test_mlp_full_size_sampled(cf):
     case = I.mlp_b2b()
     out = cf.cf_b2bgemm(case.A[0].cuda(), case.W1[0].cuda(), case.W2[0].cuda(), "relu")
