@@ -1083,361 +1083,11 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
   if (C > 1 && threadIdx.x == 0 && *reinterpret_cast<volatile unsigned*>(p.status) != 0u) settle_after_abort();
 }
 
-
-// ----------------------------------------------------------------------
-// CTA-pair form: a cluster of C pairs (2C CTAs) shares one 256-row strip.
-// Pair p owns O[:, 256p .. 256p+255]; CTA h of the pair (h = rank & 1)
-// holds rows 128h .. 128h+127 of it in TMEM.  In round r pair p computes
-// the 256 x 128 chunk S_{rC+p} with cta_group::2 MMAs (M = 256, N = 128):
-// each CTA loads its 128 rows of A and half (64 columns) of the W1 chunk,
-// so the W1 bytes per SM halve against one CTA per 128-row strip.  Each CTA
-// applies F to its 128 rows, rounds to bf16 into its own slot p and copies
-// the slot to slot p of the CTAs holding the same rows in the other pairs.
-// The pair's second GEMM (M = 256, N = 256) reads the C slots of both CTAs;
-// each CTA loads half (128 columns) of the W2 tile, halving those bytes per
-// SM too.  The pair leader (h = 0) issues every MMA; the other CTA's MMA
-// warp relays "slot c is full here" to the leader, which cannot wait on a
-// barrier in its peer's shared memory.
-namespace pair {
-constexpr int kStageBytes = 24576;         // GEMM1: A 16 KB + W1 half 8 KB; GEMM2: W2 half 16 KB
-constexpr int kMaxRing = 8;
-constexpr int kSlotBytes = 128 * 128 * 2;  // this CTA's 128 rows of one 128-wide S' chunk
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-// ring_full[8] (leader: both CTAs' bytes), ring_empty[8], s_full[2], s_free[2] (leader: both CTAs' F
-// warps), slot_full[4], slot_empty (every pair consumed this CTA's chunk), o_full, o_empty (leader: both
-// CTAs' epilogue warps), drain, slot_written (this CTA's F warps wrote its chunk), peer_slot_full[4]
-// (leader: the peer CTA's slot c is full)
-constexpr int BAR_RF = 0, BAR_RE = 8, BAR_SF = 16, BAR_SFREE = 18, BAR_SLF = 20, BAR_SLE = 24, BAR_OF = 25,
-              BAR_OE = 26, BAR_DRAIN = 27, BAR_SLW = 28, BAR_PSF = 29, kNumBars = 33;
-constexpr int kFixedBytes = 1024 + kNumBars * 8 + 16;
-__host__ __device__ constexpr int ring_for(int C) {
-  return (kSmemLimit - kFixedBytes - C * kSlotBytes) / kStageBytes > kMaxRing
-             ? kMaxRing
-             : (kSmemLimit - kFixedBytes - C * kSlotBytes) / kStageBytes;
-}
-__host__ __device__ constexpr int smem_for(int C) { return ring_for(C) * kStageBytes + C * kSlotBytes + kFixedBytes; }
-
-// Params as for mlp_kernel; here `strips` counts 256-row strips and C pairs.
-template <bool OBF16>
-__global__ void __launch_bounds__(pair::kThreads, 1) mlp_pair_kernel(const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kRing = p.ring;
-  const int kOffRing = 0;
-  const int kOffSlots = kRing * kStageBytes;
-  const int kOffBars = kOffSlots + p.C * kSlotBytes;
-  const int kOffMisc = kOffBars + kNumBars * 8;
-  auto bar = [&](int i) -> uint32_t { return sbase + kOffBars + 8 * i; };
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  const WaitCtx wc{p.timeout_cycles, abort_flag, p.status};
-  const int C = p.C;
-  const uint32_t rank = cluster_ctarank();
-  const int pr = (int)(rank >> 1);               // this CTA's pair
-  const uint32_t h = rank & 1u;                  // its half of the pair's rows
-  const uint32_t lead = rank & ~1u;              // the pair leader's rank
-  const bool leader = h == 0;
-  const uint16_t pair_mask = (uint16_t)(3u << lead);
-  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
-  const int R = p.rounds;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(bar(BAR_RF + i), 1);
-      mbar_init(bar(BAR_RE + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_SF + i), 1);
-      mbar_init(bar(BAR_SFREE + i), 2 * kEpiWarps);
-    }
-    for (int k = 0; k < C; ++k) {
-      mbar_init(bar(BAR_SLF + k), 1);
-      if (k != pr) mbar_arrive_expect_tx(bar(BAR_SLF + k), kSlotBytes);  // armed for the first round
-      mbar_init(bar(BAR_PSF + k), 1);
-    }
-    mbar_init(bar(BAR_SLE), C);  // one commit from every pair's second GEMM on this CTA's chunk
-    mbar_init(bar(BAR_OF), 1);
-    mbar_init(bar(BAR_OE), 2 * kEpiWarps);
-    mbar_init(bar(BAR_DRAIN), 1);
-    mbar_init(bar(BAR_SLW), kEpiWarps);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmW1);
-    tma_prefetch_desc(&p.tmW2);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t rs = 0, rph = 0;
-      bool ok = true;
-      auto acquire = [&]() -> bool { return mbar_wait(bar(BAR_RE + rs), rph ^ 1, wc); };
-      auto advance = [&]() {
-        if (++rs == (uint32_t)kRing) { rs = 0; rph ^= 1; }
-      };
-      auto load_g1 = [&](int strip, int b, int r) -> bool {
-        const int n = r * C + pr;  // the pair's N1 chunk
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!acquire()) return false;
-          const uint32_t dst = sbase + kOffRing + rs * kStageBytes;
-          const uint32_t fb = mapa_shared(bar(BAR_RF + rs), lead);  // both CTAs' bytes land on the leader's barrier
-          if (leader) mbar_arrive_expect_tx(bar(BAR_RF + rs), 2 * (16384 + 8192));
-          tma_load_3d_pair(dst, &p.tmA, fb, kb * 64, strip * 256 + (int)h * 128, b);
-          if (p.w1_k_major) tma_load_3d_pair(dst + 16384, &p.tmW1, fb, kb * 64, n * 128 + 64 * (int)h, b);
-          else tma_load_3d_pair(dst + 16384, &p.tmW1, fb, n * 128 + 64 * (int)h, kb * 64, b);
-          advance();
-        }
-        return true;
-      };
-      auto load_g2 = [&](int b, int r) -> bool {
-        for (int i2 = 0; i2 < C; ++i2) {
-          const int c2 = (pr + i2) % C;  // the MMA issuer's chunk order: the pair's own chunk first
-          for (int kh = 0; kh < 2; ++kh) {
-            if (!acquire()) return false;
-            const uint32_t dst = sbase + kOffRing + rs * kStageBytes;
-            const uint32_t fb = mapa_shared(bar(BAR_RF + rs), lead);
-            const int row0 = (r * C + c2) * 128 + kh * 64;
-            if (leader) mbar_arrive_expect_tx(bar(BAR_RF + rs), 2 * 16384);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-              tma_load_3d_pair(dst + i * 8192, &p.tmW2, fb, pr * 256 + (int)h * 128 + 64 * i, row0, b);
-            advance();
-          }
-        }
-        return true;
-      };
-      for (int item = cid; ok && item < p.items; item += ncl) {
-        const int b = item / p.strips, strip = item - b * p.strips;
-        ok = load_g1(strip, b, 0) && (R < 2 || load_g1(strip, b, 1));
-        for (int r = 0; ok && r < R; ++r) {
-          if (r + 2 < R) ok = load_g1(strip, b, r + 2);  // same order as the MMA issuer
-          if (ok) ok = load_g2(b, r);
-        }
-      }
-      // The leader's stage releases reach this CTA asynchronously: wait until
-      // the last release of every stage has landed before exiting (after an
-      // abort they may never come: stop at the abort flag).  The pair's loads
-      // complete on the leader's barrier; after an abort they are waited for
-      // at the end of the kernel.
-      for (int s2 = 0; s2 < kRing; ++s2) {
-        if (!acquire()) break;
-        advance();
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ------------------------------------------------ MMA issuer (leader)
-      const uint32_t id_s = idesc_bf16_f32(256, 128, p.w1_k_major ? 0u : 1u);
-      const uint32_t id_o = idesc_bf16_f32(256, 256, 1u);
-      uint32_t rs = 0, rph = 0;
-      uint32_t g = 0;  // global round counter
-      int t = 0;
-      bool ok = true;
-      constexpr uint32_t kStageStep = kStageBytes >> 4;
-      const SDesc dx = sdesc_sw128(sbase + kOffRing, 16, 1024);
-      const SDesc dw1 = sdesc_sw128(sbase + kOffRing + 16384, p.w1_k_major ? 16u : 8192u, 1024);
-      const uint32_t w1_step = p.w1_k_major ? (32u >> 4) : (2048u >> 4);  // per 16 K elements
-      const SDesc dw2 = sdesc_sw128(sbase + kOffRing, 8192, 1024);
-      const SDesc dsl = sdesc_sw128(sbase + kOffSlots, 16, 1024);
-      auto g1 = [&](uint32_t gg) -> bool {
-        // Both CTAs' F warps must be done reading the S buffer's previous contents.
-        if (!mbar_wait<true>(bar(BAR_SFREE + (gg & 1)), ((gg >> 1) & 1) ^ 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem_base + (gg & 1) * 128;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) return false;
-          tc_fence_after();
-          const uint32_t x_lo = dx.lo + rs * kStageStep, w_lo = dw1.lo + rs * kStageStep;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss_pair(d, x_lo + kk * (32u >> 4), dx.hi, w_lo + kk * w1_step, dw1.hi, id_s, (kb | kk) ? 1u : 0u);
-          mma_commit_pair(bar(BAR_RE + rs), pair_mask);
-          if (++rs == (uint32_t)kRing) { rs = 0; rph ^= 1; }
-        }
-        mma_commit_pair(bar(BAR_SF + (gg & 1)), pair_mask);
-        return true;
-      };
-      for (int item = cid; ok && item < p.items; item += ncl, ++t) {
-        const uint32_t g0 = g;
-        ok = g1(g0) && (R < 2 || g1(g0 + 1));
-        for (int r = 0; ok && r < R; ++r, ++g) {
-          if (r + 2 < R && !(ok = g1(g + 2))) break;
-          if (r == 0 && !mbar_wait<true>(bar(BAR_OE), (t & 1) ^ 1, wc)) { ok = false; break; }
-          for (int i2 = 0; ok && i2 < C; ++i2) {
-            const int c2 = (pr + i2) % C;
-            if (c2 == pr) {
-              if (!mbar_wait(bar(BAR_SLW), g & 1, wc)) { ok = false; break; }
-            } else {
-              if (!mbar_wait(bar(BAR_SLF + c2), g & 1, wc)) { ok = false; break; }
-              mbar_arrive_expect_tx(bar(BAR_SLF + c2), kSlotBytes);  // arm the next round's copy
-            }
-            // ... and the same slot in the peer CTA (relayed by its MMA warp).
-            if (!mbar_wait<true>(bar(BAR_PSF + c2), g & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            for (int kh = 0; kh < 2; ++kh) {
-              if (!mbar_wait(bar(BAR_RF + rs), rph, wc)) { ok = false; break; }
-              tc_fence_after();
-              const uint32_t w_lo = dw2.lo + rs * kStageStep;
-              const uint32_t a_lo = dsl.lo + ((uint32_t)(c2 * kSlotBytes + kh * 16384) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ss_pair(tmem_base + 256, a_lo + kk * (32u >> 4), dsl.hi, w_lo + kk * (2048u >> 4), dw2.hi, id_o,
-                            (r | i2 | kh | kk) ? 1u : 0u);
-              mma_commit_pair(bar(BAR_RE + rs), pair_mask);
-              if (++rs == (uint32_t)kRing) { rs = 0; rph ^= 1; }
-            }
-            // Pair c2's CTAs may refill their slots once every pair has consumed them.
-            if (ok) mma_commit_pair(bar(BAR_SLE), (uint16_t)(3u << (2 * c2)));
-          }
-          if (!ok) break;
-        }
-        if (!ok) break;
-        mma_commit_pair(bar(BAR_OF), pair_mask);
-      }
-      mma_commit_pair(bar(BAR_DRAIN), (uint16_t)(1u << lead));
-      mbar_wait<false, false>(bar(BAR_DRAIN), 0, wc);
-      if (ok) {
-        // Every asynchronous arrival meant for this CTA has landed before it
-        // leaves: the pairs' releases of its last chunk, and the peer's
-        // last "S free" and "O empty" arrivals.
-        if (g > 0) mbar_wait<false, true>(bar(BAR_SLE), (g - 1) & 1, wc);
-        for (uint32_t gg = g; gg < g + 2; ++gg)
-          if (!mbar_wait<true, true>(bar(BAR_SFREE + (gg & 1)), ((gg >> 1) & 1) ^ 1, wc)) break;
-        mbar_wait<true, true>(bar(BAR_OE), (t & 1) ^ 1, wc);
-      }
-    } else if (lane == 0) {
-      // ----------------------------- slot relay (the pair's second CTA)
-      uint32_t g = 0;
-      bool ok = true;
-      for (int item = cid; ok && item < p.items; item += ncl) {
-        for (int r = 0; ok && r < R; ++r, ++g) {
-          for (int i2 = 0; i2 < C; ++i2) {
-            const int c2 = (pr + i2) % C;  // the leader's order
-            if (c2 == pr) {
-              if (!mbar_wait(bar(BAR_SLW), g & 1, wc)) { ok = false; break; }
-            } else {
-              if (!mbar_wait(bar(BAR_SLF + c2), g & 1, wc)) { ok = false; break; }
-              mbar_arrive_expect_tx(bar(BAR_SLF + c2), kSlotBytes);
-            }
-            mbar_arrive_cluster(bar(BAR_PSF + c2), lead);
-          }
-        }
-      }
-      if (ok && g > 0) mbar_wait<false, true>(bar(BAR_SLE), (g - 1) & 1, wc);
-    }
-  } else {
-    // ------------------------------------------------ F warps and epilogue
-    const int q = warp & 3;
-    const int row = 32 * q + lane;
-    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    uint8_t* my_slot = smem + kOffSlots + pr * kSlotBytes;
-    const uint32_t my_slot_addr = sbase + kOffSlots + pr * kSlotBytes;
-    uint32_t g = 0;
-    int t = 0;
-    bool ok = true;
-    for (int item = cid; ok && item < p.items; item += ncl, ++t) {
-      const int b = item / p.strips, strip = item - b * p.strips;
-      for (int r = 0; r < R; ++r, ++g) {
-        const uint32_t sb = g & 1, u = g >> 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SF + sb), u & 1, wc))) { ok = false; break; }
-        tc_fence_after();
-        uint32_t w[4][16];
-        {
-          float v[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tmem_base + lane_off + sb * 128 + c * 32, v[c]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[c][e] = fmaxf(v[c][e] * p.scale, 0.0f);
-            pack_bf16(v[c], w[c]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(bar(BAR_SFREE + sb));
-          else mbar_arrive_cluster(bar(BAR_SFREE + sb), lead);
-        }
-        // This CTA's slot may be overwritten once every pair consumed its previous chunk.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLE), (g & 1) ^ 1, wc))) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) store_row_packed_sw128(my_slot, row, c * 32, w[c]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_SLW));
-        if (warp == 2) {
-          // The whole chunk is in this CTA's slot: copy it to the CTAs that
-          // hold the same rows in the other pairs.
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_SLW), g & 1, wc))) { ok = false; break; }
-          if (lane == 0) {
-            for (int k = 1; k < C; ++k) {
-              const uint32_t dst_rank = 2u * (uint32_t)((pr + k) % C) + h;
-              bulk_copy_to_peer(my_slot_addr, my_slot_addr, kSlotBytes, bar(BAR_SLF + pr), dst_rank);
-            }
-          }
-        }
-      }
-      if (!ok) break;
-      // Epilogue: this CTA's 128 x 256 block of O, straight from TMEM to HBM.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_OF), t & 1, wc))) break;
-      tc_fence_after();
-      const int orow_i = strip * 256 + (int)h * 128 + row;
-      const long long orow = (long long)b * p.stride_out + (long long)orow_i * p.ldo + pr * 256;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        float v[32];
-        tmem_ld32(tmem_base + lane_off + 256 + c * 32, v);
-        tmem_wait_ld();
-        const int col = pr * 256 + c * 32;  // columns past N2 (ragged last block) are not stored
-        if (orow_i < p.M && col < p.n2) {   // nor rows past M (ragged last strip)
-          if (col + 32 <= p.n2) store_row<32>(p.out, OBF16, orow + c * 32, v, 1.0f, p.out_v8);
-          else store_row_part<32>(p.out, OBF16, orow + c * 32, v, 1.0f, p.n2 - col);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(bar(BAR_OE));
-        else mbar_arrive_cluster(bar(BAR_OE), lead);
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();  // the peer's TMEM and every CTA's slots are in use until all are done
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
-  }
-  // After an abort (any bounded wait gave up: the status word is set),
-  // loads of the pair and slot copies may still be in flight; every CTA has
-  // stopped issuing them at the cluster barrier above, so all wait here.
-  if (threadIdx.x == 0 && *reinterpret_cast<volatile unsigned*>(p.status) != 0u) settle_after_abort();
-}
-}  // namespace pair
-
 }  // namespace mlp
 
 
 std::mutex g_mu;
-bool g_prepared[64][12] = {};  // [device][MLP fp32 / bf16 out, attention variants 0..7, MLP pairs fp32 / bf16]
+bool g_prepared[64][10] = {};  // [device][MLP fp32 / bf16 out, attention variants 0..7]
 // Resident clusters of C CTAs of the key-split attention kernel, by device,
 // kernel variant and C (0: not queried yet, -1: none fit).
 int g_attn_clusters[64][8][CF_MAX_KEY_SPLIT + 1] = {};
@@ -1511,9 +1161,6 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
                      cf_matrix* out, int64_t C, int sms, unsigned* status, cudaStream_t stream) {
   const int64_t M = A->rows, K = A->cols, N1 = W1->cols, N2 = W2->cols, batch = d->batch;
   const uint64_t bs = (uint64_t)batch;
-  // CTA pairs (256-row strips) when a batch entry has more than one 128-row
-  // strip; a single strip keeps one CTA per 128 rows.
-  const bool pairs = M > 128;
   mlp::Params p;
   std::memset(&p, 0, sizeof(p));
   cf_status s;
@@ -1527,7 +1174,7 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   if (W1->trans) {  // stored N1 x K
     const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N1, bs};
     const uint64_t st[2] = {(uint64_t)W1->ld * 2, (uint64_t)(batch > 1 ? d->strideW1 : N1 * W1->ld) * 2};
-    const uint32_t box[3] = {64, pairs ? 64u : 128u, 1};  // pairs: each CTA loads half of a 128-row chunk
+    const uint32_t box[3] = {64, 128, 1};
     if ((s = encode_tmap(&p.tmW1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, W1->ptr, dims, st, box)) != CF_OK) return s;
   } else {          // stored K x N1
     const uint64_t dims[3] = {(uint64_t)N1, (uint64_t)K, bs};
@@ -1548,49 +1195,38 @@ cf_status launch_mlp(const cf_matrix* A, const cf_matrix* W1, const cf_matrix* W
   p.out_v8 = out_aligned32(out, p.stride_out) ? 1 : 0;
   p.C = (int)C;
   p.n2 = (int)N2;
-  p.ring = pairs ? mlp::pair::ring_for((int)C) : mlp::ring_for((int)C);
+  p.ring = mlp::ring_for((int)C);
   p.kblocks = (int)((K + 63) / 64);
   p.rounds = (int)((N1 + 128 * C - 1) / (128 * C));
   p.M = (int)M;
-  p.strips = pairs ? (int)((M + 255) / 256) : (int)((M + 127) / 128);
+  p.strips = (int)((M + 127) / 128);
   p.items = (int)(batch * p.strips);
   p.scale = d->mid_op == CF_MID_RELU ? 1.0f : d->mid_scale;
   p.status = status;
   p.timeout_cycles = wait_timeout_cycles();
-  const void* fn;
-  int smem, cluster;
-  if (pairs) {
-    fn = p.out_bf16 ? reinterpret_cast<const void*>(&mlp::pair::mlp_pair_kernel<true>)
-                    : reinterpret_cast<const void*>(&mlp::pair::mlp_pair_kernel<false>);
-    smem = mlp::pair::smem_for((int)C);
-    cluster = 2 * (int)C;
-    if ((s = prepare(p.out_bf16 ? 11 : 10, fn, mlp::pair::smem_for(1))) != CF_OK) return s;  // the largest layout
-  } else {
-    fn = p.out_bf16 ? reinterpret_cast<const void*>(&mlp::mlp_kernel<true>)
-                    : reinterpret_cast<const void*>(&mlp::mlp_kernel<false>);
-    smem = mlp::smem_for((int)C);
-    cluster = (int)C;
-    if ((s = prepare(p.out_bf16 ? 1 : 0, fn, mlp::smem_for(1))) != CF_OK) return s;  // the largest layout
-  }
+  const void* fn = p.out_bf16 ? reinterpret_cast<const void*>(&mlp::mlp_kernel<true>)
+                              : reinterpret_cast<const void*>(&mlp::mlp_kernel<false>);
+  const int smem = mlp::smem_for((int)C);
+  if ((s = prepare(p.out_bf16 ? 1 : 0, fn, mlp::smem_for(1))) != CF_OK) return s;  // the largest layout
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(pairs ? mlp::pair::kThreads : mlp::kThreads, 1, 1);
+  cfg.blockDim = dim3(mlp::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
   int maxc = 0;
   if (cudaOccupancyMaxActiveClusters(&maxc, fn, &cfg) != cudaSuccess || maxc < 1) {
     cudaGetLastError();
     return CF_ERR_CUDA;
   }
   const int64_t ncl = p.items < maxc ? p.items : maxc;
-  cfg.gridDim = dim3((unsigned)(ncl * cluster), 1, 1);
+  cfg.gridDim = dim3((unsigned)(ncl * C), 1, 1);
   void* args[] = {&p};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();

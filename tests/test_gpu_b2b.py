@@ -189,10 +189,9 @@ def test_mlp_ragged(cf, M, K, N1, N2, w1_trans):
 
 @pytest.mark.parametrize("batch,M,K,N1,N2,w1_trans", [(1, 384, 128, 640, 600, False), (2, 257, 64, 384, 1024, True),
                                                        (3, 512, 96, 256, 256, False)])
-def test_mlp_pairs_batched(cf, batch, M, K, N1, N2, w1_trans):
-    # More than 128 rows: CTA pairs over 256-row strips.  Three pairs per
-    # cluster (N2 = 600), a last strip holding one row (M = 257), and batch
-    # entries.
+def test_mlp_batched(cf, batch, M, K, N1, N2, w1_trans):
+    # Batch entries (strided A, W1, W2 and output), three CTAs per cluster
+    # (N2 = 600), and a last 128-row strip holding one row (M = 257).
     rng = np.random.default_rng(batch * 1000 + M)
     t = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
     X = t(rng.standard_normal((batch, M, K)))
@@ -207,7 +206,7 @@ def test_mlp_pairs_batched(cf, batch, M, K, N1, N2, w1_trans):
         x, w1, w2 = (I.to_f64(a[b]) for a in (X, W1, W2))
         ref = O.b2bgemm(x, w1, w2, "relu")
         bound = np.abs(O.mid_op(x @ w1, "relu")) @ np.abs(w2)
-        b2b_gate(got[b], ref, bound, f"mlp pairs batch {b} {M}x{K}x{N1}x{N2}")
+        b2b_gate(got[b], ref, bound, f"mlp batch {b} {M}x{K}x{N1}x{N2}")
 
 
 def test_mlp_full_size_sampled(cf):
