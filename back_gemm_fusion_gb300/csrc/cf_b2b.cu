@@ -558,31 +558,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           l *= ex2_approx(m_last - m_new);  // 0 on this group's first chunk of the item
           m_last = m_new;
         }
-        // S' buffer sb was last read by the S' . W2 product two chunks back.
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
-        tc_fence_after();
-        // F, bf16 rounding, the S' store and (softmax) the row sum of exactly
-        // what GEMM2 consumes, 32 columns at a time.
+        // F, bf16 rounding and (softmax) the row sum of exactly what GEMM2
+        // consumes, 32 columns at a time, into registers: all of it before
+        // the wait for the S' buffer, so that this work overlaps the S' . W2
+        // product two chunks back instead of following it.
+        uint32_t w[4][16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float(&vc)[32] = part32(v, c);
-          uint32_t w[16];
           if (p.softmax) {
             fma2_32(vc, pack2f(sl2), pack2f(-m_last));  // the exp2 arguments, two per instruction
 #pragma unroll
             for (int e = 0; e < 32; ++e) vc[e] = ex2_approx(vc[e]);
-            pack_bf16(vc, w);
-            l += sum_packed_bf16(w);
+            pack_bf16(vc, w[c]);
+            l += sum_packed_bf16(w[c]);
           } else {
             // relu(bf16(scale s)) == bf16(relu(scale s)) (rounding is monotonic
             // and keeps 0): scale two per packed FMA, round, then a bf16x2 max.
             fma2_32(vc, pack2f(p.scale), pack2f(0.0f));
-            pack_bf16(vc, w);
+            pack_bf16(vc, w[c]);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) asm("max.bf16x2 %0, %0, %1;" : "+r"(w[e]) : "r"(0u));
+            for (int e = 0; e < 16; ++e) asm("max.bf16x2 %0, %0, %1;" : "+r"(w[c][e]) : "r"(0u));
           }
-          tmem_st16(tmem_base + lane_off + kTmemP + 64 * sb + 16 * c, *reinterpret_cast<float(*)[16]>(&w[0]));
         }
+        // S' buffer sb was last read by the S' . W2 product two chunks back.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + sb), (u & 1) ^ 1, wc))) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_st16(tmem_base + lane_off + kTmemP + 64 * sb + 16 * c, *reinterpret_cast<float(*)[16]>(&w[c][0]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
