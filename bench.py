@@ -83,6 +83,10 @@ NCU_STORES = {
 }
 
 
+class _NotApplicable(Exception):
+    """A comparison that the configuration has no counterpart for."""
+
+
 def percentile(xs, q: float) -> float:
     """Nearest-rank percentile (q in [0, 1]) of a non-empty list."""
     v = sorted(xs)
@@ -521,7 +525,10 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
 
     # Unfused comparison (cuBLASLt GEMM + separate epilogue kernel), same run.
     unfused = None
+    bf16_out = str(dev["out"].dtype) == "torch.bfloat16"
     try:
+        if bf16_out and not wl.is_b2b:
+            raise _NotApplicable("the unfused GEMM-epilogue comparison path writes fp32 output only")
         scratch = wl.unfused_scratch()
         for _ in range(2):
             wl.unfused_step(cf, dev, scratch, stream)
@@ -540,6 +547,8 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
                    "path": ("cuBLASLt GEMM1 -> HBM S -> mid-op kernel -> HBM bf16 S' -> cuBLASLt GEMM2"
                             if wl.is_b2b else "cuBLASLt GEMM -> HBM intermediate -> separate epilogue kernel")}
         del scratch
+    except _NotApplicable as exc:
+        unfused = {"unavailable": str(exc)}
     except Exception as exc:  # the comparison path is optional for the headline
         unfused = {"error": str(exc)[:200]}
 
