@@ -321,8 +321,12 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
                                              const float* vsm, float r_bias, float r_gamma0, float r_beta0,
                                              float sc0, float sh0) {
   float2 st;
-  // Pass 1: elementwise program, kept in TMEM; first local statistic.
-  float s1 = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
+  // Pass 1: elementwise program, kept in TMEM; first local statistic.  Each
+  // statistic is kept in four partial accumulators (element j goes to
+  // accumulator j mod 4): one epilogue warp runs per SM sub-partition, so a
+  // single chain of 32 dependent adds per chunk would expose its latency.
+  const float s1_init = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
+  float s1p[4] = {s1_init, s1_init, s1_init, s1_init};
 #pragma unroll 1
   for (int c = 0; c < nch; ++c) {
     float v[32];
@@ -351,18 +355,21 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
     if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      if (ROWOP == ROW_RMSNORM) s1 = fmaf(v[j], v[j], s1);
-      else if (ROWOP == ROW_SOFTMAX) s1 = fmaxf(s1, v[j]);
-      else s1 += v[j];
+      float& a = s1p[j & 3];
+      if (ROWOP == ROW_RMSNORM) a = fmaf(v[j], v[j], a);
+      else if (ROWOP == ROW_SOFTMAX) a = fmaxf(a, v[j]);
+      else a += v[j];
     }
   }
+  const float s1 = (ROWOP == ROW_SOFTMAX) ? fmaxf(fmaxf(s1p[0], s1p[1]), fmaxf(s1p[2], s1p[3]))
+                                          : (s1p[0] + s1p[1]) + (s1p[2] + s1p[3]);
   if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
   if (ROWOP == ROW_RMSNORM) {
     st = make_float2(s1, 0.0f);
   } else {
     // Pass 2: second local statistic about the segment's own max/mean.
     const float ref = (ROWOP == ROW_SOFTMAX) ? s1 : RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
-    float s2 = 0.0f;
+    float s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
       float v[32];
@@ -371,11 +378,12 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
       if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ROWOP == ROW_SOFTMAX ? -INFINITY : ref);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        if (ROWOP == ROW_SOFTMAX) s2 += ex2_approx((v[j] - ref) * kLog2e);
-        else { const float d = v[j] - ref; s2 = fmaf(d, d, s2); }
+        float& a = s2p[j & 3];
+        if (ROWOP == ROW_SOFTMAX) a += ex2_approx((v[j] - ref) * kLog2e);
+        else { const float d = v[j] - ref; a = fmaf(d, d, a); }
       }
     }
-    st = make_float2(ref, s2);
+    st = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
   }
 
   return st;
@@ -829,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       // before the ops that follow it.
       float sc0 = 1.0f, sh0 = 0.0f;
       if constexpr (ROWOP0 != ROW_NONE) {
-        float s1 = 0.0f;
+        float s1p[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four partial sums, as in tile_stats
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float v[32];
@@ -845,15 +853,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           }
           if (tail) mask_tail(v, p.N - n, 0.0f);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s1 = (ROWOP0 == ROW_RMSNORM) ? fmaf(v[j], v[j], s1) : s1 + v[j];
+          for (int j = 0; j < 32; ++j) {
+            float& a = s1p[j & 3];
+            a = (ROWOP0 == ROW_RMSNORM) ? fmaf(v[j], v[j], a) : a + v[j];
+          }
         }
+        const float s1 = (s1p[0] + s1p[1]) + (s1p[2] + s1p[3]);
         if (p.n_ops0 > 0) tmem_wait_st();
         float2 st0;
         if (ROWOP0 == ROW_RMSNORM) {
           st0 = make_float2(s1, 0.0f);
         } else {
           const float ref = RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
-          float s2 = 0.0f;
+          float s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
           for (int c = 0; c < nch; ++c) {
             float v[32];
@@ -863,10 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float d = v[j] - ref;
-              s2 = fmaf(d, d, s2);
+              s2p[j & 3] = fmaf(d, d, s2p[j & 3]);
             }
           }
-          st0 = make_float2(ref, s2);
+          st0 = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
         }
         if (XMODE == X_GLOBAL &&
             !global_exchange<ROWOP0, RAG>(p, p.ws_stats0, p.ws_count0, strip, tile, row, q, lane, abort_flag, wc, st0))
