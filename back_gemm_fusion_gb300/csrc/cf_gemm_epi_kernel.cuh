@@ -79,11 +79,21 @@ enum VecSlot : int { VEC_BIAS = 0, VEC_GAMMA = 1, VEC_BETA = 2, VEC_GAMMA0 = 3, 
 
 enum OpKind : int { OP_BIAS = 1, OP_SCALE = 2, OP_RELU = 3, OP_GELU_TANH = 4, OP_ADD_RESIDUAL = 5 };
 
-__device__ __forceinline__ float gelu_tanh(float x) {
-  // 0.5 x (1 + tanh(u)) == x * sigmoid(2u) == x / (1 + exp(-2u)),
-  // u = sqrt(2/pi) (x + 0.044715 x^3).
-  const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-  return __fdividef(x, 1.0f + ex2_approx(-2.0f * kLog2e * u));
+// tanh-GELU of two values: 0.5 x (1 + tanh(u)) == x * sigmoid(2u) ==
+// x / (1 + exp(-2u)), u = sqrt(2/pi) (x + 0.044715 x^3); the polynomial and
+// the scalings two per packed instruction.
+__device__ __forceinline__ void gelu_tanh2(float& x0, float& x1) {
+  float sq0 = x0, sq1 = x1, c0 = x0, c1 = x1;
+  fmul2(sq0, sq1, x0, x1);                   // x^2
+  fmul2(c0, c1, 0.044715f, 0.044715f);       // 0.044715 x
+  ffma2(c0, c1, c0, c1, sq0, sq1, x0, x1);   // x + 0.044715 x^3
+  fmul2(c0, c1, 0.7978845608028654f, 0.7978845608028654f);
+  const float m = -2.0f * kLog2e;
+  fmul2(c0, c1, m, m);
+  float e0 = ex2_approx(c0), e1 = ex2_approx(c1);
+  fadd2(e0, e1, 1.0f, 1.0f);
+  x0 = __fdividef(x0, e0);
+  x1 = __fdividef(x1, e1);
 }
 
 // Entries i..i+3 of a length-N fp32 vector (i a multiple of 4, x 16-byte
@@ -111,15 +121,15 @@ __device__ __forceinline__ void mask_tail(float (&v)[32], int cv, float fill) {
 
 // v[j] *= x[j] and v[j] += x[j] over a 32-column chunk, x the chunk's slice
 // of a staged vector in shared memory (every lane reads the same address).
+// Two columns per packed fp32x2 instruction: one epilogue warp runs per SM
+// sub-partition, so the epilogue's time is its instruction count.
 __device__ __forceinline__ void mul_vec(float (&v)[32], const float* x) {
   const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float4 g = x4[j];
-    v[4 * j + 0] *= g.x;
-    v[4 * j + 1] *= g.y;
-    v[4 * j + 2] *= g.z;
-    v[4 * j + 3] *= g.w;
+    fmul2(v[4 * j + 0], v[4 * j + 1], g.x, g.y);
+    fmul2(v[4 * j + 2], v[4 * j + 3], g.z, g.w);
   }
 }
 __device__ __forceinline__ void add_vec(float (&v)[32], const float* x) {
@@ -127,27 +137,38 @@ __device__ __forceinline__ void add_vec(float (&v)[32], const float* x) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float4 b = x4[j];
-    v[4 * j + 0] += b.x;
-    v[4 * j + 1] += b.y;
-    v[4 * j + 2] += b.z;
-    v[4 * j + 3] += b.w;
+    fadd2(v[4 * j + 0], v[4 * j + 1], b.x, b.y);
+    fadd2(v[4 * j + 2], v[4 * j + 3], b.z, b.w);
   }
 }
+// v[j] = v[j] * s + t for the whole chunk (s, t scalars).
+__device__ __forceinline__ void scale_shift(float (&v)[32], float s, float t) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) ffma2(v[j], v[j + 1], v[j], v[j + 1], s, s, t, t);
+}
 
-// Normalisation with the affine vectors: v = gamma (v sa + sh) (+ beta).
+// Normalisation with the affine vectors: v = gamma (v sa + sh) (+ beta),
+// two columns per packed instruction (the gamma product and the beta add
+// in one fused multiply-add).
 template <bool BETA>
 __device__ __forceinline__ void norm_affine(float (&v)[32], const float* gamma, const float* beta, float sa,
                                             float sh) {
   const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  const float4* b4 = reinterpret_cast<const float4*>(beta);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float4 g = g4[j];
-    v[4 * j + 0] = fmaf(v[4 * j + 0], sa, sh) * g.x;
-    v[4 * j + 1] = fmaf(v[4 * j + 1], sa, sh) * g.y;
-    v[4 * j + 2] = fmaf(v[4 * j + 2], sa, sh) * g.z;
-    v[4 * j + 3] = fmaf(v[4 * j + 3], sa, sh) * g.w;
+    const float4 b = BETA ? b4[j] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    ffma2(v[4 * j + 0], v[4 * j + 1], v[4 * j + 0], v[4 * j + 1], sa, sa, sh, sh);
+    ffma2(v[4 * j + 2], v[4 * j + 3], v[4 * j + 2], v[4 * j + 3], sa, sa, sh, sh);
+    if (BETA) {
+      ffma2(v[4 * j + 0], v[4 * j + 1], v[4 * j + 0], v[4 * j + 1], g.x, g.y, b.x, b.y);
+      ffma2(v[4 * j + 2], v[4 * j + 3], v[4 * j + 2], v[4 * j + 3], g.z, g.w, b.z, b.w);
+    } else {
+      fmul2(v[4 * j + 0], v[4 * j + 1], g.x, g.y);
+      fmul2(v[4 * j + 2], v[4 * j + 3], g.z, g.w);
+    }
   }
-  if (BETA) add_vec(v, beta);
 }
 
 // Elementwise ops [o0, o1) of the program on 32 consecutive columns n.. of
@@ -201,10 +222,9 @@ __device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)
             const uint4 w = __ldg(r4 + j);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[8 * j + 2 * e] += __uint_as_float(ww[e] << 16);
-              v[8 * j + 2 * e + 1] += __uint_as_float(ww[e] & 0xffff0000u);
-            }
+            for (int e = 0; e < 4; ++e)
+              fadd2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1], __uint_as_float(ww[e] << 16),
+                    __uint_as_float(ww[e] & 0xffff0000u));
           }
         } else {
           const float4* r4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.res) +
@@ -212,30 +232,28 @@ __device__ __forceinline__ void apply_program(const GemmEpiParams& p, float (&v)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 r = __ldg(r4 + j);
-            v[4 * j + 0] += r.x;
-            v[4 * j + 1] += r.y;
-            v[4 * j + 2] += r.z;
-            v[4 * j + 3] += r.w;
+            fadd2(v[4 * j + 0], v[4 * j + 1], r.x, r.y);
+            fadd2(v[4 * j + 2], v[4 * j + 3], r.z, r.w);
           }
         }
       }
     } else if (kind == OP_BIAS) {
       if (COLS) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += bias_r;
+        for (int j = 0; j < 32; j += 2) fadd2(v[j], v[j + 1], bias_r, bias_r);
       } else {
         add_vec(v, bias_s);
       }
     } else if (kind == OP_SCALE) {
       const float s = p.op_scalar[o];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= s;
+      for (int j = 0; j < 32; j += 2) fmul2(v[j], v[j + 1], s, s);
     } else if (kind == OP_RELU) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
     } else if (kind == OP_GELU_TANH) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+      for (int j = 0; j < 32; j += 2) gelu_tanh2(v[j], v[j + 1]);
     }
   }
 }
@@ -335,11 +353,9 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
     const int n = n0 + c * 32;
     const bool tail = RAG && n + 32 > p.N;
     if constexpr (ROWOP0 != ROW_NONE) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], sc0, sh0);
+      scale_shift(v, sc0, sh0);
       if (COLS) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = v[j] * r_gamma0 + (ROWOP0 == ROW_LAYERNORM ? r_beta0 : 0.0f);
+        scale_shift(v, r_gamma0, ROWOP0 == ROW_LAYERNORM ? r_beta0 : 0.0f);
       } else {
         if (p.gamma0) mul_vec(v, vsm + VEC_GAMMA0 * kBN + c * 32);
         if (ROWOP0 == ROW_LAYERNORM && p.beta0) add_vec(v, vsm + VEC_BETA0 * kBN + c * 32);
@@ -354,11 +370,17 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
     }
     if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float& a = s1p[j & 3];
-      if (ROWOP == ROW_RMSNORM) a = fmaf(v[j], v[j], a);
-      else if (ROWOP == ROW_SOFTMAX) a = fmaxf(a, v[j]);
-      else a += v[j];
+    for (int j = 0; j < 32; j += 4) {
+      if (ROWOP == ROW_RMSNORM) {
+        ffma2(s1p[0], s1p[1], v[j], v[j + 1], v[j], v[j + 1], s1p[0], s1p[1]);
+        ffma2(s1p[2], s1p[3], v[j + 2], v[j + 3], v[j + 2], v[j + 3], s1p[2], s1p[3]);
+      } else if (ROWOP == ROW_SOFTMAX) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s1p[k] = fmaxf(s1p[k], v[j + k]);
+      } else {
+        fadd2(s1p[0], s1p[1], v[j], v[j + 1]);
+        fadd2(s1p[2], s1p[3], v[j + 2], v[j + 3]);
+      }
     }
   }
   const float s1 = (ROWOP == ROW_SOFTMAX) ? fmaxf(fmaxf(s1p[0], s1p[1]), fmaxf(s1p[2], s1p[3]))
@@ -377,10 +399,19 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
       tmem_wait_ld();
       if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ROWOP == ROW_SOFTMAX ? -INFINITY : ref);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float& a = s2p[j & 3];
-        if (ROWOP == ROW_SOFTMAX) a += ex2_approx((v[j] - ref) * kLog2e);
-        else { const float d = v[j] - ref; a = fmaf(d, d, a); }
+      for (int j = 0; j < 32; j += 4) {
+        float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
+        fadd2(d0, d1, -ref, -ref);
+        fadd2(d2, d3, -ref, -ref);
+        if (ROWOP == ROW_SOFTMAX) {
+          fmul2(d0, d1, kLog2e, kLog2e);
+          fmul2(d2, d3, kLog2e, kLog2e);
+          fadd2(s2p[0], s2p[1], ex2_approx(d0), ex2_approx(d1));
+          fadd2(s2p[2], s2p[3], ex2_approx(d2), ex2_approx(d3));
+        } else {
+          ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
+          ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
+        }
       }
     }
     st = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
@@ -853,9 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           }
           if (tail) mask_tail(v, p.N - n, 0.0f);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float& a = s1p[j & 3];
-            a = (ROWOP0 == ROW_RMSNORM) ? fmaf(v[j], v[j], a) : a + v[j];
+          for (int j = 0; j < 32; j += 4) {
+            if (ROWOP0 == ROW_RMSNORM) {
+              ffma2(s1p[0], s1p[1], v[j], v[j + 1], v[j], v[j + 1], s1p[0], s1p[1]);
+              ffma2(s1p[2], s1p[3], v[j + 2], v[j + 3], v[j + 2], v[j + 3], s1p[2], s1p[3]);
+            } else {
+              fadd2(s1p[0], s1p[1], v[j], v[j + 1]);
+              fadd2(s1p[2], s1p[3], v[j + 2], v[j + 3]);
+            }
           }
         }
         const float s1 = (s1p[0] + s1p[1]) + (s1p[2] + s1p[3]);
@@ -873,9 +909,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             tmem_wait_ld();
             if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ref);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = v[j] - ref;
-              s2p[j & 3] = fmaf(d, d, s2p[j & 3]);
+            for (int j = 0; j < 32; j += 4) {
+              float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
+              fadd2(d0, d1, -ref, -ref);
+              fadd2(d2, d3, -ref, -ref);
+              ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
+              ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
             }
           }
           st0 = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
@@ -989,13 +1028,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           if (tail) apply_program<true, COLS>(p, v, n, m0 + row, 0, p.n_ops, bs, r_bias);
           else apply_program<false, COLS>(p, v, n, m0 + row, 0, p.n_ops, bs, r_bias);
         } else if (ROWOP == ROW_SOFTMAX) {
+          scale_shift(v, scale_a, shift_a);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], scale_a, shift_a)) * inv_sum;
+          for (int j = 0; j < 32; ++j) v[j] = ex2_approx(v[j]);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) fmul2(v[j], v[j + 1], inv_sum, inv_sum);
         } else {
           if (COLS) {
-            const float b = ROWOP == ROW_LAYERNORM ? r_beta : 0.0f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], scale_a, shift_a) * r_gamma + b;
+            scale_shift(v, scale_a, shift_a);
+            scale_shift(v, r_gamma, ROWOP == ROW_LAYERNORM ? r_beta : 0.0f);
           } else {
             norm_affine<ROWOP == ROW_LAYERNORM>(v, vsm + VEC_GAMMA * kBN + c * 32, vsm + VEC_BETA * kBN + c * 32,
                                                 scale_a, shift_a);
