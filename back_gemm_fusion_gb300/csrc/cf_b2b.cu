@@ -315,6 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
   const int nbl = j1 - j0;  // >= 1: the host sizes the split so that no range is empty
 
+  // The tensor-map fetches start before the barrier set-up, which they
+  // overlap (the first TMA load waits for its map).
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmW1);
+    tma_prefetch_desc(&p.tmW2);
+  }
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_QF), 1);
     mbar_init(bar(BAR_QE), 1);
@@ -340,11 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int i = 0; i < 8; ++i) mbar_init(bar(BAR_MLF + i), SPLIT ? p.split : 1);  // one warp of each CTA
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmW1);
-    tma_prefetch_desc(&p.tmW2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -821,6 +823,13 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const int R = p.rounds;
 
+  // The tensor-map fetches start before the barrier set-up, which they
+  // overlap (the first TMA load waits for its map).
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmW1);
+    tma_prefetch_desc(&p.tmW2);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
       mbar_init(bar(BAR_RF + i), 1);
@@ -843,11 +852,6 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     mbar_init(bar(BAR_SLW), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmW1);
-    tma_prefetch_desc(&p.tmW2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);

@@ -544,6 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   int cn = 1;
   if (XMODE == X_CLUSTER) cn = p.tiles_n;
 
+  // The tensor-map fetches start before the barrier set-up, which they
+  // overlap (the first TMA load waits for its map).
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+    tma_prefetch_desc(&p.tmOut);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
@@ -566,11 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     mbar_init(bar(BAR_XDONE + 1), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tmA);
-    tma_prefetch_desc(&p.tmB);
-    tma_prefetch_desc(&p.tmOut);
   }
   if (warp == 1) {
     if (CTA2) {
