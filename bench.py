@@ -46,18 +46,18 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # sources (kernel_source_hash) matches the one the counters were taken with
 # (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "attention_long_keys": {"read": 67437568, "write": 245248, "src": "6d01d5482c565ea4"},
-    "attention_relu": {"read": 805401344, "write": 501099008, "src": "6d01d5482c565ea4"},
-    "attention_softmax": {"read": 805405184, "write": 500781568, "src": "6d01d5482c565ea4"},
-    "chained_ln_gelu_rms": {"read": 110306816, "write": 88747008, "src": "c8fb2f7ceaf75b55"},
-    "column_layernorm": {"read": 362330880, "write": 101095936, "src": "c8fb2f7ceaf75b55"},
-    "gelu_rmsnorm": {"read": 110800640, "write": 92438016, "src": "c8fb2f7ceaf75b55"},
-    "layernorm_256": {"read": 309248, "write": 0, "src": "c8fb2f7ceaf75b55"},
-    "mlp_b2b": {"read": 50396672, "write": 24078848, "src": "6d01d5482c565ea4"},
-    "mlp_bottom": {"read": 316416, "write": 0, "src": "6d01d5482c565ea4"},
-    "postnorm_layernorm": {"read": 194507008, "write": 96028672, "src": "c8fb2f7ceaf75b55"},
-    "scaled_softmax": {"read": 1396701184, "write": 239538688, "src": "c8fb2f7ceaf75b55"},
-    "target_attention": {"read": 15002112, "write": 0, "src": "6d01d5482c565ea4"},
+    "attention_long_keys": {"read": 67437568, "write": 139008, "src": "151c4b10b4241f26"},
+    "attention_relu": {"read": 805357824, "write": 501547520, "src": "151c4b10b4241f26"},
+    "attention_softmax": {"read": 805883648, "write": 501188864, "src": "151c4b10b4241f26"},
+    "chained_ln_gelu_rms": {"read": 115811328, "write": 88339200, "src": "29f260354398346b"},
+    "column_layernorm": {"read": 312576512, "write": 98750976, "src": "29f260354398346b"},
+    "gelu_rmsnorm": {"read": 117743872, "write": 90889984, "src": "29f260354398346b"},
+    "layernorm_256": {"read": 306944, "write": 0, "src": "29f260354398346b"},
+    "mlp_b2b": {"read": 50400512, "write": 23601408, "src": "151c4b10b4241f26"},
+    "mlp_bottom": {"read": 316416, "write": 0, "src": "151c4b10b4241f26"},
+    "postnorm_layernorm": {"read": 200737280, "write": 93517312, "src": "29f260354398346b"},
+    "scaled_softmax": {"read": 1386292224, "write": 239206144, "src": "29f260354398346b"},
+    "target_attention": {"read": 15002368, "write": 0, "src": "151c4b10b4241f26"},
 }
 
 
@@ -68,18 +68,18 @@ NCU_TRAFFIC = {
 # 4-byte reductions and atomics on the workspace's arrival counters (counted
 # per 32-byte sector).  Keyed and validated like NCU_TRAFFIC.
 NCU_STORES = {
-    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
-    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
-    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
-    "chained_ln_gelu_rms": {"tma": 134217728, "st": 2097152, "red": 262144, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "column_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "gelu_rmsnorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "layernorm_256": {"tma": 262144, "st": 0, "red": 0, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
-    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
-    "postnorm_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "scaled_softmax": {"tma": 268435456, "st": 2097152, "red": 262144, "atom": 0, "src": "c8fb2f7ceaf75b55"},
-    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "6d01d5482c565ea4"},
+    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "chained_ln_gelu_rms": {"tma": 134217728, "st": 2097152, "red": 262144, "atom": 0, "src": "29f260354398346b"},
+    "column_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "29f260354398346b"},
+    "gelu_rmsnorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "29f260354398346b"},
+    "layernorm_256": {"tma": 262144, "st": 0, "red": 0, "atom": 0, "src": "29f260354398346b"},
+    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "postnorm_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "29f260354398346b"},
+    "scaled_softmax": {"tma": 268435456, "st": 2097152, "red": 262144, "atom": 0, "src": "29f260354398346b"},
+    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
 }
 
 
