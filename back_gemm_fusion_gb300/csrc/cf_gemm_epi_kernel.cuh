@@ -338,13 +338,19 @@ template <int ROWOP, bool RAG, bool COLS, int ROWOP0>
 __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t taddr, int nch, int nv, int n0, int m,
                                              const float* vsm, float r_bias, float r_gamma0, float r_beta0,
                                              float sc0, float sh0) {
-  float2 st;
-  // Pass 1: elementwise program, kept in TMEM; first local statistic.  Each
-  // statistic is kept in four partial accumulators (element j goes to
-  // accumulator j mod 4): one epilogue warp runs per SM sub-partition, so a
-  // single chain of 32 dependent adds per chunk would expose its latency.
-  const float s1_init = (ROWOP == ROW_SOFTMAX) ? -INFINITY : 0.0f;
-  float s1p[4] = {s1_init, s1_init, s1_init, s1_init};
+  // One pass: the elementwise program (its result kept in TMEM) and the
+  // segment's statistics together, so a tile publishes them after a single
+  // walk over its columns.  LayerNorm: sums of x - k and (x - k)^2 about a
+  // shift k, the segment's first value (the shifted-data form of the
+  // variance, exact for any k and accurate while k is near the mean);
+  // softmax: the online maximum and the sum of exp(x - max), rescaled when
+  // the maximum grows; RMSNorm: the sum of squares.  Each sum is kept in four
+  // partial accumulators (element j in accumulator j mod 4, two per packed
+  // fp32x2 instruction): one epilogue warp runs per SM sub-partition, so a
+  // single chain of dependent adds would expose its latency.
+  float s1p[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float shift = 0.0f;                         // LayerNorm: k
+  float run_max = -INFINITY, run_sum = 0.0f;  // softmax
 #pragma unroll 1
   for (int c = 0; c < nch; ++c) {
     float v[32];
@@ -368,55 +374,62 @@ __device__ __forceinline__ float2 tile_stats(const GemmEpiParams& p, uint32_t ta
       else apply_program<false, COLS>(p, v, n, m, o0, p.n_ops, bs, r_bias);
       tmem_st32(taddr + c * 32, v);
     }
-    if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : 0.0f);
+    if (ROWOP == ROW_LAYERNORM && c == 0) shift = v[0];  // column n0 < N: always valid
+    // Columns past N leave every statistic unchanged.
+    if (tail) mask_tail(v, p.N - n, ROWOP == ROW_SOFTMAX ? -INFINITY : ROWOP == ROW_LAYERNORM ? shift : 0.0f);
+    if (ROWOP == ROW_RMSNORM) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      if (ROWOP == ROW_RMSNORM) {
+      for (int j = 0; j < 32; j += 4) {
         ffma2(s1p[0], s1p[1], v[j], v[j + 1], v[j], v[j + 1], s1p[0], s1p[1]);
         ffma2(s1p[2], s1p[3], v[j + 2], v[j + 3], v[j + 2], v[j + 3], s1p[2], s1p[3]);
-      } else if (ROWOP == ROW_SOFTMAX) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) s1p[k] = fmaxf(s1p[k], v[j + k]);
-      } else {
-        fadd2(s1p[0], s1p[1], v[j], v[j + 1]);
-        fadd2(s1p[2], s1p[3], v[j + 2], v[j + 3]);
       }
-    }
-  }
-  const float s1 = (ROWOP == ROW_SOFTMAX) ? fmaxf(fmaxf(s1p[0], s1p[1]), fmaxf(s1p[2], s1p[3]))
-                                          : (s1p[0] + s1p[1]) + (s1p[2] + s1p[3]);
-  if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
-  if (ROWOP == ROW_RMSNORM) {
-    st = make_float2(s1, 0.0f);
-  } else {
-    // Pass 2: second local statistic about the segment's own max/mean.
-    const float ref = (ROWOP == ROW_SOFTMAX) ? s1 : RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
-    float s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
-      tmem_wait_ld();
-      if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ROWOP == ROW_SOFTMAX ? -INFINITY : ref);
+    } else if (ROWOP == ROW_LAYERNORM) {
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
         float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
-        fadd2(d0, d1, -ref, -ref);
-        fadd2(d2, d3, -ref, -ref);
-        if (ROWOP == ROW_SOFTMAX) {
-          fmul2(d0, d1, kLog2e, kLog2e);
-          fmul2(d2, d3, kLog2e, kLog2e);
-          fadd2(s2p[0], s2p[1], ex2_approx(d0), ex2_approx(d1));
-          fadd2(s2p[2], s2p[3], ex2_approx(d2), ex2_approx(d3));
-        } else {
-          ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
-          ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
-        }
+        fadd2(d0, d1, -shift, -shift);
+        fadd2(d2, d3, -shift, -shift);
+        fadd2(s1p[0], s1p[1], d0, d1);
+        fadd2(s1p[2], s1p[3], d2, d3);
+        ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
+        ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
       }
+    } else {  // softmax
+      float cm[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+      for (int j = 4; j < 32; j += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cm[k] = fmaxf(cm[k], v[j + k]);
+      }
+      const float m_new = fmaxf(run_max, fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3])));
+      if (m_new > run_max) run_sum *= ex2_approx((run_max - m_new) * kLog2e);  // 0 while run_max is -inf
+      const float sh = -m_new * kLog2e;
+      float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
+        ffma2(d0, d1, d0, d1, kLog2e, kLog2e, sh, sh);
+        ffma2(d2, d3, d2, d3, kLog2e, kLog2e, sh, sh);
+        fadd2(cs[0], cs[1], ex2_approx(d0), ex2_approx(d1));
+        fadd2(cs[2], cs[3], ex2_approx(d2), ex2_approx(d3));
+      }
+      run_sum += (cs[0] + cs[1]) + (cs[2] + cs[3]);
+      run_max = m_new;
     }
-    st = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
   }
-
+  if (ROWOP0 != ROW_NONE || p.n_ops > 0) tmem_wait_st();
+  float2 st;
+  if (ROWOP == ROW_RMSNORM) {
+    st = make_float2((s1p[0] + s1p[1]) + (s1p[2] + s1p[3]), 0.0f);
+  } else if (ROWOP == ROW_LAYERNORM) {
+    const float cnt = RAG ? (float)nv : (float)kBN;
+    const float s1 = (s1p[0] + s1p[1]) + (s1p[2] + s1p[3]);
+    const float s2 = (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]);
+    const float dm = s1 / cnt;                                     // mean - k
+    st = make_float2(shift + dm, fmaxf(s2 - s1 * dm, 0.0f));      // (mean, sum of squared deviations)
+  } else {
+    st = make_float2(run_max, run_sum);
+  }
   return st;
 }
 
