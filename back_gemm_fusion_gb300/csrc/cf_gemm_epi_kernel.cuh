@@ -883,7 +883,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       // before the ops that follow it.
       float sc0 = 1.0f, sh0 = 0.0f;
       if constexpr (ROWOP0 != ROW_NONE) {
-        float s1p[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four partial sums, as in tile_stats
+        // One pass, as in tile_stats: the sum of squares (RMSNorm), or the
+        // sums of x - k and (x - k)^2 about the segment's first value k
+        // (LayerNorm), in four partial accumulators.
+        float s1p[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float shift = 0.0f;
 #pragma unroll 1
         for (int c = 0; c < nch; ++c) {
           float v[32];
@@ -897,15 +901,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             else apply_program<false, COLS>(p, v, n, m0 + row, 0, p.n_ops0, bs, r_bias);
             tmem_st32(taddr + c * 32, v);
           }
-          if (tail) mask_tail(v, p.N - n, 0.0f);
+          if (ROWOP0 == ROW_LAYERNORM && c == 0) shift = v[0];
+          if (tail) mask_tail(v, p.N - n, ROWOP0 == ROW_LAYERNORM ? shift : 0.0f);
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             if (ROWOP0 == ROW_RMSNORM) {
               ffma2(s1p[0], s1p[1], v[j], v[j + 1], v[j], v[j + 1], s1p[0], s1p[1]);
               ffma2(s1p[2], s1p[3], v[j + 2], v[j + 3], v[j + 2], v[j + 3], s1p[2], s1p[3]);
             } else {
-              fadd2(s1p[0], s1p[1], v[j], v[j + 1]);
-              fadd2(s1p[2], s1p[3], v[j + 2], v[j + 3]);
+              float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
+              fadd2(d0, d1, -shift, -shift);
+              fadd2(d2, d3, -shift, -shift);
+              fadd2(s1p[0], s1p[1], d0, d1);
+              fadd2(s1p[2], s1p[3], d2, d3);
+              ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
+              ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
             }
           }
         }
@@ -915,24 +925,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         if (ROWOP0 == ROW_RMSNORM) {
           st0 = make_float2(s1, 0.0f);
         } else {
-          const float ref = RAG ? s1 / (float)nv : s1 * (1.0f / kBN);
-          float s2p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-          for (int c = 0; c < nch; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            tmem_wait_ld();
-            if (RAG && n0 + c * 32 + 32 > p.N) mask_tail(v, p.N - n0 - c * 32, ref);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float d0 = v[j], d1 = v[j + 1], d2 = v[j + 2], d3 = v[j + 3];
-              fadd2(d0, d1, -ref, -ref);
-              fadd2(d2, d3, -ref, -ref);
-              ffma2(s2p[0], s2p[1], d0, d1, d0, d1, s2p[0], s2p[1]);
-              ffma2(s2p[2], s2p[3], d2, d3, d2, d3, s2p[2], s2p[3]);
-            }
-          }
-          st0 = make_float2(ref, (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]));
+          const float s2 = (s2p[0] + s2p[1]) + (s2p[2] + s2p[3]);
+          const float dm = s1 / (RAG ? (float)nv : (float)kBN);
+          st0 = make_float2(shift + dm, fmaxf(s2 - s1 * dm, 0.0f));
         }
         if (XMODE == X_GLOBAL &&
             !global_exchange<ROWOP0, RAG>(p, p.ws_stats0, p.ws_count0, strip, tile, row, q, lane, abort_flag, wc, st0))
