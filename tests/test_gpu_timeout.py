@@ -8,10 +8,10 @@ cf_last_device_status, and the next call on the same context, with the
 default budget, must match the oracle.
 
 No wait is made endless and nothing faults on purpose: a timeout is the
-bounded wait's ordinary error status.  The configurations are the ones
-whose in-flight loads each CTA waits for exactly (one CTA per tile, the
-attention kernel with and without the key split, the MLP kernel with one
-CTA per cluster)."""
+bounded wait's ordinary error status.  The configurations: one CTA per
+tile and the attention and MLP kernels, whose CTAs wait for their own
+in-flight loads exactly, and CTA pairs, whose loads complete on the pair
+leader's barrier (both CTAs settle after the cluster barrier)."""
 import math
 
 import numpy as np
@@ -50,15 +50,17 @@ def _timed_out(cf, monkeypatch, call):
     return cf.cf_last_device_status()
 
 
-@pytest.mark.parametrize("N,exchange", [(2048, "global"), (256, "auto")])
-def test_gemm_epilogue_timeout_then_parity(cf, monkeypatch, N, exchange):
+@pytest.mark.parametrize("M,N,exchange", [(384, 2048, "global"), (384, 256, "auto"), (512, 2048, "global"),
+                                          (512, 256, "auto")])
+def test_gemm_epilogue_timeout_then_parity(cf, monkeypatch, M, N, exchange):
     # Three row strips (an odd count): one CTA per tile, with the workspace
-    # exchange across 8 tiles per row, or a single tile per row.
-    case = I.gemm_epilogue_case("timeout", 384, N, 1024, [("bias",), ("layernorm", 1e-5)], seed=N,
+    # exchange across 8 tiles per row, or a single tile per row.  Four strips:
+    # CTA pairs, likewise.
+    case = I.gemm_epilogue_case("timeout", M, N, 1024, [("bias",), ("layernorm", 1e-5)], seed=N,
                                 need_bias=True, need_gamma=True, need_beta=True)
     A, B = case.A.cuda(), case.B.cuda()
     vec = [t.cuda() for t in (case.bias, case.gamma, case.beta)]
-    out = torch.empty((384, N), dtype=torch.float32, device="cuda")
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
     st = _timed_out(cf, monkeypatch, lambda: cf.cf_gemm_epilogue(A, B, case.ops, *vec, out=out, exchange=exchange))
     assert st == CF_ERR_TIMEOUT
     cf.cf_gemm_epilogue(A, B, case.ops, *vec, out=out, exchange=exchange)
@@ -66,7 +68,7 @@ def test_gemm_epilogue_timeout_then_parity(cf, monkeypatch, N, exchange):
     assert cf.cf_last_device_status() == 0
     ref = O.gemm_epilogue(I.to_f64(case.A), I.to_f64(case.B), case.ops, I.to_f64(case.bias), I.to_f64(case.gamma),
                           I.to_f64(case.beta))
-    assert_rows_close(out.cpu().numpy(), ref, what=f"after a timeout, N={N} {exchange}")
+    assert_rows_close(out.cpu().numpy(), ref, what=f"after a timeout, {M}x{N} {exchange}")
 
 
 @pytest.mark.parametrize("key_split", [1, 4])
