@@ -112,3 +112,25 @@ def test_chained_static_order_wide_rows(cf, M, N):
     ref = O.gemm_epilogue(I.to_f64(case.A)[rows], I.to_f64(case.B), case.ops, I.to_f64(case.bias),
                           I.to_f64(case.gamma), None)
     assert_rows_close(out[rows].cpu().numpy(), ref, what=f"chained wide rows {M}x{N}")
+
+
+def test_row_width_limit(cf):
+    # The widest rows the workspace exchange accepts: 304 tiles per strip on
+    # one-CTA workers (one strip, an odd count), twice the 152 workers of a
+    # 152-SM GB300: N = 77,824 runs (claimed items, two tiles of the strip per
+    # worker) and matches the oracle; one tile more is refused on the host.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K = 128, 64
+    N = 2 * sms * 256
+    ops = [("scale", 0.125), ("softmax",)]
+    case = I.gemm_epilogue_case("widest", M, N, K, ops, seed=5)
+    A, B = case.A.cuda(), case.B.cuda()
+    out = cf.cf_gemm_epilogue(A, B, case.ops)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    rows = sample_rows(M, 24, seed=4)
+    ref = O.gemm_epilogue(I.to_f64(case.A)[rows], I.to_f64(case.B), case.ops, None, None, None)
+    assert_rows_close(out[rows].cpu().numpy(), ref, what=f"softmax over {N} columns")
+    wider = I.gemm_epilogue_case("too_wide", M, N + 256, K, ops, seed=6)
+    with pytest.raises(cf.CFError):
+        cf.cf_gemm_epilogue(wider.A.cuda(), wider.B.cuda(), wider.ops)
