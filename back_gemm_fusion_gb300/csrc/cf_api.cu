@@ -236,12 +236,13 @@ cf_status validate_gemm_epi(const cf_matrix* A, const cf_matrix* B, const float*
   if (plan->cols && B->trans != 1) return CF_ERR_UNSUPPORTED_SHAPE;
   // Any M >= 1: rows past M are zero-filled by the TMA loads and clipped by
   // the TMA stores of the last (ragged) 128-row strip; rows are independent.
-  // K >= 64 with K % 8 == 0: the last 64-wide K block reads zeros past K
+  // K >= 8 with K % 8 == 0: the last (or only) 64-wide K block reads zeros
+  // past K
   // (TMA out-of-bounds fill), which add nothing to the products.
   // Any N >= 1: the last 256-column tile of a row may be ragged; its B
   // columns past N load as zeros, the epilogue keeps them out of the row
   // statistics and never reads a vector past N, and the TMA stores clip them.
-  if (K % 8 != 0 || K < kBK) return CF_ERR_UNSUPPORTED_SHAPE;
+  if (K % 8 != 0 || K < 8) return CF_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t)1 << 31 || N > (int64_t)1 << 31 || K > (int64_t)1 << 31) return CF_ERR_UNSUPPORTED_SHAPE;
   const int64_t tiles_n = (kN + kBN - 1) / kBN;
   if (epi->exchange == CF_XCHG_CLUSTER && plan->rowop != ROW_NONE && tiles_n > kMaxClusterCtas)

@@ -1,4 +1,4 @@
-// cf_b2bgemm.cu -- fused back-to-back GEMM: O = bf16(F(A . W1)) . W2 with the
+// cf_b2b.cu -- fused back-to-back GEMM: O = bf16(F(A . W1)) . W2 with the
 // intermediate S' never written to global memory.
 //
 // ComFuse review, "What carries the argument": the B2BGEMM schedule keeps the
@@ -1282,9 +1282,10 @@ extern "C" cf_status cf_b2bgemm(const cf_matrix* A, const cf_matrix* W1, const c
   // (K % 8 == 0), any N1 >= 1 (a ragged last 128-key chunk is masked).
   const bool attn_shape = W1->trans == 1 && K % 8 == 0 && K >= 8 && K <= 128 && N2 >= 1 && N2 <= 128 && N1 >= 1;
   // MLP shape: N2 <= 256 C with C <= 4 CTAs per cluster (the last CTA's
-  // block may be ragged), any N1 >= 1, elementwise F only.
+  // block may be ragged), any N1 >= 1, K >= 8 (a K below 64 is one
+  // zero-filled 64-wide block), elementwise F only.
   const int64_t C = (N2 + 255) / 256;
-  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 64 && C >= 1 &&
+  const bool mlp_shape = !attn_shape && d->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 8 && C >= 1 &&
                          C <= mlp::kMaxC && N1 >= 1;
   if (!attn_shape && !mlp_shape) return CF_ERR_UNSUPPORTED_SHAPE;
 

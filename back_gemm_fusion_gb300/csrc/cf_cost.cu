@@ -94,7 +94,7 @@ extern "C" cf_status cf_cost_gemm_epilogue(const cf_matrix* A, const cf_matrix* 
   if (epi->version < 1 || epi->version > 3 || epi->n_ops > CF_EPI_MAX_OPS) return CF_ERR_INVALID_ARG;
   if (A->trans != 0 || A->cols != B->rows || A->rows < 0 || B->cols < 0) return CF_ERR_INVALID_ARG;
   const double M = (double)A->rows, N = (double)B->cols, K = (double)A->cols;
-  if ((A->cols % 8) != 0 || A->cols < 64) return CF_ERR_UNSUPPORTED_SHAPE;
+  if ((A->cols % 8) != 0 || A->cols < 8) return CF_ERR_UNSUPPORTED_SHAPE;
   int n_red = 0, has_res = 0, n_vec = 0;
   double instr = 6.0;  // TMEM load, statistics and the final store per element
   for (uint32_t i = 0; i < epi->n_ops; ++i) {
@@ -161,7 +161,7 @@ extern "C" cf_status cf_cost_b2bgemm(const cf_matrix* A, const cf_matrix* W1, co
   if (W1->rows != K || W2->rows != N1) return CF_ERR_INVALID_ARG;
   const bool attn = W1->trans == 1 && K % 8 == 0 && K >= 8 && K <= 128 && N2 >= 1 && N2 <= 128 && N1 >= 1;
   const int64_t C = (N2 + 255) / 256;
-  const bool mlp = !attn && desc->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 64 && C >= 1 && C <= 4 &&
+  const bool mlp = !attn && desc->mid_op != CF_MID_SCALE_SOFTMAX && K % 8 == 0 && K >= 8 && C >= 1 && C <= 4 &&
                    N1 >= 1;
   if (!attn && !mlp) return CF_ERR_UNSUPPORTED_SHAPE;
   const Dev d = dev_model(dm);

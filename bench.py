@@ -46,18 +46,18 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # sources (kernel_source_hash) matches the one the counters were taken with
 # (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "attention_long_keys": {"read": 67437568, "write": 139008, "src": "151c4b10b4241f26"},
-    "attention_relu": {"read": 805357824, "write": 501547520, "src": "151c4b10b4241f26"},
-    "attention_softmax": {"read": 805883648, "write": 501188864, "src": "151c4b10b4241f26"},
+    "attention_long_keys": {"read": 67437568, "write": 296704, "src": "3a96206cef88617b"},
+    "attention_relu": {"read": 805474560, "write": 501778688, "src": "3a96206cef88617b"},
+    "attention_softmax": {"read": 805428224, "write": 502090752, "src": "3a96206cef88617b"},
     "chained_ln_gelu_rms": {"read": 115985408, "write": 88527104, "src": "2ebf5273d3cc2d77"},
     "column_layernorm": {"read": 309405696, "write": 99708160, "src": "2ebf5273d3cc2d77"},
     "gelu_rmsnorm": {"read": 118271744, "write": 90887936, "src": "2ebf5273d3cc2d77"},
     "layernorm_256": {"read": 306688, "write": 0, "src": "2ebf5273d3cc2d77"},
-    "mlp_b2b": {"read": 50400512, "write": 23601408, "src": "151c4b10b4241f26"},
-    "mlp_bottom": {"read": 316416, "write": 0, "src": "151c4b10b4241f26"},
+    "mlp_b2b": {"read": 50508800, "write": 23389696, "src": "3a96206cef88617b"},
+    "mlp_bottom": {"read": 316160, "write": 0, "src": "3a96206cef88617b"},
     "postnorm_layernorm": {"read": 199381504, "write": 92698880, "src": "2ebf5273d3cc2d77"},
     "scaled_softmax": {"read": 1387041024, "write": 239633664, "src": "2ebf5273d3cc2d77"},
-    "target_attention": {"read": 15002368, "write": 0, "src": "151c4b10b4241f26"},
+    "target_attention": {"read": 15002112, "write": 0, "src": "3a96206cef88617b"},
 }
 
 
@@ -68,18 +68,18 @@ NCU_TRAFFIC = {
 # 4-byte reductions and atomics on the workspace's arrival counters (counted
 # per 32-byte sector).  Keyed and validated like NCU_TRAFFIC.
 NCU_STORES = {
-    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
-    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
-    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
     "chained_ln_gelu_rms": {"tma": 134217728, "st": 2097152, "red": 262144, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "column_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "gelu_rmsnorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "layernorm_256": {"tma": 262144, "st": 0, "red": 0, "atom": 0, "src": "2ebf5273d3cc2d77"},
-    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
-    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
     "postnorm_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "scaled_softmax": {"tma": 268435456, "st": 2097152, "red": 262144, "atom": 0, "src": "2ebf5273d3cc2d77"},
-    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "151c4b10b4241f26"},
+    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
 }
 
 

@@ -190,7 +190,8 @@ typedef struct {
  * Shape rules (this version): any M >= 0 (a ragged last 128-row strip is
  * handled), any N >= 0 (a ragged last 256-column tile is handled: its
  * columns past N stay out of the row statistics and are not stored), K % 8
- * == 0 with K >= 64 (a ragged last 64-wide K block reads zeros), all
+ * == 0 with K >= 8 (a ragged last, or only, 64-wide K block reads zeros
+ * past K), all
  * pointers and leading dims 16-byte aligned; the cluster exchange takes rows
  * of at most 16 tiles (N <= 4096).  Through the workspace every tile of a
  * row strip waits for its strip-mates and each CTA (or CTA pair) holds two
@@ -319,7 +320,7 @@ typedef struct {
  *     (K % 8 == 0) and N2 <= 128 (both computed as 128 with zero padding),
  *     any N1 >= 1 (keys past N1 in the last 128-key chunk are masked); any
  *     mid op (the softmax normalises over all N1);
- *   MLP shape: mid op ReLU or scaled ReLU, K % 8 == 0 with K >= 64,
+ *   MLP shape: mid op ReLU or scaled ReLU, K % 8 == 0 with K >= 8,
  *     N2 <= 1024 (C = ceil(N2 / 256) CTAs per cluster), any N1 >= 1.
  *   The softmax mid op needs mid_scale > 0 (CF_ERR_INVALID_ARG otherwise).
  *   Both: any M >= 0 (a ragged last 128-row block is handled), pointers and

@@ -84,7 +84,15 @@ def test_validation_errors(lib):
     A5, B5, O5 = _mats(K=96)
     assert _call(lib, A5, B5, O5, LN) in (0, 4, 8)          # ragged K (K % 8 == 0) is supported
     A6, B6, O6 = _mats(K=56)
-    assert _call(lib, A6, B6, O6, LN) == 2                  # K below one 64-wide block
+    assert _call(lib, A6, B6, O6, LN) in (0, 4, 8)          # K below 64: one zero-filled block
+    A6, B6, O6 = _mats(K=8)
+    assert _call(lib, A6, B6, O6, LN) in (0, 4, 8)
+    A6, B6, O6 = _mats(K=0)
+    A6.ld = 8
+    assert _call(lib, A6, B6, O6, LN) == 2                  # no K at all
+    A6, B6, O6 = _mats(K=60)
+    A6.ld, B6.cols, O6.cols = 64, 256, 256
+    assert _call(lib, A6, B6, O6, LN) == 2                  # K % 8 != 0
     A6, B6, O6 = _mats(a_ptr=0x10008)
     assert _call(lib, A6, B6, O6, LN) == 3                  # misaligned pointer
     A7, B7, O7 = _mats()
@@ -249,6 +257,8 @@ def test_b2b_shape_rules(lib):
     assert call(256, 256, 200, 300, op="relu", trans=False) in ok       # MLP, ragged N1 and N2
     assert call(256, 256, 512, 1000, op="relu", trans=False) in ok      # MLP, C = 4, last block ragged
     assert call(256, 256, 512, 1100, op="relu", trans=False) == 2       # MLP, C = 5 > 4
+    assert call(256, 16, 512, 256, op="relu", trans=False) in ok        # MLP, K below one 64-wide block
+    assert call(256, 8, 512, 256, op="relu", trans=True) in ok
 
 
 def test_dynamic_exchange_rules(lib):

@@ -90,8 +90,11 @@ def test_monotonic_and_device_overrides(lib):
     fast = B.cf_cost_gemm_epilogue(8192, 4096, 4096, GELU_RMS, device={"tensor_tflops": 2 * 1908.0})
     assert fast["mainloop_us"] == pytest.approx(base["mainloop_us"] / 2, rel=1e-12)
     assert fast["fused_us"] < base["fused_us"]
-    with pytest.raises(B.CFError):               # K below one 64-wide block
-        B.cf_cost_gemm_epilogue(256, 256, 56, LN)
+    # K below one 64-wide block costs that block's main loop; K % 8 != 0 is refused.
+    assert B.cf_cost_gemm_epilogue(256, 256, 16, LN)["mainloop_us"] == \
+        pytest.approx(B.cf_cost_gemm_epilogue(256, 256, 64, LN)["mainloop_us"], rel=1e-12)
+    with pytest.raises(B.CFError):
+        B.cf_cost_gemm_epilogue(256, 256, 60, LN)
     # Rows up to twice the resident CTAs in tiles (304 x 256 = 77,824) are
     # accepted, wider ones refused like the fused call refuses them.
     assert B.cf_cost_gemm_epilogue(1024, 77824, 256, SOFTMAX)["fused_us"] > 0

@@ -187,6 +187,22 @@ def test_mlp_ragged(cf, M, K, N1, N2, w1_trans):
     b2b_gate(out.cpu().numpy(), ref, bound, f"mlp ragged {M}x{K}x{N1}x{N2} trans={w1_trans}")
 
 
+@pytest.mark.parametrize("M,K,N1,N2,w1_trans", [(64, 16, 512, 256, False), (300, 8, 256, 1024, True),
+                                                (129, 56, 384, 600, False), (1, 24, 128, 512, True)])
+def test_mlp_short_k(cf, M, K, N1, N2, w1_trans):
+    # K below one 64-wide block (a first layer over a few dense features,
+    # 13 padded to 16): the only K block of X and W1 reads zeros past K.
+    X, W1, W2 = _mlp_case(M, K, N1, N2, seed=M * 11 + K)
+    W1d = W1.t().contiguous().cuda() if w1_trans else W1.cuda()
+    out = cf.cf_b2bgemm(X.cuda(), W1d, W2.cuda(), "relu", 1.0, w1_trans=w1_trans)
+    torch.cuda.synchronize()
+    assert cf.cf_last_device_status() == 0
+    x, w1, w2 = (I.to_f64(t) for t in (X, W1, W2))
+    ref = O.b2bgemm(x, w1, w2, "relu", 1.0)
+    bound = np.abs(O.mid_op(x @ w1, "relu", 1.0)) @ np.abs(w2)
+    b2b_gate(out.cpu().numpy(), ref, bound, f"mlp short K {M}x{K}x{N1}x{N2} trans={w1_trans}")
+
+
 @pytest.mark.parametrize("batch,M,K,N1,N2,w1_trans", [(1, 384, 128, 640, 600, False), (2, 257, 64, 384, 1024, True),
                                                        (3, 512, 96, 256, 256, False)])
 def test_mlp_batched(cf, batch, M, K, N1, N2, w1_trans):

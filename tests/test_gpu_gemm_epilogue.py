@@ -115,6 +115,23 @@ def test_ragged_k(cf, M, K, rowop, b_trans):
                       what=f"ragged K={K} M={M} {rowop} b_trans={b_trans}")
 
 
+@pytest.mark.parametrize("M,N,K,rowop,b_trans,exchange", [
+    (128, 512, 8, "none", False, "auto"), (300, 512, 16, "layernorm", True, "auto"),
+    (256, 1024, 24, "rmsnorm", False, "cluster"), (200, 768, 56, "softmax", True, "auto"),
+    (384, 4096, 16, "layernorm", False, "global"), (129, 2056, 40, "softmax", False, "global_dynamic")])
+def test_short_k(cf, M, N, K, rowop, b_trans, exchange):
+    # K below one 64-wide block (e.g. a first layer over 13 dense features
+    # padded to 16): the only K block reads zeros past K.
+    ops = {"none": [("bias",), ("relu",)], "layernorm": [("bias",), ("layernorm", 1e-5)],
+           "rmsnorm": [("bias",), ("gelu_tanh",), ("rmsnorm", 1e-6)],
+           "softmax": [("scale", 0.125), ("softmax",)]}[rowop]
+    case = I.gemm_epilogue_case("short_k", M, N, K, ops, seed=M + N + K, need_bias=True, need_gamma=True,
+                                need_beta=True)
+    assert_rows_close(_run(cf, case, b_trans, exchange=exchange), _oracle(case),
+                      strict=1e-4 if rowop == "none" else 2e-3,
+                      what=f"short K={K} {M}x{N} {rowop} b_trans={b_trans} {exchange}")
+
+
 @pytest.mark.parametrize("res_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M,N,K,prog", [(256, 512, 128, "layernorm"), (333, 1024, 256, "rmsnorm"),
                                         (256, 4352, 128, "softmax"), (200, 256, 64, "none"),
