@@ -452,18 +452,26 @@ def max_over_ranks(dist, v: float) -> float:
     return float(t.item())
 
 
-def time_oracle(wl: Workload, budget_s: float):
-    """Time the oracle on a seeded row sample sized to about budget_s seconds."""
+def time_oracle(wl: Workload, budget_s: float, resize: bool = True):
+    """Time the oracle on a seeded row sample sized to about budget_s seconds
+    (resize: size it once more when the first sample ran well under budget;
+    the reference arm's many short steps skip that)."""
     rng = np.random.default_rng(0)
     n = 16 if wl.is_b2b else 64
     t0 = time.perf_counter()
     flops = wl.oracle_rows(np.sort(rng.choice(wl.rows, size=min(n, wl.rows), replace=False)))
     dt = time.perf_counter() - t0
     rows = int(min(wl.rows, max(n, n * budget_s / max(dt, 1e-3))))
-    sample = np.sort(rng.choice(wl.rows, size=rows, replace=False))
-    t0 = time.perf_counter()
-    flops = wl.oracle_rows(sample)
-    dt = time.perf_counter() - t0
+    for _ in range(2 if resize else 1):
+        sample = np.sort(rng.choice(wl.rows, size=rows, replace=False))
+        t0 = time.perf_counter()
+        flops = wl.oracle_rows(sample)
+        dt = time.perf_counter() - t0
+        # The small pilot over-estimates the cost per row (fixed costs per
+        # call): size the sample once more when it ran well under budget.
+        if dt >= 0.6 * budget_s or rows >= wl.rows:
+            break
+        rows = int(min(wl.rows, rows * budget_s / max(dt, 1e-3)))
     return flops / dt / 1e12, rows, dt
 
 
@@ -473,10 +481,10 @@ def run_reference(args, wl: Workload, dist, rank, world):
         return
     cores = os.cpu_count()
     for _ in range(args.warmup):
-        time_oracle(wl, args.ref_step_seconds / 4)
+        time_oracle(wl, args.ref_step_seconds / 4, resize=False)
     vals, rows_used, secs = [], 0, 0.0
     for _ in range(args.steps):
-        v, rows_used, dt = time_oracle(wl, args.ref_step_seconds)
+        v, rows_used, dt = time_oracle(wl, args.ref_step_seconds, resize=False)
         vals.append(v)
         secs += dt
     value = statistics.mean(vals)
