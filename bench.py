@@ -43,21 +43,22 @@ METRIC = "fused TFLOP/s & % of GB300 roofline; intermediate HBM bytes (target 0)
 # from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,... -k <fused
 # kernel> -c 1 bench.py --workload W --once` on a GB300 (fp32 output), keyed
 # by workload; valid only while the hash of the workload's kernel family
-# sources (kernel_source_hash) matches the one the counters were taken with
+# sources (kernel_source_hash) matches the one the counters were taken with,
+# and for the workloads sized by --rows only at the rows they were taken at
 # (profiles/ has the summaries and commands).
 NCU_TRAFFIC = {
-    "attention_long_keys": {"read": 67437568, "write": 296704, "src": "3a96206cef88617b"},
-    "attention_relu": {"read": 805474560, "write": 501778688, "src": "3a96206cef88617b"},
-    "attention_softmax": {"read": 805428224, "write": 502090752, "src": "3a96206cef88617b"},
+    "attention_long_keys": {"read": 67437568, "write": 290560, "src": "2be13edd6b10da33"},
+    "attention_relu": {"read": 805388800, "write": 502074880, "src": "2be13edd6b10da33"},
+    "attention_softmax": {"read": 805359104, "write": 501249792, "src": "2be13edd6b10da33"},
     "chained_ln_gelu_rms": {"read": 115985408, "write": 88527104, "src": "2ebf5273d3cc2d77"},
     "column_layernorm": {"read": 309405696, "write": 99708160, "src": "2ebf5273d3cc2d77"},
     "gelu_rmsnorm": {"read": 118271744, "write": 90887936, "src": "2ebf5273d3cc2d77"},
     "layernorm_256": {"read": 306688, "write": 0, "src": "2ebf5273d3cc2d77"},
-    "mlp_b2b": {"read": 50508800, "write": 23389696, "src": "3a96206cef88617b"},
-    "mlp_bottom": {"read": 316160, "write": 0, "src": "3a96206cef88617b"},
+    "mlp_b2b": {"read": 50491648, "write": 23822592, "src": "2be13edd6b10da33"},
+    "mlp_bottom": {"read": 316160, "write": 0, "rows": 64, "src": "2be13edd6b10da33"},
     "postnorm_layernorm": {"read": 199381504, "write": 92698880, "src": "2ebf5273d3cc2d77"},
     "scaled_softmax": {"read": 1387041024, "write": 239633664, "src": "2ebf5273d3cc2d77"},
-    "target_attention": {"read": 15002112, "write": 0, "src": "3a96206cef88617b"},
+    "target_attention": {"read": 15002368, "write": 0, "rows": 64, "src": "2be13edd6b10da33"},
 }
 
 
@@ -68,18 +69,18 @@ NCU_TRAFFIC = {
 # 4-byte reductions and atomics on the workspace's arrival counters (counted
 # per 32-byte sector).  Keyed and validated like NCU_TRAFFIC.
 NCU_STORES = {
-    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
-    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
-    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "attention_long_keys": {"tma": 0, "st": 524288, "red": 0, "atom": 0, "src": "2be13edd6b10da33"},
+    "attention_relu": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "2be13edd6b10da33"},
+    "attention_softmax": {"tma": 0, "st": 536870912, "red": 0, "atom": 0, "src": "2be13edd6b10da33"},
     "chained_ln_gelu_rms": {"tma": 134217728, "st": 2097152, "red": 262144, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "column_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "gelu_rmsnorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "layernorm_256": {"tma": 262144, "st": 0, "red": 0, "atom": 0, "src": "2ebf5273d3cc2d77"},
-    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
-    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "mlp_b2b": {"tma": 0, "st": 67108864, "red": 0, "atom": 0, "src": "2be13edd6b10da33"},
+    "mlp_bottom": {"tma": 0, "st": 65536, "red": 0, "atom": 0, "rows": 64, "src": "2be13edd6b10da33"},
     "postnorm_layernorm": {"tma": 134217728, "st": 1048576, "red": 131072, "atom": 0, "src": "2ebf5273d3cc2d77"},
     "scaled_softmax": {"tma": 268435456, "st": 2097152, "red": 262144, "atom": 0, "src": "2ebf5273d3cc2d77"},
-    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "src": "3a96206cef88617b"},
+    "target_attention": {"tma": 0, "st": 16777216, "red": 0, "atom": 0, "rows": 64, "src": "2be13edd6b10da33"},
 }
 
 
@@ -147,6 +148,9 @@ class Workload:
     def __init__(self, name: str, seed: int = 0, exchange: str = "auto", rows: int = 64, out_dtype: str = "fp32"):
         self.name = name
         self.exchange = exchange
+        # --rows sizes these two workloads (the bottom MLP's rows, target
+        # attention's users); the stored counters hold for one size only.
+        self.size_rows = rows if name in ("mlp_bottom", "target_attention") else None
         self.out_dtype = torch.bfloat16 if out_dtype == "bf16" else torch.float32
         ob = 2.0 if out_dtype == "bf16" else 4.0
         if name == "gelu_rmsnorm":
@@ -687,15 +691,18 @@ def measure(args, wl: Workload, cf, peaks, dist, rank, world, local, steps: int,
     t_roof = max(wl.flops / (peaks["bf16_tflops"] * 1e12), wl.bytes / (peaks["hbm_gbs"] * 1e9))
     src = kernel_source_hash(wl.is_b2b)
     fp32 = wl.out_dtype == torch.float32  # counters taken with fp32 out
+    def counters_hold(entry):
+        return entry and entry.get("src") == src and entry.get("rows") == wl.size_rows
+
     tr = NCU_TRAFFIC.get(wl.name) if fp32 else None
-    tr = tr if tr and tr.get("src") == src else None
+    tr = tr if counters_hold(tr) else None
     traffic = (tr["read"] + tr["write"]) if tr else None
     # The page's own test: global store bytes of one launch beyond the
     # output and the row-statistics workspace (an intermediate would have
     # to be stored), from the store counters; the counter updates are
     # listed apart.
     stc = NCU_STORES.get(wl.name) if fp32 else None
-    stc = stc if stc and stc.get("src") == src else None
+    stc = stc if counters_hold(stc) else None
     inter = (stc["tma"] + stc["st"] - wl.out_bytes - wl.stat_bytes) if stc else None
     return {
         "workload": wl.name, "value": value, "ms_per_step": ms_step, "tflops": tflops,
